@@ -1,0 +1,115 @@
+"""Seeded synthetic inputs for the paged decode path (shared by tests and bench).
+
+This module only draws random numbers and lays out index metadata. It holds
+none of the attention, append or copy arithmetic, and it imports neither the
+CUDA binding nor the CPU oracle, so both sides can take their inputs from it.
+
+Workloads (named by what they are; all use 16-token blocks):
+
+* ``tiny_f32``     -- 3 sequences, 4 query / 2 KV heads, head_dim 64, fp32,
+  a 16-block pool handed out in an order drawn from seed 0.
+* ``llama8k``      -- Llama-3-8B decode layer: batch 32, 32 q / 8 kv heads,
+  head_dim 128, bf16, every context 8192 tokens, block tables a random
+  permutation (seed 1) of a 16384-block pool.
+* ``mixed``        -- continuous-batching mix: batch 256, Llama-3-8B heads,
+  lengths log-uniform on [16, 32768] (seed 2), tables packed from a shuffled
+  pool of exactly ``sum(ceil(len/16))`` blocks.
+* ``long128k``     -- 70B GQA heads (64 q / 8 kv), batch 4, 131072 tokens
+  each, tables a permutation (seed 3) of a 32768-block pool.
+* ``prefix``       -- batch 64, Llama-3-8B heads, a 4096-token (256-block)
+  shared prefix plus private suffixes uniform in [1, 2048] (seed 4).
+
+Values are standard normal. Large tensors are drawn on the device with a
+seeded ``torch.Generator``; the oracle reads the same tensors back, so
+parity never depends on two machines drawing identical numbers.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+BLOCK_SIZE = 16
+
+CONFIGS = {
+    "tiny_f32": dict(batch=3, q_heads=4, kv_heads=2, head_dim=64, dtype="f32",
+                     num_blocks=16, seed=0),
+    "llama8k": dict(batch=32, q_heads=32, kv_heads=8, head_dim=128, dtype="bf16",
+                    context=8192, num_blocks=16384, seed=1),
+    "mixed": dict(batch=256, q_heads=32, kv_heads=8, head_dim=128, dtype="bf16",
+                  min_len=16, max_len=32768, seed=2),
+    "long128k": dict(batch=4, q_heads=64, kv_heads=8, head_dim=128, dtype="bf16",
+                     context=131072, num_blocks=32768, seed=3),
+    "prefix": dict(batch=64, q_heads=32, kv_heads=8, head_dim=128, dtype="bf16",
+                   prefix=4096, min_suffix=1, max_suffix=2048, seed=4),
+}
+
+
+def blocks_needed(tokens) -> np.ndarray:
+    """ceil(tokens / 16) element-wise (how many blocks hold that many tokens)."""
+    t = np.asarray(tokens, dtype=np.int64)
+    return (t + BLOCK_SIZE - 1) // BLOCK_SIZE
+
+
+def permuted_tables(num_blocks: int, batch: int, blocks_per_seq: int, seed: int) -> np.ndarray:
+    """int32 [batch][blocks_per_seq]: the first batch*blocks_per_seq entries of a
+    random permutation of the pool's ids (numpy ``default_rng(seed)``)."""
+    perm = np.random.default_rng(seed).permutation(num_blocks)
+    need = batch * blocks_per_seq
+    if need > num_blocks:
+        raise ValueError("pool too small")
+    return perm[:need].reshape(batch, blocks_per_seq).astype(np.int32)
+
+
+def log_uniform_lengths(batch: int, lo: int, hi: int, seed: int) -> np.ndarray:
+    """int64 lengths ``rint(exp(U(ln lo, ln hi)))`` (numpy ``default_rng(seed)``)."""
+    u = np.random.default_rng(seed).uniform(math.log(lo), math.log(hi), size=batch)
+    return np.clip(np.rint(np.exp(u)), lo, hi).astype(np.int64)
+
+
+def packed_tables(lengths, seed: int, extra_blocks: int = 0):
+    """Tables drawing ``ceil(len/16)`` distinct ids per sequence from one shuffled
+    pool of exactly ``sum(ceil(len/16)) + extra_blocks`` blocks.
+
+    Returns ``(tables int32 [batch][max_blocks] padded with -1, num_blocks)``.
+    """
+    nb = blocks_needed(lengths)
+    num_blocks = int(nb.sum()) + int(extra_blocks)
+    perm = np.random.default_rng(seed + 1000).permutation(num_blocks)
+    width = max(1, int(nb.max()))
+    tables = np.full((len(nb), width), -1, dtype=np.int32)
+    off = 0
+    for i, n in enumerate(nb):
+        tables[i, :n] = perm[off:off + n]
+        off += n
+    return tables, num_blocks
+
+
+def uniform_suffixes(batch: int, lo: int, hi: int, seed: int) -> np.ndarray:
+    """int64 suffix lengths uniform on [lo, hi] (numpy ``default_rng(seed)``)."""
+    return np.random.default_rng(seed).integers(lo, hi + 1, size=batch).astype(np.int64)
+
+
+def slot_of(tables: np.ndarray, positions) -> np.ndarray:
+    """Physical slot id of logical position ``positions[i]`` of sequence ``i``.
+
+    A slot id names one 16-token block row: ``block_id * 16 + offset``. This
+    is how a host-side block manager addresses the new token of a step.
+    """
+    pos = np.asarray(positions, dtype=np.int64)
+    rows = np.arange(len(pos))
+    return tables[rows, pos // BLOCK_SIZE].astype(np.int64) * BLOCK_SIZE + pos % BLOCK_SIZE
+
+
+def numpy_normal(shape, seed: int) -> np.ndarray:
+    """float32 standard normal from numpy ``default_rng(seed)`` (small inputs)."""
+    return np.random.default_rng(seed).standard_normal(shape, dtype=np.float32)
+
+
+def torch_normal(shape, seed: int, dtype, device):
+    """Standard normal drawn by a seeded ``torch.Generator`` on ``device``."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    return torch.randn(tuple(shape), generator=gen, device=device, dtype=torch.float32).to(dtype)
