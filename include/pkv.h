@@ -1,0 +1,206 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache decode path for GB300 (sm_103a).
+ *
+ * The problem (release page "NeuralOps v1.3.4: Serving Primitives & KV Cache
+ * Optimization", Architectural Breakdown 1 "Paged KV Cache Engine"): attention
+ * K/V memory is cut into fixed 16-token physical blocks; a per-sequence block
+ * table maps logical tokens to physical blocks; new tokens are written
+ * through a slot mapping; a block is added only when a sequence crosses a
+ * block boundary. "Notebook 10. KV cache and serving: bytes, pages, and
+ * ceilings", section 5, adds prefix sharing with copy-on-write of a shared
+ * partial final block.
+ *
+ * Cache layout (one layer): two pools, K and V, each
+ *     pool[num_blocks][num_kv_heads][16][head_dim]
+ * contiguous, row-major, elements of `dtype`, base address 16-byte aligned
+ * (1024-byte alignment recommended). A slot id is `block_id * 16 + offset`.
+ * Logical token t of sequence i lives in block block_tables[i][t / 16] at
+ * offset t % 16.
+ *
+ * Conventions shared by every call:
+ *  - All pointers named *device* are CUDA device pointers on the current
+ *    device; the caller owns every buffer (including the workspace) and the
+ *    library allocates no device memory.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns without waiting, except in PKV_FLAG_CHECKED mode.
+ *  - Host-visible arguments are validated before anything is enqueued. A call
+ *    that returns an error status has written no byte of any output buffer
+ *    ("validate first; keep old state intact if an input is rejected",
+ *    notebook "PyTorch bridge - B17"; "OOM cannot leave a partially mutated
+ *    pool", notebook section 5).
+ *  - Indices that live in device memory (slot ids, block ids, context
+ *    lengths, copy pairs) are checked on the device:
+ *      * default (fast) mode: an out-of-range entry is never dereferenced; it
+ *        is skipped (append/copy) or treated as an absent token (attention),
+ *        and bit PKV_DEVERR_RANGE is set in the sticky device status that
+ *        pkv_device_status() reads.
+ *      * PKV_FLAG_CHECKED: a validation kernel runs first, the call waits for
+ *        it, and a bad index returns PKV_ERR_RANGE / PKV_ERR_OVERLAP with
+ *        nothing written.
+ *  - Every wait inside a kernel is bounded; if one runs out the kernel stops,
+ *    sets PKV_DEVERR_TIMEOUT in the sticky device status and returns.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_NULL = 1,        /* a required pointer is NULL                     */
+    PKV_ERR_SHAPE = 2,       /* a size or geometry field is invalid            */
+    PKV_ERR_DTYPE = 3,       /* unsupported element type                       */
+    PKV_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned               */
+    PKV_ERR_RANGE = 5,       /* a device-resident index is out of range        */
+    PKV_ERR_OVERLAP = 6,     /* duplicate slots / copy destinations            */
+    PKV_ERR_WORKSPACE = 7,   /* workspace NULL or smaller than required        */
+    PKV_ERR_TIMEOUT = 8,     /* a bounded in-kernel wait ran out               */
+    PKV_ERR_CUDA = 9,        /* a CUDA runtime call failed                     */
+    PKV_ERR_UNSUPPORTED = 10 /* valid request this build does not implement    */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Geometry of one layer's K and V pools. */
+typedef struct {
+    int64_t num_blocks;    /* physical blocks in each pool, >= 1              */
+    int32_t block_size;    /* tokens per block; must be 16                     */
+    int32_t num_kv_heads;  /* KV heads stored per token, >= 1                  */
+    int32_t head_dim;      /* 64 or 128                                        */
+    int32_t dtype;         /* pkv_dtype of pools, new K/V, q and out           */
+} pkv_cache_desc;
+
+/* flags */
+#define PKV_FLAG_CHECKED 1u    /* validate device-resident indices first (syncs) */
+
+/* Bits of the sticky device status (pkv_device_status). */
+#define PKV_DEVERR_TIMEOUT 1u
+#define PKV_DEVERR_RANGE 2u
+
+/* Decode tuning. Pass NULL for the defaults. */
+typedef struct {
+    int32_t kernel;     /* 0 = choose; 1 = CUDA-core kernel; 2 = tensor-core
+                           (mma.sync) kernel: bf16 only, head_dim 64/128,
+                           at most 8 query heads per KV head               */
+    int32_t num_ctas;   /* 0 = one wave of resident CTAs; > 0 forces that
+                           many CTAs (tests use it to force context splits) */
+} pkv_decode_opts;
+
+/*
+ * pkv_append -- slot-mapped write of one step's new K/V.
+ * (release page, Highlights "slot mapping" and Architectural Breakdown 1
+ * "Fragment-Free Growth"; notebook section 5 `append`.)
+ *
+ * For each token t < num_tokens with s = slot_mapping[t] >= 0, and each KV
+ * head h:  k_cache[s/16][h][s%16][:] = k[t][h][:]  and the same for v.
+ * s < 0 skips the token (padding).
+ *
+ *   k, v          device, [num_tokens][num_kv_heads][head_dim] of desc->dtype,
+ *                 contiguous, 16-byte aligned. Read only.
+ *   slot_mapping  device, int64 [num_tokens]. Read only.
+ *   k_cache,
+ *   v_cache       device pools (layout above). Written at the named slots only.
+ *   num_tokens    >= 0; 0 enqueues nothing.
+ * Errors: NULL pointers, bad geometry, misalignment (host-side); with
+ * PKV_FLAG_CHECKED also a slot >= num_blocks*16 (PKV_ERR_RANGE) or the same
+ * slot named twice (PKV_ERR_OVERLAP; checked for num_tokens <= 16384, larger
+ * checked calls return PKV_ERR_UNSUPPORTED). In fast mode a repeated slot
+ * receives one of the tokens, unspecified which.
+ */
+PKV_API pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping,
+                      int64_t num_tokens, void* k_cache, void* v_cache,
+                      const pkv_cache_desc* desc, uint32_t flags, void* stream);
+
+/*
+ * pkv_copy_blocks -- whole-block copy for copy-on-write.
+ * (notebook section 5: before a sequence appends into a shared partial final
+ * block it takes a private replacement; this call moves the data.)
+ *
+ * For each pair p < num_pairs: block pairs[p][1] of both pools becomes a copy
+ * of block pairs[p][0] (all KV heads, all 16 slots, K and V). The copies act
+ * as one step: destinations must be distinct and must not also be sources.
+ *
+ *   src_dst_pairs device, int64 [num_pairs][2] = {src, dst}. Read only.
+ *   num_pairs     >= 0; 0 enqueues nothing (a valid no-op).
+ * Errors: as pkv_append; with PKV_FLAG_CHECKED a block id outside
+ * [0, num_blocks) gives PKV_ERR_RANGE and a repeated destination or a
+ * destination that is also a source gives PKV_ERR_OVERLAP (num_pairs <= 16384).
+ */
+PKV_API pkv_status pkv_copy_blocks(const int64_t* src_dst_pairs, int64_t num_pairs,
+                           void* k_cache, void* v_cache,
+                           const pkv_cache_desc* desc, uint32_t flags, void* stream);
+
+/*
+ * pkv_decode_workspace_size -- bytes of device workspace pkv_decode_attention
+ * needs for these sizes and options on the current device.
+ */
+PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                 int32_t max_blocks_per_seq,
+                                 const pkv_cache_desc* desc,
+                                 const pkv_decode_opts* opts);
+
+/*
+ * pkv_decode_attention -- one decode query per sequence against its paged
+ * context, grouped-query heads.
+ * (notebook project demo, Demo 2 `attention`: softmax of the scaled logits
+ * with the maximum subtracted, times V; notebook section 3: K/V storage scales
+ * with the KV heads, the work with the query heads.)
+ *
+ * For sequence i < batch, query head h < num_q_heads, G = num_q_heads /
+ * num_kv_heads, j = h / G, n = context_lens[i]:
+ *     s_t = scale * dot(q[i][h], K_j(t)),  t < n
+ *     out[i][h] = sum_t softmax(s)_t * V_j(t)
+ * where K_j(t) / V_j(t) is row t % 16 of KV head j in block
+ * block_tables[i][t / 16]. n == 0 gives a zero row. Accumulation is fp32;
+ * out is written once, rounded to nearest-even into desc->dtype.
+ *
+ *   q             device, [batch][num_q_heads][head_dim], desc->dtype.
+ *   block_tables  device, int32 [batch][max_blocks_per_seq]; entries at
+ *                 index >= ceil(n/16) are never read.
+ *   context_lens  device, int32 [batch], 0 <= n <= max_blocks_per_seq*16.
+ *   out           device, [batch][num_q_heads][head_dim], desc->dtype.
+ *   workspace     device, >= pkv_decode_workspace_size(...) bytes, 256-byte
+ *                 aligned; its contents need no initialisation.
+ *   opts          NULL or tuning (above).
+ * Errors: host-side checks as above plus num_q_heads % num_kv_heads != 0
+ * (PKV_ERR_SHAPE) and a short workspace (PKV_ERR_WORKSPACE); with
+ * PKV_FLAG_CHECKED a context length outside [0, max_blocks_per_seq*16] or a
+ * block id outside [0, num_blocks) among the blocks a sequence uses gives
+ * PKV_ERR_RANGE. batch may exceed any internal limit: the call splits it.
+ */
+PKV_API pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t batch,
+                                int32_t num_q_heads, float scale, void* out,
+                                void* workspace, size_t workspace_bytes,
+                                const pkv_cache_desc* desc, uint32_t flags,
+                                const pkv_decode_opts* opts, void* stream);
+
+/*
+ * pkv_device_status -- read (and with clear != 0, reset) the sticky device
+ * status of the current device: an OR of PKV_DEVERR_* bits set by kernels
+ * since the last clear. Waits for `stream`. Returns PKV_OK or PKV_ERR_CUDA.
+ */
+PKV_API pkv_status pkv_device_status(uint32_t* bits_out, int clear, void* stream);
+
+/* Human-readable name of a status code (static string). */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+PKV_API int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,241 @@
+// The extern "C" entry points declared in include/pkv.h: argument
+// validation, the optional checked mode, and dispatch to the kernels.
+//
+// Validation order follows the pages' rule for a rejected input: everything
+// that can be checked on the host is checked before any work is enqueued, and
+// in checked mode the device-resident indices are verified (and the call
+// waits for the verdict) before any output byte is written.
+#include <math.h>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+// Sticky device status ([0], PKV_DEVERR_* bits) and the verdict word of the
+// current checked call ([1]). One copy per device.
+static __device__ unsigned int g_pkv_status[2];
+
+namespace pkv {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    unsigned int* status = nullptr;
+    int sm_count = 0;
+};
+
+DeviceInfo& device_info() {
+    static std::mutex mu;
+    static DeviceInfo info[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo& d = info[dev];
+    if (d.status == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pkv_status) == cudaSuccess) d.status = static_cast<unsigned int*>(p);
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) d.sm_count = n;
+    }
+    return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status check_desc(const pkv_cache_desc* d) {
+    if (d == nullptr) return PKV_ERR_NULL;
+    if (d->block_size != 16 || d->num_blocks < 1 || d->num_kv_heads < 1) return PKV_ERR_SHAPE;
+    if (d->head_dim != 64 && d->head_dim != 128) return PKV_ERR_SHAPE;
+    if (d->dtype != PKV_F32 && d->dtype != PKV_BF16) return PKV_ERR_DTYPE;
+    // Rows of one pool (block, head, slot) are addressed with 32-bit coordinates.
+    if (d->num_blocks * d->num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_SHAPE;
+    return PKV_OK;
+}
+
+// Runs one validation launch in checked mode and waits for its verdict.
+template <typename F>
+pkv_status run_checked(F launch, cudaStream_t s) {
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    unsigned int* verdict = status + 1;
+    if (cudaMemsetAsync(verdict, 0, sizeof(unsigned int), s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (launch(verdict) != cudaSuccess) return PKV_ERR_CUDA;
+    unsigned int host = 0;
+    if (cudaMemcpyAsync(&host, verdict, sizeof(unsigned int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (host & kVerdictRange) return PKV_ERR_RANGE;
+    if (host & kVerdictOverlap) return PKV_ERR_OVERLAP;
+    return PKV_OK;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    const int n = device_info().sm_count;
+    return n > 0 ? n : 1;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_NULL: return "PKV_ERR_NULL";
+        case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE";
+        case PKV_ERR_DTYPE: return "PKV_ERR_DTYPE";
+        case PKV_ERR_ALIGN: return "PKV_ERR_ALIGN";
+        case PKV_ERR_RANGE: return "PKV_ERR_RANGE";
+        case PKV_ERR_OVERLAP: return "PKV_ERR_OVERLAP";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    }
+    return "PKV_ERR_UNKNOWN";
+}
+
+int32_t pkv_version(void) { return 100; }
+
+pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                      void* v_cache, const pkv_cache_desc* desc, uint32_t flags, void* stream) {
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return PKV_ERR_SHAPE;
+    if (k_cache == nullptr || v_cache == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    if (num_tokens == 0) return PKV_OK;
+    if (k == nullptr || v == nullptr || slot_mapping == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)) return PKV_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    if (flags & PKV_FLAG_CHECKED) {
+        if (num_tokens > 16384) return PKV_ERR_UNSUPPORTED;
+        const int64_t num_slots = desc->num_blocks * 16;
+        st = run_checked([&](unsigned int* verdict) { return launch_check_slots(slot_mapping, num_tokens, num_slots, verdict, s); }, s);
+        if (st != PKV_OK) return st;
+    }
+    return launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, *desc, status, s) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks(const int64_t* pairs, int64_t num_pairs, void* k_cache, void* v_cache,
+                           const pkv_cache_desc* desc, uint32_t flags, void* stream) {
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0) return PKV_ERR_SHAPE;
+    if (k_cache == nullptr || v_cache == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    if (num_pairs == 0) return PKV_OK;
+    if (pairs == nullptr) return PKV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(pairs) & 7u) return PKV_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    if (flags & PKV_FLAG_CHECKED) {
+        if (num_pairs > 16384) return PKV_ERR_UNSUPPORTED;
+        st = run_checked([&](unsigned int* verdict) { return launch_check_pairs(pairs, num_pairs, desc->num_blocks, verdict, s); }, s);
+        if (st != PKV_OK) return st;
+    }
+    return launch_copy_blocks(pairs, num_pairs, k_cache, v_cache, *desc, status, s) == cudaSuccess ? PKV_OK
+                                                                                                   : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                 const pkv_cache_desc* desc, const pkv_decode_opts* opts) {
+    if (check_desc(desc) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
+        return 0;
+    DecodePlan plan;
+    if (decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan) != PKV_OK) return 0;
+    return decode_header_bytes() +
+           decode_partial_bytes(plan.num_ctas, num_q_heads / desc->num_kv_heads, desc->head_dim);
+}
+
+pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                                int32_t num_q_heads, float scale, void* out, void* workspace,
+                                size_t workspace_bytes, const pkv_cache_desc* desc, uint32_t flags,
+                                const pkv_decode_opts* opts, void* stream) {
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
+    if (!isfinite(scale)) return PKV_ERR_SHAPE;
+    if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
+    if (batch == 0) return PKV_OK;
+    if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
+        return PKV_ERR_SHAPE;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace) return PKV_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_ALIGN;
+    DecodePlan plan;
+    const int rc = decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan);
+    if (rc != PKV_OK) return static_cast<pkv_status>(rc);
+    const int G = num_q_heads / desc->num_kv_heads;
+    const size_t need = decode_header_bytes() + decode_partial_bytes(plan.num_ctas, G, desc->head_dim);
+    if (workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    if (flags & PKV_FLAG_CHECKED) {
+        st = run_checked([&](unsigned int* verdict) {
+            return launch_check_decode(block_tables, max_blocks_per_seq, context_lens, batch, desc->num_blocks,
+                                       verdict, s);
+        }, s);
+        if (st != PKV_OK) return st;
+    }
+    const int elem = desc->dtype == PKV_BF16 ? 2 : 4;
+    const int64_t row = static_cast<int64_t>(num_q_heads) * desc->head_dim * elem;
+    for (int32_t b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {
+        const int32_t nb = batch - b0 < kMaxBatchPerLaunch ? batch - b0 : kMaxBatchPerLaunch;
+        DecodeArgs a;
+        a.q = static_cast<const char*>(q) + b0 * row;
+        a.k_cache = k_cache;
+        a.v_cache = v_cache;
+        a.tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
+        a.lens = context_lens + b0;
+        a.out = static_cast<char*>(out) + b0 * row;
+        a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + decode_header_bytes());
+        a.status = status;
+        a.num_blocks = desc->num_blocks;
+        a.max_blocks = max_blocks_per_seq;
+        a.batch = nb;
+        a.q_heads = num_q_heads;
+        a.kv_heads = desc->num_kv_heads;
+        a.head_dim = desc->head_dim;
+        a.group = G;
+        a.dtype = desc->dtype;
+        a.num_ctas = plan.num_ctas;
+        a.scale = scale;
+        if (launch_decode(a, plan, s) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_device_status(uint32_t* bits_out, int clear, void* stream) {
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int host = 0;
+    if (cudaMemcpyAsync(&host, status, sizeof(unsigned int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (clear) {
+        if (cudaMemsetAsync(status, 0, sizeof(unsigned int), s) != cudaSuccess) return PKV_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    if (bits_out) *bits_out = host;
+    return PKV_OK;
+}
+
+}  // extern "C"

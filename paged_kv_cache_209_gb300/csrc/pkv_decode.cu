@@ -1,0 +1,883 @@
+// Split-context decode attention over the paged KV cache, and the
+// log-sum-exp merge of split pieces.
+//
+// Work decomposition. One unit of work is one (sequence i, KV head h, block
+// b): 16 tokens of one head, 2 x 16 x head_dim elements of K and V. Units are
+// ordered i-major, then h, then b; the units of one (i, h) form a segment. A
+// launch of C CTAs gives CTA c the contiguous units [c*U/C, (c+1)*U/C), so
+// every CTA reads the same number of blocks (to within one) whatever the mix
+// of context lengths. A segment that lies wholly inside one CTA's range is
+// finished there and its output row written directly; a segment cut by a
+// range boundary leaves one fp32 piece (unnormalised accumulator, running
+// max, running sum) per CTA it touches, and the merge kernel combines those
+// pieces by log-sum-exp weights.
+//
+// All query heads of a KV head (the GQA group, G <= 8) are computed from one
+// read of each K/V byte.
+//
+// Tensor-core kernel (bf16): one producer warp streams the blocks of the
+// CTA's range through an NST-stage shared-memory ring with 2-D TMA loads
+// (128-byte swizzle, so ldmatrix reads are bank-conflict free). Four consumer
+// warps take the units round robin. Per unit a warp computes
+//     S^T[16 tokens][8 heads] = K[16][D] * Q^T[D][8]        (mma m16n8k16)
+// runs the online softmax in fp32 on the accumulator fragments, transposes
+// P^T into the B-operand layout with movmatrix, and accumulates
+//     O^T[D][8] += V^T[D][16] * P^T[16][8]                   (mma m16n8k16)
+// with P split as hi + lo bf16 (P itself is fp32; the split keeps ~16
+// significant bits, enough for the fp32-accumulation tolerance). At the end
+// of a segment piece the four warps' (m, l, O) are combined through shared
+// memory.
+//
+// CUDA-core kernel (fp32 or bf16, any G <= 16): four warps, direct loads,
+// lanes split the head dimension; used for fp32 caches and as a second,
+// independent implementation in the tests.
+#include <math.h>
+#include <mutex>
+#include <type_traits>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// ------------------------------------------------------------------ schedule
+// s_pre[i] = sum_{i' <= i} ceil(len_i' / 16) over this launch's sequences,
+// s_len[i] = len_i clamped to [0, max_blocks * 16].
+__device__ void build_prefix(int32_t* s_pre, int32_t* s_len, const int32_t* __restrict__ lens, int batch,
+                             int max_blocks, unsigned int* status) {
+    const int cap = max_blocks * 16;
+    for (int i = threadIdx.x; i < batch; i += blockDim.x) {
+        int n = lens[i];
+        if (n < 0 || n > cap) {
+            if (blockIdx.x == 0) atomicOr(status, PKV_DEVERR_RANGE);
+            n = n < 0 ? 0 : cap;
+        }
+        s_len[i] = n;
+        s_pre[i] = (n + 15) >> 4;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry = 0;
+        for (int base = 0; base < batch; base += 32) {
+            int x = base + lane < batch ? s_pre[base + lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (base + lane < batch) s_pre[base + lane] = x + carry;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+    }
+    __syncthreads();
+}
+
+struct Piece {
+    int seq, head;
+    int blk_from, blk_to;  // blocks [from, to) of the sequence
+    bool complete;         // the piece is the whole segment
+    bool first;            // the piece opens this CTA's range
+};
+
+// Walks the segment pieces of the unit range [start, end).
+struct Walker {
+    const int32_t* pre;
+    int kv_heads;
+    long long start, u, end;
+    int i, h, nb;
+    long long seg_base;
+
+    __device__ void init(const int32_t* pre_, int batch, int kvh, long long a, long long b) {
+        pre = pre_;
+        kv_heads = kvh;
+        start = u = a;
+        end = b;
+        if (u >= end) return;
+        int lo = 0, hi = batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (static_cast<long long>(pre[mid]) * kvh > u)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        i = lo;
+        const int excl = i ? pre[i - 1] : 0;
+        nb = pre[i] - excl;
+        seg_base = static_cast<long long>(kvh) * excl;
+        h = static_cast<int>((u - seg_base) / nb);
+    }
+
+    __device__ bool next(Piece& p) {
+        if (u >= end) return false;
+        const long long s0 = seg_base + static_cast<long long>(h) * nb;
+        const long long s1 = s0 + nb;
+        const long long pe = s1 < end ? s1 : end;
+        p.seq = i;
+        p.head = h;
+        p.blk_from = static_cast<int>(u - s0);
+        p.blk_to = static_cast<int>(pe - s0);
+        p.complete = (u == s0) && (pe == s1);
+        p.first = (u == start);
+        u = pe;
+        if (u < end) {
+            if (++h == kv_heads) {
+                h = 0;
+                do {
+                    ++i;
+                } while (pre[i] == pre[i - 1]);
+                const int excl = pre[i - 1];
+                nb = pre[i] - excl;
+                seg_base = static_cast<long long>(kv_heads) * excl;
+            }
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ long long range_start(long long c, long long U, long long C) { return c * U / C; }
+
+// The CTA whose range holds unit u: max c with range_start(c) <= u.
+__device__ __forceinline__ long long cta_of(long long u, long long U, long long C) { return ((u + 1) * C - 1) / U; }
+
+__device__ __forceinline__ float* piece_slot(float* partials, long long cta, int slot, int G, int D) {
+    return partials + (cta * 2 + slot) * static_cast<long long>(G) * (D + 2);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_out(T* p, float x);
+template <>
+__device__ __forceinline__ void store_out<float>(float* p, float x) {
+    *p = x;
+}
+template <>
+__device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+    *p = __float2bfloat16_rn(x);
+}
+
+template <typename T>
+__device__ __forceinline__ float load_f32(const T* p);
+template <>
+__device__ __forceinline__ float load_f32<float>(const float* p) {
+    return __ldg(p);
+}
+template <>
+__device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+}
+
+// Combine the per-warp states of one segment piece (already in shared
+// memory) and write either the final output row or this CTA's piece.
+// Executed by `nthreads` threads with thread index `tid`.
+template <typename T, int D>
+__device__ __forceinline__ void combine_warps(const float* sm_o, const float* sm_m, const float* sm_l, int nwarps,
+                                              int G, const Piece& pc, const DecodeArgs& a, long long cta, int tid,
+                                              int nthreads) {
+    for (int e = tid; e < G * D; e += nthreads) {
+        const int g = e / D;
+        const int d = e - g * D;
+        float M = neg_inf();
+        for (int w = 0; w < nwarps; ++w) M = fmaxf(M, sm_m[w * 8 + g]);
+        const float base = (M == neg_inf()) ? 0.f : M;
+        float o = 0.f, L = 0.f;
+        for (int w = 0; w < nwarps; ++w) {
+            const float mw = sm_m[w * 8 + g];
+            const float wt = (mw == neg_inf()) ? 0.f : ex2(mw - base);
+            o += wt * sm_o[(w * 8 + g) * D + d];
+            L += wt * sm_l[w * 8 + g];
+        }
+        if (pc.complete) {
+            T* dst = static_cast<T*>(a.out) +
+                     (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G + g) * D + d;
+            store_out<T>(dst, L > 0.f ? o / L : 0.f);
+        } else {
+            float* slot = piece_slot(a.partials, cta, pc.first ? 0 : 1, G, D) + g * (D + 2);
+            slot[d] = o;
+            if (d == 0) {
+                slot[D] = M;
+                slot[D + 1] = L;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ tensor-core kernel
+template <int D>
+struct Tc {
+    static constexpr int kStages = 8;
+    static constexpr int kConsumers = 4;
+    static constexpr int kThreads = (kConsumers + 1) * 32;
+    static constexpr int kHalves = D / 64;                  // 64-column TMA boxes per row
+    static constexpr int kPoolBytes = 16 * D * 2;           // one block, one head, one pool
+    static constexpr int kStageBytes = 2 * kPoolBytes;      // K then V
+    static constexpr int kScratchFloats = 2 * kConsumers * 8 * D;  // double-buffered O
+    // shared memory layout (offsets from a 1024-byte aligned base)
+    static constexpr int kOffBars = kStages * kStageBytes;
+    static constexpr int kOffFlags = kOffBars + (2 * kStages + 1) * 8;
+    static constexpr int kOffScratch = ((kOffFlags + kStages * 4 + 4 + 15) / 16) * 16;
+    static constexpr int kOffML = kOffScratch + kScratchFloats * 4;
+    static constexpr int kOffPre = kOffML + 2 * 2 * kConsumers * 8 * 4;
+    static size_t smem_bytes(int batch) { return 1024 + kOffPre + 2 * static_cast<size_t>(batch) * 4; }
+};
+
+template <int D>
+__global__ void __launch_bounds__(Tc<D>::kThreads, 2)
+    decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV) {
+    using C = Tc<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* merge_bar = empty + C::kStages;
+    int* stage_ok = reinterpret_cast<int*>(smem + C::kOffFlags);
+    volatile int* abort_flag = stage_ok + C::kStages;
+    float* sm_o = reinterpret_cast<float*>(smem + C::kOffScratch);
+    float* sm_m = reinterpret_cast<float*>(smem + C::kOffML);          // [2][4][8]
+    float* sm_l = sm_m + 2 * C::kConsumers * 8;                          // [2][4][8]
+    int32_t* s_pre = reinterpret_cast<int32_t*>(smem + C::kOffPre);
+    int32_t* s_len = s_pre + a.batch;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(merge_bar, C::kConsumers);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    build_prefix(s_pre, s_len, a.lens, a.batch, a.max_blocks, a.status);  // contains __syncthreads
+
+    const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
+    const long long cta = blockIdx.x;
+    const long long ua = range_start(cta, U, a.num_ctas);
+    const long long ub = range_start(cta + 1, U, a.num_ctas);
+    const int G = a.group;
+
+    if (warp == C::kConsumers) {
+        // ------------------------------------------------ producer warp
+        Walker wk;
+        wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
+        long long k = 0;
+        Piece pc;
+        bool ok = true;
+        while (ok && wk.next(pc)) {
+            const int32_t* trow = a.tables + static_cast<long long>(pc.seq) * a.max_blocks + pc.blk_from;
+            const int cnt_piece = pc.blk_to - pc.blk_from;
+            int cur = lane < cnt_piece ? __ldg(trow + lane) : 0;
+            for (int b0 = 0; ok && b0 < cnt_piece; b0 += 32) {
+                const int nidx = b0 + 32 + lane;
+                const int nxt = nidx < cnt_piece ? __ldg(trow + nidx) : 0;
+                const int cnt = min(32, cnt_piece - b0);
+                for (int e = 0; e < cnt; ++e, ++k) {
+                    const int bid = __shfl_sync(0xffffffffu, cur, e);
+                    int good = 1;
+                    if (lane == 0) {
+                        const int s = static_cast<int>(k % C::kStages);
+                        const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1) ^ 1u;
+                        if (!mbar_wait(&empty[s], par, a.status, abort_flag)) {
+                            good = 0;
+                        } else if (bid >= 0 && bid < a.num_blocks) {
+                            stage_ok[s] = 1;
+                            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                            uint8_t* st = smem + s * C::kStageBytes;
+                            const int y = (bid * a.kv_heads + pc.head) * 16;
+#pragma unroll
+                            for (int hf = 0; hf < C::kHalves; ++hf) tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s]);
+#pragma unroll
+                            for (int hf = 0; hf < C::kHalves; ++hf)
+                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s]);
+                        } else {
+                            stage_ok[s] = 0;
+                            atomicOr(a.status, PKV_DEVERR_RANGE);
+                            mbar_arrive(&full[s]);
+                        }
+                    }
+                    good = __shfl_sync(0xffffffffu, good, 0);
+                    if (!good) {
+                        ok = false;
+                        break;
+                    }
+                }
+                cur = nxt;
+            }
+        }
+        // After an abort, wait (bounded) for the copies still in flight
+        // into the ring before the CTA may exit.
+        if (!ok && lane == 0) {
+            const long long first = k > C::kStages ? k - C::kStages : 0;
+            for (long long u = first; u < k; ++u)
+                mbar_wait(&full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    const int gid = lane >> 2;  // fragment row group
+    const int tig = lane & 3;   // thread in group
+    const float scale_log2 = a.scale * kLog2e;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+
+    // ldmatrix lane addressing (see the header comment): the 8x8 matrix a
+    // lane addresses is q8 = lane / 8, its row r8 = lane % 8.
+    const int q8 = lane >> 3, r8 = lane & 7;
+    const int k_row = r8 + 8 * (q8 & 1);      // K: token row of this lane's address
+    const int k_chunk = q8 >> 1;              // K: +0 / +1 16-byte chunk within a k-step
+    const int v_row = r8 + 8 * (q8 >> 1);     // V: token row
+    const int v_chunk = q8 & 1;               // V: +0 / +1 chunk within an m-tile
+
+    Walker wk;
+    wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
+    long long k = 0;
+    int piece_idx = 0;
+    Piece pc;
+    while (wk.next(pc)) {
+        // Q^T fragments: B operand of S^T = K Q^T; column n = query head gid.
+        uint32_t qf[D / 16][2];
+        {
+            const bool live = gid < G;
+            const __nv_bfloat16* qrow =
+                q + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G + (live ? gid : 0)) * D;
+            const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                qf[j][0] = live ? __ldg(q32 + (16 * j + 2 * tig) / 2) : 0u;
+                qf[j][1] = live ? __ldg(q32 + (16 * j + 2 * tig + 8) / 2) : 0u;
+            }
+        }
+        float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+        float o[D / 16][4];
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        const int n_ctx = s_len[pc.seq];
+
+        for (int blk = pc.blk_from; blk < pc.blk_to; ++blk, ++k) {
+            if (static_cast<int>(k & (C::kConsumers - 1)) != warp) continue;
+            const int s = static_cast<int>(k % C::kStages);
+            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag)) return;
+            const int valid = min(16, n_ctx - blk * 16);
+            if (stage_ok[s]) {
+                const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
+                const uint32_t vbase = kbase + C::kPoolBytes;
+                // ---- S^T = K Q^T
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    const int gc = 2 * j + k_chunk;
+                    const uint32_t addr = kbase + (gc >> 3) * 2048 + k_row * 128 + (((gc & 7) ^ r8) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(addr, a0, a1, a2, a3);
+                    mma_bf16_16816(sacc, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+                }
+                // sacc: [0] (t=gid, g=2tig) [1] (t=gid, g=2tig+1) [2] (t=gid+8, g=2tig) [3] (t=gid+8, g=2tig+1)
+                float x0 = gid < valid ? sacc[0] * scale_log2 : neg_inf();
+                float x1 = gid < valid ? sacc[1] * scale_log2 : neg_inf();
+                float x2 = gid + 8 < valid ? sacc[2] * scale_log2 : neg_inf();
+                float x3 = gid + 8 < valid ? sacc[3] * scale_log2 : neg_inf();
+                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float b0 = mn0 == neg_inf() ? 0.f : mn0;
+                const float b1 = mn1 == neg_inf() ? 0.f : mn1;
+                const float al0 = ex2(m0 - b0), al1 = ex2(m1 - b1);
+                const float p0 = ex2(x0 - b0), p1 = ex2(x1 - b1), p2 = ex2(x2 - b0), p3 = ex2(x3 - b1);
+                l0 = l0 * al0 + (p0 + p2);
+                l1 = l1 * al1 + (p1 + p3);
+                if (__any_sync(0xffffffffu, (mn0 != m0) || (mn1 != m1))) {
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        o[i][0] *= al0;
+                        o[i][1] *= al1;
+                        o[i][2] *= al0;
+                        o[i][3] *= al1;
+                    }
+                }
+                m0 = mn0;
+                m1 = mn1;
+                // ---- P^T as bf16 hi + lo, moved into the B-operand layout
+                const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+                const uint32_t l01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
+                const uint32_t l23 = pack_bf16x2(p2 - bf16lo_to_f32(h23), p3 - bf16hi_to_f32(h23));
+                const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+                const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+                // ---- O^T += V^T P^T; rows past the context are zeroed (they may hold anything)
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (valid < 16) {
+                    mlo = (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
+                    mhi = (2 * tig + 8 < valid ? 0x0000ffffu : 0u) | (2 * tig + 9 < valid ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    const int gc = 2 * i + v_chunk;
+                    const uint32_t addr = vbase + (gc >> 3) * 2048 + v_row * 128 + (((gc & 7) ^ r8) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+                    a0 &= mlo;
+                    a1 &= mlo;
+                    a2 &= mhi;
+                    a3 &= mhi;
+                    mma_bf16_16816(o[i], a0, a1, a2, a3, bh0, bh1);
+                    mma_bf16_16816(o[i], a0, a1, a2, a3, bl0, bl1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        // ---- combine the four warps' states for this piece
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        const int buf = piece_idx & 1;
+        float* bo = sm_o + buf * (C::kConsumers * 8 * D);
+        float* bm = sm_m + buf * (C::kConsumers * 8);
+        float* bl = sm_l + buf * (C::kConsumers * 8);
+        const int g0 = 2 * tig, g1 = 2 * tig + 1;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+            const int d = 16 * i + gid;
+            if (g0 < G) {
+                bo[(warp * 8 + g0) * D + d] = o[i][0];
+                bo[(warp * 8 + g0) * D + d + 8] = o[i][2];
+            }
+            if (g1 < G) {
+                bo[(warp * 8 + g1) * D + d] = o[i][1];
+                bo[(warp * 8 + g1) * D + d + 8] = o[i][3];
+            }
+        }
+        if (gid == 0) {
+            bm[warp * 8 + g0] = m0;
+            bm[warp * 8 + g1] = m1;
+            bl[warp * 8 + g0] = l0;
+            bl[warp * 8 + g1] = l1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_bar);
+        if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
+        combine_warps<__nv_bfloat16, D>(bo, bm, bl, C::kConsumers, G, pc, a, cta, threadIdx.x,
+                                        C::kConsumers * 32);
+        ++piece_idx;
+    }
+}
+
+// ------------------------------------------------------------------ CUDA-core kernel
+template <typename T, int D, int GMAX>
+struct Cc {
+    static constexpr int kWarps = 4;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kPer = D / 32;  // head-dim elements per lane
+};
+
+template <typename T, int D, int GMAX>
+__global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
+    using C = Cc<T, D, GMAX>;
+    extern __shared__ float smem_f[];
+    float* sm_o = smem_f;                                        // [warps][GMAX][D]
+    float* sm_m = sm_o + C::kWarps * GMAX * D;                   // [warps][GMAX]
+    float* sm_l = sm_m + C::kWarps * GMAX;
+    int32_t* s_pre = reinterpret_cast<int32_t*>(sm_l + C::kWarps * GMAX);
+    int32_t* s_len = s_pre + a.batch;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    build_prefix(s_pre, s_len, a.lens, a.batch, a.max_blocks, a.status);
+
+    const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
+    const long long cta = blockIdx.x;
+    const long long ua = range_start(cta, U, a.num_ctas);
+    const long long ub = range_start(cta + 1, U, a.num_ctas);
+    const int G = a.group;
+    const float scale_log2 = a.scale * kLog2e;
+    const T* q = static_cast<const T*>(a.q);
+    const T* kc = static_cast<const T*>(a.k_cache);
+    const T* vc = static_cast<const T*>(a.v_cache);
+
+    Walker wk;
+    wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
+    long long k = 0;
+    Piece pc;
+    while (wk.next(pc)) {
+        float qr[GMAX][C::kPer];
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g)
+#pragma unroll
+            for (int e = 0; e < C::kPer; ++e)
+                qr[g][e] = g < G ? load_f32<T>(q + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G + g) * D +
+                                               lane + 32 * e)
+                                 : 0.f;
+        float m[GMAX], l[GMAX], o[GMAX][C::kPer];
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+            m[g] = neg_inf();
+            l[g] = 0.f;
+#pragma unroll
+            for (int e = 0; e < C::kPer; ++e) o[g][e] = 0.f;
+        }
+        const int n_ctx = s_len[pc.seq];
+        const int32_t* trow = a.tables + static_cast<long long>(pc.seq) * a.max_blocks;
+        for (int blk = pc.blk_from; blk < pc.blk_to; ++blk, ++k) {
+            if (static_cast<int>(k & (C::kWarps - 1)) != warp) continue;
+            const int bid = __ldg(trow + blk);
+            if (bid < 0 || bid >= a.num_blocks) {
+                if (lane == 0) atomicOr(a.status, PKV_DEVERR_RANGE);
+                continue;
+            }
+            const int valid = min(16, n_ctx - blk * 16);
+            const long long row0 = (static_cast<long long>(bid) * a.kv_heads + pc.head) * 16;
+            for (int t = 0; t < valid; ++t) {
+                const T* krow = kc + (row0 + t) * D;
+                const T* vrow = vc + (row0 + t) * D;
+                float kv[C::kPer], vv[C::kPer];
+#pragma unroll
+                for (int e = 0; e < C::kPer; ++e) {
+                    kv[e] = load_f32<T>(krow + lane + 32 * e);
+                    vv[e] = load_f32<T>(vrow + lane + 32 * e);
+                }
+#pragma unroll
+                for (int g = 0; g < GMAX; ++g) {
+                    if (g >= G) break;
+                    float dot = 0.f;
+#pragma unroll
+                    for (int e = 0; e < C::kPer; ++e) dot = fmaf(qr[g][e], kv[e], dot);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+                    const float x = dot * scale_log2;
+                    const float mn = fmaxf(m[g], x);
+                    const float al = ex2(m[g] - mn);
+                    const float p = ex2(x - mn);
+                    l[g] = l[g] * al + p;
+#pragma unroll
+                    for (int e = 0; e < C::kPer; ++e) o[g][e] = fmaf(o[g][e], al, p * vv[e]);
+                    m[g] = mn;
+                }
+            }
+        }
+        // combine the warps, 8 heads at a time
+        __syncthreads();
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+            if (g >= G) break;
+#pragma unroll
+            for (int e = 0; e < C::kPer; ++e) sm_o[(warp * GMAX + g) * D + lane + 32 * e] = o[g][e];
+            if (lane == 0) {
+                sm_m[warp * GMAX + g] = m[g];
+                sm_l[warp * GMAX + g] = l[g];
+            }
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
+            const int g = e / D;
+            const int d = e - g * D;
+            float M = neg_inf();
+            for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, sm_m[w * GMAX + g]);
+            const float base = (M == neg_inf()) ? 0.f : M;
+            float ov = 0.f, L = 0.f;
+            for (int w = 0; w < C::kWarps; ++w) {
+                const float mw = sm_m[w * GMAX + g];
+                const float wt = (mw == neg_inf()) ? 0.f : ex2(mw - base);
+                ov += wt * sm_o[(w * GMAX + g) * D + d];
+                L += wt * sm_l[w * GMAX + g];
+            }
+            if (pc.complete) {
+                T* dst = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G + g) * D + d;
+                store_out<T>(dst, L > 0.f ? ov / L : 0.f);
+            } else {
+                float* slot = piece_slot(a.partials, cta, pc.first ? 0 : 1, G, D) + g * (D + 2);
+                slot[d] = ov;
+                if (d == 0) {
+                    slot[D] = M;
+                    slot[D + 1] = L;
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ merge kernel
+// One CTA per sequence. Writes zeros for an empty sequence and combines the
+// pieces of every segment that the split kernel cut.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
+    __shared__ long long s_sum[2][8];
+    const int i = blockIdx.x;
+    const int cap = a.max_blocks * 16;
+    long long before = 0, total = 0;
+    for (int j = threadIdx.x; j < a.batch; j += blockDim.x) {
+        int n = a.lens[j];
+        n = n < 0 ? 0 : (n > cap ? cap : n);
+        const long long nb = (n + 15) >> 4;
+        total += nb;
+        if (j < i) before += nb;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, off);
+        total += __shfl_xor_sync(0xffffffffu, total, off);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_sum[0][threadIdx.x >> 5] = before;
+        s_sum[1][threadIdx.x >> 5] = total;
+    }
+    __syncthreads();
+    before = total = 0;
+    for (int w = 0; w < 8; ++w) {
+        before += s_sum[0][w];
+        total += s_sum[1][w];
+    }
+    int n = a.lens[i];
+    n = n < 0 ? 0 : (n > cap ? cap : n);
+    const long long nb = (n + 15) >> 4;
+    const int G = a.group;
+    T* out = static_cast<T*>(a.out) + static_cast<long long>(i) * a.q_heads * D;
+    if (nb == 0) {
+        for (int e = threadIdx.x; e < a.q_heads * D; e += blockDim.x) store_out<T>(out + e, 0.f);
+        return;
+    }
+    const long long U = static_cast<long long>(a.kv_heads) * total;
+    const long long C = a.num_ctas;
+    for (int h = 0; h < a.kv_heads; ++h) {
+        const long long S0 = a.kv_heads * before + h * nb;
+        const long long S1 = S0 + nb;
+        const long long c0 = cta_of(S0, U, C), c1 = cta_of(S1 - 1, U, C);
+        if (c0 == c1) continue;
+        const int slot0 = (S0 == range_start(c0, U, C)) ? 0 : 1;
+        for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+            const int g = e / D;
+            const int d = e - g * D;
+            float M = neg_inf();
+            for (long long c = c0; c <= c1; ++c) {
+                if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
+                const float* p = piece_slot(a.partials, c, c == c0 ? slot0 : 0, G, D) + g * (D + 2);
+                M = fmaxf(M, p[D]);
+            }
+            const float base = (M == neg_inf()) ? 0.f : M;
+            float ov = 0.f, L = 0.f;
+            for (long long c = c0; c <= c1; ++c) {
+                if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
+                const float* p = piece_slot(a.partials, c, c == c0 ? slot0 : 0, G, D) + g * (D + 2);
+                const float wt = (p[D] == neg_inf()) ? 0.f : ex2(p[D] - base);
+                ov += wt * p[d];
+                L += wt * p[D + 1];
+            }
+            store_out<T>(out + (h * G + g) * D + d, L > 0.f ? ov / L : 0.f);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D view of a pool: rows of head_dim bf16 (one token of one head), boxes of
+// 16 rows x 64 columns with the 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K>
+int occupancy(K kernel, int threads, size_t smem) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) n = 0;
+    return n;
+}
+
+struct OccKey {
+    int dev, kernel, variant;
+    size_t smem;
+};
+
+int cached_occupancy(int kernel_id, int variant, size_t smem, int threads, const void* fnptr,
+                     int (*query)(const void*, int, size_t)) {
+    static std::mutex mu;
+    static OccKey keys[64];
+    static int vals[64];
+    static int used = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i].dev == dev && keys[i].kernel == kernel_id && keys[i].variant == variant && keys[i].smem == smem)
+            return vals[i];
+    const int n = query(fnptr, threads, smem);
+    if (used < 64) {
+        keys[used] = OccKey{dev, kernel_id, variant, smem};
+        vals[used] = n;
+        ++used;
+    }
+    return n;
+}
+
+template <int D>
+int tc_query(const void*, int threads, size_t smem) {
+    return occupancy(decode_tc_kernel<D>, threads, smem);
+}
+template <typename T, int D, int GMAX>
+int cc_query(const void*, int threads, size_t smem) {
+    return occupancy(decode_cc_kernel<T, D, GMAX>, threads, smem);
+}
+
+template <typename T, int D, int GMAX>
+size_t cc_smem(int batch) {
+    return static_cast<size_t>(4) * GMAX * D * 4 + 2 * 4 * GMAX * 4 + 2 * static_cast<size_t>(batch) * 4;
+}
+
+int variant_of(int dtype, int D, int gmax) { return (dtype == PKV_BF16 ? 4 : 0) + (D == 128 ? 2 : 0) + (gmax == 16 ? 1 : 0); }
+
+template <typename T, int D, int GMAX>
+cudaError_t run_cc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(decode_cc_kernel<T, D, GMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    decode_cc_kernel<T, D, GMAX><<<grid, 128, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t run_tc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
+    CUtensorMap tmK, tmV;
+    const int64_t rows = a.num_blocks * a.kv_heads * 16;
+    if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
+        return cudaErrorInvalidValue;
+    cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    decode_tc_kernel<D><<<grid, Tc<D>::kThreads, smem, s>>>(a, tmK, tmV);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t run_merge(const DecodeArgs& a, cudaStream_t s) {
+    merge_kernel<T, D><<<a.batch, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_header_bytes() { return 256; }
+
+size_t decode_partial_bytes(int num_ctas, int group, int head_dim) {
+    return static_cast<size_t>(num_ctas) * 2 * group * (head_dim + 2) * sizeof(float);
+}
+
+int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t max_blocks,
+                const pkv_decode_opts* opts, DecodePlan* plan) {
+    (void)max_blocks;
+    const int G = q_heads / d.num_kv_heads;
+    const int want = opts ? opts->kernel : 0;
+    const bool tc_ok = d.dtype == PKV_BF16 && G <= 8 && (d.head_dim == 64 || d.head_dim == 128);
+    int kernel = want;
+    if (kernel == 0) kernel = tc_ok ? 2 : 1;
+    if (kernel == 2 && !tc_ok) return PKV_ERR_UNSUPPORTED;
+    if (kernel == 1 && G > 16) return PKV_ERR_UNSUPPORTED;
+    if (kernel != 1 && kernel != 2) return PKV_ERR_UNSUPPORTED;
+    const int chunk = batch < kMaxBatchPerLaunch ? (batch < 1 ? 1 : batch) : kMaxBatchPerLaunch;
+    int per_sm = 0;
+    size_t smem = 0;
+    if (kernel == 2) {
+        if (d.head_dim == 128) {
+            smem = Tc<128>::smem_bytes(chunk);
+            per_sm = cached_occupancy(2, 128, smem, Tc<128>::kThreads, nullptr, tc_query<128>);
+        } else {
+            smem = Tc<64>::smem_bytes(chunk);
+            per_sm = cached_occupancy(2, 64, smem, Tc<64>::kThreads, nullptr, tc_query<64>);
+        }
+    } else {
+        const int gmax = G <= 8 ? 8 : 16;
+        const int v = variant_of(d.dtype, d.head_dim, gmax);
+#define PKV_CC_CASE(T, DD, GM)                                                      \
+    if (v == variant_of(std::is_same<T, float>::value ? PKV_F32 : PKV_BF16, DD, GM)) { \
+        smem = cc_smem<T, DD, GM>(chunk);                                           \
+        per_sm = cached_occupancy(1, v, smem, 128, nullptr, cc_query<T, DD, GM>);   \
+    }
+        PKV_CC_CASE(float, 64, 8)
+        PKV_CC_CASE(float, 64, 16)
+        PKV_CC_CASE(float, 128, 8)
+        PKV_CC_CASE(float, 128, 16)
+        PKV_CC_CASE(__nv_bfloat16, 64, 8)
+        PKV_CC_CASE(__nv_bfloat16, 64, 16)
+        PKV_CC_CASE(__nv_bfloat16, 128, 8)
+        PKV_CC_CASE(__nv_bfloat16, 128, 16)
+#undef PKV_CC_CASE
+    }
+    if (per_sm < 1) per_sm = 1;
+    plan->kernel = kernel;
+    plan->smem = smem;
+    plan->num_ctas = (opts && opts->num_ctas > 0) ? opts->num_ctas : device_sm_count() * per_sm;
+    return PKV_OK;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
+    cudaError_t err = cudaSuccess;
+    const int D = a.head_dim;
+    if (plan.kernel == 2) {
+        err = D == 128 ? run_tc<128>(a, plan.num_ctas, plan.smem, s) : run_tc<64>(a, plan.num_ctas, plan.smem, s);
+    } else {
+        const bool g16 = a.group > 8;
+        if (a.dtype == PKV_F32) {
+            if (D == 128)
+                err = g16 ? run_cc<float, 128, 16>(a, plan.num_ctas, plan.smem, s)
+                          : run_cc<float, 128, 8>(a, plan.num_ctas, plan.smem, s);
+            else
+                err = g16 ? run_cc<float, 64, 16>(a, plan.num_ctas, plan.smem, s)
+                          : run_cc<float, 64, 8>(a, plan.num_ctas, plan.smem, s);
+        } else {
+            if (D == 128)
+                err = g16 ? run_cc<__nv_bfloat16, 128, 16>(a, plan.num_ctas, plan.smem, s)
+                          : run_cc<__nv_bfloat16, 128, 8>(a, plan.num_ctas, plan.smem, s);
+            else
+                err = g16 ? run_cc<__nv_bfloat16, 64, 16>(a, plan.num_ctas, plan.smem, s)
+                          : run_cc<__nv_bfloat16, 64, 8>(a, plan.num_ctas, plan.smem, s);
+        }
+    }
+    if (err != cudaSuccess) return err;
+    if (a.dtype == PKV_F32)
+        return D == 128 ? run_merge<float, 128>(a, s) : run_merge<float, 64>(a, s);
+    return D == 128 ? run_merge<__nv_bfloat16, 128>(a, s) : run_merge<__nv_bfloat16, 64>(a, s);
+}
+
+}  // namespace pkv

@@ -1,0 +1,205 @@
+"""Thin ctypes binding of libpkv.so (include/pkv.h), same function names.
+
+Only argument marshalling happens here: tensors become device pointers, the
+cache geometry becomes a ``pkv_cache_desc``, the current torch stream is
+passed through, and a non-OK status raises ``PkvError``. Every step of the
+decode path runs in the library's CUDA kernels. There is no fallback: if
+``libpkv.so`` is missing or a tensor is not on a CUDA device, the call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_F32, PKV_BF16 = 0, 1
+PKV_FLAG_CHECKED = 1
+PKV_DEVERR_TIMEOUT, PKV_DEVERR_RANGE = 1, 2
+STATUS_NAMES = ["PKV_OK", "PKV_ERR_NULL", "PKV_ERR_SHAPE", "PKV_ERR_DTYPE", "PKV_ERR_ALIGN", "PKV_ERR_RANGE",
+                "PKV_ERR_OVERLAP", "PKV_ERR_WORKSPACE", "PKV_ERR_TIMEOUT", "PKV_ERR_CUDA", "PKV_ERR_UNSUPPORTED"]
+
+
+class PkvError(RuntimeError):
+    """A libpkv call returned a status other than PKV_OK."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        self.name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else f"status {status}"
+        super().__init__(f"{fn}: {self.name}")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class DecodeOpts(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32)]
+
+
+_lib = None
+
+EXPORTS = ("pkv_append", "pkv_copy_blocks", "pkv_decode_workspace_size", "pkv_decode_attention",
+           "pkv_device_status", "pkv_status_string", "pkv_version")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpkv.so once and declare the signatures of include/pkv.h."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with paged_kv_cache_209_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+    desc_p, opts_p = ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeOpts)
+    lib.pkv_append.argtypes = [vp, vp, vp, i64, vp, vp, desc_p, u32, vp]
+    lib.pkv_append.restype = ctypes.c_int
+    lib.pkv_copy_blocks.argtypes = [vp, i64, vp, vp, desc_p, u32, vp]
+    lib.pkv_copy_blocks.restype = ctypes.c_int
+    lib.pkv_decode_workspace_size.argtypes = [i32, i32, i32, desc_p, opts_p]
+    lib.pkv_decode_workspace_size.restype = ctypes.c_size_t
+    lib.pkv_decode_attention.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp,
+                                         ctypes.c_size_t, desc_p, u32, opts_p, vp]
+    lib.pkv_decode_attention.restype = ctypes.c_int
+    lib.pkv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, vp]
+    lib.pkv_device_status.restype = ctypes.c_int
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_version.argtypes = []
+    lib.pkv_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise PkvError(fn, status)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libpkv takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libpkv takes contiguous tensors only")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return PKV_F32
+    if dt == torch.bfloat16:
+        return PKV_BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    """Geometry of a pool tensor shaped [num_blocks][kv_heads][16][head_dim]."""
+    if k_cache.dim() != 4:
+        raise ValueError("a pool is [num_blocks][num_kv_heads][16][head_dim]")
+    nb, hkv, bs, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d, _dtype_code(k_cache.dtype))
+
+
+def _same_pools(k_cache, v_cache):
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("K and V pools must have one shape and dtype")
+
+
+def pkv_append(k, v, slot_mapping, k_cache, v_cache, flags: int = 0, stream=None) -> None:
+    """Write k[t], v[t] ([T][kv_heads][head_dim]) into slot slot_mapping[t] of the pools."""
+    lib = load_library()
+    _same_pools(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    T = int(slot_mapping.numel())
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping is int64")
+    if T:
+        want = (T, desc.num_kv_heads, desc.head_dim)
+        if tuple(k.shape) != want or tuple(v.shape) != want or k.dtype != k_cache.dtype or v.dtype != k_cache.dtype:
+            raise ValueError(f"k and v must be {want} of the pool dtype")
+    _check("pkv_append", lib.pkv_append(_ptr(k) if T else None, _ptr(v) if T else None,
+                                        _ptr(slot_mapping) if T else None, T, _ptr(k_cache), _ptr(v_cache),
+                                        ctypes.byref(desc), flags, _stream(stream)))
+
+
+def pkv_copy_blocks(src_dst_pairs, k_cache, v_cache, flags: int = 0, stream=None) -> None:
+    """Copy block src onto block dst of both pools for every int64 (src, dst) row."""
+    lib = load_library()
+    _same_pools(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    n = int(src_dst_pairs.numel() // 2) if src_dst_pairs is not None else 0
+    if n and (src_dst_pairs.dtype != torch.int64 or src_dst_pairs.shape[-1] != 2):
+        raise ValueError("src_dst_pairs is int64 [n][2]")
+    _check("pkv_copy_blocks", lib.pkv_copy_blocks(_ptr(src_dst_pairs) if n else None, n, _ptr(k_cache),
+                                                  _ptr(v_cache), ctypes.byref(desc), flags, _stream(stream)))
+
+
+def _opts(kernel: int, num_ctas: int):
+    if kernel == 0 and num_ctas == 0:
+        return None
+    return ctypes.byref(DecodeOpts(kernel, num_ctas))
+
+
+def pkv_decode_workspace_size(batch: int, num_q_heads: int, max_blocks_per_seq: int, k_cache,
+                              kernel: int = 0, num_ctas: int = 0) -> int:
+    lib = load_library()
+    desc = cache_desc(k_cache)
+    return int(lib.pkv_decode_workspace_size(batch, num_q_heads, max_blocks_per_seq, ctypes.byref(desc),
+                                             _opts(kernel, num_ctas)))
+
+
+def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=None,
+                         workspace=None, flags: int = 0, kernel: int = 0, num_ctas: int = 0, stream=None):
+    """Decode attention; returns ``out`` ([batch][q_heads][head_dim], q's dtype)."""
+    lib = load_library()
+    _same_pools(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    batch, q_heads, d = q.shape
+    if d != desc.head_dim or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [batch][q_heads][head_dim] of the pool dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens are int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != batch or context_lens.shape != (batch,):
+        raise ValueError("block_tables is [batch][max_blocks], context_lens [batch]")
+    max_blocks = int(block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    need = pkv_decode_workspace_size(batch, q_heads, max_blocks, k_cache, kernel, num_ctas)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check("pkv_decode_attention", lib.pkv_decode_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
+        q_heads, ctypes.c_float(scale), _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags,
+        _opts(kernel, num_ctas), _stream(stream)))
+    return out
+
+
+def pkv_device_status(clear: bool = False, stream=None) -> int:
+    """Sticky PKV_DEVERR_* bits of the current device (waits for the stream)."""
+    lib = load_library()
+    bits = ctypes.c_uint32(0)
+    _check("pkv_device_status", lib.pkv_device_status(ctypes.byref(bits), int(clear), _stream(stream)))
+    return int(bits.value)
+
+
+def pkv_status_string(status: int) -> str:
+    return load_library().pkv_status_string(status).decode()
+
+
+def pkv_version() -> int:
+    return int(load_library().pkv_version())

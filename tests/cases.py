@@ -1,0 +1,126 @@
+"""Inputs for the GPU parity tests, built on the CPU.
+
+Index metadata (tables, lengths, slot mappings, copy pairs) for the
+workloads with sharing comes from the oracle's page-pool simulator, so the
+copy-on-write pairs are the ones the notebook's rules produce. Values are
+seeded draws from ``paged_kv_cache_209_gb300.workloads``. Nothing here calls
+the CUDA library.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle.paged_pool import PagedKVPool
+from paged_kv_cache_209_gb300 import workloads as W
+
+B = 16
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> numpy uint16 bit patterns (host copy)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host_view(t: torch.Tensor) -> np.ndarray:
+    """Host numpy view the oracle reads: float32 values or bf16 bits."""
+    if t.dtype == torch.bfloat16:
+        return bf16_bits(t)
+    return t.detach().cpu().numpy()
+
+
+def dtype_name(t: torch.Tensor) -> str:
+    return "bf16" if t.dtype == torch.bfloat16 else "f32"
+
+
+def padded_tables(pool: PagedKVPool, seqs, width: int | None = None) -> np.ndarray:
+    tabs = [list(pool.page_table(s)) for s in seqs]
+    w = width or max(1, max(len(t) for t in tabs))
+    out = np.full((len(seqs), w), -1, dtype=np.int32)
+    for i, t in enumerate(tabs):
+        out[i, :len(t)] = t
+    return out
+
+
+def tiny_case(dtype=torch.float32, head_dim=64, q_heads=4, kv_heads=2, poison=False):
+    """The 3-sequence workload: seq 1 holds 9 tokens, seq 0 shares its first 6
+    (a shared partial block), seq 2 holds 33; then one step appends one token
+    to each sequence in index order (seq 0 copies the shared block first)."""
+    cfg = W.CONFIGS["tiny_f32"]
+    perm = np.random.default_rng(cfg["seed"]).permutation(cfg["num_blocks"])
+    pool = PagedKVPool(cfg["num_blocks"], B, pop_order=perm)
+    pool.create(1)
+    pool.append(1, 9)
+    pool.share_prefix(1, 0, 6)
+    pool.create(2)
+    pool.append(2, 33)
+    seqs = [0, 1, 2]
+    lens_before = np.array([pool.sequence_length(s) for s in seqs], dtype=np.int32)
+    tables_before = padded_tables(pool, seqs, width=4)
+    slots = []
+    for s in seqs:
+        n = pool.sequence_length(s)
+        pool.append(s, 1)
+        slots.append(pool.slots(s, n, 1)[0])
+    pairs = pool.take_copy_pairs()
+    lens_after = np.array([pool.sequence_length(s) for s in seqs], dtype=np.int32)
+    tables_after = padded_tables(pool, seqs, width=4)
+    nb = cfg["num_blocks"]
+    kp = W.numpy_normal((nb, kv_heads, B, head_dim), 101)
+    vp = W.numpy_normal((nb, kv_heads, B, head_dim), 102)
+    if poison:
+        used = set()
+        for i, s in enumerate(seqs):
+            for t in range(int(lens_before[i])):
+                used.add((int(tables_before[i][t // B]), t % B))
+        for blk in range(nb):
+            for sl in range(B):
+                if (blk, sl) not in used:
+                    kp[blk, :, sl, :] = np.nan
+                    vp[blk, :, sl, :] = np.inf
+    return dict(
+        q=torch.from_numpy(W.numpy_normal((3, q_heads, head_dim), 100)).to(dtype),
+        k_pool=torch.from_numpy(kp).to(dtype), v_pool=torch.from_numpy(vp).to(dtype),
+        k_new=torch.from_numpy(W.numpy_normal((3, kv_heads, head_dim), 103)).to(dtype),
+        v_new=torch.from_numpy(W.numpy_normal((3, kv_heads, head_dim), 104)).to(dtype),
+        slots=np.array(slots, dtype=np.int64), pairs=np.array(pairs, dtype=np.int64).reshape(-1, 2),
+        lens_before=lens_before, lens_after=lens_after, tables_before=tables_before,
+        tables_after=tables_after, kv_heads=kv_heads, scale=1.0 / np.sqrt(head_dim))
+
+
+def random_case(seed, lens, q_heads, kv_heads, head_dim, dtype, extra_blocks=5, width=None, poison=False):
+    """Sequences of the given lengths on a shuffled pool (private blocks)."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, dtype=np.int64)
+    nbs = (lens + B - 1) // B
+    num_blocks = int(nbs.sum()) + extra_blocks
+    perm = rng.permutation(num_blocks)
+    w = width or max(1, int(nbs.max()) if len(nbs) else 1)
+    tables = np.full((len(lens), w), -1, dtype=np.int32)
+    off = 0
+    for i, n in enumerate(nbs):
+        tables[i, :n] = perm[off:off + n]
+        off += n
+    kp = W.numpy_normal((num_blocks, kv_heads, B, head_dim), seed * 7 + 1)
+    vp = W.numpy_normal((num_blocks, kv_heads, B, head_dim), seed * 7 + 2)
+    if poison:
+        live = np.zeros((num_blocks, B), dtype=bool)
+        for i, n in enumerate(lens):
+            for t in range(int(n)):
+                live[tables[i, t // B], t % B] = True
+        kp[~live] = np.nan
+        vp[~live] = -np.inf
+    q = W.numpy_normal((len(lens), q_heads, head_dim), seed * 7 + 3)
+    return dict(q=torch.from_numpy(q).to(dtype), k_pool=torch.from_numpy(kp).to(dtype),
+                v_pool=torch.from_numpy(vp).to(dtype), tables=tables,
+                lens=lens.astype(np.int32), kv_heads=kv_heads, scale=1.0 / np.sqrt(head_dim))
+
+
+def attention_errors(got: torch.Tensor, want: np.ndarray):
+    g = got.detach().float().cpu().numpy().astype(np.float64)
+    diff = g - want
+    max_abs = float(np.abs(diff).max()) if diff.size else 0.0
+    denom = float(np.linalg.norm(want))
+    rel = float(np.linalg.norm(diff) / denom) if denom > 0 else float(np.linalg.norm(diff))
+    return max_abs, rel
