@@ -1,0 +1,42 @@
+"""Run decode steps of a named workload, for profiling under ncu.
+
+    python -m paged_kv_cache_209_gb300.profile_case --workload llama8k --steps 5
+
+One step is the hot path of the benchmark: block copy (no pairs in these
+workloads), slot-mapped append, decode attention. No timing, no CPU oracle:
+this only drives the kernels so that a profiler can capture them.
+"""
+
+import argparse
+
+import torch
+
+from paged_kv_cache_209_gb300 import pkv, workloads
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="llama8k", choices=["llama8k", "long128k", "mixed", "prefix"])
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--kernel", type=int, default=0)
+    args = ap.parse_args()
+    torch.cuda.set_device(0)
+    w = workloads.device_workload(args.workload, torch.device("cuda", 0))
+    out = torch.empty_like(w["q"])
+    need = pkv.pkv_decode_workspace_size(w["q"].shape[0], w["q"].shape[1], w["tables"].shape[1], w["k_pool"],
+                                         kernel=args.kernel)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for _ in range(args.steps):
+        pkv.pkv_copy_blocks(w["pairs"], w["k_pool"], w["v_pool"])
+        pkv.pkv_append(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"])
+        pkv.pkv_decode_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"], out=out,
+                                 workspace=ws, kernel=args.kernel)
+    torch.cuda.synchronize()
+    bits = pkv.pkv_device_status()
+    if bits:
+        raise SystemExit(f"device status {bits}")
+    print(f"{args.workload}: {args.steps} steps ok")
+
+
+if __name__ == "__main__":
+    main()

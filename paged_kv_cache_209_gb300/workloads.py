@@ -113,3 +113,56 @@ def torch_normal(shape, seed: int, dtype, device):
     gen = torch.Generator(device=device)
     gen.manual_seed(int(seed))
     return torch.randn(tuple(shape), generator=gen, device=device, dtype=torch.float32).to(dtype)
+
+
+def device_workload(name: str, device, seed_offset: int = 0) -> dict:
+    """Full-size inputs of one decode step of a named workload, on ``device``.
+
+    Returns the K/V pools, q, the step's new K/V rows with their slots, the
+    copy pairs (none for these workloads), block tables and the context
+    lengths *after* the step's append (the new token is attended to).
+    """
+    import torch
+
+    cfg = CONFIGS[name]
+    bf = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    B, HQ, HKV, D = cfg["batch"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
+    seed = cfg["seed"] + seed_offset
+    if name in ("llama8k", "long128k"):
+        lens = np.full(B, cfg["context"], dtype=np.int64)
+        tables = permuted_tables(cfg["num_blocks"], B, cfg["context"] // BLOCK_SIZE, cfg["seed"])
+        num_blocks = cfg["num_blocks"]
+    elif name == "mixed":
+        lens = log_uniform_lengths(B, cfg["min_len"], cfg["max_len"], cfg["seed"])
+        tables, num_blocks = packed_tables(lens, cfg["seed"])
+    elif name == "prefix":
+        suffix = uniform_suffixes(B, cfg["min_suffix"], cfg["max_suffix"], cfg["seed"])
+        lens = cfg["prefix"] + suffix + 1
+        n_prefix = cfg["prefix"] // BLOCK_SIZE
+        n_private = blocks_needed(lens) - n_prefix
+        num_blocks = n_prefix + int(n_private.sum())
+        perm = np.random.default_rng(cfg["seed"] + 1000).permutation(num_blocks)
+        width = int(blocks_needed(lens).max())
+        tables = np.full((B, width), -1, dtype=np.int32)
+        off = n_prefix
+        for i in range(B):
+            tables[i, :n_prefix] = perm[:n_prefix]           # the shared prefix blocks
+            tables[i, n_prefix:n_prefix + n_private[i]] = perm[off:off + n_private[i]]
+            off += n_private[i]
+    else:
+        raise ValueError(f"no device workload {name!r}")
+    slots = slot_of(tables, lens - 1)
+    return dict(
+        name=name, cfg=cfg, num_blocks=num_blocks,
+        k_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed, bf, device),
+        v_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed + 1, bf, device),
+        q=torch_normal((B, HQ, D), seed + 2, bf, device),
+        k_new=torch_normal((B, HKV, D), seed + 3, bf, device),
+        v_new=torch_normal((B, HKV, D), seed + 4, bf, device),
+        slots=torch.from_numpy(slots).to(device),
+        pairs=torch.zeros((0, 2), dtype=torch.int64, device=device),
+        tables=torch.from_numpy(tables.astype(np.int32)).to(device),
+        lens=torch.from_numpy(lens.astype(np.int32)).to(device),
+        tables_np=tables.astype(np.int32), lens_np=lens.astype(np.int32), slots_np=slots,
+        scale=1.0 / math.sqrt(D),
+    )

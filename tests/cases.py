@@ -109,8 +109,8 @@ def random_case(seed, lens, q_heads, kv_heads, head_dim, dtype, extra_blocks=5, 
         for i, n in enumerate(lens):
             for t in range(int(n)):
                 live[tables[i, t // B], t % B] = True
-        kp[~live] = np.nan
-        vp[~live] = -np.inf
+        kp.transpose(0, 2, 1, 3)[~live] = np.nan     # [blk][slot][head][d] view
+        vp.transpose(0, 2, 1, 3)[~live] = -np.inf
     q = W.numpy_normal((len(lens), q_heads, head_dim), seed * 7 + 3)
     return dict(q=torch.from_numpy(q).to(dtype), k_pool=torch.from_numpy(kp).to(dtype),
                 v_pool=torch.from_numpy(vp).to(dtype), tables=tables,

@@ -1,0 +1,121 @@
+"""Full-size parity on the four bf16 workloads, in the benchmark's launch
+configuration (default kernel choice and CTA count).
+
+One decode step runs on the GPU (block copy, append, attention). The append
+is checked bit-exactly over both whole pools against the oracle's append on
+a host copy; attention is checked on sampled (sequence, KV head) pairs that
+the float64 oracle computes one by one (the longest and shortest sequences
+are always sampled), and for every sequence against the independent
+CUDA-core kernel.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import cases
+from oracle import attention as OA
+from oracle import kv_ops as OK
+from oracle.paged_pool import PagedKVPool
+from paged_kv_cache_209_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, REL_L2 = 1e-2, 2e-3
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_209_gb300 import pkv as P
+    P.load_library()
+    return P
+
+
+def run_step(pkv, w, kernel=0):
+    pkv.pkv_copy_blocks(w["pairs"], w["k_pool"], w["v_pool"])
+    pkv.pkv_append(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"])
+    return pkv.pkv_decode_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"],
+                                    kernel=kernel)
+
+
+def sample_pairs(lens, kv_heads, n, seed):
+    rng = np.random.default_rng(seed)
+    seqs = {int(np.argmax(lens)), int(np.argmin(lens))}
+    while len(seqs) < min(n, len(lens)):
+        seqs.add(int(rng.integers(len(lens))))
+    return [(i, int(rng.integers(kv_heads))) for i in sorted(seqs)]
+
+
+def check_workload(pkv, w, n_samples):
+    kv_heads = w["cfg"]["kv_heads"]
+    G = w["cfg"]["q_heads"] // kv_heads
+    hk, hv = cases.host_view(w["k_pool"]), cases.host_view(w["v_pool"])
+    pairs_np = w["pairs"].cpu().numpy()
+    OK.copy_blocks(hk, hv, pairs_np)
+    OK.append_tokens(hk, hv, cases.host_view(w["k_new"]), cases.host_view(w["v_new"]), w["slots_np"])
+    out = run_step(pkv, w)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert np.array_equal(cases.host_view(w["k_pool"]), hk), "K pool differs after copy + append"
+    assert np.array_equal(cases.host_view(w["v_pool"]), hv), "V pool differs after copy + append"
+    q = cases.host_view(w["q"])
+    worst = 0.0
+    for (i, j) in sample_pairs(w["lens_np"], kv_heads, n_samples, 99):
+        want = OA.decode_attention_pair(q, hk, hv, w["tables_np"], w["lens_np"], w["scale"], i, j, kv_heads, "bf16")
+        ma, rl = cases.attention_errors(out[i, j * G:(j + 1) * G], want)
+        assert ma <= MAX_ABS and rl <= REL_L2, (i, j, ma, rl)
+        worst = max(worst, rl)
+    # every row against the CUDA-core kernel (a second implementation)
+    ref = pkv.pkv_decode_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"], kernel=1)
+    d = (out.float() - ref.float())
+    rel_all = (d.norm() / ref.float().norm()).item()
+    assert rel_all <= 2e-3 and d.abs().max().item() <= 1e-2, rel_all
+    return worst
+
+
+@pytest.mark.parametrize("name,n_samples", [("llama8k", 6), ("long128k", 4), ("mixed", 8), ("prefix", 6)])
+def test_full_size_workload(pkv, name, n_samples):
+    w = W.device_workload(name, torch.device("cuda", 0))
+    check_workload(pkv, w, n_samples)
+    del w
+    torch.cuda.empty_cache()
+
+
+def test_prefix_with_copy_on_write_pairs(pkv):
+    """Prefix workload where odd sequence 2i+1 shares all of sequence 2i, so
+    their partial last block is shared; the step's appends (index order)
+    produce up to 32 copy-on-write pairs through the page-pool simulator."""
+    cfg = W.CONFIGS["prefix"]
+    suffix = W.uniform_suffixes(cfg["batch"], cfg["min_suffix"], cfg["max_suffix"], cfg["seed"])
+    n_prefix_blocks = cfg["prefix"] // 16
+    total = n_prefix_blocks + int(sum(W.blocks_needed(suffix[0::2]))) + cfg["batch"] + 8
+    pool = PagedKVPool(total, 16, pop_order=np.random.default_rng(41).permutation(total))
+    pool.create("root")
+    pool.append("root", cfg["prefix"])
+    for i in range(0, cfg["batch"], 2):
+        pool.share_prefix("root", i, cfg["prefix"])
+        pool.append(i, int(suffix[i]))
+        pool.share_prefix(i, i + 1, pool.sequence_length(i))
+    seqs = list(range(cfg["batch"]))
+    slots = []
+    for s in seqs:
+        n = pool.sequence_length(s)
+        pool.append(s, 1)
+        slots.append(pool.slots(s, n, 1)[0])
+    pairs = np.array(pool.take_copy_pairs(), dtype=np.int64).reshape(-1, 2)
+    assert 16 <= len(pairs) <= 32
+    tables = cases.padded_tables(pool, seqs)
+    lens = np.array([pool.sequence_length(s) for s in seqs], dtype=np.int32)
+    dev = torch.device("cuda", 0)
+    HKV, D = cfg["kv_heads"], cfg["head_dim"]
+    w = dict(cfg=cfg, k_pool=W.torch_normal((total, HKV, 16, D), 51, torch.bfloat16, dev),
+             v_pool=W.torch_normal((total, HKV, 16, D), 52, torch.bfloat16, dev),
+             q=W.torch_normal((cfg["batch"], cfg["q_heads"], D), 53, torch.bfloat16, dev),
+             k_new=W.torch_normal((cfg["batch"], HKV, D), 54, torch.bfloat16, dev),
+             v_new=W.torch_normal((cfg["batch"], HKV, D), 55, torch.bfloat16, dev),
+             slots=torch.from_numpy(np.array(slots, np.int64)).to(dev), slots_np=np.array(slots, np.int64),
+             pairs=torch.from_numpy(pairs).to(dev), tables=torch.from_numpy(tables).to(dev),
+             lens=torch.from_numpy(lens).to(dev), tables_np=tables, lens_np=lens, scale=1.0 / np.sqrt(D))
+    check_workload(pkv, w, 8)
