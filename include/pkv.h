@@ -144,6 +144,13 @@ PKV_API pkv_status pkv_copy_blocks(const int64_t* src_dst_pairs, int64_t num_pai
 /*
  * pkv_decode_workspace_size -- bytes of device workspace pkv_decode_attention
  * needs for these sizes and options on the current device.
+ *
+ * The workspace holds the fp32 pieces of context segments that the kernel
+ * splits across CTAs and one counter per (sequence, KV head, warp) that
+ * finds the CTA which merges them. Zero-fill it once before its first use
+ * (cudaMemset); every completed call leaves the counters at zero again. Use
+ * one workspace per in-flight call, and zero it again after a call that set
+ * PKV_DEVERR_TIMEOUT.
  */
 PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
                                  int32_t max_blocks_per_seq,
@@ -163,7 +170,8 @@ PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
  *     out[i][h] = sum_t softmax(s)_t * V_j(t)
  * where K_j(t) / V_j(t) is row t % 16 of KV head j in block
  * block_tables[i][t / 16]. n == 0 gives a zero row. Accumulation is fp32;
- * out is written once, rounded to nearest-even into desc->dtype.
+ * out is written once, rounded to nearest-even into desc->dtype. One kernel
+ * launch per 1024 sequences.
  *
  *   q             device, [batch][num_q_heads][head_dim], desc->dtype.
  *   block_tables  device, int32 [batch][max_blocks_per_seq]; entries at
@@ -171,7 +179,7 @@ PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
  *   context_lens  device, int32 [batch], 0 <= n <= max_blocks_per_seq*16.
  *   out           device, [batch][num_q_heads][head_dim], desc->dtype.
  *   workspace     device, >= pkv_decode_workspace_size(...) bytes, 256-byte
- *                 aligned; its contents need no initialisation.
+ *                 aligned, zero-filled before its first use (see above).
  *   opts          NULL or tuning (above).
  * Errors: host-side checks as above plus num_q_heads % num_kv_heads != 0
  * (PKV_ERR_SHAPE) and a short workspace (PKV_ERR_WORKSPACE); with

@@ -156,8 +156,9 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max
         return 0;
     DecodePlan plan;
     if (decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan) != PKV_OK) return 0;
-    return decode_header_bytes() +
-           decode_partial_bytes(plan.num_ctas, num_q_heads / desc->num_kv_heads, desc->head_dim);
+    return decode_workspace_layout(batch, desc->num_kv_heads, plan.num_ctas, num_q_heads / desc->num_kv_heads,
+                                   desc->head_dim)
+        .total;
 }
 
 pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -182,8 +183,8 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
     const int rc = decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan);
     if (rc != PKV_OK) return static_cast<pkv_status>(rc);
     const int G = num_q_heads / desc->num_kv_heads;
-    const size_t need = decode_header_bytes() + decode_partial_bytes(plan.num_ctas, G, desc->head_dim);
-    if (workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    const WorkspaceLayout wl = decode_workspace_layout(batch, desc->num_kv_heads, plan.num_ctas, G, desc->head_dim);
+    if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned int* status = device_info().status;
     if (status == nullptr) return PKV_ERR_CUDA;
@@ -205,7 +206,8 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
         a.tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
         a.lens = context_lens + b0;
         a.out = static_cast<char*>(out) + b0 * row;
-        a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + decode_header_bytes());
+        a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.partials_offset);
+        a.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + wl.counters_offset);
         a.status = status;
         a.num_blocks = desc->num_blocks;
         a.max_blocks = max_blocks_per_seq;

@@ -9,8 +9,10 @@
 // of context lengths. A segment that lies wholly inside one CTA's range is
 // finished there and its output row written directly; a segment cut by a
 // range boundary leaves one fp32 piece (unnormalised accumulator, running
-// max, running sum) per CTA it touches, and the merge kernel combines those
-// pieces by log-sum-exp weights.
+// max, running sum) per CTA it touches; the CTA that finishes the last piece
+// of such a segment (found with an atomic counter in the workspace) combines
+// the pieces by log-sum-exp weights and writes the output row. One launch
+// per call, no separate merge kernel.
 //
 // All query heads of a KV head (the GQA group, G <= 8) are computed from one
 // read of each K/V byte.
@@ -83,6 +85,8 @@ struct Piece {
     int blk_from, blk_to;  // blocks [from, to) of the sequence
     bool complete;         // the piece is the whole segment
     bool first;            // the piece opens this CTA's range
+    long long seg_start;   // first unit of the segment
+    int seg_len;           // units (blocks) of the segment
 };
 
 // Walks the segment pieces of the unit range [start, end).
@@ -125,6 +129,8 @@ struct Walker {
         p.blk_to = static_cast<int>(pe - s0);
         p.complete = (u == s0) && (pe == s1);
         p.first = (u == start);
+        p.seg_start = s0;
+        p.seg_len = nb;
         u = pe;
         if (u < end) {
             if (++h == kv_heads) {
@@ -146,8 +152,11 @@ __device__ __forceinline__ long long range_start(long long c, long long U, long 
 // The CTA whose range holds unit u: max c with range_start(c) <= u.
 __device__ __forceinline__ long long cta_of(long long u, long long U, long long C) { return ((u + 1) * C - 1) / U; }
 
-__device__ __forceinline__ float* piece_slot(float* partials, long long cta, int slot, int G, int D) {
-    return partials + (cta * 2 + slot) * static_cast<long long>(G) * (D + 2);
+// Workspace slice of CTA `cta`, piece slot `slot` (0: the piece that opens
+// the CTA's range, 1: the one that closes it), consumer warp `warp`:
+// S accumulator values, then G maxima, then G sums.
+__device__ __forceinline__ float* piece_slice(float* partials, long long cta, int slot, int warp, int S, int G) {
+    return partials + ((cta * 2 + slot) * 4 + warp) * static_cast<long long>(S + 2 * G);
 }
 
 template <typename T>
@@ -172,38 +181,110 @@ __device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16* p)
     return __bfloat162float(*p);
 }
 
-// Combine the per-warp states of one segment piece (already in shared
-// memory) and write either the final output row or this CTA's piece.
-// Executed by `nthreads` threads with thread index `tid`.
+// Pieces of one segment: every CTA whose unit range meets [S0, S1).
+__device__ __forceinline__ int pieces_of_segment(long long c0, long long c1, long long U, long long C) {
+    if (U >= C) return static_cast<int>(c1 - c0 + 1);  // no CTA range is empty
+    int n = 0;
+    for (long long c = c0; c <= c1; ++c) n += range_start(c, U, C) < range_start(c + 1, U, C);
+    return n;
+}
+
+// Finish one segment piece for the elements of warp `warp`'s slice.
+//
+// The four consumer warps of a CTA each own a fixed slice of the G x D output
+// elements of the segment (S = G*D/4 elements; element e is head e / D, dim
+// e % D). The per-warp online-softmax states (O, m, l) of the piece are in
+// shared memory (sm_o[(w*gstride + g)*D + d], sm_m/sm_l[w*gstride + g]).
+// A whole segment is normalised and written out directly. A cut segment's
+// piece goes to this CTA's slot in the workspace; the warp then bumps the
+// segment's counter for its slice, and the warp that brings it to the number
+// of pieces merges every piece of its slice by log-sum-exp weights, writes the
+// output and puts the counter back to zero for the next call.
 template <typename T, int D>
-__device__ __forceinline__ void combine_warps(const float* sm_o, const float* sm_m, const float* sm_l, int nwarps,
-                                              int G, const Piece& pc, const DecodeArgs& a, long long cta, int tid,
-                                              int nthreads) {
-    for (int e = tid; e < G * D; e += nthreads) {
+__device__ void finish_piece(const float* sm_o, const float* sm_m, const float* sm_l, int gstride, int G,
+                             const Piece& pc, const DecodeArgs& a, long long cta, long long U, int warp,
+                             int lane) {
+    const int S = G * D / 4;
+    const int e0 = warp * S;
+    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
+    float* slice = nullptr;
+    if (!pc.complete) slice = piece_slice(a.partials, cta, pc.first ? 0 : 1, warp, S, G);
+    for (int e = e0 + lane; e < e0 + S; e += 32) {
         const int g = e / D;
         const int d = e - g * D;
         float M = neg_inf();
-        for (int w = 0; w < nwarps; ++w) M = fmaxf(M, sm_m[w * 8 + g]);
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * gstride + g]);
         const float base = (M == neg_inf()) ? 0.f : M;
         float o = 0.f, L = 0.f;
-        for (int w = 0; w < nwarps; ++w) {
-            const float mw = sm_m[w * 8 + g];
+        for (int w = 0; w < 4; ++w) {
+            const float mw = sm_m[w * gstride + g];
             const float wt = (mw == neg_inf()) ? 0.f : ex2(mw - base);
-            o += wt * sm_o[(w * 8 + g) * D + d];
-            L += wt * sm_l[w * 8 + g];
+            o += wt * sm_o[(w * gstride + g) * D + d];
+            L += wt * sm_l[w * gstride + g];
         }
-        if (pc.complete) {
-            T* dst = static_cast<T*>(a.out) +
-                     (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G + g) * D + d;
-            store_out<T>(dst, L > 0.f ? o / L : 0.f);
-        } else {
-            float* slot = piece_slot(a.partials, cta, pc.first ? 0 : 1, G, D) + g * (D + 2);
-            slot[d] = o;
-            if (d == 0) {
-                slot[D] = M;
-                slot[D + 1] = L;
-            }
+        if (pc.complete)
+            store_out<T>(out_row + e, L > 0.f ? o / L : 0.f);
+        else
+            slice[e - e0] = o;
+    }
+    if (pc.complete) return;
+    if (lane < G) {
+        float M = neg_inf();
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * gstride + lane]);
+        const float base = (M == neg_inf()) ? 0.f : M;
+        float L = 0.f;
+        for (int w = 0; w < 4; ++w) {
+            const float mw = sm_m[w * gstride + lane];
+            L += (mw == neg_inf()) ? 0.f : ex2(mw - base) * sm_l[w * gstride + lane];
         }
+        slice[S + lane] = M;
+        slice[S + G + lane] = L;
+    }
+    __threadfence();
+    __syncwarp();
+    const long long C = a.num_ctas;
+    const long long S0 = pc.seg_start, S1 = pc.seg_start + pc.seg_len;
+    const long long c0 = cta_of(S0, U, C), c1 = cta_of(S1 - 1, U, C);
+    const int npieces = pieces_of_segment(c0, c1, U, C);
+    int* counter = a.counters + (static_cast<long long>(pc.seq) * a.kv_heads + pc.head) * 4 + warp;
+    int last = 0;
+    if (lane == 0) last = atomicAdd(counter, 1) == npieces - 1;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    const int slot0 = (S0 == range_start(c0, U, C)) ? 0 : 1;
+    for (int e = e0 + lane; e < e0 + S; e += 32) {
+        const int g = e / D;
+        float M = neg_inf();
+        for (long long c = c0; c <= c1; ++c) {
+            if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
+            const float* p = piece_slice(a.partials, c, c == c0 ? slot0 : 0, warp, S, G);
+            M = fmaxf(M, __ldcg(p + S + g));
+        }
+        const float base = (M == neg_inf()) ? 0.f : M;
+        float o = 0.f, L = 0.f;
+        for (long long c = c0; c <= c1; ++c) {
+            if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
+            const float* p = piece_slice(a.partials, c, c == c0 ? slot0 : 0, warp, S, G);
+            const float mp = __ldcg(p + S + g);
+            const float wt = (mp == neg_inf()) ? 0.f : ex2(mp - base);
+            o += wt * __ldcg(p + (e - e0));
+            L += wt * __ldcg(p + S + G + g);
+        }
+        store_out<T>(out_row + e, L > 0.f ? o / L : 0.f);
+    }
+    if (lane == 0) *counter = 0;
+}
+
+// Rows of sequences with no tokens are zero; CTA c writes those of the
+// sequences i with i % num_ctas == c.
+template <typename T>
+__device__ void zero_empty_rows(const int32_t* s_len, const DecodeArgs& a, int tid, int nthreads) {
+    const int row = a.q_heads * a.head_dim;
+    for (int i = blockIdx.x; i < a.batch; i += a.num_ctas) {
+        if (s_len[i] != 0) continue;
+        T* out = static_cast<T*>(a.out) + static_cast<long long>(i) * row;
+        for (int e = tid; e < row; e += nthreads) store_out<T>(out + e, 0.f);
     }
 }
 
@@ -340,6 +421,7 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
     const int v_row = r8 + 8 * (q8 >> 1);     // V: token row
     const int v_chunk = q8 & 1;               // V: +0 / +1 chunk within an m-tile
 
+    zero_empty_rows<__nv_bfloat16>(s_len, a, threadIdx.x, C::kConsumers * 32);
     Walker wk;
     wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
     long long k = 0;
@@ -474,8 +556,7 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_bar);
         if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
-        combine_warps<__nv_bfloat16, D>(bo, bm, bl, C::kConsumers, G, pc, a, cta, threadIdx.x,
-                                        C::kConsumers * 32);
+        finish_piece<__nv_bfloat16, D>(bo, bm, bl, 8, G, pc, a, cta, U, warp, lane);
         ++piece_idx;
     }
 }
@@ -512,6 +593,7 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
     const T* kc = static_cast<const T*>(a.k_cache);
     const T* vc = static_cast<const T*>(a.v_cache);
 
+    zero_empty_rows<T>(s_len, a, threadIdx.x, C::kThreads);
     Walker wk;
     wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
     long long k = 0;
@@ -572,7 +654,7 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
                 }
             }
         }
-        // combine the warps, 8 heads at a time
+        // publish each warp's state, then finish the piece slice by slice
         __syncthreads();
 #pragma unroll
         for (int g = 0; g < GMAX; ++g) {
@@ -585,103 +667,8 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
             }
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
-            const int g = e / D;
-            const int d = e - g * D;
-            float M = neg_inf();
-            for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, sm_m[w * GMAX + g]);
-            const float base = (M == neg_inf()) ? 0.f : M;
-            float ov = 0.f, L = 0.f;
-            for (int w = 0; w < C::kWarps; ++w) {
-                const float mw = sm_m[w * GMAX + g];
-                const float wt = (mw == neg_inf()) ? 0.f : ex2(mw - base);
-                ov += wt * sm_o[(w * GMAX + g) * D + d];
-                L += wt * sm_l[w * GMAX + g];
-            }
-            if (pc.complete) {
-                T* dst = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G + g) * D + d;
-                store_out<T>(dst, L > 0.f ? ov / L : 0.f);
-            } else {
-                float* slot = piece_slot(a.partials, cta, pc.first ? 0 : 1, G, D) + g * (D + 2);
-                slot[d] = ov;
-                if (d == 0) {
-                    slot[D] = M;
-                    slot[D + 1] = L;
-                }
-            }
-        }
+        finish_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, U, warp, lane);
         __syncthreads();
-    }
-}
-
-// ------------------------------------------------------------------ merge kernel
-// One CTA per sequence. Writes zeros for an empty sequence and combines the
-// pieces of every segment that the split kernel cut.
-template <typename T, int D>
-__global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
-    __shared__ long long s_sum[2][8];
-    const int i = blockIdx.x;
-    const int cap = a.max_blocks * 16;
-    long long before = 0, total = 0;
-    for (int j = threadIdx.x; j < a.batch; j += blockDim.x) {
-        int n = a.lens[j];
-        n = n < 0 ? 0 : (n > cap ? cap : n);
-        const long long nb = (n + 15) >> 4;
-        total += nb;
-        if (j < i) before += nb;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        before += __shfl_xor_sync(0xffffffffu, before, off);
-        total += __shfl_xor_sync(0xffffffffu, total, off);
-    }
-    if ((threadIdx.x & 31) == 0) {
-        s_sum[0][threadIdx.x >> 5] = before;
-        s_sum[1][threadIdx.x >> 5] = total;
-    }
-    __syncthreads();
-    before = total = 0;
-    for (int w = 0; w < 8; ++w) {
-        before += s_sum[0][w];
-        total += s_sum[1][w];
-    }
-    int n = a.lens[i];
-    n = n < 0 ? 0 : (n > cap ? cap : n);
-    const long long nb = (n + 15) >> 4;
-    const int G = a.group;
-    T* out = static_cast<T*>(a.out) + static_cast<long long>(i) * a.q_heads * D;
-    if (nb == 0) {
-        for (int e = threadIdx.x; e < a.q_heads * D; e += blockDim.x) store_out<T>(out + e, 0.f);
-        return;
-    }
-    const long long U = static_cast<long long>(a.kv_heads) * total;
-    const long long C = a.num_ctas;
-    for (int h = 0; h < a.kv_heads; ++h) {
-        const long long S0 = a.kv_heads * before + h * nb;
-        const long long S1 = S0 + nb;
-        const long long c0 = cta_of(S0, U, C), c1 = cta_of(S1 - 1, U, C);
-        if (c0 == c1) continue;
-        const int slot0 = (S0 == range_start(c0, U, C)) ? 0 : 1;
-        for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-            const int g = e / D;
-            const int d = e - g * D;
-            float M = neg_inf();
-            for (long long c = c0; c <= c1; ++c) {
-                if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
-                const float* p = piece_slot(a.partials, c, c == c0 ? slot0 : 0, G, D) + g * (D + 2);
-                M = fmaxf(M, p[D]);
-            }
-            const float base = (M == neg_inf()) ? 0.f : M;
-            float ov = 0.f, L = 0.f;
-            for (long long c = c0; c <= c1; ++c) {
-                if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
-                const float* p = piece_slot(a.partials, c, c == c0 ? slot0 : 0, G, D) + g * (D + 2);
-                const float wt = (p[D] == neg_inf()) ? 0.f : ex2(p[D] - base);
-                ov += wt * p[d];
-                L += wt * p[D + 1];
-            }
-            store_out<T>(out + (h * G + g) * D + d, L > 0.f ? ov / L : 0.f);
-        }
     }
 }
 
@@ -790,18 +777,18 @@ cudaError_t run_tc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <typename T, int D>
-cudaError_t run_merge(const DecodeArgs& a, cudaStream_t s) {
-    merge_kernel<T, D><<<a.batch, 256, 0, s>>>(a);
-    return cudaGetLastError();
-}
-
 }  // namespace
 
-size_t decode_header_bytes() { return 256; }
-
-size_t decode_partial_bytes(int num_ctas, int group, int head_dim) {
-    return static_cast<size_t>(num_ctas) * 2 * group * (head_dim + 2) * sizeof(float);
+WorkspaceLayout decode_workspace_layout(int batch, int kv_heads, int num_ctas, int group, int head_dim) {
+    const int chunk = batch < kMaxBatchPerLaunch ? batch : kMaxBatchPerLaunch;
+    WorkspaceLayout w;
+    w.counters_offset = 256;
+    const size_t counters = static_cast<size_t>(chunk) * kv_heads * 4 * sizeof(int);
+    w.partials_offset = w.counters_offset + ((counters + 255) / 256) * 256;
+    // per CTA: 2 piece slots x 4 warp slices x (G*D/4 values + G maxima + G sums)
+    const size_t per_cta = 2 * 4 * (static_cast<size_t>(group) * head_dim / 4 + 2 * group) * sizeof(float);
+    w.total = w.partials_offset + static_cast<size_t>(num_ctas) * per_cta;
+    return w;
 }
 
 int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t max_blocks,
@@ -874,10 +861,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
                           : run_cc<__nv_bfloat16, 64, 8>(a, plan.num_ctas, plan.smem, s);
         }
     }
-    if (err != cudaSuccess) return err;
-    if (a.dtype == PKV_F32)
-        return D == 128 ? run_merge<float, 128>(a, s) : run_merge<float, 64>(a, s);
-    return D == 128 ? run_merge<__nv_bfloat16, 128>(a, s) : run_merge<__nv_bfloat16, 64>(a, s);
+    return err;
 }
 
 }  // namespace pkv

@@ -36,7 +36,8 @@ struct DecodeArgs {
     const int32_t* tables;
     const int32_t* lens;
     void* out;
-    float* partials;  // [num_ctas][2][G][D + 2] fp32 pieces of split segments
+    float* partials;  // fp32 pieces of cut segments: [num_ctas][2 slots][4 warps][G*D/4 + 2G]
+    int* counters;    // [batch][kv_heads][4 warps]; zero between calls
     unsigned int* status;
     int64_t num_blocks;
     int32_t max_blocks;
@@ -59,10 +60,13 @@ struct DecodePlan {
 
 // Largest batch one launch handles (sequence prefix sums live in shared
 // memory); pkv_decode_attention splits bigger batches.
-constexpr int kMaxBatchPerLaunch = 2048;
+constexpr int kMaxBatchPerLaunch = 1024;
 
-size_t decode_header_bytes();
-size_t decode_partial_bytes(int num_ctas, int group, int head_dim);
+// Workspace: 256-byte header (reserved), merge counters, piece slots.
+struct WorkspaceLayout {
+    size_t counters_offset, partials_offset, total;
+};
+WorkspaceLayout decode_workspace_layout(int batch, int kv_heads, int num_ctas, int group, int head_dim);
 int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t max_blocks,
                 const pkv_decode_opts* opts, DecodePlan* plan);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);

@@ -157,6 +157,7 @@ def _opts(kernel: int, num_ctas: int):
 
 def pkv_decode_workspace_size(batch: int, num_q_heads: int, max_blocks_per_seq: int, k_cache,
                               kernel: int = 0, num_ctas: int = 0) -> int:
+    """Workspace bytes; allocate them zero-filled (``torch.zeros``) and reuse them."""
     lib = load_library()
     desc = cache_desc(k_cache)
     return int(lib.pkv_decode_workspace_size(batch, num_q_heads, max_blocks_per_seq, ctypes.byref(desc),
@@ -181,7 +182,7 @@ def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale:
         out = torch.empty_like(q)
     need = pkv_decode_workspace_size(batch, q_heads, max_blocks, k_cache, kernel, num_ctas)
     if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
     _check("pkv_decode_attention", lib.pkv_decode_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
         q_heads, ctypes.c_float(scale), _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags,

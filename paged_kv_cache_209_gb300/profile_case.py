@@ -25,7 +25,7 @@ def main():
     out = torch.empty_like(w["q"])
     need = pkv.pkv_decode_workspace_size(w["q"].shape[0], w["q"].shape[1], w["tables"].shape[1], w["k_pool"],
                                          kernel=args.kernel)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     for _ in range(args.steps):
         pkv.pkv_copy_blocks(w["pairs"], w["k_pool"], w["v_pool"])
         pkv.pkv_append(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"])

@@ -298,3 +298,21 @@ def test_host_side_rejections(pkv):
         pkv.pkv_decode_attention(q.float(), kp.float(), vp.float(), dev(c["tables"], torch.int32),
                                  dev(c["lens"], torch.int32), 0.1, kernel=2)
     assert e.value.name == "PKV_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("num_ctas", [0, 37, 500])
+def test_workspace_reuse_leaves_counters_zero(pkv, num_ctas):
+    """The merge counters in the workspace are back at zero after every call,
+    so one zero-filled workspace serves any number of calls identically."""
+    c = cases.random_case(38, [100, 2000, 3, 517, 4096], 32, 8, 128, torch.bfloat16)
+    q, kp, vp = dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"])
+    tables, lens = dev(c["tables"], torch.int32), dev(c["lens"], torch.int32)
+    need = pkv.pkv_decode_workspace_size(5, 32, c["tables"].shape[1], kp, num_ctas=num_ctas)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    outs = [pkv.pkv_decode_attention(q, kp, vp, tables, lens, c["scale"], workspace=ws, num_ctas=num_ctas)
+            for _ in range(3)]
+    torch.cuda.synchronize()
+    counters = ws[256:256 + 5 * 8 * 4 * 4]
+    assert torch.count_nonzero(counters).item() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    check_close(outs[0], oracle_attention(c, c["tables"], c["lens"]))
