@@ -43,14 +43,24 @@ WORKLOAD = "llama8k"
 FALLBACK_HBM_GBS = 6800.0
 
 
-def workload_desc(cfg):
-    return (f"Llama-3-8B decode layer: batch {cfg['batch']}, {cfg['q_heads']} q / {cfg['kv_heads']} kv heads, "
-            f"head_dim {cfg['head_dim']}, context {cfg['context']} tokens, 16-token blocks, "
-            f"{cfg['num_blocks']}-block shuffled pool, bf16")
+WORKLOAD_NAMES = {
+    "llama8k": "Llama-3-8B decode layer, every context 8192 tokens",
+    "long128k": "70B-GQA decode layer, every context 131072 tokens",
+    "mixed": "continuous-batching mix, contexts log-uniform on [16, 32768]",
+    "prefix": "4096-token prefix shared by all sequences + private suffixes uniform in [1, 2048]",
+}
+L2_NOTE = {
+    "llama8k": "inputs larger than L2 (1 GiB K+V per step)",
+    "long128k": "inputs larger than L2 (2 GiB K+V per step)",
+    "mixed": "inputs larger than L2 (4.65 GB K+V per step)",
+    "prefix": "unique K+V (0.33 GB) larger than L2; the 16 MiB shared prefix is re-read from L2 by every "
+              "sequence, so logical GB/s can exceed HBM bandwidth",
+}
 
 
-def kv_bytes_per_step(cfg):
-    return cfg["batch"] * cfg["context"] * 2 * cfg["kv_heads"] * cfg["head_dim"] * 2
+def workload_desc(name, cfg, lens):
+    return (f"{WORKLOAD_NAMES[name]}: batch {cfg['batch']}, {cfg['q_heads']} q / {cfg['kv_heads']} kv heads, "
+            f"head_dim {cfg['head_dim']}, 16-token blocks, shuffled pool, bf16, {int(lens.sum())} KV tokens")
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -138,10 +148,10 @@ def kernel_source_sha():
     return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(workload):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "decode_llama8k.md")
+    p = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
     if not os.path.exists(p):
         return None
     text = open(p).read()
@@ -183,42 +193,43 @@ def cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, seqs):
 
 
 def run_reference(args, cfg):
-    """--impl reference: the CPU oracle, timed per step on a bounded sample."""
+    """--impl reference: the CPU oracle, timed per step on a bounded sample:
+    one (sequence, KV head) of the workload's longest sequence."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
     import torch
-    rng_seqs = [0]
-    tables = W.permuted_tables(cfg["num_blocks"], cfg["batch"], cfg["context"] // 16, cfg["seed"])
-    lens = np.full(cfg["batch"], cfg["context"], dtype=np.int32)
-    # Only the sampled sequences' blocks are materialised (on the host).
-    ids = np.unique(tables[rng_seqs].reshape(-1))
-    remap = -np.ones(cfg["num_blocks"], dtype=np.int64)
-    remap[ids] = np.arange(len(ids))
+    tables_all, lens_all, _ = W.workload_index(args.workload)
+    i0 = int(np.argmax(lens_all))
+    lens = lens_all[i0:i0 + 1].astype(np.int32)
+    n_used = int((lens[0] + 15) // 16)
+    ids = tables_all[i0, :n_used]
+    # Only the sampled sequence's blocks are materialised (on the host).
     g = torch.Generator().manual_seed(cfg["seed"])
-    shape = (len(ids), cfg["kv_heads"], 16, cfg["head_dim"])
+    shape = (n_used, cfg["kv_heads"], 16, cfg["head_dim"])
     kp = torch.randn(shape, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     vp = torch.randn(shape, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     q = torch.randn((1, cfg["q_heads"], cfg["head_dim"]), generator=g).to(torch.bfloat16)
     q = q.view(torch.int16).numpy().view(np.uint16)
-    t = remap[tables[rng_seqs]]
+    t = np.arange(n_used, dtype=np.int64)[None, :]   # block j of the sample sits at index j of the sub-pool
+    assert len(np.unique(ids)) == n_used
     scale = 1.0 / np.sqrt(cfg["head_dim"])
-    pairs = [(0, 0)]  # one (sequence, KV head): 8192 tokens, 4 MiB of K+V per step
+    pairs = [(0, 0)]
     for _ in range(args.warmup):
-        oracle_sample_rate(q, kp, vp, t, lens[:1], scale, cfg["kv_heads"], pairs)
+        oracle_sample_rate(q, kp, vp, t, lens, scale, cfg["kv_heads"], pairs)
     tot_b, tot_s = 0, 0.0
     for _ in range(args.steps):
-        b, s, _ = oracle_sample_rate(q, kp, vp, t, lens[:1], scale, cfg["kv_heads"], pairs)
+        b, s_, _ = oracle_sample_rate(q, kp, vp, t, lens, scale, cfg["kv_heads"], pairs)
         tot_b += b
-        tot_s += s
+        tot_s += s_
     gbs = tot_b / tot_s / 1e9
+    sample = f"1 sequence x 1 KV head ({int(lens[0])} tokens, bf16 K+V) per step"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "sample": "1 sequence x 1 KV head (8192 tokens) per step"},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "1 sequence x 1 KV head (8192 tokens, 4 MiB of bf16 K+V) per step"},
+        "config": {"workload": workload_desc(args.workload, cfg, lens_all), "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "kv_tokens_per_s": round(tot_b / (2 * cfg["kv_heads"] * cfg["head_dim"] * 2) / tot_s, 1),
     }
@@ -239,29 +250,16 @@ def run_pkv(args, cfg):
     from paged_kv_cache_209_gb300 import pkv
     pkv.load_library()
 
+    w = W.device_workload(args.workload, device, seed_offset=1000 * rank)
     B, HQ, HKV, D = cfg["batch"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
-    NB, CTX = cfg["num_blocks"], cfg["context"]
-    MAXB = CTX // 16
-    seed = cfg["seed"] + 1000 * rank
-    bf = torch.bfloat16
-    k_pool = W.torch_normal((NB, HKV, 16, D), seed, bf, device)
-    v_pool = W.torch_normal((NB, HKV, 16, D), seed + 1, bf, device)
-    q_host = W.torch_normal((B, HQ, D), seed + 2, bf, "cpu")
-    kn_host = W.torch_normal((B, HKV, D), seed + 3, bf, "cpu")
-    vn_host = W.torch_normal((B, HKV, D), seed + 4, bf, "cpu")
-    tables_np = W.permuted_tables(NB, B, MAXB, cfg["seed"])
-    lens_np = np.full(B, CTX, dtype=np.int32)
-    slots_np = W.slot_of(tables_np, lens_np.astype(np.int64) - 1)
-    q = q_host.to(device)
-    kn, vn = kn_host.to(device), vn_host.to(device)
-    tables = torch.from_numpy(tables_np).to(device)
-    lens = torch.from_numpy(lens_np).to(device)
-    slots = torch.from_numpy(slots_np).to(device)
-    pairs = torch.zeros((0, 2), dtype=torch.int64, device=device)
-    out = torch.empty((B, HQ, D), dtype=bf, device=device)
+    k_pool, v_pool, q, kn, vn = w["k_pool"], w["v_pool"], w["q"], w["k_new"], w["v_new"]
+    tables, lens, slots, pairs = w["tables"], w["lens"], w["slots"], w["pairs"]
+    tables_np, lens_np = w["tables_np"], w["lens_np"]
+    MAXB = tables.shape[1]
+    out = torch.empty((B, HQ, D), dtype=q.dtype, device=device)
     ws_bytes = pkv.pkv_decode_workspace_size(B, HQ, MAXB, k_pool)
     workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
-    scale = 1.0 / float(np.sqrt(D))
+    scale = w["scale"]
     stream = torch.cuda.current_stream()
 
     def step():
@@ -296,27 +294,20 @@ def run_pkv(args, cfg):
     barrier(ws)
     clocks = sampler.stop() if sampler else None
     ms_total = max_over_ranks(start.elapsed_time(end), ws, device)
-    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    dec_ms = [e0.elapsed_time(e1) for e0, e1 in ev_dec]
     dec_avg_ms = max_over_ranks(sum(dec_ms) / len(dec_ms), ws, device)
     status_bits = pkv.pkv_device_status(clear=False)
 
     # -------- end-to-end: per-step inputs from pinned host memory, result back to the host
-    q_pin = q_host.pin_memory()
-    kn_pin, vn_pin = kn_host.pin_memory(), vn_host.pin_memory()
-    slots_pin = torch.from_numpy(slots_np).pin_memory()
-    tables_pin = torch.from_numpy(tables_np).pin_memory()
-    lens_pin = torch.from_numpy(lens_np).pin_memory()
-    out_pin = torch.empty((B, HQ, D), dtype=bf).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (q_pin, kn_pin, vn_pin, slots_pin, tables_pin, lens_pin))
+    pins = [t.cpu().pin_memory() for t in (q, kn, vn, slots, tables, lens)]
+    devs = [q, kn, vn, slots, tables, lens]
+    out_pin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pins)
     d2h = out_pin.numel() * out_pin.element_size()
 
     def e2e_step():
-        q.copy_(q_pin, non_blocking=True)
-        kn.copy_(kn_pin, non_blocking=True)
-        vn.copy_(vn_pin, non_blocking=True)
-        slots.copy_(slots_pin, non_blocking=True)
-        tables.copy_(tables_pin, non_blocking=True)
-        lens.copy_(lens_pin, non_blocking=True)
+        for dst, src in zip(devs, pins):
+            dst.copy_(src, non_blocking=True)
         step()
         out_pin.copy_(out, non_blocking=True)
 
@@ -337,19 +328,22 @@ def run_pkv(args, cfg):
             dist.destroy_process_group()
         return
 
-    kvb = kv_bytes_per_step(cfg)
+    kv_tokens = int(lens_np.sum())
+    kvb = kv_tokens * 2 * HKV * D * q.element_size()
     total_kv = kvb * ws
     ms_per_step = ms_total / args.steps
     value = total_kv / (ms_per_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    # algorithmic bytes of one decode call: K+V read, q read, out written,
-    # block tables and lengths read, split pieces written and read back
-    alg_bytes = kvb + q.numel() * 2 + out.numel() * 2 + tables.numel() * 4 + lens.numel() * 4
+    # algorithmic bytes of one decode call: K+V of every live token read once,
+    # q read, out written, block-table entries and lengths read
+    used_entries = int(((lens_np.astype(np.int64) + 15) // 16).sum())
+    alg_bytes = kvb + q.numel() * q.element_size() + out.numel() * out.element_size() + used_entries * 4 + B * 4
     achieved = alg_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_traffic(args.workload)
 
     # -------- CPU oracle baseline on a bounded sample of the same workload
-    sample_seqs = [0, 1]
+    order = np.argsort(-lens_np)
+    sample_seqs = sorted({int(order[0]), int(order[len(order) // 2])})
     qh, kph, vph, th, lh = cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, sample_seqs)
     pairs_list = [(i, j) for i in range(len(sample_seqs)) for j in range(HKV)]
     cb, cs, cdone = oracle_sample_rate(qh, kph, vph, th, lh, scale, HKV, pairs_list, time_budget_s=20.0)
@@ -359,17 +353,19 @@ def run_pkv(args, cfg):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "l2": "inputs larger than L2 (1 GiB K+V per step)",
-                   "step": "copy_blocks (0 pairs) + append (32 tokens) + decode attention",
+        "config": {"workload": workload_desc(args.workload, cfg, lens_np),
+                   "l2": L2_NOTE[args.workload],
+                   "step": f"copy_blocks ({int(pairs.shape[0])} pairs) + append ({B} tokens) + decode attention",
                    "kernel": "tensor-core split-context kernel, merge fused"},
         "hbm_frac": round(value / peak, 4),
-        "kv_tokens_per_s": round(cfg["batch"] * cfg["context"] * ws / (ms_per_step * 1e-3), 1),
+        "kv_tokens_per_s": round(kv_tokens * ws / (ms_per_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_tc_kernel<128> (one launch per pkv_decode_attention call)",
                      "avg_launch_ms": round(dec_avg_ms, 5), "algorithmic_bytes": alg_bytes},
         "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{cdone} (sequence, KV head) pairs of 8192 tokens, float64 NumPy oracle"},
+                         "sample": f"{cdone} (sequence, KV head) pairs of sequences {sample_seqs}, "
+                                   f"float64 NumPy oracle, one thread"},
         "e2e": {"value": round(total_kv / (e2e_s / args.steps) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -388,10 +384,12 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_NAMES), default=WORKLOAD,
+                    help="default: the 8K Llama-3-8B layer the headline metric is quoted on")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    cfg = dict(W.CONFIGS[WORKLOAD])
+    cfg = dict(W.CONFIGS[args.workload])
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

@@ -196,14 +196,11 @@ __device__ __forceinline__ int pieces_of_segment(long long c0, long long c1, lon
 // e % D). The per-warp online-softmax states (O, m, l) of the piece are in
 // shared memory (sm_o[(w*gstride + g)*D + d], sm_m/sm_l[w*gstride + g]).
 // A whole segment is normalised and written out directly. A cut segment's
-// piece goes to this CTA's slot in the workspace; the warp then bumps the
-// segment's counter for its slice, and the warp that brings it to the number
-// of pieces merges every piece of its slice by log-sum-exp weights, writes the
-// output and puts the counter back to zero for the next call.
+// piece goes to this CTA's slot in the workspace; it is announced later by
+// signal_piece. Returns true for a cut segment.
 template <typename T, int D>
-__device__ void finish_piece(const float* sm_o, const float* sm_m, const float* sm_l, int gstride, int G,
-                             const Piece& pc, const DecodeArgs& a, long long cta, long long U, int warp,
-                             int lane) {
+__device__ bool write_piece(const float* sm_o, const float* sm_m, const float* sm_l, int gstride, int G,
+                            const Piece& pc, const DecodeArgs& a, long long cta, int warp, int lane) {
     const int S = G * D / 4;
     const int e0 = warp * S;
     T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
@@ -227,7 +224,7 @@ __device__ void finish_piece(const float* sm_o, const float* sm_m, const float* 
         else
             slice[e - e0] = o;
     }
-    if (pc.complete) return;
+    if (pc.complete) return false;
     if (lane < G) {
         float M = neg_inf();
         for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * gstride + lane]);
@@ -240,8 +237,18 @@ __device__ void finish_piece(const float* sm_o, const float* sm_m, const float* 
         slice[S + lane] = M;
         slice[S + G + lane] = L;
     }
-    __threadfence();
-    __syncwarp();
+    return true;
+}
+
+// Announce a written piece of a cut segment (the caller has fenced its
+// writes): bump the segment's counter for this warp's slice; the warp that
+// brings it to the number of pieces merges every piece of its slice by
+// log-sum-exp weights, writes the output and puts the counter back to zero
+// for the next call.
+template <typename T, int D>
+__device__ void signal_piece(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane) {
+    const int S = G * D / 4;
+    const int e0 = warp * S;
     const long long C = a.num_ctas;
     const long long S0 = pc.seg_start, S1 = pc.seg_start + pc.seg_len;
     const long long c0 = cta_of(S0, U, C), c1 = cta_of(S1 - 1, U, C);
@@ -252,28 +259,39 @@ __device__ void finish_piece(const float* sm_o, const float* sm_m, const float* 
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __threadfence();
+    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
     const int slot0 = (S0 == range_start(c0, U, C)) ? 0 : 1;
     for (int e = e0 + lane; e < e0 + S; e += 32) {
         const int g = e / D;
-        float M = neg_inf();
-        for (long long c = c0; c <= c1; ++c) {
-            if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
-            const float* p = piece_slice(a.partials, c, c == c0 ? slot0 : 0, warp, S, G);
-            M = fmaxf(M, __ldcg(p + S + g));
-        }
-        const float base = (M == neg_inf()) ? 0.f : M;
-        float o = 0.f, L = 0.f;
+        float M = neg_inf(), o = 0.f, L = 0.f;   // online log-sum-exp over the pieces
         for (long long c = c0; c <= c1; ++c) {
             if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
             const float* p = piece_slice(a.partials, c, c == c0 ? slot0 : 0, warp, S, G);
             const float mp = __ldcg(p + S + g);
-            const float wt = (mp == neg_inf()) ? 0.f : ex2(mp - base);
-            o += wt * __ldcg(p + (e - e0));
-            L += wt * __ldcg(p + S + G + g);
+            const float op = __ldcg(p + (e - e0));
+            const float lp = __ldcg(p + S + G + g);
+            if (mp == neg_inf()) continue;
+            const float Mn = fmaxf(M, mp);
+            const float ws = (M == neg_inf()) ? 0.f : ex2(M - Mn);
+            const float wp = ex2(mp - Mn);
+            o = o * ws + op * wp;
+            L = L * ws + lp * wp;
+            M = Mn;
         }
         store_out<T>(out_row + e, L > 0.f ? o / L : 0.f);
     }
     if (lane == 0) *counter = 0;
+}
+
+// After the CTA's last piece: fence this warp's piece writes once, then
+// announce the (at most two) cut pieces of the range, first and last.
+template <typename T, int D>
+__device__ void signal_pending(const Piece* pending, int npending, int G, const DecodeArgs& a, long long U,
+                               int warp, int lane) {
+    if (npending == 0) return;
+    __threadfence();
+    __syncwarp();
+    for (int i = 0; i < npending; ++i) signal_piece<T, D>(pending[i], G, a, U, warp, lane);
 }
 
 // Rows of sequences with no tokens are zero; CTA c writes those of the
@@ -427,6 +445,8 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
     long long k = 0;
     int piece_idx = 0;
     Piece pc;
+    Piece pending[2];  // cut pieces of this range: only its first and its last can be cut
+    int npending = 0;
     while (wk.next(pc)) {
         // Q^T fragments: B operand of S^T = K Q^T; column n = query head gid.
         uint32_t qf[D / 16][2];
@@ -556,9 +576,10 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_bar);
         if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
-        finish_piece<__nv_bfloat16, D>(bo, bm, bl, 8, G, pc, a, cta, U, warp, lane);
+        if (write_piece<__nv_bfloat16, D>(bo, bm, bl, 8, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
         ++piece_idx;
     }
+    signal_pending<__nv_bfloat16, D>(pending, npending, G, a, U, warp, lane);
 }
 
 // ------------------------------------------------------------------ CUDA-core kernel
@@ -598,6 +619,8 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
     wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
     long long k = 0;
     Piece pc;
+    Piece pending[2];
+    int npending = 0;
     while (wk.next(pc)) {
         float qr[GMAX][C::kPer];
 #pragma unroll
@@ -667,9 +690,10 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
             }
         }
         __syncthreads();
-        finish_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, U, warp, lane);
+        if (write_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
         __syncthreads();
     }
+    signal_pending<T, D>(pending, npending, G, a, U, warp, lane);
 }
 
 // ------------------------------------------------------------------ host side

@@ -115,19 +115,14 @@ def torch_normal(shape, seed: int, dtype, device):
     return torch.randn(tuple(shape), generator=gen, device=device, dtype=torch.float32).to(dtype)
 
 
-def device_workload(name: str, device, seed_offset: int = 0) -> dict:
-    """Full-size inputs of one decode step of a named workload, on ``device``.
+def workload_index(name: str):
+    """Index metadata of a named workload: ``(tables int32, lens int64, num_blocks)``.
 
-    Returns the K/V pools, q, the step's new K/V rows with their slots, the
-    copy pairs (none for these workloads), block tables and the context
-    lengths *after* the step's append (the new token is attended to).
+    ``lens`` are the context lengths after the step's append (the new token
+    is attended to).
     """
-    import torch
-
     cfg = CONFIGS[name]
-    bf = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
-    B, HQ, HKV, D = cfg["batch"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
-    seed = cfg["seed"] + seed_offset
+    B = cfg["batch"]
     if name in ("llama8k", "long128k"):
         lens = np.full(B, cfg["context"], dtype=np.int64)
         tables = permuted_tables(cfg["num_blocks"], B, cfg["context"] // BLOCK_SIZE, cfg["seed"])
@@ -150,7 +145,24 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
             tables[i, n_prefix:n_prefix + n_private[i]] = perm[off:off + n_private[i]]
             off += n_private[i]
     else:
-        raise ValueError(f"no device workload {name!r}")
+        raise ValueError(f"no workload {name!r}")
+    return tables.astype(np.int32), lens, num_blocks
+
+
+def device_workload(name: str, device, seed_offset: int = 0) -> dict:
+    """Full-size inputs of one decode step of a named workload, on ``device``.
+
+    Returns the K/V pools, q, the step's new K/V rows with their slots, the
+    copy pairs (none for these workloads), block tables and the context
+    lengths *after* the step's append (the new token is attended to).
+    """
+    import torch
+
+    cfg = CONFIGS[name]
+    bf = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    B, HQ, HKV, D = cfg["batch"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
+    seed = cfg["seed"] + seed_offset
+    tables, lens, num_blocks = workload_index(name)
     slots = slot_of(tables, lens - 1)
     return dict(
         name=name, cfg=cfg, num_blocks=num_blocks,
@@ -161,8 +173,8 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
         v_new=torch_normal((B, HKV, D), seed + 4, bf, device),
         slots=torch.from_numpy(slots).to(device),
         pairs=torch.zeros((0, 2), dtype=torch.int64, device=device),
-        tables=torch.from_numpy(tables.astype(np.int32)).to(device),
+        tables=torch.from_numpy(tables).to(device),
         lens=torch.from_numpy(lens.astype(np.int32)).to(device),
-        tables_np=tables.astype(np.int32), lens_np=lens.astype(np.int32), slots_np=slots,
+        tables_np=tables, lens_np=lens.astype(np.int32), slots_np=slots,
         scale=1.0 / math.sqrt(D),
     )
