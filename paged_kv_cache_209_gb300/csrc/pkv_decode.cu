@@ -245,7 +245,12 @@ __device__ bool write_piece(const float* sm_o, const float* sm_m, const float* s
 // brings it to the number of pieces merges every piece of its slice by
 // log-sum-exp weights, writes the output and puts the counter back to zero
 // for the next call.
-template <typename T, int D>
+//
+// The merge runs at the tail of the kernel, so it is written for latency:
+// a lane owns NPER elements of the slice and issues the loads of CHUNK pieces
+// x NPER elements before it uses any of them (one round trip per CHUNK
+// pieces instead of one per piece and element).
+template <typename T, int D, int NPER, int CHUNK>
 __device__ void signal_piece(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane) {
     const int S = G * D / 4;
     const int e0 = warp * S;
@@ -261,37 +266,61 @@ __device__ void signal_piece(const Piece& pc, int G, const DecodeArgs& a, long l
     __threadfence();
     T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
     const int slot0 = (S0 == range_start(c0, U, C)) ? 0 : 1;
-    for (int e = e0 + lane; e < e0 + S; e += 32) {
-        const int g = e / D;
-        float M = neg_inf(), o = 0.f, L = 0.f;   // online log-sum-exp over the pieces
-        for (long long c = c0; c <= c1; ++c) {
-            if (c > c0 && range_start(c, U, C) == range_start(c + 1, U, C)) continue;
-            const float* p = piece_slice(a.partials, c, c == c0 ? slot0 : 0, warp, S, G);
-            const float mp = __ldcg(p + S + g);
-            const float op = __ldcg(p + (e - e0));
-            const float lp = __ldcg(p + S + G + g);
-            if (mp == neg_inf()) continue;
-            const float Mn = fmaxf(M, mp);
-            const float ws = (M == neg_inf()) ? 0.f : ex2(M - Mn);
-            const float wp = ex2(mp - Mn);
-            o = o * ws + op * wp;
-            L = L * ws + lp * wp;
-            M = Mn;
+    float M[NPER], O[NPER], L[NPER];
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        M[j] = neg_inf();
+        O[j] = 0.f;
+        L[j] = 0.f;
+    }
+    for (long long cb = c0; cb <= c1; cb += CHUNK) {
+        float mv[CHUNK][NPER], ov[CHUNK][NPER], lv[CHUNK][NPER];
+#pragma unroll
+        for (int q = 0; q < CHUNK; ++q) {
+            // CTA cb+q holds a piece unless it is past c1 or its range is empty
+            const long long cq = cb + q;
+            const bool has = cq <= c1 && (cq == c0 || range_start(cq, U, C) < range_start(cq + 1, U, C));
+            const float* pq = piece_slice(a.partials, has ? cq : c0, cq == c0 ? slot0 : 0, warp, S, G);
+#pragma unroll
+            for (int j = 0; j < NPER; ++j) {
+                const int e = lane + 32 * j;   // element index within the slice
+                const bool live = has && e < S;
+                const int g = (e0 + e) / D;
+                mv[q][j] = live ? __ldcg(pq + S + g) : neg_inf();
+                ov[q][j] = live ? __ldcg(pq + e) : 0.f;
+                lv[q][j] = live ? __ldcg(pq + S + G + g) : 0.f;
+            }
         }
-        store_out<T>(out_row + e, L > 0.f ? o / L : 0.f);
+#pragma unroll
+        for (int q = 0; q < CHUNK; ++q)
+#pragma unroll
+            for (int j = 0; j < NPER; ++j) {
+                if (mv[q][j] == neg_inf()) continue;
+                const float Mn = fmaxf(M[j], mv[q][j]);
+                const float ws = (M[j] == neg_inf()) ? 0.f : ex2(M[j] - Mn);
+                const float wp = ex2(mv[q][j] - Mn);
+                O[j] = O[j] * ws + ov[q][j] * wp;
+                L[j] = L[j] * ws + lv[q][j] * wp;
+                M[j] = Mn;
+            }
+    }
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        const int e = lane + 32 * j;
+        if (e < S) store_out<T>(out_row + e0 + e, L[j] > 0.f ? O[j] / L[j] : 0.f);
     }
     if (lane == 0) *counter = 0;
 }
 
 // After the CTA's last piece: fence this warp's piece writes once, then
 // announce the (at most two) cut pieces of the range, first and last.
-template <typename T, int D>
+template <typename T, int D, int NPER, int CHUNK>
 __device__ void signal_pending(const Piece* pending, int npending, int G, const DecodeArgs& a, long long U,
                                int warp, int lane) {
     if (npending == 0) return;
     __threadfence();
     __syncwarp();
-    for (int i = 0; i < npending; ++i) signal_piece<T, D>(pending[i], G, a, U, warp, lane);
+    for (int i = 0; i < npending; ++i) signal_piece<T, D, NPER, CHUNK>(pending[i], G, a, U, warp, lane);
 }
 
 // Rows of sequences with no tokens are zero; CTA c writes those of the
@@ -579,7 +608,8 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
         if (write_piece<__nv_bfloat16, D>(bo, bm, bl, 8, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
         ++piece_idx;
     }
-    signal_pending<__nv_bfloat16, D>(pending, npending, G, a, U, warp, lane);
+    // a warp's slice is G*D/4 <= 2*D elements: at most D/16 per lane
+    signal_pending<__nv_bfloat16, D, D / 16, 2>(pending, npending, G, a, U, warp, lane);
 }
 
 // ------------------------------------------------------------------ CUDA-core kernel
@@ -693,7 +723,7 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
         if (write_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
         __syncthreads();
     }
-    signal_pending<T, D>(pending, npending, G, a, U, warp, lane);
+    signal_pending<T, D, GMAX * D / 128, (GMAX > 8 ? 2 : 4)>(pending, npending, G, a, U, warp, lane);
 }
 
 // ------------------------------------------------------------------ host side
