@@ -388,6 +388,10 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
+    // Everything above touches no input; from here on the previous kernel in
+    // the stream (typically the append) must be complete.
+    grid_dependency_wait();
+    allow_dependents();
     build_prefix(s_pre, s_len, a.lens, a.batch, a.max_blocks, a.status);  // contains __syncthreads
 
     const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
@@ -632,6 +636,8 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    grid_dependency_wait();
+    allow_dependents();
     build_prefix(s_pre, s_len, a.lens, a.batch, a.max_blocks, a.status);
 
     const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
@@ -816,8 +822,7 @@ cudaError_t run_cc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(decode_cc_kernel<T, D, GMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
-    decode_cc_kernel<T, D, GMAX><<<grid, 128, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_cc_kernel<T, D, GMAX>, dim3(grid), dim3(128), smem, s, a);
 }
 
 template <int D>
@@ -827,8 +832,7 @@ cudaError_t run_tc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
     if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    decode_tc_kernel<D><<<grid, Tc<D>::kThreads, smem, s>>>(a, tmK, tmV);
-    return cudaGetLastError();
+    return launch_pdl(decode_tc_kernel<D>, dim3(grid), dim3(Tc<D>::kThreads), smem, s, a, tmK, tmV);
 }
 
 }  // namespace

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const uint4* __restric
                                                           uint4* __restrict__ kc, uint4* __restrict__ vc,
                                                           int64_t num_slots, int kv_heads, int vecs_per_row,
                                                           unsigned int* status) {
+    grid_dependency_wait();  // a block copy before us may target the same block
+    allow_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < 2 * per_pool;
          idx += stride) {
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const int64_t* __restric
                                                         uint4* __restrict__ kc, uint4* __restrict__ vc,
                                                         int64_t num_blocks, int64_t block_vecs,
                                                         unsigned int* status) {
+    grid_dependency_wait();
+    allow_dependents();
     const int64_t per_pair = 2 * block_vecs;
     const int64_t total = num_pairs * per_pair;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -125,19 +129,18 @@ cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, in
                           void* v_cache, const pkv_cache_desc& d, unsigned int* status, cudaStream_t s) {
     const int vecs_per_row = d.head_dim * elem_bytes(d.dtype) / 16;
     const int64_t per_pool = num_tokens * d.num_kv_heads * vecs_per_row;
-    append_kernel<<<grid_for(2 * per_pool, kThreads), kThreads, 0, s>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, per_pool, static_cast<uint4*>(k_cache),
-        static_cast<uint4*>(v_cache), d.num_blocks * 16, d.num_kv_heads, vecs_per_row, status);
-    return cudaGetLastError();
+    return launch_pdl(append_kernel, dim3(grid_for(2 * per_pool, kThreads)), dim3(kThreads), 0, s,
+                      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, per_pool,
+                      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), d.num_blocks * 16, d.num_kv_heads,
+                      vecs_per_row, status);
 }
 
 cudaError_t launch_copy_blocks(const int64_t* pairs, int64_t num_pairs, void* k_cache, void* v_cache,
                                const pkv_cache_desc& d, unsigned int* status, cudaStream_t s) {
     const int64_t block_vecs = static_cast<int64_t>(d.num_kv_heads) * 16 * d.head_dim * elem_bytes(d.dtype) / 16;
-    copy_kernel<<<grid_for(num_pairs * 2 * block_vecs, kThreads), kThreads, 0, s>>>(
-        pairs, num_pairs, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), d.num_blocks, block_vecs,
-        status);
-    return cudaGetLastError();
+    return launch_pdl(copy_kernel, dim3(grid_for(num_pairs * 2 * block_vecs, kThreads)), dim3(kThreads), 0, s,
+                      pairs, num_pairs, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), d.num_blocks,
+                      block_vecs, status);
 }
 
 cudaError_t launch_check_slots(const int64_t* slots, int64_t n, int64_t num_slots, unsigned int* verdict,
