@@ -46,16 +46,24 @@ def _compile(src: str, obj: str, extra: list[str]) -> tuple[str, int, str]:
     return src, p.returncode, (p.stdout + p.stderr)
 
 
-def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
-    """Compile and link ``libpkv.so``; returns its path. Raises on failure."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False,
+          defines: dict | None = None, out_dir: str | None = None) -> str:
+    """Compile and link ``libpkv.so``; returns its path. Raises on failure.
+
+    ``defines`` adds ``-D`` build-time knobs (e.g. ``{"PKV_TC_STAGES": 12}``);
+    with ``out_dir`` the objects and the library go there instead of in-tree.
+    """
+    build_dir = BUILD if out_dir is None else os.path.join(out_dir, "_build")
+    lib_path = LIB if out_dir is None else os.path.join(out_dir, "libpkv.so")
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_time = _newest_header()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra += [f"-D{k}={v}" for k, v in (defines or {}).items()]
     jobs = []
     objs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         stale = force or ptxas_info or not os.path.exists(obj) or \
             os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_time)
@@ -68,13 +76,13 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
                     sys.stderr.write(f"== {os.path.basename(src)} (rc={rc})\n{log}")
                 if rc:
                     raise RuntimeError(f"nvcc failed on {src}")
-    if jobs or force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        cmd = [_nvcc(), *ARCH, "-shared", "-o", LIB, *objs, "-lcuda"] if False else \
-            [_nvcc(), *ARCH, "-shared", "-o", LIB, *objs]
+    if jobs or force or not os.path.exists(lib_path) or \
+            os.path.getmtime(lib_path) < max(os.path.getmtime(o) for o in objs):
+        cmd = [_nvcc(), *ARCH, "-shared", "-o", lib_path, *objs]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode:
             raise RuntimeError("link failed:\n" + p.stdout + p.stderr)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -336,9 +336,15 @@ __device__ void zero_empty_rows(const int32_t* s_len, const DecodeArgs& a, int t
 }
 
 // ------------------------------------------------------------------ tensor-core kernel
+// Depth of the shared-memory ring of the tensor-core kernel (blocks in flight
+// per CTA); a build-time tuning knob.
+#ifndef PKV_TC_STAGES
+#define PKV_TC_STAGES 8
+#endif
+
 template <int D>
 struct Tc {
-    static constexpr int kStages = 8;
+    static constexpr int kStages = PKV_TC_STAGES;
     static constexpr int kConsumers = 4;
     static constexpr int kThreads = (kConsumers + 1) * 32;
     static constexpr int kHalves = D / 64;                  // 64-column TMA boxes per row
