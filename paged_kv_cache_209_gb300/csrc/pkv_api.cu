@@ -208,6 +208,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
         a.out = static_cast<char*>(out) + b0 * row;
         a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.partials_offset);
         a.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + wl.counters_offset);
+        a.trace = wl.trace_offset ? static_cast<char*>(workspace) + wl.trace_offset : nullptr;
         a.status = status;
         a.num_blocks = desc->num_blocks;
         a.max_blocks = max_blocks_per_seq;

@@ -47,6 +47,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Build-time tracing (PKV_TRACE): each CTA of the tensor-core kernel records
+// %globaltimer stamps in a per-CTA row of 8 words placed after the piece
+// slots in the workspace: [0] entry, [1] prologue done, [2] first copy
+// issued, [3] first block received, [4] last block consumed, [5] exit.
+#ifdef PKV_TRACE
+#define PKV_STAMP(a, cta, i) (reinterpret_cast<unsigned long long*>((a).trace))[(cta) * 8 + (i)] = global_ns()
+#else
+#define PKV_STAMP(a, cta, i) ((void)0)
+#endif
+
 // ------------------------------------------------------------------ schedule
 // s_pre[i] = sum_{i' <= i} ceil(len_i' / 16) over this launch's sequences,
 // s_len[i] = len_i clamped to [0, max_blocks * 16].
@@ -346,6 +356,11 @@ template <int D>
 struct Tc {
     static constexpr int kStages = PKV_TC_STAGES;
     static constexpr int kConsumers = 4;
+    // Unit k goes to stage k % kStages and to consumer warp k % kConsumers. A
+    // stage must always meet the same warp: otherwise a warp could wait on a
+    // stage two phases ahead of its last use, and a parity wait cannot tell
+    // those phases apart.
+    static_assert(kStages % kConsumers == 0, "ring depth must be a multiple of the consumer warps");
     static constexpr int kThreads = (kConsumers + 1) * 32;
     static constexpr int kHalves = D / 64;                  // 64-column TMA boxes per row
     static constexpr int kPoolBytes = 16 * D * 2;           // one block, one head, one pool
@@ -380,6 +395,7 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) PKV_STAMP(a, blockIdx.x, 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -399,6 +415,7 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
     grid_dependency_wait();
     allow_dependents();
     build_prefix(s_pre, s_len, a.lens, a.batch, a.max_blocks, a.status);  // contains __syncthreads
+    if (threadIdx.x == 0) PKV_STAMP(a, blockIdx.x, 1);
 
     const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
     const long long cta = blockIdx.x;
@@ -439,6 +456,7 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
 #pragma unroll
                             for (int hf = 0; hf < C::kHalves; ++hf)
                                 tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s]);
+                            if (k == 0) PKV_STAMP(a, blockIdx.x, 2);
                         } else {
                             stage_ok[s] = 0;
                             atomicOr(a.status, PKV_DEVERR_RANGE);
@@ -510,6 +528,7 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
             if (static_cast<int>(k & (C::kConsumers - 1)) != warp) continue;
             const int s = static_cast<int>(k % C::kStages);
             if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag)) return;
+            if (k == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 3);
             const int valid = min(16, n_ctx - blk * 16);
             if (stage_ok[s]) {
                 const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
@@ -618,8 +637,10 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
         if (write_piece<__nv_bfloat16, D>(bo, bm, bl, 8, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
         ++piece_idx;
     }
+    if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 4);
     // a warp's slice is G*D/4 <= 2*D elements: at most D/16 per lane
     signal_pending<__nv_bfloat16, D, D / 16, 2>(pending, npending, G, a, U, warp, lane);
+    if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 5);
 }
 
 // ------------------------------------------------------------------ CUDA-core kernel
@@ -852,6 +873,12 @@ WorkspaceLayout decode_workspace_layout(int batch, int kv_heads, int num_ctas, i
     // per CTA: 2 piece slots x 4 warp slices x (G*D/4 values + G maxima + G sums)
     const size_t per_cta = 2 * 4 * (static_cast<size_t>(group) * head_dim / 4 + 2 * group) * sizeof(float);
     w.total = w.partials_offset + static_cast<size_t>(num_ctas) * per_cta;
+#ifdef PKV_TRACE
+    w.trace_offset = (w.total + 255) / 256 * 256;
+    w.total = w.trace_offset + static_cast<size_t>(num_ctas) * 64;
+#else
+    w.trace_offset = 0;
+#endif
     return w;
 }
 

@@ -38,6 +38,7 @@ struct DecodeArgs {
     void* out;
     float* partials;  // fp32 pieces of cut segments: [num_ctas][2 slots][4 warps][G*D/4 + 2G]
     int* counters;    // [batch][kv_heads][4 warps]; zero between calls
+    void* trace;      // per-CTA timestamps (PKV_TRACE builds only)
     unsigned int* status;
     int64_t num_blocks;
     int32_t max_blocks;
@@ -64,7 +65,7 @@ constexpr int kMaxBatchPerLaunch = 1024;
 
 // Workspace: 256-byte header (reserved), merge counters, piece slots.
 struct WorkspaceLayout {
-    size_t counters_offset, partials_offset, total;
+    size_t counters_offset, partials_offset, trace_offset, total;
 };
 WorkspaceLayout decode_workspace_layout(int batch, int kv_heads, int num_ctas, int group, int head_dim);
 int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t max_blocks,
