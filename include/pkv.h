@@ -196,6 +196,39 @@ PKV_API pkv_status pkv_decode_attention(const void* q, const void* k_cache, cons
                                 const pkv_decode_opts* opts, void* stream);
 
 /*
+ * pkv_decode_attention_noalloc -- pkv_decode_attention without a
+ * caller-provided workspace. The pages have no counterpart to this call; it
+ * exists for callers that cannot allocate device memory: plugins running
+ * inside a framework whose memory pool they do not own, latency-critical
+ * paths that cannot take cudaMalloc's implicit synchronisation, deployments
+ * with a device-memory budget fixed at start-up.
+ *
+ * Arguments, results and errors are those of pkv_decode_attention, minus
+ * `workspace` / `workspace_bytes`. The workspace is a fixed array of
+ * PKV_NOALLOC_SCRATCH_BYTES inside the library, held in device memory by
+ * every GPU that loads the library until the process exits. A call whose
+ * workspace (pkv_decode_workspace_size) would exceed it returns
+ * PKV_ERR_WORKSPACE and writes nothing.
+ *
+ *  - The call allocates nothing: no cudaMalloc, cudaFree or allocating
+ *    library routine. It clears the array's merge counters with one
+ *    cudaMemsetAsync on `stream` before the kernel.
+ *  - Every call on a device shares the one array: calls that can overlap on
+ *    the GPU (different streams without ordering between them) race and give
+ *    wrong results. Order them, e.g. issue them on one stream.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture begins.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+PKV_API pkv_status pkv_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                const int32_t* context_lens, int32_t batch,
+                                                int32_t num_q_heads, float scale, void* out,
+                                                const pkv_cache_desc* desc, uint32_t flags,
+                                                const pkv_decode_opts* opts, void* stream);
+
+/*
  * pkv_device_status -- read (and with clear != 0, reset) the sticky device
  * status of the current device: an OR of PKV_DEVERR_* bits set by kernels
  * since the last clear. Waits for `stream`. Returns PKV_OK or PKV_ERR_CUDA.

@@ -46,7 +46,10 @@ class DecodeOpts(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("pkv_append", "pkv_copy_blocks", "pkv_decode_workspace_size", "pkv_decode_attention",
-           "pkv_device_status", "pkv_status_string", "pkv_version")
+           "pkv_decode_attention_noalloc", "pkv_device_status", "pkv_status_string", "pkv_version")
+
+# Size of the library's built-in workspace used by pkv_decode_attention_noalloc.
+PKV_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -68,6 +71,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_decode_attention.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp,
                                          ctypes.c_size_t, desc_p, u32, opts_p, vp]
     lib.pkv_decode_attention.restype = ctypes.c_int
+    lib.pkv_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp,
+                                                 desc_p, u32, opts_p, vp]
+    lib.pkv_decode_attention_noalloc.restype = ctypes.c_int
     lib.pkv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, vp]
     lib.pkv_device_status.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -187,6 +193,29 @@ def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale:
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
         q_heads, ctypes.c_float(scale), _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags,
         _opts(kernel, num_ctas), _stream(stream)))
+    return out
+
+
+def pkv_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=None,
+                                 flags: int = 0, kernel: int = 0, num_ctas: int = 0, stream=None):
+    """Decode attention on the library's built-in workspace (no device allocation
+    by the library; ``out`` is allocated here only when the caller passes none)."""
+    lib = load_library()
+    _same_pools(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    batch, q_heads, d = q.shape
+    if d != desc.head_dim or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [batch][q_heads][head_dim] of the pool dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens are int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != batch or context_lens.shape != (batch,):
+        raise ValueError("block_tables is [batch][max_blocks], context_lens [batch]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pkv_decode_attention_noalloc", lib.pkv_decode_attention_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        batch, q_heads, ctypes.c_float(scale), _ptr(out), ctypes.byref(desc), flags, _opts(kernel, num_ctas),
+        _stream(stream)))
     return out
 
 
