@@ -346,15 +346,12 @@ __device__ void zero_empty_rows(const int32_t* s_len, const DecodeArgs& a, int t
 }
 
 // ------------------------------------------------------------------ tensor-core kernel
-// Depth of the shared-memory ring of the tensor-core kernel (blocks in flight
-// per CTA); a build-time tuning knob.
-#ifndef PKV_TC_STAGES
-#define PKV_TC_STAGES 8
-#endif
-
-template <int D>
+// Tensor-core kernel configuration. NST is the depth of the shared-memory ring
+// (blocks in flight per CTA); the host picks the deepest ring that still fits
+// two CTAs per SM.
+template <int D, int NST>
 struct Tc {
-    static constexpr int kStages = PKV_TC_STAGES;
+    static constexpr int kStages = NST;
     static constexpr int kConsumers = 4;
     // Unit k goes to stage k % kStages and to consumer warp k % kConsumers. A
     // stage must always meet the same warp: otherwise a warp could wait on a
@@ -365,32 +362,37 @@ struct Tc {
     static constexpr int kHalves = D / 64;                  // 64-column TMA boxes per row
     static constexpr int kPoolBytes = 16 * D * 2;           // one block, one head, one pool
     static constexpr int kStageBytes = 2 * kPoolBytes;      // K then V
-    static constexpr int kScratchFloats = 2 * kConsumers * 8 * D;  // double-buffered O
-    // shared memory layout (offsets from a 1024-byte aligned base)
+    // shared memory layout (offsets from a 1024-byte aligned base): the ring,
+    // then full[NST], empty[NST], merge and free barriers, stage flags and the
+    // abort flag, then the combine scratch (4 warps x G x (D + 2) floats) and
+    // the per-sequence prefix sums and lengths.
     static constexpr int kOffBars = kStages * kStageBytes;
-    static constexpr int kOffFlags = kOffBars + (2 * kStages + 1) * 8;
+    static constexpr int kOffFlags = kOffBars + (2 * kStages + 2) * 8;
     static constexpr int kOffScratch = ((kOffFlags + kStages * 4 + 4 + 15) / 16) * 16;
-    static constexpr int kOffML = kOffScratch + kScratchFloats * 4;
-    static constexpr int kOffPre = kOffML + 2 * 2 * kConsumers * 8 * 4;
-    static size_t smem_bytes(int batch) { return 1024 + kOffPre + 2 * static_cast<size_t>(batch) * 4; }
+    static constexpr size_t scratch_floats(int G) { return static_cast<size_t>(kConsumers) * G * (D + 2); }
+    static size_t smem_bytes(int G, int batch) {
+        return 1024 + kOffScratch + scratch_floats(G) * 4 + 2 * static_cast<size_t>(batch) * 4;
+    }
 };
 
-template <int D>
-__global__ void __launch_bounds__(Tc<D>::kThreads, 2)
+template <int D, int NST>
+__global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
-    using C = Tc<D>;
+    using C = Tc<D, NST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
     uint64_t* empty = full + C::kStages;
-    uint64_t* merge_bar = empty + C::kStages;
+    uint64_t* merge_bar = empty + C::kStages;  // all four warps published their piece state
+    uint64_t* free_bar = merge_bar + 1;        // all four warps finished reading it
     int* stage_ok = reinterpret_cast<int*>(smem + C::kOffFlags);
     volatile int* abort_flag = stage_ok + C::kStages;
-    float* sm_o = reinterpret_cast<float*>(smem + C::kOffScratch);
-    float* sm_m = reinterpret_cast<float*>(smem + C::kOffML);          // [2][4][8]
-    float* sm_l = sm_m + 2 * C::kConsumers * 8;                          // [2][4][8]
-    int32_t* s_pre = reinterpret_cast<int32_t*>(smem + C::kOffPre);
+    const int G = a.group;
+    float* sm_o = reinterpret_cast<float*>(smem + C::kOffScratch);      // [4][G][D]
+    float* sm_m = sm_o + C::kConsumers * G * D;                          // [4][G]
+    float* sm_l = sm_m + C::kConsumers * G;                              // [4][G]
+    int32_t* s_pre = reinterpret_cast<int32_t*>(sm_l + C::kConsumers * G);
     int32_t* s_len = s_pre + a.batch;
 
     const int warp = threadIdx.x >> 5;
@@ -403,6 +405,7 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
             mbar_init(&empty[s], 1);
         }
         mbar_init(merge_bar, C::kConsumers);
+        mbar_init(free_bar, C::kConsumers);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -421,7 +424,6 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
     const long long cta = blockIdx.x;
     const long long ua = range_start(cta, U, a.num_ctas);
     const long long ub = range_start(cta + 1, U, a.num_ctas);
-    const int G = a.group;
 
     if (warp == C::kConsumers) {
         // ------------------------------------------------ producer warp
@@ -608,33 +610,40 @@ __global__ void __launch_bounds__(Tc<D>::kThreads, 2)
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
-        const int buf = piece_idx & 1;
-        float* bo = sm_o + buf * (C::kConsumers * 8 * D);
-        float* bm = sm_m + buf * (C::kConsumers * 8);
-        float* bl = sm_l + buf * (C::kConsumers * 8);
+        // the single scratch buffer is free once every warp has read the
+        // previous piece's states
+        if (piece_idx > 0 &&
+            !mbar_wait(free_bar, static_cast<uint32_t>((piece_idx - 1) & 1), a.status, abort_flag))
+            return;
         const int g0 = 2 * tig, g1 = 2 * tig + 1;
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) {
             const int d = 16 * i + gid;
             if (g0 < G) {
-                bo[(warp * 8 + g0) * D + d] = o[i][0];
-                bo[(warp * 8 + g0) * D + d + 8] = o[i][2];
+                sm_o[(warp * G + g0) * D + d] = o[i][0];
+                sm_o[(warp * G + g0) * D + d + 8] = o[i][2];
             }
             if (g1 < G) {
-                bo[(warp * 8 + g1) * D + d] = o[i][1];
-                bo[(warp * 8 + g1) * D + d + 8] = o[i][3];
+                sm_o[(warp * G + g1) * D + d] = o[i][1];
+                sm_o[(warp * G + g1) * D + d + 8] = o[i][3];
             }
         }
         if (gid == 0) {
-            bm[warp * 8 + g0] = m0;
-            bm[warp * 8 + g1] = m1;
-            bl[warp * 8 + g0] = l0;
-            bl[warp * 8 + g1] = l1;
+            if (g0 < G) {
+                sm_m[warp * G + g0] = m0;
+                sm_l[warp * G + g0] = l0;
+            }
+            if (g1 < G) {
+                sm_m[warp * G + g1] = m1;
+                sm_l[warp * G + g1] = l1;
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_bar);
         if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
-        if (write_piece<__nv_bfloat16, D>(bo, bm, bl, 8, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
+        if (write_piece<__nv_bfloat16, D>(sm_o, sm_m, sm_l, G, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(free_bar);
         ++piece_idx;
     }
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 4);
@@ -828,9 +837,9 @@ int cached_occupancy(int kernel_id, int variant, size_t smem, int threads, const
     return n;
 }
 
-template <int D>
+template <int D, int NST>
 int tc_query(const void*, int threads, size_t smem) {
-    return occupancy(decode_tc_kernel<D>, threads, smem);
+    return occupancy(decode_tc_kernel<D, NST>, threads, smem);
 }
 template <typename T, int D, int GMAX>
 int cc_query(const void*, int threads, size_t smem) {
@@ -852,14 +861,15 @@ cudaError_t run_cc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
     return launch_pdl(decode_cc_kernel<T, D, GMAX>, dim3(grid), dim3(128), smem, s, a);
 }
 
-template <int D>
+template <int D, int NST>
 cudaError_t run_tc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
     CUtensorMap tmK, tmV;
     const int64_t rows = a.num_blocks * a.kv_heads * 16;
     if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
         return cudaErrorInvalidValue;
-    cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    return launch_pdl(decode_tc_kernel<D>, dim3(grid), dim3(Tc<D>::kThreads), smem, s, a, tmK, tmV);
+    cudaFuncSetAttribute(decode_tc_kernel<D, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    return launch_pdl(decode_tc_kernel<D, NST>, dim3(grid), dim3(Tc<D, NST>::kThreads), smem, s, a, tmK, tmV);
 }
 
 }  // namespace
@@ -896,14 +906,31 @@ int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t
     const int chunk = batch < kMaxBatchPerLaunch ? (batch < 1 ? 1 : batch) : kMaxBatchPerLaunch;
     int per_sm = 0;
     size_t smem = 0;
+    int stages = 0;
     if (kernel == 2) {
-        if (d.head_dim == 128) {
-            smem = Tc<128>::smem_bytes(chunk);
-            per_sm = cached_occupancy(2, 128, smem, Tc<128>::kThreads, nullptr, tc_query<128>);
-        } else {
-            smem = Tc<64>::smem_bytes(chunk);
-            per_sm = cached_occupancy(2, 64, smem, Tc<64>::kThreads, nullptr, tc_query<64>);
+        // the deepest ring that keeps two CTAs per SM (more blocks in flight)
+        const int want_st = opts ? opts->stages : 0;
+        for (int st : {12, 8}) {
+            if (want_st && want_st != st) continue;
+            size_t sm = 0;
+            int n = 0;
+            if (d.head_dim == 128) {
+                sm = st == 12 ? Tc<128, 12>::smem_bytes(G, chunk) : Tc<128, 8>::smem_bytes(G, chunk);
+                n = st == 12 ? cached_occupancy(2, 128 * 100 + st, sm, 160, nullptr, tc_query<128, 12>)
+                             : cached_occupancy(2, 128 * 100 + st, sm, 160, nullptr, tc_query<128, 8>);
+            } else {
+                sm = st == 12 ? Tc<64, 12>::smem_bytes(G, chunk) : Tc<64, 8>::smem_bytes(G, chunk);
+                n = st == 12 ? cached_occupancy(2, 64 * 100 + st, sm, 160, nullptr, tc_query<64, 12>)
+                             : cached_occupancy(2, 64 * 100 + st, sm, 160, nullptr, tc_query<64, 8>);
+            }
+            if (n >= 2 || want_st == st || st == 8) {
+                stages = st;
+                smem = sm;
+                per_sm = n;
+                break;
+            }
         }
+        if (stages == 0) return PKV_ERR_UNSUPPORTED;
     } else {
         const int gmax = G <= 8 ? 8 : 16;
         const int v = variant_of(d.dtype, d.head_dim, gmax);
@@ -924,6 +951,7 @@ int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t
     }
     if (per_sm < 1) per_sm = 1;
     plan->kernel = kernel;
+    plan->stages = stages;
     plan->smem = smem;
     plan->num_ctas = (opts && opts->num_ctas > 0) ? opts->num_ctas : device_sm_count() * per_sm;
     return PKV_OK;
@@ -933,7 +961,12 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
     cudaError_t err = cudaSuccess;
     const int D = a.head_dim;
     if (plan.kernel == 2) {
-        err = D == 128 ? run_tc<128>(a, plan.num_ctas, plan.smem, s) : run_tc<64>(a, plan.num_ctas, plan.smem, s);
+        if (D == 128)
+            err = plan.stages == 12 ? run_tc<128, 12>(a, plan.num_ctas, plan.smem, s)
+                                    : run_tc<128, 8>(a, plan.num_ctas, plan.smem, s);
+        else
+            err = plan.stages == 12 ? run_tc<64, 12>(a, plan.num_ctas, plan.smem, s)
+                                    : run_tc<64, 8>(a, plan.num_ctas, plan.smem, s);
     } else {
         const bool g16 = a.group > 8;
         if (a.dtype == PKV_F32) {

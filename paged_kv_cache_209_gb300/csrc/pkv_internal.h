@@ -55,6 +55,7 @@ struct DecodeArgs {
 // Which kernel a decode call runs and on how many CTAs.
 struct DecodePlan {
     int kernel;    // 1 CUDA-core, 2 tensor-core
+    int stages;    // ring depth of the tensor-core kernel
     int num_ctas;  // CTAs of the split kernel
     size_t smem;   // dynamic shared memory of the split kernel
 };

@@ -40,7 +40,7 @@ class CacheDesc(ctypes.Structure):
 
 
 class DecodeOpts(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32)]
+    _fields_ = [("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32)]
 
 
 _lib = None
@@ -155,23 +155,24 @@ def pkv_copy_blocks(src_dst_pairs, k_cache, v_cache, flags: int = 0, stream=None
                                                   _ptr(v_cache), ctypes.byref(desc), flags, _stream(stream)))
 
 
-def _opts(kernel: int, num_ctas: int):
-    if kernel == 0 and num_ctas == 0:
+def _opts(kernel: int, num_ctas: int, stages: int = 0):
+    if kernel == 0 and num_ctas == 0 and stages == 0:
         return None
-    return ctypes.byref(DecodeOpts(kernel, num_ctas))
+    return ctypes.byref(DecodeOpts(kernel, num_ctas, stages))
 
 
 def pkv_decode_workspace_size(batch: int, num_q_heads: int, max_blocks_per_seq: int, k_cache,
-                              kernel: int = 0, num_ctas: int = 0) -> int:
+                              kernel: int = 0, num_ctas: int = 0, stages: int = 0) -> int:
     """Workspace bytes; allocate them zero-filled (``torch.zeros``) and reuse them."""
     lib = load_library()
     desc = cache_desc(k_cache)
     return int(lib.pkv_decode_workspace_size(batch, num_q_heads, max_blocks_per_seq, ctypes.byref(desc),
-                                             _opts(kernel, num_ctas)))
+                                             _opts(kernel, num_ctas, stages)))
 
 
 def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=None,
-                         workspace=None, flags: int = 0, kernel: int = 0, num_ctas: int = 0, stream=None):
+                         workspace=None, flags: int = 0, kernel: int = 0, num_ctas: int = 0, stages: int = 0,
+                         stream=None):
     """Decode attention; returns ``out`` ([batch][q_heads][head_dim], q's dtype)."""
     lib = load_library()
     _same_pools(k_cache, v_cache)
@@ -186,13 +187,13 @@ def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale:
     max_blocks = int(block_tables.shape[1])
     if out is None:
         out = torch.empty_like(q)
-    need = pkv_decode_workspace_size(batch, q_heads, max_blocks, k_cache, kernel, num_ctas)
+    need = pkv_decode_workspace_size(batch, q_heads, max_blocks, k_cache, kernel, num_ctas, stages)
     if workspace is None:
         workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
     _check("pkv_decode_attention", lib.pkv_decode_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
         q_heads, ctypes.c_float(scale), _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags,
-        _opts(kernel, num_ctas), _stream(stream)))
+        _opts(kernel, num_ctas, stages), _stream(stream)))
     return out
 
 

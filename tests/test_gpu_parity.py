@@ -316,3 +316,15 @@ def test_workspace_reuse_leaves_counters_zero(pkv, num_ctas):
     assert torch.count_nonzero(counters).item() == 0
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
     check_close(outs[0], oracle_attention(c, c["tables"], c["lens"]))
+
+
+@pytest.mark.parametrize("stages", [8, 12])
+@pytest.mark.parametrize("shape", [0, 1, 2])
+def test_ring_depths_agree(pkv, stages, shape):
+    """Both ring depths of the tensor-core kernel give the oracle's result
+    (the planner picks one; both must be correct)."""
+    lens, qh, kvh, d = SHAPES[shape]
+    c = cases.random_case(40 + shape, lens, qh, kvh, d, torch.bfloat16, poison=True)
+    got = run_attention(pkv, dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]), c["tables"], c["lens"],
+                        c["scale"], kernel=2, stages=stages, num_ctas=37)
+    check_close(got, oracle_attention(c, c["tables"], c["lens"]))
