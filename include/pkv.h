@@ -95,7 +95,7 @@ typedef struct {
                            at most 8 query heads per KV head               */
     int32_t num_ctas;   /* 0 = one wave of resident CTAs; > 0 forces that
                            many CTAs (tests use it to force context splits) */
-    int32_t stages;     /* tensor-core kernel ring depth: 0 = choose, 8 or 12 */
+    int32_t stages;     /* tensor-core kernel ring depth: 0 = default (8), 8 or 12 */
 } pkv_decode_opts;
 
 /*

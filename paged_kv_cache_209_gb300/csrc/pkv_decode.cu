@@ -207,7 +207,7 @@ __device__ __forceinline__ int pieces_of_segment(long long c0, long long c1, lon
 // shared memory (sm_o[(w*gstride + g)*D + d], sm_m/sm_l[w*gstride + g]).
 // A whole segment is normalised and written out directly. A cut segment's
 // piece goes to this CTA's slot in the workspace; it is announced later by
-// signal_piece. Returns true for a cut segment.
+// signal_pending. Returns true for a cut segment.
 template <typename T, int D>
 __device__ bool write_piece(const float* sm_o, const float* sm_m, const float* sm_l, int gstride, int G,
                             const Piece& pc, const DecodeArgs& a, long long cta, int warp, int lane) {
@@ -250,87 +250,152 @@ __device__ bool write_piece(const float* sm_o, const float* sm_m, const float* s
     return true;
 }
 
-// Announce a written piece of a cut segment (the caller has fenced its
-// writes): bump the segment's counter for this warp's slice; the warp that
-// brings it to the number of pieces merges every piece of its slice by
-// log-sum-exp weights, writes the output and puts the counter back to zero
-// for the next call.
-//
-// The merge runs at the tail of the kernel, so it is written for latency:
-// a lane owns NPER elements of the slice and issues the loads of CHUNK pieces
-// x NPER elements before it uses any of them (one round trip per CHUNK
-// pieces instead of one per piece and element).
-template <typename T, int D, int NPER, int CHUNK>
-__device__ void signal_piece(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane) {
+// CTA holding piece p (0-based) of the segment that starts at unit S0 and
+// whose first piece is in CTA c0. With at least one unit per CTA every range
+// is non-empty, so pieces sit in consecutive CTAs; with fewer units than CTAs
+// every non-empty range holds one unit, so piece p is unit S0 + p's CTA.
+__device__ __forceinline__ long long piece_cta(long long S0, long long c0, int p, long long U, long long C) {
+    return U >= C ? c0 + p : cta_of(S0 + p, U, C);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Merge every piece of this warp's slice of a cut segment and write the
+// output row. Runs at the tail of the kernel, so it is written for latency,
+// in rounds of up to 32 pieces:
+//   1. lane p loads piece p's maxima and sums for the (at most three) heads
+//      of the slice; warp reductions give the new running maxima and sums
+//      (one load round trip);
+//   2. with the weights known, each lane accumulates its NPER elements over
+//      the pieces, four pieces' loads in flight at a time.
+template <typename T, int D, int NPER, int NG>
+__device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane,
+                            long long c0, int slot0, int npieces) {
     const int S = G * D / 4;
     const int e0 = warp * S;
     const long long C = a.num_ctas;
-    const long long S0 = pc.seg_start, S1 = pc.seg_start + pc.seg_len;
-    const long long c0 = cta_of(S0, U, C), c1 = cta_of(S1 - 1, U, C);
-    const int npieces = pieces_of_segment(c0, c1, U, C);
-    int* counter = a.counters + (static_cast<long long>(pc.seq) * a.kv_heads + pc.head) * 4 + warp;
-    int last = 0;
-    if (lane == 0) last = atomicAdd(counter, 1) == npieces - 1;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
-    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
-    const int slot0 = (S0 == range_start(c0, U, C)) ? 0 : 1;
-    float M[NPER], O[NPER], L[NPER];
+    const int g_first = e0 / D;
+    const int ng = (e0 + S - 1) / D - g_first + 1;  // heads of the slice, <= NG
+    float M[NG], L[NG], O[NPER];
 #pragma unroll
-    for (int j = 0; j < NPER; ++j) {
-        M[j] = neg_inf();
-        O[j] = 0.f;
-        L[j] = 0.f;
+    for (int k = 0; k < NG; ++k) {
+        M[k] = neg_inf();
+        L[k] = 0.f;
     }
-    for (long long cb = c0; cb <= c1; cb += CHUNK) {
-        float mv[CHUNK][NPER], ov[CHUNK][NPER], lv[CHUNK][NPER];
 #pragma unroll
-        for (int q = 0; q < CHUNK; ++q) {
-            // CTA cb+q holds a piece unless it is past c1 or its range is empty
-            const long long cq = cb + q;
-            const bool has = cq <= c1 && (cq == c0 || range_start(cq, U, C) < range_start(cq + 1, U, C));
-            const float* pq = piece_slice(a.partials, has ? cq : c0, cq == c0 ? slot0 : 0, warp, S, G);
+    for (int j = 0; j < NPER; ++j) O[j] = 0.f;
+    for (int base = 0; base < npieces; base += 32) {
+        const int p = base + lane;
+        const bool live = p < npieces;
+        const float* mine =
+            live ? piece_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, S, G)
+                 : a.partials;
+        float wp[NG];
 #pragma unroll
-            for (int j = 0; j < NPER; ++j) {
-                const int e = lane + 32 * j;   // element index within the slice
-                const bool live = has && e < S;
-                const int g = (e0 + e) / D;
-                mv[q][j] = live ? __ldcg(pq + S + g) : neg_inf();
-                ov[q][j] = live ? __ldcg(pq + e) : 0.f;
-                lv[q][j] = live ? __ldcg(pq + S + G + g) : 0.f;
-            }
+        for (int k = 0; k < NG; ++k) {
+            const bool ok = live && k < ng;
+            const float mp = ok ? __ldcg(mine + S + g_first + k) : neg_inf();
+            const float lp = ok ? __ldcg(mine + S + G + g_first + k) : 0.f;
+            const float Mn = fmaxf(M[k], warp_max(mp));
+            const float base_k = (Mn == neg_inf()) ? 0.f : Mn;
+            const float sc = (M[k] == neg_inf()) ? 0.f : ex2(M[k] - base_k);
+            wp[k] = (mp == neg_inf()) ? 0.f : ex2(mp - base_k);
+            L[k] = L[k] * sc + warp_sum(wp[k] * lp);
+#pragma unroll
+            for (int j = 0; j < NPER; ++j)
+                if ((e0 + lane + 32 * j) / D - g_first == k) O[j] *= sc;
+            M[k] = Mn;
         }
+        const int nq = min(32, npieces - base);
+        for (int q = 0; q < nq; q += 4) {
+            float w[4][NG];
+            const float* ptr[4];
+            float ov[4][NPER];
 #pragma unroll
-        for (int q = 0; q < CHUNK; ++q)
+            for (int u = 0; u < 4; ++u) {
+                const bool ok = q + u < nq;
+                const int src = (q + u) & 31;
 #pragma unroll
-            for (int j = 0; j < NPER; ++j) {
-                if (mv[q][j] == neg_inf()) continue;
-                const float Mn = fmaxf(M[j], mv[q][j]);
-                const float ws = (M[j] == neg_inf()) ? 0.f : ex2(M[j] - Mn);
-                const float wp = ex2(mv[q][j] - Mn);
-                O[j] = O[j] * ws + ov[q][j] * wp;
-                L[j] = L[j] * ws + lv[q][j] * wp;
-                M[j] = Mn;
+                for (int k = 0; k < NG; ++k) w[u][k] = __shfl_sync(0xffffffffu, ok ? wp[k] : 0.f, src);
+                ptr[u] = reinterpret_cast<const float*>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), src));
+#pragma unroll
+                for (int j = 0; j < NPER; ++j) {
+                    const int e = lane + 32 * j;
+                    ov[u][j] = (ok && e < S) ? __ldcg(ptr[u] + e) : 0.f;
+                }
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int j = 0; j < NPER; ++j) {
+                    const int kj = (e0 + lane + 32 * j) / D - g_first;
+                    float wj = 0.f;
+#pragma unroll
+                    for (int k = 0; k < NG; ++k) wj = kj == k ? w[u][k] : wj;
+                    O[j] += wj * ov[u][j];
+                }
+        }
     }
+    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
         const int e = lane + 32 * j;
-        if (e < S) store_out<T>(out_row + e0 + e, L[j] > 0.f ? O[j] / L[j] : 0.f);
+        if (e >= S) continue;
+        const int kj = (e0 + e) / D - g_first;
+        float Lj = 0.f;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) Lj = kj == k ? L[k] : Lj;
+        store_out<T>(out_row + e0 + e, Lj > 0.f ? O[j] / Lj : 0.f);
     }
-    if (lane == 0) *counter = 0;
 }
 
 // After the CTA's last piece: fence this warp's piece writes once, then
-// announce the (at most two) cut pieces of the range, first and last.
-template <typename T, int D, int NPER, int CHUNK>
+// announce the (at most two) cut pieces of the range -- the counter updates
+// of both go out together. A warp whose update completes a segment's count
+// merges that segment's slice and puts the counter back to zero for the
+// next call.
+template <typename T, int D, int NPER, int NG>
 __device__ void signal_pending(const Piece* pending, int npending, int G, const DecodeArgs& a, long long U,
                                int warp, int lane) {
     if (npending == 0) return;
     __threadfence();
     __syncwarp();
-    for (int i = 0; i < npending; ++i) signal_piece<T, D, NPER, CHUNK>(pending[i], G, a, U, warp, lane);
+    const long long C = a.num_ctas;
+    long long c0s[2];
+    int nps[2];
+    int* counters[2];
+    int old[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        if (i >= npending) break;
+        const Piece& pc = pending[i];
+        c0s[i] = cta_of(pc.seg_start, U, C);
+        const long long c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
+        nps[i] = pieces_of_segment(c0s[i], c1, U, C);
+        counters[i] = a.counters + (static_cast<long long>(pc.seq) * a.kv_heads + pc.head) * 4 + warp;
+        if (lane == 0) old[i] = atomicAdd(counters[i], 1);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        if (i >= npending) break;
+        const int last = __shfl_sync(0xffffffffu, old[i] == nps[i] - 1 ? 1 : 0, 0);
+        if (!last) continue;
+        __threadfence();
+        const Piece& pc = pending[i];
+        const int slot0 = (pc.seg_start == range_start(c0s[i], U, C)) ? 0 : 1;
+        merge_slice<T, D, NPER, NG>(pc, G, a, U, warp, lane, c0s[i], slot0, nps[i]);
+        if (lane == 0) *counters[i] = 0;
+    }
 }
 
 // Rows of sequences with no tokens are zero; CTA c writes those of the
@@ -363,13 +428,14 @@ struct Tc {
     static constexpr int kPoolBytes = 16 * D * 2;           // one block, one head, one pool
     static constexpr int kStageBytes = 2 * kPoolBytes;      // K then V
     // shared memory layout (offsets from a 1024-byte aligned base): the ring,
-    // then full[NST], empty[NST], merge and free barriers, stage flags and the
-    // abort flag, then the combine scratch (4 warps x G x (D + 2) floats) and
-    // the per-sequence prefix sums and lengths.
+    // then full[NST], empty[NST], the merge barrier, stage flags and the abort
+    // flag, then the combine scratch (two buffers of 4 warps x G x (D + 2)
+    // floats, alternating between pieces) and the per-sequence prefix sums
+    // and lengths.
     static constexpr int kOffBars = kStages * kStageBytes;
     static constexpr int kOffFlags = kOffBars + (2 * kStages + 2) * 8;
     static constexpr int kOffScratch = ((kOffFlags + kStages * 4 + 4 + 15) / 16) * 16;
-    static constexpr size_t scratch_floats(int G) { return static_cast<size_t>(kConsumers) * G * (D + 2); }
+    static constexpr size_t scratch_floats(int G) { return 2 * static_cast<size_t>(kConsumers) * G * (D + 2); }
     static size_t smem_bytes(int G, int batch) {
         return 1024 + kOffScratch + scratch_floats(G) * 4 + 2 * static_cast<size_t>(batch) * 4;
     }
@@ -385,14 +451,12 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
     uint64_t* empty = full + C::kStages;
     uint64_t* merge_bar = empty + C::kStages;  // all four warps published their piece state
-    uint64_t* free_bar = merge_bar + 1;        // all four warps finished reading it
     int* stage_ok = reinterpret_cast<int*>(smem + C::kOffFlags);
     volatile int* abort_flag = stage_ok + C::kStages;
     const int G = a.group;
-    float* sm_o = reinterpret_cast<float*>(smem + C::kOffScratch);      // [4][G][D]
-    float* sm_m = sm_o + C::kConsumers * G * D;                          // [4][G]
-    float* sm_l = sm_m + C::kConsumers * G;                              // [4][G]
-    int32_t* s_pre = reinterpret_cast<int32_t*>(sm_l + C::kConsumers * G);
+    float* scratch = reinterpret_cast<float*>(smem + C::kOffScratch);   // 2 x {[4][G][D], [4][G], [4][G]}
+    const int buf_floats = C::kConsumers * G * (D + 2);
+    int32_t* s_pre = reinterpret_cast<int32_t*>(scratch + 2 * buf_floats);
     int32_t* s_len = s_pre + a.batch;
 
     const int warp = threadIdx.x >> 5;
@@ -405,7 +469,6 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
             mbar_init(&empty[s], 1);
         }
         mbar_init(merge_bar, C::kConsumers);
-        mbar_init(free_bar, C::kConsumers);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -610,11 +673,12 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
-        // the single scratch buffer is free once every warp has read the
-        // previous piece's states
-        if (piece_idx > 0 &&
-            !mbar_wait(free_bar, static_cast<uint32_t>((piece_idx - 1) & 1), a.status, abort_flag))
-            return;
+        // Alternate two scratch buffers: a warp can only be one piece ahead of
+        // the others (the merge barrier below), so it never overwrites a
+        // buffer that another warp still reads.
+        float* sm_o = scratch + (piece_idx & 1) * buf_floats;   // [4][G][D]
+        float* sm_m = sm_o + C::kConsumers * G * D;             // [4][G]
+        float* sm_l = sm_m + C::kConsumers * G;                 // [4][G]
         const int g0 = 2 * tig, g1 = 2 * tig + 1;
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) {
@@ -642,13 +706,12 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         if (lane == 0) mbar_arrive(merge_bar);
         if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
         if (write_piece<__nv_bfloat16, D>(sm_o, sm_m, sm_l, G, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(free_bar);
         ++piece_idx;
     }
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 4);
-    // a warp's slice is G*D/4 <= 2*D elements: at most D/16 per lane
-    signal_pending<__nv_bfloat16, D, D / 16, 2>(pending, npending, G, a, U, warp, lane);
+    // G <= 8: a warp's slice is G*D/4 <= 2*D elements, at most D/16 per lane
+    // and at most three heads
+    signal_pending<__nv_bfloat16, D, D / 16, 3>(pending, npending, G, a, U, warp, lane);
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 5);
 }
 
@@ -765,7 +828,7 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
         if (write_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
         __syncthreads();
     }
-    signal_pending<T, D, GMAX * D / 128, (GMAX > 8 ? 2 : 4)>(pending, npending, G, a, U, warp, lane);
+    signal_pending<T, D, GMAX * D / 128, GMAX / 4 + 1>(pending, npending, G, a, U, warp, lane);
 }
 
 // ------------------------------------------------------------------ host side
@@ -908,9 +971,10 @@ int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t
     size_t smem = 0;
     int stages = 0;
     if (kernel == 2) {
-        // the deepest ring that keeps two CTAs per SM (more blocks in flight)
+        // 8 stages by default (measured faster than 12 at two CTAs per SM on
+        // every workload); 12 on request
         const int want_st = opts ? opts->stages : 0;
-        for (int st : {12, 8}) {
+        for (int st : {8, 12}) {
             if (want_st && want_st != st) continue;
             size_t sm = 0;
             int n = 0;
@@ -923,7 +987,7 @@ int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t
                 n = st == 12 ? cached_occupancy(2, 64 * 100 + st, sm, 160, nullptr, tc_query<64, 12>)
                              : cached_occupancy(2, 64 * 100 + st, sm, 160, nullptr, tc_query<64, 8>);
             }
-            if (n >= 2 || want_st == st || st == 8) {
+            if (want_st == st || (want_st == 0 && st == 8)) {
                 stages = st;
                 smem = sm;
                 per_sm = n;

@@ -328,3 +328,22 @@ def test_ring_depths_agree(pkv, stages, shape):
     got = run_attention(pkv, dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]), c["tables"], c["lens"],
                         c["scale"], kernel=2, stages=stages, num_ctas=37)
     check_close(got, oracle_attention(c, c["tables"], c["lens"]))
+
+
+@pytest.mark.parametrize("kernel,q_heads,kv_heads,head_dim", [
+    (1, 32, 2, 128),   # G = 16: a warp slice spans four heads
+    (1, 12, 1, 64),    # G = 12
+    (1, 6, 1, 128),    # G = 6: slices cut heads in half
+    (2, 6, 1, 128),
+    (2, 3, 1, 64),     # G = 3
+    (2, 5, 1, 128),    # G = 5
+])
+def test_group_sizes_with_cut_segments(pkv, kernel, q_heads, kv_heads, head_dim):
+    """Group sizes whose warp slices do not align with heads, with segments
+    cut across many CTAs so that every piece goes through the merge."""
+    c = cases.random_case(50 + q_heads, [700, 33, 2000, 1], q_heads, kv_heads, head_dim, torch.bfloat16,
+                          poison=True)
+    for num_ctas in (1, 23, 181):
+        got = run_attention(pkv, dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]), c["tables"], c["lens"],
+                            c["scale"], kernel=kernel, num_ctas=num_ctas)
+        check_close(got, oracle_attention(c, c["tables"], c["lens"]))
