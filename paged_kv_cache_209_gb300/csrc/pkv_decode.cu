@@ -258,25 +258,34 @@ __device__ __forceinline__ long long piece_cta(long long S0, long long c0, int p
     return U >= C ? c0 + p : cta_of(S0 + p, U, C);
 }
 
-__device__ __forceinline__ float warp_max(float x) {
+// Loads of one piece for one lane: the lane's NPER accumulator elements and
+// the maxima / sums of the (at most NG) heads they belong to.
+template <int NPER, int NG>
+struct PieceVals {
+    float m[NG], l[NG], o[NPER];
+};
+
+template <int NPER, int NG>
+__device__ __forceinline__ void load_piece(PieceVals<NPER, NG>& v, const float* p, bool live, int S, int G,
+                                           int g_first, int ng, int lane) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
-    return x;
-}
-__device__ __forceinline__ float warp_sum(float x) {
+    for (int k = 0; k < NG; ++k) {
+        const bool ok = live && k < ng;
+        v.m[k] = ok ? __ldcg(p + S + g_first + k) : neg_inf();
+        v.l[k] = ok ? __ldcg(p + S + G + g_first + k) : 0.f;
+    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-    return x;
+    for (int j = 0; j < NPER; ++j) {
+        const int e = lane + 32 * j;
+        v.o[j] = (live && e < S) ? __ldcg(p + e) : 0.f;
+    }
 }
 
 // Merge every piece of this warp's slice of a cut segment and write the
-// output row. Runs at the tail of the kernel, so it is written for latency,
-// in rounds of up to 32 pieces:
-//   1. lane p loads piece p's maxima and sums for the (at most three) heads
-//      of the slice; warp reductions give the new running maxima and sums
-//      (one load round trip);
-//   2. with the weights known, each lane accumulates its NPER elements over
-//      the pieces, four pieces' loads in flight at a time.
+// output row. This runs at the tail of the kernel while other CTAs still
+// stream, when a load round trip costs microseconds, so the loop is
+// software-pipelined: the loads of the next two pieces are in flight while
+// the current two are combined (online log-sum-exp, per head).
 template <typename T, int D, int NPER, int NG>
 __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane,
                             long long c0, int slot0, int npieces) {
@@ -285,6 +294,9 @@ __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long lo
     const long long C = a.num_ctas;
     const int g_first = e0 / D;
     const int ng = (e0 + S - 1) / D - g_first + 1;  // heads of the slice, <= NG
+    int kj[NPER];                                   // head slot of each of the lane's elements
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) kj[j] = (e0 + lane + 32 * j) / D - g_first;
     float M[NG], L[NG], O[NPER];
 #pragma unroll
     for (int k = 0; k < NG; ++k) {
@@ -293,68 +305,52 @@ __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long lo
     }
 #pragma unroll
     for (int j = 0; j < NPER; ++j) O[j] = 0.f;
-    for (int base = 0; base < npieces; base += 32) {
-        const int p = base + lane;
-        const bool live = p < npieces;
-        const float* mine =
-            live ? piece_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, S, G)
-                 : a.partials;
-        float wp[NG];
+    auto ptr = [&](int p) {
+        return piece_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, S, G);
+    };
+    PieceVals<NPER, NG> cur[2], nxt[2];
 #pragma unroll
-        for (int k = 0; k < NG; ++k) {
-            const bool ok = live && k < ng;
-            const float mp = ok ? __ldcg(mine + S + g_first + k) : neg_inf();
-            const float lp = ok ? __ldcg(mine + S + G + g_first + k) : 0.f;
-            const float Mn = fmaxf(M[k], warp_max(mp));
-            const float base_k = (Mn == neg_inf()) ? 0.f : Mn;
-            const float sc = (M[k] == neg_inf()) ? 0.f : ex2(M[k] - base_k);
-            wp[k] = (mp == neg_inf()) ? 0.f : ex2(mp - base_k);
-            L[k] = L[k] * sc + warp_sum(wp[k] * lp);
+    for (int u = 0; u < 2; ++u) load_piece(cur[u], u < npieces ? ptr(u) : a.partials, u < npieces, S, G, g_first, ng, lane);
+    for (int p0 = 0; p0 < npieces; p0 += 2) {
 #pragma unroll
-            for (int j = 0; j < NPER; ++j)
-                if ((e0 + lane + 32 * j) / D - g_first == k) O[j] *= sc;
-            M[k] = Mn;
+        for (int u = 0; u < 2; ++u) {
+            const int p = p0 + 2 + u;
+            load_piece(nxt[u], p < npieces ? ptr(p) : a.partials, p < npieces, S, G, g_first, ng, lane);
         }
-        const int nq = min(32, npieces - base);
-        for (int q = 0; q < nq; q += 4) {
-            float w[4][NG];
-            const float* ptr[4];
-            float ov[4][NPER];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const bool ok = q + u < nq;
-                const int src = (q + u) & 31;
+        for (int u = 0; u < 2; ++u) {
+            float sc[NG], w[NG];
 #pragma unroll
-                for (int k = 0; k < NG; ++k) w[u][k] = __shfl_sync(0xffffffffu, ok ? wp[k] : 0.f, src);
-                ptr[u] = reinterpret_cast<const float*>(
-                    __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), src));
-#pragma unroll
-                for (int j = 0; j < NPER; ++j) {
-                    const int e = lane + 32 * j;
-                    ov[u][j] = (ok && e < S) ? __ldcg(ptr[u] + e) : 0.f;
-                }
+            for (int k = 0; k < NG; ++k) {
+                const float Mn = fmaxf(M[k], cur[u].m[k]);
+                const float base = (Mn == neg_inf()) ? 0.f : Mn;
+                sc[k] = (M[k] == neg_inf()) ? 0.f : ex2(M[k] - base);
+                w[k] = (cur[u].m[k] == neg_inf()) ? 0.f : ex2(cur[u].m[k] - base);
+                L[k] = L[k] * sc[k] + w[k] * cur[u].l[k];
+                M[k] = Mn;
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int j = 0; j < NPER; ++j) {
+                float scj = 0.f, wj = 0.f;
 #pragma unroll
-                for (int j = 0; j < NPER; ++j) {
-                    const int kj = (e0 + lane + 32 * j) / D - g_first;
-                    float wj = 0.f;
-#pragma unroll
-                    for (int k = 0; k < NG; ++k) wj = kj == k ? w[u][k] : wj;
-                    O[j] += wj * ov[u][j];
+                for (int k = 0; k < NG; ++k) {
+                    scj = kj[j] == k ? sc[k] : scj;
+                    wj = kj[j] == k ? w[k] : wj;
                 }
+                O[j] = O[j] * scj + wj * cur[u].o[j];
+            }
         }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) cur[u] = nxt[u];
     }
     T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
         const int e = lane + 32 * j;
         if (e >= S) continue;
-        const int kj = (e0 + e) / D - g_first;
         float Lj = 0.f;
 #pragma unroll
-        for (int k = 0; k < NG; ++k) Lj = kj == k ? L[k] : Lj;
+        for (int k = 0; k < NG; ++k) Lj = kj[j] == k ? L[k] : Lj;
         store_out<T>(out_row + e0 + e, Lj > 0.f ? O[j] / Lj : 0.f);
     }
 }
