@@ -50,7 +50,8 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // Build-time tracing (PKV_TRACE): each CTA of the tensor-core kernel records
 // %globaltimer stamps in a per-CTA row of 8 words placed after the piece
 // slots in the workspace: [0] entry, [1] prologue done, [2] first copy
-// issued, [3] first block received, [4] last block consumed, [5] exit.
+// issued, [3] first block received, [4] last block consumed, [5] exit,
+// [6] the SM the CTA ran on.
 #ifdef PKV_TRACE
 #define PKV_STAMP(a, cta, i) (reinterpret_cast<unsigned long long*>((a).trace))[(cta) * 8 + (i)] = global_ns()
 #else
@@ -458,6 +459,9 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) PKV_STAMP(a, blockIdx.x, 0);
+#ifdef PKV_TRACE
+    if (threadIdx.x == 0) reinterpret_cast<unsigned long long*>(a.trace)[blockIdx.x * 8 + 6] = sm_id();
+#endif
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -486,6 +490,9 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
 
     if (warp == C::kConsumers) {
         // ------------------------------------------------ producer warp
+        // K/V blocks are read once per call: stream them with evict-first so
+        // the block tables, q and the merge pieces stay in L2.
+        const uint64_t kv_policy = l2_evict_first_policy();
         Walker wk;
         wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
         long long k = 0;
@@ -513,10 +520,11 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
                             uint8_t* st = smem + s * C::kStageBytes;
                             const int y = (bid * a.kv_heads + pc.head) * 16;
 #pragma unroll
-                            for (int hf = 0; hf < C::kHalves; ++hf) tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s]);
+                            for (int hf = 0; hf < C::kHalves; ++hf)
+                                tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
 #pragma unroll
                             for (int hf = 0; hf < C::kHalves; ++hf)
-                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s]);
+                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
                             if (k == 0) PKV_STAMP(a, blockIdx.x, 2);
                         } else {
                             stage_ok[s] = 0;
