@@ -96,6 +96,7 @@ struct Piece {
     int blk_from, blk_to;  // blocks [from, to) of the sequence
     bool complete;         // the piece is the whole segment
     bool first;            // the piece opens this CTA's range
+    bool last;             // the piece closes this CTA's range
     long long seg_start;   // first unit of the segment
     int seg_len;           // units (blocks) of the segment
 };
@@ -140,6 +141,7 @@ struct Walker {
         p.blk_to = static_cast<int>(pe - s0);
         p.complete = (u == s0) && (pe == s1);
         p.first = (u == start);
+        p.last = (pe == end);
         p.seg_start = s0;
         p.seg_len = nb;
         u = pe;
@@ -200,55 +202,113 @@ __device__ __forceinline__ int pieces_of_segment(long long c0, long long c1, lon
     return n;
 }
 
-// Finish one segment piece for the elements of warp `warp`'s slice.
-//
+// ------------------------------------------------------------------ piece ends
 // The four consumer warps of a CTA each own a fixed slice of the G x D output
-// elements of the segment (S = G*D/4 elements; element e is head e / D, dim
-// e % D). The per-warp online-softmax states (O, m, l) of the piece are in
-// shared memory (sm_o[(w*gstride + g)*D + d], sm_m/sm_l[w*gstride + g]).
-// A whole segment is normalised and written out directly. A cut segment's
-// piece goes to this CTA's slot in the workspace; it is announced later by
-// signal_pending. Returns true for a cut segment.
-template <typename T, int D>
-__device__ bool write_piece(const float* sm_o, const float* sm_m, const float* sm_l, int gstride, int G,
-                            const Piece& pc, const DecodeArgs& a, long long cta, int warp, int lane) {
+// elements of a segment: S = G*D/4 elements, element e is head e / D, dim
+// e % D; lane `lane` holds elements e0 + lane + 32*j. A slice touches at most
+// NG heads (slot k is head g_first + k).
+
+template <int NPER, int NG>
+struct SliceState {
+    float o[NPER];       // unnormalised accumulators of the lane's elements
+    float m[NG], l[NG];  // running maximum (base 2) and sum per head of the slice
+};
+
+// One warp's slice of a piece, combined from the four warps' online-softmax
+// states in shared memory (sm_o[(w*gstride + g)*D + d], sm_m / sm_l[w*gstride
+// + g]).
+template <int D, int NPER, int NG>
+__device__ SliceState<NPER, NG> combine_slice(const float* sm_o, const float* sm_m, const float* sm_l, int gstride,
+                                              int G, int warp, int lane) {
     const int S = G * D / 4;
     const int e0 = warp * S;
-    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
-    float* slice = nullptr;
-    if (!pc.complete) slice = piece_slice(a.partials, cta, pc.first ? 0 : 1, warp, S, G);
-    for (int e = e0 + lane; e < e0 + S; e += 32) {
-        const int g = e / D;
-        const int d = e - g * D;
+    const int g_first = e0 / D;
+    const int ng = (e0 + S - 1) / D - g_first + 1;
+    SliceState<NPER, NG> st;
+    float wt[NG][4];
+#pragma unroll
+    for (int k = 0; k < NG; ++k) {
+        const int g = g_first + k;
         float M = neg_inf();
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * gstride + g]);
-        const float base = (M == neg_inf()) ? 0.f : M;
-        float o = 0.f, L = 0.f;
-        for (int w = 0; w < 4; ++w) {
-            const float mw = sm_m[w * gstride + g];
-            const float wt = (mw == neg_inf()) ? 0.f : ex2(mw - base);
-            o += wt * sm_o[(w * gstride + g) * D + d];
-            L += wt * sm_l[w * gstride + g];
-        }
-        if (pc.complete)
-            store_out<T>(out_row + e, L > 0.f ? o / L : 0.f);
-        else
-            slice[e - e0] = o;
-    }
-    if (pc.complete) return false;
-    if (lane < G) {
-        float M = neg_inf();
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * gstride + lane]);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, k < ng ? sm_m[w * gstride + g] : neg_inf());
         const float base = (M == neg_inf()) ? 0.f : M;
         float L = 0.f;
+#pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const float mw = sm_m[w * gstride + lane];
-            L += (mw == neg_inf()) ? 0.f : ex2(mw - base) * sm_l[w * gstride + lane];
+            const float mw = k < ng ? sm_m[w * gstride + g] : neg_inf();
+            wt[k][w] = (mw == neg_inf()) ? 0.f : ex2(mw - base);
+            L += (k < ng) ? wt[k][w] * sm_l[w * gstride + g] : 0.f;
         }
-        slice[S + lane] = M;
-        slice[S + G + lane] = L;
+        st.m[k] = M;
+        st.l[k] = L;
     }
-    return true;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        const int e = e0 + lane + 32 * j;
+        float o = 0.f;
+        if (e < e0 + S) {
+            const int g = e / D;
+            const int d = e - g * D;
+            const int kj = g - g_first;
+#pragma unroll
+            for (int k = 0; k < NG; ++k)
+                if (k == kj)
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) o += wt[k][w] * sm_o[(w * gstride + g) * D + d];
+        }
+        st.o[j] = o;
+    }
+    return st;
+}
+
+// Normalise a finished slice and write it to the output row.
+template <typename T, int D, int NPER, int NG>
+__device__ void write_out(const SliceState<NPER, NG>& st, const Piece& pc, int G, const DecodeArgs& a, int warp,
+                          int lane) {
+    const int S = G * D / 4;
+    const int e0 = warp * S;
+    const int g_first = e0 / D;
+    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        const int e = lane + 32 * j;
+        if (e >= S) continue;
+        const int kj = (e0 + e) / D - g_first;
+        float Lj = 0.f;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) Lj = kj == k ? st.l[k] : Lj;
+        store_out<T>(out_row + e0 + e, Lj > 0.f ? st.o[j] / Lj : 0.f);
+    }
+}
+
+// Store a slice as a piece in the workspace: S accumulators, then the maxima
+// and sums of the slice's heads (at index S + g and S + G + g).
+template <int D, int NPER, int NG>
+__device__ void store_slice(const SliceState<NPER, NG>& st, float* slice, int G, int warp, int lane) {
+    const int S = G * D / 4;
+    const int e0 = warp * S;
+    const int g_first = e0 / D;
+    const int ng = (e0 + S - 1) / D - g_first + 1;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        const int e = lane + 32 * j;
+        if (e < S) slice[e] = st.o[j];
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < NG; ++k)
+            if (k < ng) {
+                slice[S + g_first + k] = st.m[k];
+                slice[S + G + g_first + k] = st.l[k];
+            }
+    }
+}
+
+__device__ __forceinline__ int load_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // CTA holding piece p (0-based) of the segment that starts at unit S0 and
@@ -262,12 +322,7 @@ __device__ __forceinline__ long long piece_cta(long long S0, long long c0, int p
 // Loads of one piece for one lane: the lane's NPER accumulator elements and
 // the maxima / sums of the (at most NG) heads they belong to.
 template <int NPER, int NG>
-struct PieceVals {
-    float m[NG], l[NG], o[NPER];
-};
-
-template <int NPER, int NG>
-__device__ __forceinline__ void load_piece(PieceVals<NPER, NG>& v, const float* p, bool live, int S, int G,
+__device__ __forceinline__ void load_piece(SliceState<NPER, NG>& v, const float* p, bool live, int S, int G,
                                            int g_first, int ng, int lane) {
 #pragma unroll
     for (int k = 0; k < NG; ++k) {
@@ -282,53 +337,54 @@ __device__ __forceinline__ void load_piece(PieceVals<NPER, NG>& v, const float* 
     }
 }
 
-// Merge every piece of this warp's slice of a cut segment and write the
-// output row. This runs at the tail of the kernel while other CTAs still
-// stream, when a load round trip costs microseconds, so the loop is
-// software-pipelined: the loads of the next two pieces are in flight while
-// the current two are combined (online log-sum-exp, per head).
+// Merge the pieces of this warp's slice of a cut segment and write the output
+// row. `own` (if not null) is this CTA's piece, still in registers: its slot
+// in the workspace is not read. This runs at the tail of the kernel while
+// other CTAs still stream, when a load round trip costs microseconds, so the
+// loop is software-pipelined: the loads of the next two pieces are in flight
+// while the current two are combined (online log-sum-exp, per head).
 template <typename T, int D, int NPER, int NG>
-__device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane,
-                            long long c0, int slot0, int npieces) {
+__device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, long long c0, int slot0,
+                            int npieces, const SliceState<NPER, NG>* own, long long own_cta, int warp, int lane) {
     const int S = G * D / 4;
     const int e0 = warp * S;
     const long long C = a.num_ctas;
     const int g_first = e0 / D;
-    const int ng = (e0 + S - 1) / D - g_first + 1;  // heads of the slice, <= NG
-    int kj[NPER];                                   // head slot of each of the lane's elements
+    const int ng = (e0 + S - 1) / D - g_first + 1;
+    int kj[NPER];
 #pragma unroll
     for (int j = 0; j < NPER; ++j) kj[j] = (e0 + lane + 32 * j) / D - g_first;
-    float M[NG], L[NG], O[NPER];
+    SliceState<NPER, NG> acc;
 #pragma unroll
     for (int k = 0; k < NG; ++k) {
-        M[k] = neg_inf();
-        L[k] = 0.f;
+        acc.m[k] = own ? own->m[k] : neg_inf();
+        acc.l[k] = own ? own->l[k] : 0.f;
     }
 #pragma unroll
-    for (int j = 0; j < NPER; ++j) O[j] = 0.f;
+    for (int j = 0; j < NPER; ++j) acc.o[j] = own ? own->o[j] : 0.f;
+    auto live = [&](int p) { return p < npieces && !(own && piece_cta(pc.seg_start, c0, p, U, C) == own_cta); };
     auto ptr = [&](int p) {
-        return piece_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, S, G);
+        return p < npieces
+                   ? piece_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, S, G)
+                   : a.partials;
     };
-    PieceVals<NPER, NG> cur[2], nxt[2];
+    SliceState<NPER, NG> cur[2], nxt[2];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) load_piece(cur[u], u < npieces ? ptr(u) : a.partials, u < npieces, S, G, g_first, ng, lane);
+    for (int u = 0; u < 2; ++u) load_piece(cur[u], ptr(u), live(u), S, G, g_first, ng, lane);
     for (int p0 = 0; p0 < npieces; p0 += 2) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int p = p0 + 2 + u;
-            load_piece(nxt[u], p < npieces ? ptr(p) : a.partials, p < npieces, S, G, g_first, ng, lane);
-        }
+        for (int u = 0; u < 2; ++u) load_piece(nxt[u], ptr(p0 + 2 + u), live(p0 + 2 + u), S, G, g_first, ng, lane);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             float sc[NG], w[NG];
 #pragma unroll
             for (int k = 0; k < NG; ++k) {
-                const float Mn = fmaxf(M[k], cur[u].m[k]);
+                const float Mn = fmaxf(acc.m[k], cur[u].m[k]);
                 const float base = (Mn == neg_inf()) ? 0.f : Mn;
-                sc[k] = (M[k] == neg_inf()) ? 0.f : ex2(M[k] - base);
+                sc[k] = (acc.m[k] == neg_inf()) ? 0.f : ex2(acc.m[k] - base);
                 w[k] = (cur[u].m[k] == neg_inf()) ? 0.f : ex2(cur[u].m[k] - base);
-                L[k] = L[k] * sc[k] + w[k] * cur[u].l[k];
-                M[k] = Mn;
+                acc.l[k] = acc.l[k] * sc[k] + w[k] * cur[u].l[k];
+                acc.m[k] = Mn;
             }
 #pragma unroll
             for (int j = 0; j < NPER; ++j) {
@@ -338,61 +394,98 @@ __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long lo
                     scj = kj[j] == k ? sc[k] : scj;
                     wj = kj[j] == k ? w[k] : wj;
                 }
-                O[j] = O[j] * scj + wj * cur[u].o[j];
+                acc.o[j] = acc.o[j] * scj + wj * cur[u].o[j];
             }
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) cur[u] = nxt[u];
     }
-    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
-#pragma unroll
-    for (int j = 0; j < NPER; ++j) {
-        const int e = lane + 32 * j;
-        if (e >= S) continue;
-        float Lj = 0.f;
-#pragma unroll
-        for (int k = 0; k < NG; ++k) Lj = kj[j] == k ? L[k] : Lj;
-        store_out<T>(out_row + e0 + e, Lj > 0.f ? O[j] / Lj : 0.f);
+    write_out<T, D, NPER, NG>(acc, pc, G, a, warp, lane);
+}
+
+// Bookkeeping of one consumer warp for the cut first piece of its CTA's
+// range, announced as soon as it is stored and checked after the range. It
+// lives in shared memory (one per warp), written and read by lane 0, so it
+// holds no registers across the main loop.
+struct EarlyPiece {
+    int has;
+    int old;  // counter value before our update
+    Piece pc;
+};
+
+__device__ __forceinline__ int* segment_counter(const DecodeArgs& a, const Piece& pc, int warp) {
+    return a.counters + (static_cast<long long>(pc.seq) * a.kv_heads + pc.head) * 4 + warp;
+}
+
+// Finish the range's last piece, cut. The counter is read first: if every
+// other piece is already in, this warp merges at once from its registers (no
+// store, no fence, no update); otherwise it stores its piece, fences and
+// counts itself in, and merges if it turned out to be last. The merging warp
+// puts the counter back to zero for the next call.
+template <typename T, int D, int NPER, int NG>
+__device__ void finish_last(const SliceState<NPER, NG>& st, const Piece& pc, int G, const DecodeArgs& a, long long U,
+                            long long cta, int warp, int lane) {
+    const long long C = a.num_ctas;
+    const long long c0 = cta_of(pc.seg_start, U, C), c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
+    const int np = pieces_of_segment(c0, c1, U, C);
+    const int slot0 = (pc.seg_start == range_start(c0, U, C)) ? 0 : 1;
+    int* counter = segment_counter(a, pc, warp);
+    const int seen = __shfl_sync(0xffffffffu, lane == 0 ? load_acquire(counter) : 0, 0);
+    if (seen == np - 1) {
+        merge_slice<T, D, NPER, NG>(pc, G, a, U, c0, slot0, np, &st, cta, warp, lane);
+        if (lane == 0) *counter = 0;
+        return;
+    }
+    store_slice<D, NPER, NG>(st, piece_slice(a.partials, cta, pc.first ? 0 : 1, warp, G * D / 4, G), G, warp, lane);
+    __threadfence();
+    __syncwarp();
+    const int old = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(counter, 1) : 0, 0);
+    if (old == np - 1) {
+        __threadfence();
+        merge_slice<T, D, NPER, NG>(pc, G, a, U, c0, slot0, np, nullptr, -1, warp, lane);
+        if (lane == 0) *counter = 0;
     }
 }
 
-// After the CTA's last piece: fence this warp's piece writes once, then
-// announce the (at most two) cut pieces of the range -- the counter updates
-// of both go out together. A warp whose update completes a segment's count
-// merges that segment's slice and puts the counter back to zero for the
-// next call.
+// Finish one piece of the range. Whole segments are written out. The range's
+// first piece, if cut and not also its last, goes to workspace slot 0 and its
+// counter is bumped right away (the result is only looked at after the range,
+// so the warp does not wait for it). The range's last piece, if cut, is
+// finished at once (it is the end of the range).
 template <typename T, int D, int NPER, int NG>
-__device__ void signal_pending(const Piece* pending, int npending, int G, const DecodeArgs& a, long long U,
-                               int warp, int lane) {
-    if (npending == 0) return;
-    __threadfence();
-    __syncwarp();
-    const long long C = a.num_ctas;
-    long long c0s[2];
-    int nps[2];
-    int* counters[2];
-    int old[2] = {0, 0};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        if (i >= npending) break;
-        const Piece& pc = pending[i];
-        c0s[i] = cta_of(pc.seg_start, U, C);
-        const long long c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
-        nps[i] = pieces_of_segment(c0s[i], c1, U, C);
-        counters[i] = a.counters + (static_cast<long long>(pc.seq) * a.kv_heads + pc.head) * 4 + warp;
-        if (lane == 0) old[i] = atomicAdd(counters[i], 1);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        if (i >= npending) break;
-        const int last = __shfl_sync(0xffffffffu, old[i] == nps[i] - 1 ? 1 : 0, 0);
-        if (!last) continue;
+__device__ void end_piece(EarlyPiece* early, const SliceState<NPER, NG>& st, const Piece& pc, int G,
+                          const DecodeArgs& a, long long U, long long cta, int warp, int lane) {
+    if (pc.complete) {
+        write_out<T, D, NPER, NG>(st, pc, G, a, warp, lane);
+    } else if (pc.first && !pc.last) {
+        store_slice<D, NPER, NG>(st, piece_slice(a.partials, cta, 0, warp, G * D / 4, G), G, warp, lane);
         __threadfence();
-        const Piece& pc = pending[i];
-        const int slot0 = (pc.seg_start == range_start(c0s[i], U, C)) ? 0 : 1;
-        merge_slice<T, D, NPER, NG>(pc, G, a, U, warp, lane, c0s[i], slot0, nps[i]);
-        if (lane == 0) *counters[i] = 0;
+        __syncwarp();
+        if (lane == 0) {
+            early->old = atomicAdd(segment_counter(a, pc, warp), 1);
+            early->pc = pc;
+            early->has = 1;
+        }
+    } else {
+        finish_last<T, D, NPER, NG>(st, pc, G, a, U, cta, warp, lane);
     }
+}
+
+// After the range: if this warp's update of the first piece's counter
+// completed the count, merge that segment.
+template <typename T, int D, int NPER, int NG>
+__device__ void finish_early(const EarlyPiece* early, int G, const DecodeArgs& a, long long U, int warp, int lane) {
+    __syncwarp();
+    if (!early->has) return;
+    const Piece pc = early->pc;
+    const long long C = a.num_ctas;
+    const long long c0 = cta_of(pc.seg_start, U, C), c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
+    const int np = pieces_of_segment(c0, c1, U, C);
+    if (early->old != np - 1) return;
+    __threadfence();
+    const int slot0 = (pc.seg_start == range_start(c0, U, C)) ? 0 : 1;
+    merge_slice<T, D, NPER, NG>(pc, G, a, U, c0, slot0, np, nullptr, -1, warp, lane);
+    if (lane == 0) *segment_counter(a, pc, warp) = 0;
 }
 
 // Rows of sequences with no tokens are zero; CTA c writes those of the
@@ -571,8 +664,11 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     long long k = 0;
     int piece_idx = 0;
     Piece pc;
-    Piece pending[2];  // cut pieces of this range: only its first and its last can be cut
-    int npending = 0;
+    // only the first and the last piece of a range can be cut
+    __shared__ EarlyPiece early_sm[C::kConsumers];
+    EarlyPiece* early = &early_sm[warp];
+    if (lane == 0) early->has = 0;
+    __syncwarp();
     while (wk.next(pc)) {
         // Q^T fragments: B operand of S^T = K Q^T; column n = query head gid.
         uint32_t qf[D / 16][2];
@@ -709,13 +805,14 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_bar);
         if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
-        if (write_piece<__nv_bfloat16, D>(sm_o, sm_m, sm_l, G, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
+        // G <= 8: a warp's slice is G*D/4 <= 2*D elements, at most D/16 per
+        // lane and at most three heads
+        const SliceState<D / 16, 3> st = combine_slice<D, D / 16, 3>(sm_o, sm_m, sm_l, G, G, warp, lane);
+        end_piece<__nv_bfloat16, D>(early, st, pc, G, a, U, cta, warp, lane);
         ++piece_idx;
     }
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 4);
-    // G <= 8: a warp's slice is G*D/4 <= 2*D elements, at most D/16 per lane
-    // and at most three heads
-    signal_pending<__nv_bfloat16, D, D / 16, 3>(pending, npending, G, a, U, warp, lane);
+    finish_early<__nv_bfloat16, D, D / 16, 3>(early, G, a, U, warp, lane);
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 5);
 }
 
@@ -758,8 +855,11 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
     wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
     long long k = 0;
     Piece pc;
-    Piece pending[2];
-    int npending = 0;
+    constexpr int kPer = GMAX * D / 128, kHeads = GMAX / 4 + 1;
+    __shared__ EarlyPiece early_sm[C::kWarps];
+    EarlyPiece* early = &early_sm[warp];
+    if (lane == 0) early->has = 0;
+    __syncwarp();
     while (wk.next(pc)) {
         float qr[GMAX][C::kPer];
 #pragma unroll
@@ -829,10 +929,11 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
             }
         }
         __syncthreads();
-        if (write_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
+        const SliceState<kPer, kHeads> st = combine_slice<D, kPer, kHeads>(sm_o, sm_m, sm_l, GMAX, G, warp, lane);
+        end_piece<T, D>(early, st, pc, G, a, U, cta, warp, lane);
         __syncthreads();
     }
-    signal_pending<T, D, GMAX * D / 128, GMAX / 4 + 1>(pending, npending, G, a, U, warp, lane);
+    finish_early<T, D, kPer, kHeads>(early, G, a, U, warp, lane);
 }
 
 // ------------------------------------------------------------------ host side
