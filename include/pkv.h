@@ -83,6 +83,12 @@ typedef struct {
 
 /* flags */
 #define PKV_FLAG_CHECKED 1u    /* validate device-resident indices first (syncs) */
+/* Test hook for failure detection, pkv_decode_attention with the tensor-core
+ * kernel only (opts->kernel == 2): the kernel's producer warp issues no copies,
+ * so every consumer wait runs out after 20 ms instead of 2 s. The call itself
+ * returns PKV_OK; the sticky device status then reports PKV_DEVERR_TIMEOUT and
+ * `out` holds no result. Nothing is in flight when the kernel returns. */
+#define PKV_FLAG_TEST_STALL 0x80000000u
 
 /* Bits of the sticky device status (pkv_device_status). */
 #define PKV_DEVERR_TIMEOUT 1u

@@ -171,6 +171,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
     if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
     if (!isfinite(scale)) return PKV_ERR_SHAPE;
     if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
+    if ((flags & PKV_FLAG_TEST_STALL) && !(opts != nullptr && opts->kernel == 2)) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
     if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
         return PKV_ERR_SHAPE;
@@ -219,6 +220,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
         a.group = G;
         a.dtype = desc->dtype;
         a.num_ctas = plan.num_ctas;
+        a.test_stall = (flags & PKV_FLAG_TEST_STALL) ? 1 : 0;
         a.scale = scale;
         if (launch_decode(a, plan, s) != cudaSuccess) return PKV_ERR_CUDA;
     }

@@ -586,6 +586,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         // K/V blocks are read once per call: stream them with evict-first so
         // the block tables, q and the merge pieces stay in L2.
         const uint64_t kv_policy = l2_evict_first_policy();
+        if (a.test_stall) return;  // test hook: nothing is ever issued, so every consumer wait runs out
         Walker wk;
         wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
         long long k = 0;
@@ -692,7 +693,9 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         for (int blk = pc.blk_from; blk < pc.blk_to; ++blk, ++k) {
             if (static_cast<int>(k & (C::kConsumers - 1)) != warp) continue;
             const int s = static_cast<int>(k % C::kStages);
-            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag)) return;
+            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag,
+                           a.test_stall ? kTestWaitLimitNs : kWaitLimitNs))
+                return;
             if (k == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 3);
             const int valid = min(16, n_ctx - blk * 16);
             if (stage_ok[s]) {

@@ -34,8 +34,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // Upper bound for any in-kernel wait, in nanoseconds of %globaltimer. A
 // healthy wait ends in microseconds; this only stops a kernel that would
-// otherwise spin forever.
+// otherwise spin forever. The stall test hook uses a short limit.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr unsigned long long kTestWaitLimitNs = 20000000ull;
 
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
@@ -78,15 +79,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed. Gives up when
-// *abort becomes nonzero (another warp gave up) or after kWaitLimitNs; in the
+// *abort becomes nonzero (another warp gave up) or after limit_ns; in the
 // second case it sets PKV_DEVERR_TIMEOUT in *status and raises *abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
-                                          volatile int* abort) {
+                                          volatile int* abort, unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (abort != nullptr && *abort) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             atomicOr(status, PKV_DEVERR_TIMEOUT);
             if (abort != nullptr) *abort = 1;
             return false;

@@ -49,6 +49,7 @@ struct DecodeArgs {
     int32_t group;  // q_heads / kv_heads
     int32_t dtype;
     int32_t num_ctas;
+    int32_t test_stall;  // PKV_FLAG_TEST_STALL: the producer issues nothing
     float scale;
 };
 

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_F32, PKV_BF16 = 0, 1
 PKV_FLAG_CHECKED = 1
+PKV_FLAG_TEST_STALL = 0x80000000
 PKV_DEVERR_TIMEOUT, PKV_DEVERR_RANGE = 1, 2
 STATUS_NAMES = ["PKV_OK", "PKV_ERR_NULL", "PKV_ERR_SHAPE", "PKV_ERR_DTYPE", "PKV_ERR_ALIGN", "PKV_ERR_RANGE",
                 "PKV_ERR_OVERLAP", "PKV_ERR_WORKSPACE", "PKV_ERR_TIMEOUT", "PKV_ERR_CUDA", "PKV_ERR_UNSUPPORTED"]

@@ -347,3 +347,22 @@ def test_group_sizes_with_cut_segments(pkv, kernel, q_heads, kv_heads, head_dim)
         got = run_attention(pkv, dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]), c["tables"], c["lens"],
                             c["scale"], kernel=kernel, num_ctas=num_ctas)
         check_close(got, oracle_attention(c, c["tables"], c["lens"]))
+
+
+def test_bounded_wait_runs_out_and_is_reported(pkv):
+    """Failure detection: with the stall hook the producer issues nothing, the
+    consumers' bounded waits run out, the kernel returns and the sticky
+    status says so; the context stays usable for the next call."""
+    c = cases.random_case(71, [300, 40, 1000], 32, 8, 128, torch.bfloat16)
+    args = (dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]), c["tables"], c["lens"], c["scale"])
+    pkv.pkv_device_status(clear=True)
+    run_attention(pkv, *args, kernel=2, flags=pkv.PKV_FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) & pkv.PKV_DEVERR_TIMEOUT
+    got = run_attention(pkv, *args, kernel=2)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) == 0
+    check_close(got, oracle_attention(c, c["tables"], c["lens"]))
+    with pytest.raises(pkv.PkvError) as e:      # the hook exists for the tensor-core kernel only
+        run_attention(pkv, *args, kernel=1, flags=pkv.PKV_FLAG_TEST_STALL)
+    assert e.value.name == "PKV_ERR_UNSUPPORTED"
