@@ -770,6 +770,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
             if (lane == 0) mbar_arrive(&empty[s]);
         }
 
+        if (pc.last && warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 4);
         // ---- combine the four warps' states for this piece
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -814,7 +815,6 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         end_piece<__nv_bfloat16, D>(early, st, pc, G, a, U, cta, warp, lane);
         ++piece_idx;
     }
-    if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 4);
     finish_early<__nv_bfloat16, D, D / 16, 3>(early, G, a, U, warp, lane);
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 5);
 }
