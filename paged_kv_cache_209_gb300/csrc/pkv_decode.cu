@@ -228,20 +228,26 @@ __device__ SliceState<NPER, NG> combine_slice(const float* sm_o, const float* sm
     float wt[NG][4];
 #pragma unroll
     for (int k = 0; k < NG; ++k) {
-        const int g = g_first + k;
-        float M = neg_inf();
+        st.m[k] = neg_inf();
+        st.l[k] = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, k < ng ? sm_m[w * gstride + g] : neg_inf());
-        const float base = (M == neg_inf()) ? 0.f : M;
-        float L = 0.f;
+        for (int w = 0; w < 4; ++w) wt[k][w] = 0.f;
+        if (k < ng) {
+            const int g = g_first + k;
+            float mw[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float mw = k < ng ? sm_m[w * gstride + g] : neg_inf();
-            wt[k][w] = (mw == neg_inf()) ? 0.f : ex2(mw - base);
-            L += (k < ng) ? wt[k][w] * sm_l[w * gstride + g] : 0.f;
+            for (int w = 0; w < 4; ++w) mw[w] = sm_m[w * gstride + g];
+            const float M = fmaxf(fmaxf(mw[0], mw[1]), fmaxf(mw[2], mw[3]));
+            const float base = (M == neg_inf()) ? 0.f : M;
+            float L = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                wt[k][w] = (mw[w] == neg_inf()) ? 0.f : ex2(mw[w] - base);
+                L += wt[k][w] * sm_l[w * gstride + g];
+            }
+            st.m[k] = M;
+            st.l[k] = L;
         }
-        st.m[k] = M;
-        st.l[k] = L;
     }
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
@@ -251,11 +257,15 @@ __device__ SliceState<NPER, NG> combine_slice(const float* sm_o, const float* sm
             const int g = e / D;
             const int d = e - g * D;
             const int kj = g - g_first;
+            float w4[4];
 #pragma unroll
-            for (int k = 0; k < NG; ++k)
-                if (k == kj)
+            for (int w = 0; w < 4; ++w) {
+                w4[w] = 0.f;
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) o += wt[k][w] * sm_o[(w * gstride + g) * D + d];
+                for (int k = 0; k < NG; ++k) w4[w] = kj == k ? wt[k][w] : w4[w];
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) o += w4[w] * sm_o[(w * gstride + g) * D + d];
         }
         st.o[j] = o;
     }
@@ -447,6 +457,27 @@ __device__ void finish_last(const SliceState<NPER, NG>& st, const Piece& pc, int
     }
 }
 
+// Finish a piece that is not the range's last: a whole segment is written
+// out; a cut one (the range's first piece) goes to workspace slot 0 and its
+// counter is bumped right away -- the result is only looked at after the
+// range, so the warp does not wait for it.
+template <typename T, int D, int NPER, int NG>
+__device__ void end_mid_piece(EarlyPiece* early, const SliceState<NPER, NG>& st, const Piece& pc, int G,
+                              const DecodeArgs& a, long long cta, int warp, int lane) {
+    if (pc.complete) {
+        write_out<T, D, NPER, NG>(st, pc, G, a, warp, lane);
+        return;
+    }
+    store_slice<D, NPER, NG>(st, piece_slice(a.partials, cta, 0, warp, G * D / 4, G), G, warp, lane);
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+        early->old = atomicAdd(segment_counter(a, pc, warp), 1);
+        early->pc = pc;
+        early->has = 1;
+    }
+}
+
 // Finish one piece of the range. Whole segments are written out. The range's
 // first piece, if cut and not also its last, goes to workspace slot 0 and its
 // counter is bumped right away (the result is only looked at after the range,
@@ -587,53 +618,72 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         // the block tables, q and the merge pieces stay in L2.
         const uint64_t kv_policy = l2_evict_first_policy();
         if (a.test_stall) return;  // test hook: nothing is ever issued, so every consumer wait runs out
-        Walker wk;
-        wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
+        // Lane l looks up unit ua + base + l (block id and KV head) one batch
+        // of 32 units ahead, across segment boundaries, so a run of short
+        // segments never waits for its block-table entries.
+        auto lookup = [&](long long u, int& bid, int& head) {
+            bid = 0;
+            head = 0;
+            if (u >= ub) return;
+            int lo = 0, hi = a.batch - 1;  // sequence: first i with Hkv * pre[i] > u
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (static_cast<long long>(s_pre[mid]) * a.kv_heads > u)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            const int excl = lo ? s_pre[lo - 1] : 0;
+            const int nb = s_pre[lo] - excl;
+            const long long local = u - static_cast<long long>(a.kv_heads) * excl;
+            head = static_cast<int>(local / nb);
+            const int blk = static_cast<int>(local - static_cast<long long>(head) * nb);
+            bid = __ldg(a.tables + static_cast<long long>(lo) * a.max_blocks + blk);
+        };
+        const long long n = ub - ua;
         long long k = 0;
-        Piece pc;
         bool ok = true;
-        while (ok && wk.next(pc)) {
-            const int32_t* trow = a.tables + static_cast<long long>(pc.seq) * a.max_blocks + pc.blk_from;
-            const int cnt_piece = pc.blk_to - pc.blk_from;
-            int cur = lane < cnt_piece ? __ldg(trow + lane) : 0;
-            for (int b0 = 0; ok && b0 < cnt_piece; b0 += 32) {
-                const int nidx = b0 + 32 + lane;
-                const int nxt = nidx < cnt_piece ? __ldg(trow + nidx) : 0;
-                const int cnt = min(32, cnt_piece - b0);
-                for (int e = 0; e < cnt; ++e, ++k) {
-                    const int bid = __shfl_sync(0xffffffffu, cur, e);
-                    int good = 1;
-                    if (lane == 0) {
-                        const int s = static_cast<int>(k % C::kStages);
-                        const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1) ^ 1u;
-                        if (!mbar_wait(&empty[s], par, a.status, abort_flag)) {
-                            good = 0;
-                        } else if (bid >= 0 && bid < a.num_blocks) {
-                            stage_ok[s] = 1;
-                            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                            uint8_t* st = smem + s * C::kStageBytes;
-                            const int y = (bid * a.kv_heads + pc.head) * 16;
+        int bid_cur, head_cur;
+        lookup(ua + lane, bid_cur, head_cur);
+        for (long long base = 0; ok && base < n; base += 32) {
+            int bid_nxt, head_nxt;
+            lookup(ua + base + 32 + lane, bid_nxt, head_nxt);
+            const int cnt = static_cast<int>(n - base < 32 ? n - base : 32);
+            for (int e = 0; e < cnt; ++e, ++k) {
+                const int bid = __shfl_sync(0xffffffffu, bid_cur, e);
+                const int head = __shfl_sync(0xffffffffu, head_cur, e);
+                int good = 1;
+                if (lane == 0) {
+                    const int s = static_cast<int>(k % C::kStages);
+                    const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1) ^ 1u;
+                    if (!mbar_wait(&empty[s], par, a.status, abort_flag)) {
+                        good = 0;
+                    } else if (bid >= 0 && bid < a.num_blocks) {
+                        stage_ok[s] = 1;
+                        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                        uint8_t* st = smem + s * C::kStageBytes;
+                        const int y = (bid * a.kv_heads + head) * 16;
 #pragma unroll
-                            for (int hf = 0; hf < C::kHalves; ++hf)
-                                tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
+                        for (int hf = 0; hf < C::kHalves; ++hf)
+                            tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
 #pragma unroll
-                            for (int hf = 0; hf < C::kHalves; ++hf)
-                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
-                            if (k == 0) PKV_STAMP(a, blockIdx.x, 2);
-                        } else {
-                            stage_ok[s] = 0;
-                            atomicOr(a.status, PKV_DEVERR_RANGE);
-                            mbar_arrive(&full[s]);
-                        }
-                    }
-                    good = __shfl_sync(0xffffffffu, good, 0);
-                    if (!good) {
-                        ok = false;
-                        break;
+                        for (int hf = 0; hf < C::kHalves; ++hf)
+                            tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
+                        if (k == 0) PKV_STAMP(a, blockIdx.x, 2);
+                    } else {
+                        stage_ok[s] = 0;
+                        atomicOr(a.status, PKV_DEVERR_RANGE);
+                        mbar_arrive(&full[s]);
                     }
                 }
-                cur = nxt;
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
             }
+            bid_cur = bid_nxt;
+            head_cur = head_nxt;
         }
         // After an abort, wait (bounded) for the copies still in flight
         // into the ring before the CTA may exit.
@@ -670,20 +720,23 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     EarlyPiece* early = &early_sm[warp];
     if (lane == 0) early->has = 0;
     __syncwarp();
-    while (wk.next(pc)) {
-        // Q^T fragments: B operand of S^T = K Q^T; column n = query head gid.
-        uint32_t qf[D / 16][2];
-        {
-            const bool live = gid < G;
-            const __nv_bfloat16* qrow =
-                q + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G + (live ? gid : 0)) * D;
-            const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
+    // Q^T fragments (B operand of S^T = K Q^T; column n = query head gid) of
+    // a piece. The next piece's are loaded while this piece's states are
+    // being combined, so a run of short segments does not wait for Q.
+    auto load_q = [&](uint32_t (&f)[D / 16][2], const Piece& p) {
+        const bool live = gid < G;
+        const __nv_bfloat16* qrow = q + (static_cast<long long>(p.seq) * a.q_heads + p.head * G + (live ? gid : 0)) * D;
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
 #pragma unroll
-            for (int j = 0; j < D / 16; ++j) {
-                qf[j][0] = live ? __ldg(q32 + (16 * j + 2 * tig) / 2) : 0u;
-                qf[j][1] = live ? __ldg(q32 + (16 * j + 2 * tig + 8) / 2) : 0u;
-            }
+        for (int j = 0; j < D / 16; ++j) {
+            f[j][0] = live ? __ldg(q32 + (16 * j + 2 * tig) / 2) : 0u;
+            f[j][1] = live ? __ldg(q32 + (16 * j + 2 * tig + 8) / 2) : 0u;
         }
+    };
+    uint32_t qf[D / 16][2];
+    bool have = wk.next(pc);
+    if (have) load_q(qf, pc);
+    while (have) {
         float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
         float o[D / 16][4];
 #pragma unroll
@@ -808,12 +861,23 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_bar);
-        if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
         // G <= 8: a warp's slice is G*D/4 <= 2*D elements, at most D/16 per
         // lane and at most three heads
+        if (pc.last) {
+            // the range's last piece: nothing to prefetch; it may merge
+            if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
+            const SliceState<D / 16, 3> st = combine_slice<D, D / 16, 3>(sm_o, sm_m, sm_l, G, G, warp, lane);
+            end_piece<__nv_bfloat16, D>(early, st, pc, G, a, U, cta, warp, lane);
+            break;
+        }
+        Piece nx;
+        have = wk.next(nx);
+        load_q(qf, nx);  // in flight during the barrier and the combine
+        if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
         const SliceState<D / 16, 3> st = combine_slice<D, D / 16, 3>(sm_o, sm_m, sm_l, G, G, warp, lane);
-        end_piece<__nv_bfloat16, D>(early, st, pc, G, a, U, cta, warp, lane);
+        end_mid_piece<__nv_bfloat16, D>(early, st, pc, G, a, cta, warp, lane);
         ++piece_idx;
+        pc = nx;
     }
     finish_early<__nv_bfloat16, D, D / 16, 3>(early, G, a, U, warp, lane);
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 5);
