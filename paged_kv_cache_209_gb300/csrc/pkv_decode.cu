@@ -354,7 +354,7 @@ __device__ __forceinline__ void load_piece(SliceState<NPER, NG>& v, const float*
 // loop is software-pipelined: the loads of the next two pieces are in flight
 // while the current two are combined (online log-sum-exp, per head).
 template <typename T, int D, int NPER, int NG>
-__device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, long long c0, int slot0,
+__device__ __noinline__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, long long c0, int slot0,
                             int npieces, const SliceState<NPER, NG>* own, long long own_cta, int warp, int lane) {
     const int S = G * D / 4;
     const int e0 = warp * S;
@@ -433,7 +433,7 @@ __device__ __forceinline__ int* segment_counter(const DecodeArgs& a, const Piece
 // counts itself in, and merges if it turned out to be last. The merging warp
 // puts the counter back to zero for the next call.
 template <typename T, int D, int NPER, int NG>
-__device__ void finish_last(const SliceState<NPER, NG>& st, const Piece& pc, int G, const DecodeArgs& a, long long U,
+__device__ __noinline__ void finish_last(const SliceState<NPER, NG>& st, const Piece& pc, int G, const DecodeArgs& a, long long U,
                             long long cta, int warp, int lane) {
     const long long C = a.num_ctas;
     const long long c0 = cta_of(pc.seg_start, U, C), c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
@@ -505,7 +505,7 @@ __device__ void end_piece(EarlyPiece* early, const SliceState<NPER, NG>& st, con
 // After the range: if this warp's update of the first piece's counter
 // completed the count, merge that segment.
 template <typename T, int D, int NPER, int NG>
-__device__ void finish_early(const EarlyPiece* early, int G, const DecodeArgs& a, long long U, int warp, int lane) {
+__device__ __noinline__ void finish_early(const EarlyPiece* early, int G, const DecodeArgs& a, long long U, int warp, int lane) {
     __syncwarp();
     if (!early->has) return;
     const Piece pc = early->pc;
@@ -522,7 +522,7 @@ __device__ void finish_early(const EarlyPiece* early, int G, const DecodeArgs& a
 // Rows of sequences with no tokens are zero; CTA c writes those of the
 // sequences i with i % num_ctas == c.
 template <typename T>
-__device__ void zero_empty_rows(const int32_t* s_len, const DecodeArgs& a, int tid, int nthreads) {
+__device__ __noinline__ void zero_empty_rows(const int32_t* s_len, const DecodeArgs& a, int tid, int nthreads) {
     const int row = a.q_heads * a.head_dim;
     for (int i = blockIdx.x; i < a.batch; i += a.num_ctas) {
         if (s_len[i] != 0) continue;
