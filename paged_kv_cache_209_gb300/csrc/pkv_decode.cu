@@ -96,7 +96,6 @@ struct Piece {
     int blk_from, blk_to;  // blocks [from, to) of the sequence
     bool complete;         // the piece is the whole segment
     bool first;            // the piece opens this CTA's range
-    bool last;             // the piece closes this CTA's range
     long long seg_start;   // first unit of the segment
     int seg_len;           // units (blocks) of the segment
 };
@@ -141,7 +140,6 @@ struct Walker {
         p.blk_to = static_cast<int>(pe - s0);
         p.complete = (u == s0) && (pe == s1);
         p.first = (u == start);
-        p.last = (pe == end);
         p.seg_start = s0;
         p.seg_len = nb;
         u = pe;
@@ -202,123 +200,55 @@ __device__ __forceinline__ int pieces_of_segment(long long c0, long long c1, lon
     return n;
 }
 
-// ------------------------------------------------------------------ piece ends
+// Finish one segment piece for the elements of warp `warp`'s slice.
+//
 // The four consumer warps of a CTA each own a fixed slice of the G x D output
-// elements of a segment: S = G*D/4 elements, element e is head e / D, dim
-// e % D; lane `lane` holds elements e0 + lane + 32*j. A slice touches at most
-// NG heads (slot k is head g_first + k).
-
-template <int NPER, int NG>
-struct SliceState {
-    float o[NPER];       // unnormalised accumulators of the lane's elements
-    float m[NG], l[NG];  // running maximum (base 2) and sum per head of the slice
-};
-
-// One warp's slice of a piece, combined from the four warps' online-softmax
-// states in shared memory (sm_o[(w*gstride + g)*D + d], sm_m / sm_l[w*gstride
-// + g]).
-template <int D, int NPER, int NG>
-__device__ SliceState<NPER, NG> combine_slice(const float* sm_o, const float* sm_m, const float* sm_l, int gstride,
-                                              int G, int warp, int lane) {
+// elements of the segment (S = G*D/4 elements; element e is head e / D, dim
+// e % D). The per-warp online-softmax states (O, m, l) of the piece are in
+// shared memory (sm_o[(w*gstride + g)*D + d], sm_m/sm_l[w*gstride + g]).
+// A whole segment is normalised and written out directly. A cut segment's
+// piece goes to this CTA's slot in the workspace; it is announced later by
+// signal_pending. Returns true for a cut segment.
+template <typename T, int D>
+__device__ bool write_piece(const float* sm_o, const float* sm_m, const float* sm_l, int gstride, int G,
+                            const Piece& pc, const DecodeArgs& a, long long cta, int warp, int lane) {
     const int S = G * D / 4;
     const int e0 = warp * S;
-    const int g_first = e0 / D;
-    const int ng = (e0 + S - 1) / D - g_first + 1;
-    SliceState<NPER, NG> st;
-    float wt[NG][4];
-#pragma unroll
-    for (int k = 0; k < NG; ++k) {
-        st.m[k] = neg_inf();
-        st.l[k] = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) wt[k][w] = 0.f;
-        if (k < ng) {
-            const int g = g_first + k;
-            float mw[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) mw[w] = sm_m[w * gstride + g];
-            const float M = fmaxf(fmaxf(mw[0], mw[1]), fmaxf(mw[2], mw[3]));
-            const float base = (M == neg_inf()) ? 0.f : M;
-            float L = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                wt[k][w] = (mw[w] == neg_inf()) ? 0.f : ex2(mw[w] - base);
-                L += wt[k][w] * sm_l[w * gstride + g];
-            }
-            st.m[k] = M;
-            st.l[k] = L;
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < NPER; ++j) {
-        const int e = e0 + lane + 32 * j;
-        float o = 0.f;
-        if (e < e0 + S) {
-            const int g = e / D;
-            const int d = e - g * D;
-            const int kj = g - g_first;
-            float w4[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                w4[w] = 0.f;
-#pragma unroll
-                for (int k = 0; k < NG; ++k) w4[w] = kj == k ? wt[k][w] : w4[w];
-            }
-#pragma unroll
-            for (int w = 0; w < 4; ++w) o += w4[w] * sm_o[(w * gstride + g) * D + d];
-        }
-        st.o[j] = o;
-    }
-    return st;
-}
-
-// Normalise a finished slice and write it to the output row.
-template <typename T, int D, int NPER, int NG>
-__device__ void write_out(const SliceState<NPER, NG>& st, const Piece& pc, int G, const DecodeArgs& a, int warp,
-                          int lane) {
-    const int S = G * D / 4;
-    const int e0 = warp * S;
-    const int g_first = e0 / D;
     T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
-#pragma unroll
-    for (int j = 0; j < NPER; ++j) {
-        const int e = lane + 32 * j;
-        if (e >= S) continue;
-        const int kj = (e0 + e) / D - g_first;
-        float Lj = 0.f;
-#pragma unroll
-        for (int k = 0; k < NG; ++k) Lj = kj == k ? st.l[k] : Lj;
-        store_out<T>(out_row + e0 + e, Lj > 0.f ? st.o[j] / Lj : 0.f);
+    float* slice = nullptr;
+    if (!pc.complete) slice = piece_slice(a.partials, cta, pc.first ? 0 : 1, warp, S, G);
+    for (int e = e0 + lane; e < e0 + S; e += 32) {
+        const int g = e / D;
+        const int d = e - g * D;
+        float M = neg_inf();
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * gstride + g]);
+        const float base = (M == neg_inf()) ? 0.f : M;
+        float o = 0.f, L = 0.f;
+        for (int w = 0; w < 4; ++w) {
+            const float mw = sm_m[w * gstride + g];
+            const float wt = (mw == neg_inf()) ? 0.f : ex2(mw - base);
+            o += wt * sm_o[(w * gstride + g) * D + d];
+            L += wt * sm_l[w * gstride + g];
+        }
+        if (pc.complete)
+            store_out<T>(out_row + e, L > 0.f ? o / L : 0.f);
+        else
+            slice[e - e0] = o;
     }
-}
-
-// Store a slice as a piece in the workspace: S accumulators, then the maxima
-// and sums of the slice's heads (at index S + g and S + G + g).
-template <int D, int NPER, int NG>
-__device__ void store_slice(const SliceState<NPER, NG>& st, float* slice, int G, int warp, int lane) {
-    const int S = G * D / 4;
-    const int e0 = warp * S;
-    const int g_first = e0 / D;
-    const int ng = (e0 + S - 1) / D - g_first + 1;
-#pragma unroll
-    for (int j = 0; j < NPER; ++j) {
-        const int e = lane + 32 * j;
-        if (e < S) slice[e] = st.o[j];
+    if (pc.complete) return false;
+    if (lane < G) {
+        float M = neg_inf();
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * gstride + lane]);
+        const float base = (M == neg_inf()) ? 0.f : M;
+        float L = 0.f;
+        for (int w = 0; w < 4; ++w) {
+            const float mw = sm_m[w * gstride + lane];
+            L += (mw == neg_inf()) ? 0.f : ex2(mw - base) * sm_l[w * gstride + lane];
+        }
+        slice[S + lane] = M;
+        slice[S + G + lane] = L;
     }
-    if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < NG; ++k)
-            if (k < ng) {
-                slice[S + g_first + k] = st.m[k];
-                slice[S + G + g_first + k] = st.l[k];
-            }
-    }
-}
-
-__device__ __forceinline__ int load_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+    return true;
 }
 
 // CTA holding piece p (0-based) of the segment that starts at unit S0 and
@@ -332,7 +262,12 @@ __device__ __forceinline__ long long piece_cta(long long S0, long long c0, int p
 // Loads of one piece for one lane: the lane's NPER accumulator elements and
 // the maxima / sums of the (at most NG) heads they belong to.
 template <int NPER, int NG>
-__device__ __forceinline__ void load_piece(SliceState<NPER, NG>& v, const float* p, bool live, int S, int G,
+struct PieceVals {
+    float m[NG], l[NG], o[NPER];
+};
+
+template <int NPER, int NG>
+__device__ __forceinline__ void load_piece(PieceVals<NPER, NG>& v, const float* p, bool live, int S, int G,
                                            int g_first, int ng, int lane) {
 #pragma unroll
     for (int k = 0; k < NG; ++k) {
@@ -347,54 +282,53 @@ __device__ __forceinline__ void load_piece(SliceState<NPER, NG>& v, const float*
     }
 }
 
-// Merge the pieces of this warp's slice of a cut segment and write the output
-// row. `own` (if not null) is this CTA's piece, still in registers: its slot
-// in the workspace is not read. This runs at the tail of the kernel while
-// other CTAs still stream, when a load round trip costs microseconds, so the
-// loop is software-pipelined: the loads of the next two pieces are in flight
-// while the current two are combined (online log-sum-exp, per head).
+// Merge every piece of this warp's slice of a cut segment and write the
+// output row. This runs at the tail of the kernel while other CTAs still
+// stream, when a load round trip costs microseconds, so the loop is
+// software-pipelined: the loads of the next two pieces are in flight while
+// the current two are combined (online log-sum-exp, per head).
 template <typename T, int D, int NPER, int NG>
-__device__ __noinline__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, long long c0, int slot0,
-                            int npieces, const SliceState<NPER, NG>* own, long long own_cta, int warp, int lane) {
+__device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane,
+                            long long c0, int slot0, int npieces) {
     const int S = G * D / 4;
     const int e0 = warp * S;
     const long long C = a.num_ctas;
     const int g_first = e0 / D;
-    const int ng = (e0 + S - 1) / D - g_first + 1;
-    int kj[NPER];
+    const int ng = (e0 + S - 1) / D - g_first + 1;  // heads of the slice, <= NG
+    int kj[NPER];                                   // head slot of each of the lane's elements
 #pragma unroll
     for (int j = 0; j < NPER; ++j) kj[j] = (e0 + lane + 32 * j) / D - g_first;
-    SliceState<NPER, NG> acc;
+    float M[NG], L[NG], O[NPER];
 #pragma unroll
     for (int k = 0; k < NG; ++k) {
-        acc.m[k] = own ? own->m[k] : neg_inf();
-        acc.l[k] = own ? own->l[k] : 0.f;
+        M[k] = neg_inf();
+        L[k] = 0.f;
     }
 #pragma unroll
-    for (int j = 0; j < NPER; ++j) acc.o[j] = own ? own->o[j] : 0.f;
-    auto live = [&](int p) { return p < npieces && !(own && piece_cta(pc.seg_start, c0, p, U, C) == own_cta); };
+    for (int j = 0; j < NPER; ++j) O[j] = 0.f;
     auto ptr = [&](int p) {
-        return p < npieces
-                   ? piece_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, S, G)
-                   : a.partials;
+        return piece_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, S, G);
     };
-    SliceState<NPER, NG> cur[2], nxt[2];
+    PieceVals<NPER, NG> cur[2], nxt[2];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) load_piece(cur[u], ptr(u), live(u), S, G, g_first, ng, lane);
+    for (int u = 0; u < 2; ++u) load_piece(cur[u], u < npieces ? ptr(u) : a.partials, u < npieces, S, G, g_first, ng, lane);
     for (int p0 = 0; p0 < npieces; p0 += 2) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) load_piece(nxt[u], ptr(p0 + 2 + u), live(p0 + 2 + u), S, G, g_first, ng, lane);
+        for (int u = 0; u < 2; ++u) {
+            const int p = p0 + 2 + u;
+            load_piece(nxt[u], p < npieces ? ptr(p) : a.partials, p < npieces, S, G, g_first, ng, lane);
+        }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             float sc[NG], w[NG];
 #pragma unroll
             for (int k = 0; k < NG; ++k) {
-                const float Mn = fmaxf(acc.m[k], cur[u].m[k]);
+                const float Mn = fmaxf(M[k], cur[u].m[k]);
                 const float base = (Mn == neg_inf()) ? 0.f : Mn;
-                sc[k] = (acc.m[k] == neg_inf()) ? 0.f : ex2(acc.m[k] - base);
+                sc[k] = (M[k] == neg_inf()) ? 0.f : ex2(M[k] - base);
                 w[k] = (cur[u].m[k] == neg_inf()) ? 0.f : ex2(cur[u].m[k] - base);
-                acc.l[k] = acc.l[k] * sc[k] + w[k] * cur[u].l[k];
-                acc.m[k] = Mn;
+                L[k] = L[k] * sc[k] + w[k] * cur[u].l[k];
+                M[k] = Mn;
             }
 #pragma unroll
             for (int j = 0; j < NPER; ++j) {
@@ -404,125 +338,67 @@ __device__ __noinline__ void merge_slice(const Piece& pc, int G, const DecodeArg
                     scj = kj[j] == k ? sc[k] : scj;
                     wj = kj[j] == k ? w[k] : wj;
                 }
-                acc.o[j] = acc.o[j] * scj + wj * cur[u].o[j];
+                O[j] = O[j] * scj + wj * cur[u].o[j];
             }
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) cur[u] = nxt[u];
     }
-    write_out<T, D, NPER, NG>(acc, pc, G, a, warp, lane);
+    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        const int e = lane + 32 * j;
+        if (e >= S) continue;
+        float Lj = 0.f;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) Lj = kj[j] == k ? L[k] : Lj;
+        store_out<T>(out_row + e0 + e, Lj > 0.f ? O[j] / Lj : 0.f);
+    }
 }
 
-// Bookkeeping of one consumer warp for the cut first piece of its CTA's
-// range, announced as soon as it is stored and checked after the range. It
-// lives in shared memory (one per warp), written and read by lane 0, so it
-// holds no registers across the main loop.
-struct EarlyPiece {
-    int has;
-    int old;  // counter value before our update
-    Piece pc;
-};
-
-__device__ __forceinline__ int* segment_counter(const DecodeArgs& a, const Piece& pc, int warp) {
-    return a.counters + (static_cast<long long>(pc.seq) * a.kv_heads + pc.head) * 4 + warp;
-}
-
-// Finish the range's last piece, cut. The counter is read first: if every
-// other piece is already in, this warp merges at once from its registers (no
-// store, no fence, no update); otherwise it stores its piece, fences and
-// counts itself in, and merges if it turned out to be last. The merging warp
-// puts the counter back to zero for the next call.
+// After the CTA's last piece: fence this warp's piece writes once, then
+// announce the (at most two) cut pieces of the range -- the counter updates
+// of both go out together. A warp whose update completes a segment's count
+// merges that segment's slice and puts the counter back to zero for the
+// next call.
 template <typename T, int D, int NPER, int NG>
-__device__ __noinline__ void finish_last(const SliceState<NPER, NG>& st, const Piece& pc, int G, const DecodeArgs& a, long long U,
-                            long long cta, int warp, int lane) {
+__device__ void signal_pending(const Piece* pending, int npending, int G, const DecodeArgs& a, long long U,
+                               int warp, int lane) {
+    if (npending == 0) return;
+    __threadfence();
+    __syncwarp();
     const long long C = a.num_ctas;
-    const long long c0 = cta_of(pc.seg_start, U, C), c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
-    const int np = pieces_of_segment(c0, c1, U, C);
-    const int slot0 = (pc.seg_start == range_start(c0, U, C)) ? 0 : 1;
-    int* counter = segment_counter(a, pc, warp);
-    const int seen = __shfl_sync(0xffffffffu, lane == 0 ? load_acquire(counter) : 0, 0);
-    if (seen == np - 1) {
-        merge_slice<T, D, NPER, NG>(pc, G, a, U, c0, slot0, np, &st, cta, warp, lane);
-        if (lane == 0) *counter = 0;
-        return;
+    long long c0s[2];
+    int nps[2];
+    int* counters[2];
+    int old[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        if (i >= npending) break;
+        const Piece& pc = pending[i];
+        c0s[i] = cta_of(pc.seg_start, U, C);
+        const long long c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
+        nps[i] = pieces_of_segment(c0s[i], c1, U, C);
+        counters[i] = a.counters + (static_cast<long long>(pc.seq) * a.kv_heads + pc.head) * 4 + warp;
+        if (lane == 0) old[i] = atomicAdd(counters[i], 1);
     }
-    store_slice<D, NPER, NG>(st, piece_slice(a.partials, cta, pc.first ? 0 : 1, warp, G * D / 4, G), G, warp, lane);
-    __threadfence();
-    __syncwarp();
-    const int old = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(counter, 1) : 0, 0);
-    if (old == np - 1) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        if (i >= npending) break;
+        const int last = __shfl_sync(0xffffffffu, old[i] == nps[i] - 1 ? 1 : 0, 0);
+        if (!last) continue;
         __threadfence();
-        merge_slice<T, D, NPER, NG>(pc, G, a, U, c0, slot0, np, nullptr, -1, warp, lane);
-        if (lane == 0) *counter = 0;
+        const Piece& pc = pending[i];
+        const int slot0 = (pc.seg_start == range_start(c0s[i], U, C)) ? 0 : 1;
+        merge_slice<T, D, NPER, NG>(pc, G, a, U, warp, lane, c0s[i], slot0, nps[i]);
+        if (lane == 0) *counters[i] = 0;
     }
-}
-
-// Finish a piece that is not the range's last: a whole segment is written
-// out; a cut one (the range's first piece) goes to workspace slot 0 and its
-// counter is bumped right away -- the result is only looked at after the
-// range, so the warp does not wait for it.
-template <typename T, int D, int NPER, int NG>
-__device__ void end_mid_piece(EarlyPiece* early, const SliceState<NPER, NG>& st, const Piece& pc, int G,
-                              const DecodeArgs& a, long long cta, int warp, int lane) {
-    if (pc.complete) {
-        write_out<T, D, NPER, NG>(st, pc, G, a, warp, lane);
-        return;
-    }
-    store_slice<D, NPER, NG>(st, piece_slice(a.partials, cta, 0, warp, G * D / 4, G), G, warp, lane);
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) {
-        early->old = atomicAdd(segment_counter(a, pc, warp), 1);
-        early->pc = pc;
-        early->has = 1;
-    }
-}
-
-// Finish one piece of the range. Whole segments are written out. The range's
-// first piece, if cut and not also its last, goes to workspace slot 0 and its
-// counter is bumped right away (the result is only looked at after the range,
-// so the warp does not wait for it). The range's last piece, if cut, is
-// finished at once (it is the end of the range).
-template <typename T, int D, int NPER, int NG>
-__device__ void end_piece(EarlyPiece* early, const SliceState<NPER, NG>& st, const Piece& pc, int G,
-                          const DecodeArgs& a, long long U, long long cta, int warp, int lane) {
-    if (pc.complete) {
-        write_out<T, D, NPER, NG>(st, pc, G, a, warp, lane);
-    } else if (pc.first && !pc.last) {
-        store_slice<D, NPER, NG>(st, piece_slice(a.partials, cta, 0, warp, G * D / 4, G), G, warp, lane);
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) {
-            early->old = atomicAdd(segment_counter(a, pc, warp), 1);
-            early->pc = pc;
-            early->has = 1;
-        }
-    } else {
-        finish_last<T, D, NPER, NG>(st, pc, G, a, U, cta, warp, lane);
-    }
-}
-
-// After the range: if this warp's update of the first piece's counter
-// completed the count, merge that segment.
-template <typename T, int D, int NPER, int NG>
-__device__ __noinline__ void finish_early(const EarlyPiece* early, int G, const DecodeArgs& a, long long U, int warp, int lane) {
-    __syncwarp();
-    if (!early->has) return;
-    const Piece pc = early->pc;
-    const long long C = a.num_ctas;
-    const long long c0 = cta_of(pc.seg_start, U, C), c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
-    const int np = pieces_of_segment(c0, c1, U, C);
-    if (early->old != np - 1) return;
-    __threadfence();
-    const int slot0 = (pc.seg_start == range_start(c0, U, C)) ? 0 : 1;
-    merge_slice<T, D, NPER, NG>(pc, G, a, U, c0, slot0, np, nullptr, -1, warp, lane);
-    if (lane == 0) *segment_counter(a, pc, warp) = 0;
 }
 
 // Rows of sequences with no tokens are zero; CTA c writes those of the
 // sequences i with i % num_ctas == c.
 template <typename T>
-__device__ __noinline__ void zero_empty_rows(const int32_t* s_len, const DecodeArgs& a, int tid, int nthreads) {
+__device__ void zero_empty_rows(const int32_t* s_len, const DecodeArgs& a, int tid, int nthreads) {
     const int row = a.q_heads * a.head_dim;
     for (int i = blockIdx.x; i < a.batch; i += a.num_ctas) {
         if (s_len[i] != 0) continue;
@@ -618,72 +494,53 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         // the block tables, q and the merge pieces stay in L2.
         const uint64_t kv_policy = l2_evict_first_policy();
         if (a.test_stall) return;  // test hook: nothing is ever issued, so every consumer wait runs out
-        // Lane l looks up unit ua + base + l (block id and KV head) one batch
-        // of 32 units ahead, across segment boundaries, so a run of short
-        // segments never waits for its block-table entries.
-        auto lookup = [&](long long u, int& bid, int& head) {
-            bid = 0;
-            head = 0;
-            if (u >= ub) return;
-            int lo = 0, hi = a.batch - 1;  // sequence: first i with Hkv * pre[i] > u
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (static_cast<long long>(s_pre[mid]) * a.kv_heads > u)
-                    hi = mid;
-                else
-                    lo = mid + 1;
-            }
-            const int excl = lo ? s_pre[lo - 1] : 0;
-            const int nb = s_pre[lo] - excl;
-            const long long local = u - static_cast<long long>(a.kv_heads) * excl;
-            head = static_cast<int>(local / nb);
-            const int blk = static_cast<int>(local - static_cast<long long>(head) * nb);
-            bid = __ldg(a.tables + static_cast<long long>(lo) * a.max_blocks + blk);
-        };
-        const long long n = ub - ua;
+        Walker wk;
+        wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
         long long k = 0;
+        Piece pc;
         bool ok = true;
-        int bid_cur, head_cur;
-        lookup(ua + lane, bid_cur, head_cur);
-        for (long long base = 0; ok && base < n; base += 32) {
-            int bid_nxt, head_nxt;
-            lookup(ua + base + 32 + lane, bid_nxt, head_nxt);
-            const int cnt = static_cast<int>(n - base < 32 ? n - base : 32);
-            for (int e = 0; e < cnt; ++e, ++k) {
-                const int bid = __shfl_sync(0xffffffffu, bid_cur, e);
-                const int head = __shfl_sync(0xffffffffu, head_cur, e);
-                int good = 1;
-                if (lane == 0) {
-                    const int s = static_cast<int>(k % C::kStages);
-                    const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1) ^ 1u;
-                    if (!mbar_wait(&empty[s], par, a.status, abort_flag)) {
-                        good = 0;
-                    } else if (bid >= 0 && bid < a.num_blocks) {
-                        stage_ok[s] = 1;
-                        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                        uint8_t* st = smem + s * C::kStageBytes;
-                        const int y = (bid * a.kv_heads + head) * 16;
+        while (ok && wk.next(pc)) {
+            const int32_t* trow = a.tables + static_cast<long long>(pc.seq) * a.max_blocks + pc.blk_from;
+            const int cnt_piece = pc.blk_to - pc.blk_from;
+            int cur = lane < cnt_piece ? __ldg(trow + lane) : 0;
+            for (int b0 = 0; ok && b0 < cnt_piece; b0 += 32) {
+                const int nidx = b0 + 32 + lane;
+                const int nxt = nidx < cnt_piece ? __ldg(trow + nidx) : 0;
+                const int cnt = min(32, cnt_piece - b0);
+                for (int e = 0; e < cnt; ++e, ++k) {
+                    const int bid = __shfl_sync(0xffffffffu, cur, e);
+                    int good = 1;
+                    if (lane == 0) {
+                        const int s = static_cast<int>(k % C::kStages);
+                        const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1) ^ 1u;
+                        if (!mbar_wait(&empty[s], par, a.status, abort_flag)) {
+                            good = 0;
+                        } else if (bid >= 0 && bid < a.num_blocks) {
+                            stage_ok[s] = 1;
+                            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                            uint8_t* st = smem + s * C::kStageBytes;
+                            const int y = (bid * a.kv_heads + pc.head) * 16;
 #pragma unroll
-                        for (int hf = 0; hf < C::kHalves; ++hf)
-                            tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
+                            for (int hf = 0; hf < C::kHalves; ++hf)
+                                tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
 #pragma unroll
-                        for (int hf = 0; hf < C::kHalves; ++hf)
-                            tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
-                        if (k == 0) PKV_STAMP(a, blockIdx.x, 2);
-                    } else {
-                        stage_ok[s] = 0;
-                        atomicOr(a.status, PKV_DEVERR_RANGE);
-                        mbar_arrive(&full[s]);
+                            for (int hf = 0; hf < C::kHalves; ++hf)
+                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
+                            if (k == 0) PKV_STAMP(a, blockIdx.x, 2);
+                        } else {
+                            stage_ok[s] = 0;
+                            atomicOr(a.status, PKV_DEVERR_RANGE);
+                            mbar_arrive(&full[s]);
+                        }
+                    }
+                    good = __shfl_sync(0xffffffffu, good, 0);
+                    if (!good) {
+                        ok = false;
+                        break;
                     }
                 }
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
-                    ok = false;
-                    break;
-                }
+                cur = nxt;
             }
-            bid_cur = bid_nxt;
-            head_cur = head_nxt;
         }
         // After an abort, wait (bounded) for the copies still in flight
         // into the ring before the CTA may exit.
@@ -715,28 +572,22 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     long long k = 0;
     int piece_idx = 0;
     Piece pc;
-    // only the first and the last piece of a range can be cut
-    __shared__ EarlyPiece early_sm[C::kConsumers];
-    EarlyPiece* early = &early_sm[warp];
-    if (lane == 0) early->has = 0;
-    __syncwarp();
-    // Q^T fragments (B operand of S^T = K Q^T; column n = query head gid) of
-    // a piece. The next piece's are loaded while this piece's states are
-    // being combined, so a run of short segments does not wait for Q.
-    auto load_q = [&](uint32_t (&f)[D / 16][2], const Piece& p) {
-        const bool live = gid < G;
-        const __nv_bfloat16* qrow = q + (static_cast<long long>(p.seq) * a.q_heads + p.head * G + (live ? gid : 0)) * D;
-        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
+    Piece pending[2];  // cut pieces of this range: only its first and its last can be cut
+    int npending = 0;
+    while (wk.next(pc)) {
+        // Q^T fragments: B operand of S^T = K Q^T; column n = query head gid.
+        uint32_t qf[D / 16][2];
+        {
+            const bool live = gid < G;
+            const __nv_bfloat16* qrow =
+                q + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G + (live ? gid : 0)) * D;
+            const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-            f[j][0] = live ? __ldg(q32 + (16 * j + 2 * tig) / 2) : 0u;
-            f[j][1] = live ? __ldg(q32 + (16 * j + 2 * tig + 8) / 2) : 0u;
+            for (int j = 0; j < D / 16; ++j) {
+                qf[j][0] = live ? __ldg(q32 + (16 * j + 2 * tig) / 2) : 0u;
+                qf[j][1] = live ? __ldg(q32 + (16 * j + 2 * tig + 8) / 2) : 0u;
+            }
         }
-    };
-    uint32_t qf[D / 16][2];
-    bool have = wk.next(pc);
-    if (have) load_q(qf, pc);
-    while (have) {
         float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
         float o[D / 16][4];
 #pragma unroll
@@ -754,35 +605,44 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
             if (stage_ok[s]) {
                 const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
                 const uint32_t vbase = kbase + C::kPoolBytes;
-                // ---- S^T = K Q^T
-                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                // ---- S^T = K Q^T, even and odd k-steps on two accumulators
+                // (two independent MMA chains of D/32 instead of one of D/16)
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < D / 16; ++j) {
                     const int gc = 2 * j + k_chunk;
                     const uint32_t addr = kbase + (gc >> 3) * 2048 + k_row * 128 + (((gc & 7) ^ r8) << 4);
                     uint32_t a0, a1, a2, a3;
                     ldmatrix_x4(addr, a0, a1, a2, a3);
-                    mma_bf16_16816(sacc, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+                    if (j & 1)
+                        mma_bf16_16816(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+                    else
+                        mma_bf16_16816(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
                 }
                 // sacc: [0] (t=gid, g=2tig) [1] (t=gid, g=2tig+1) [2] (t=gid+8, g=2tig) [3] (t=gid+8, g=2tig+1)
-                float x0 = gid < valid ? sacc[0] * scale_log2 : neg_inf();
-                float x1 = gid < valid ? sacc[1] * scale_log2 : neg_inf();
-                float x2 = gid + 8 < valid ? sacc[2] * scale_log2 : neg_inf();
-                float x3 = gid + 8 < valid ? sacc[3] * scale_log2 : neg_inf();
+                const float x0 = gid < valid ? (sa[0] + sb[0]) * scale_log2 : neg_inf();
+                const float x1 = gid < valid ? (sa[1] + sb[1]) * scale_log2 : neg_inf();
+                const float x2 = gid + 8 < valid ? (sa[2] + sb[2]) * scale_log2 : neg_inf();
+                const float x3 = gid + 8 < valid ? (sa[3] + sb[3]) * scale_log2 : neg_inf();
+                // Lazy rescale: the running maximum m only has to bound the
+                // scores closely enough that 2^(x - m) cannot overflow; the
+                // output is exact for any m, since O and l use the same one.
+                // So the cross-lane maximum and the rescale of O run only when
+                // some score exceeds m by more than 8 (a factor 256); most
+                // blocks after the first skip them.
                 float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+                if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float b0 = mn0 == neg_inf() ? 0.f : mn0;
-                const float b1 = mn1 == neg_inf() ? 0.f : mn1;
-                const float al0 = ex2(m0 - b0), al1 = ex2(m1 - b1);
-                const float p0 = ex2(x0 - b0), p1 = ex2(x1 - b1), p2 = ex2(x2 - b0), p3 = ex2(x3 - b1);
-                l0 = l0 * al0 + (p0 + p2);
-                l1 = l1 * al1 + (p1 + p3);
-                if (__any_sync(0xffffffffu, (mn0 != m0) || (mn1 != m1))) {
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float nb0 = mn0 == neg_inf() ? 0.f : mn0;
+                    const float nb1 = mn1 == neg_inf() ? 0.f : mn1;
+                    const float al0 = ex2(m0 - nb0), al1 = ex2(m1 - nb1);
+                    l0 *= al0;
+                    l1 *= al1;
 #pragma unroll
                     for (int i = 0; i < D / 16; ++i) {
                         o[i][0] *= al0;
@@ -790,9 +650,14 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
                         o[i][2] *= al0;
                         o[i][3] *= al1;
                     }
+                    m0 = mn0;
+                    m1 = mn1;
                 }
-                m0 = mn0;
-                m1 = mn1;
+                const float b0 = m0 == neg_inf() ? 0.f : m0;
+                const float b1 = m1 == neg_inf() ? 0.f : m1;
+                const float p0 = ex2(x0 - b0), p1 = ex2(x1 - b1), p2 = ex2(x2 - b0), p3 = ex2(x3 - b1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
                 // ---- P^T as bf16 hi + lo, moved into the B-operand layout
                 const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
                 const uint32_t l01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
@@ -823,7 +688,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
             if (lane == 0) mbar_arrive(&empty[s]);
         }
 
-        if (pc.last && warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 4);
+        if (warp == 0 && lane == 0 && wk.u >= wk.end) PKV_STAMP(a, blockIdx.x, 4);
         // ---- combine the four warps' states for this piece
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -861,25 +726,13 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_bar);
-        // G <= 8: a warp's slice is G*D/4 <= 2*D elements, at most D/16 per
-        // lane and at most three heads
-        if (pc.last) {
-            // the range's last piece: nothing to prefetch; it may merge
-            if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
-            const SliceState<D / 16, 3> st = combine_slice<D, D / 16, 3>(sm_o, sm_m, sm_l, G, G, warp, lane);
-            end_piece<__nv_bfloat16, D>(early, st, pc, G, a, U, cta, warp, lane);
-            break;
-        }
-        Piece nx;
-        have = wk.next(nx);
-        load_q(qf, nx);  // in flight during the barrier and the combine
         if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
-        const SliceState<D / 16, 3> st = combine_slice<D, D / 16, 3>(sm_o, sm_m, sm_l, G, G, warp, lane);
-        end_mid_piece<__nv_bfloat16, D>(early, st, pc, G, a, cta, warp, lane);
+        if (write_piece<__nv_bfloat16, D>(sm_o, sm_m, sm_l, G, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
         ++piece_idx;
-        pc = nx;
     }
-    finish_early<__nv_bfloat16, D, D / 16, 3>(early, G, a, U, warp, lane);
+    // G <= 8: a warp's slice is G*D/4 <= 2*D elements, at most D/16 per lane
+    // and at most three heads
+    signal_pending<__nv_bfloat16, D, D / 16, 3>(pending, npending, G, a, U, warp, lane);
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 5);
 }
 
@@ -922,11 +775,8 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
     wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
     long long k = 0;
     Piece pc;
-    constexpr int kPer = GMAX * D / 128, kHeads = GMAX / 4 + 1;
-    __shared__ EarlyPiece early_sm[C::kWarps];
-    EarlyPiece* early = &early_sm[warp];
-    if (lane == 0) early->has = 0;
-    __syncwarp();
+    Piece pending[2];
+    int npending = 0;
     while (wk.next(pc)) {
         float qr[GMAX][C::kPer];
 #pragma unroll
@@ -996,11 +846,10 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
             }
         }
         __syncthreads();
-        const SliceState<kPer, kHeads> st = combine_slice<D, kPer, kHeads>(sm_o, sm_m, sm_l, GMAX, G, warp, lane);
-        end_piece<T, D>(early, st, pc, G, a, U, cta, warp, lane);
+        if (write_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
         __syncthreads();
     }
-    finish_early<T, D, kPer, kHeads>(early, G, a, U, warp, lane);
+    signal_pending<T, D, GMAX * D / 128, GMAX / 4 + 1>(pending, npending, G, a, U, warp, lane);
 }
 
 // ------------------------------------------------------------------ host side
