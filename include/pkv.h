@@ -67,7 +67,11 @@ typedef enum {
     PKV_ERR_WORKSPACE = 7,   /* workspace NULL or smaller than required        */
     PKV_ERR_TIMEOUT = 8,     /* a bounded in-kernel wait ran out               */
     PKV_ERR_CUDA = 9,        /* a CUDA runtime call failed                     */
-    PKV_ERR_UNSUPPORTED = 10 /* valid request this build does not implement    */
+    PKV_ERR_UNSUPPORTED = 10, /* valid request this build does not implement   */
+    PKV_ERR_OUT_OF_BLOCKS = 11, /* block pool: not enough free blocks            */
+    PKV_ERR_UNKNOWN_SEQUENCE = 12, /* block pool: no such sequence               */
+    PKV_ERR_EXISTS = 13,      /* block pool: the sequence already exists         */
+    PKV_ERR_INVARIANT = 14    /* block pool: an internal invariant is broken     */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -234,6 +238,83 @@ PKV_API pkv_status pkv_decode_attention_noalloc(const void* q, const void* k_cac
                                                 int32_t num_q_heads, float scale, void* out,
                                                 const pkv_cache_desc* desc, uint32_t flags,
                                                 const pkv_decode_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Block pool: the host-side page table that decides where tokens go.
+ * ("Notebook 10. KV cache and serving: bytes, pages, and ceilings",
+ * section 5 "Page pool: prefix sharing and copy-on-write"; release page,
+ * Architectural Breakdown 1: physical block allocator, block table,
+ * fragment-free growth; Highlights: dynamic block reclamation.)
+ *
+ * The pool tracks, per physical block, how many sequences reference it, and
+ * per sequence its length and block table. It stores no K/V: it produces the
+ * slot ids for pkv_append, the copy-on-write pairs for pkv_copy_blocks and the
+ * block tables for pkv_decode_attention.
+ *  - A fresh pool hands out block ids in `pop_order` (default 0, 1, 2, ...);
+ *    freed blocks are reused most-recently-freed first.
+ *  - An append first counts the blocks it needs (one private replacement if
+ *    the sequence's last block is partial and shared, plus one per 16 new
+ *    tokens past the last block's room) and fails with PKV_ERR_OUT_OF_BLOCKS,
+ *    leaving the pool unchanged, if too few are free.
+ *  - Appending into a shared partial last block first replaces it with a
+ *    private block (copy-on-write); the call reports the pair (old, new) the
+ *    cache must copy before the new tokens are written.
+ *  - share_prefix creates a sequence whose first tokens are another's, by
+ *    referencing the source's first ceil(prefix / block_size) blocks.
+ *  - release drops a sequence; blocks nobody references return to the pool.
+ * Sequence ids are caller-chosen int64 values. A pool is not thread-safe.
+ * Host memory only; no CUDA call is made.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_pool pkv_pool;
+
+typedef struct {
+    int64_t total_blocks;
+    int64_t free_blocks;
+    int64_t allocated_blocks;          /* referenced by at least one sequence   */
+    int64_t physical_capacity_tokens;  /* allocated_blocks * block_size         */
+    int64_t physical_payload_tokens;   /* live slots, each block counted once   */
+    int64_t logical_tokens;            /* sum of sequence lengths               */
+    int64_t internal_waste_tokens;     /* capacity - payload                    */
+    int64_t sharing_savings_tokens;    /* logical - payload                     */
+    int64_t sequences;
+} pkv_pool_stats;
+
+/* total_blocks in [1, 2^31); block_size >= 1 (16 for the kernels); pop_order
+ * NULL or a permutation of [0, total_blocks). *out receives the pool. */
+PKV_API pkv_status pkv_pool_create(int64_t total_blocks, int32_t block_size, const int64_t* pop_order,
+                                   pkv_pool** out);
+PKV_API void pkv_pool_destroy(pkv_pool* pool);
+/* Register an empty sequence (PKV_ERR_EXISTS if the id is taken). */
+PKV_API pkv_status pkv_pool_add_sequence(pkv_pool* pool, int64_t seq);
+/* Grow `seq` by `tokens` tokens. slots_out (NULL or `tokens` entries) gets the
+ * slot ids of the new tokens; copy_pair_out (NULL or 2 entries) the
+ * copy-on-write pair {old, new} when *num_pairs_out is 1. */
+PKV_API pkv_status pkv_pool_append(pkv_pool* pool, int64_t seq, int64_t tokens, int64_t* slots_out,
+                                   int64_t* copy_pair_out, int32_t* num_pairs_out);
+/* One append per listed sequence, in list order (the decode step). slots_out
+ * gets sum(tokens) slot ids in list order; pairs_out ([n][2]) the copy-on-write
+ * pairs, *num_pairs_out of them. Each append is preflighted on its own: on
+ * PKV_ERR_OUT_OF_BLOCKS the first *num_done_out appends have been applied. */
+PKV_API pkv_status pkv_pool_append_batch(pkv_pool* pool, const int64_t* seqs, const int64_t* tokens, int64_t n,
+                                         int64_t* slots_out, int64_t* pairs_out, int64_t* num_pairs_out,
+                                         int64_t* num_done_out);
+/* Create `target` sharing the first `prefix_tokens` tokens of `source`. */
+PKV_API pkv_status pkv_pool_share_prefix(pkv_pool* pool, int64_t source, int64_t target, int64_t prefix_tokens);
+/* Drop `seq`; its unreferenced blocks become free (most recently freed first). */
+PKV_API pkv_status pkv_pool_release(pkv_pool* pool, int64_t seq);
+PKV_API pkv_status pkv_pool_sequence_length(const pkv_pool* pool, int64_t seq, int64_t* length_out);
+/* Block table of `seq`: *num_blocks_out entries are written if they fit in
+ * `capacity` (else PKV_ERR_SHAPE and only *num_blocks_out is set). */
+PKV_API pkv_status pkv_pool_page_table(const pkv_pool* pool, int64_t seq, int32_t* table_out, int64_t capacity,
+                                       int64_t* num_blocks_out);
+/* Tables of n sequences as rows of `width` int32 entries padded with -1, and
+ * their lengths: the block_tables / context_lens of pkv_decode_attention. */
+PKV_API pkv_status pkv_pool_block_tables(const pkv_pool* pool, const int64_t* seqs, int64_t n, int32_t* tables_out,
+                                         int64_t width, int32_t* lens_out);
+PKV_API pkv_status pkv_pool_get_stats(const pkv_pool* pool, pkv_pool_stats* out);
+/* Check every invariant of section 5 (free list, table lengths, reference
+ * counts, fills); PKV_ERR_INVARIANT if one is broken. */
+PKV_API pkv_status pkv_pool_validate(const pkv_pool* pool);
 
 /*
  * pkv_device_status -- read (and with clear != 0, reset) the sticky device

@@ -1,4 +1,5 @@
-"""Build libpkv.so in-tree: every .cu under csrc/ compiled for sm_103a.
+"""Build libpkv.so in-tree: every .cu (and host-only .cpp) under csrc/,
+compiled for sm_103a.
 
 Usage: ``python -m paged_kv_cache_209_gb300.build`` (or call ``build()``).
 Objects go to ``_build/`` beside this file; the shared library lands next to
@@ -56,14 +57,14 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False,
     build_dir = BUILD if out_dir is None else os.path.join(out_dir, "_build")
     lib_path = LIB if out_dir is None else os.path.join(out_dir, "libpkv.so")
     os.makedirs(build_dir, exist_ok=True)
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     hdr_time = _newest_header()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     extra += [f"-D{k}={v}" for k, v in (defines or {}).items()]
     jobs = []
     objs = []
     for src in sources:
-        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         stale = force or ptxas_info or not os.path.exists(obj) or \
             os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_time)

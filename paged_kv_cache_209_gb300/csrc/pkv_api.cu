@@ -98,6 +98,10 @@ const char* pkv_status_string(pkv_status s) {
         case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
         case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
         case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS";
+        case PKV_ERR_UNKNOWN_SEQUENCE: return "PKV_ERR_UNKNOWN_SEQUENCE";
+        case PKV_ERR_EXISTS: return "PKV_ERR_EXISTS";
+        case PKV_ERR_INVARIANT: return "PKV_ERR_INVARIANT";
     }
     return "PKV_ERR_UNKNOWN";
 }

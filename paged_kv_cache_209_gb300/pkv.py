@@ -23,7 +23,8 @@ PKV_FLAG_CHECKED = 1
 PKV_FLAG_TEST_STALL = 0x80000000
 PKV_DEVERR_TIMEOUT, PKV_DEVERR_RANGE = 1, 2
 STATUS_NAMES = ["PKV_OK", "PKV_ERR_NULL", "PKV_ERR_SHAPE", "PKV_ERR_DTYPE", "PKV_ERR_ALIGN", "PKV_ERR_RANGE",
-                "PKV_ERR_OVERLAP", "PKV_ERR_WORKSPACE", "PKV_ERR_TIMEOUT", "PKV_ERR_CUDA", "PKV_ERR_UNSUPPORTED"]
+                "PKV_ERR_OVERLAP", "PKV_ERR_WORKSPACE", "PKV_ERR_TIMEOUT", "PKV_ERR_CUDA", "PKV_ERR_UNSUPPORTED",
+                "PKV_ERR_OUT_OF_BLOCKS", "PKV_ERR_UNKNOWN_SEQUENCE", "PKV_ERR_EXISTS", "PKV_ERR_INVARIANT"]
 
 
 class PkvError(RuntimeError):
@@ -40,6 +41,12 @@ class CacheDesc(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
+class PoolStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "total_blocks", "free_blocks", "allocated_blocks", "physical_capacity_tokens", "physical_payload_tokens",
+        "logical_tokens", "internal_waste_tokens", "sharing_savings_tokens", "sequences")]
+
+
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32)]
 
@@ -47,7 +54,10 @@ class DecodeOpts(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("pkv_append", "pkv_copy_blocks", "pkv_decode_workspace_size", "pkv_decode_attention",
-           "pkv_decode_attention_noalloc", "pkv_device_status", "pkv_status_string", "pkv_version")
+           "pkv_decode_attention_noalloc", "pkv_device_status", "pkv_status_string", "pkv_version",
+           "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_add_sequence", "pkv_pool_append", "pkv_pool_append_batch",
+           "pkv_pool_share_prefix", "pkv_pool_release", "pkv_pool_sequence_length", "pkv_pool_page_table",
+           "pkv_pool_block_tables", "pkv_pool_get_stats", "pkv_pool_validate")
 
 # Size of the library's built-in workspace used by pkv_decode_attention_noalloc.
 PKV_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
@@ -81,6 +91,24 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_version.argtypes = []
     lib.pkv_version.restype = i32
+    pp, i64p, i32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+    lib.pkv_pool_create.argtypes = [i64, i32, vp, ctypes.POINTER(ctypes.c_void_p)]
+    lib.pkv_pool_destroy.argtypes = [pp]
+    lib.pkv_pool_destroy.restype = None
+    lib.pkv_pool_add_sequence.argtypes = [pp, i64]
+    lib.pkv_pool_append.argtypes = [pp, i64, i64, vp, vp, i32p]
+    lib.pkv_pool_append_batch.argtypes = [pp, vp, vp, i64, vp, vp, i64p, i64p]
+    lib.pkv_pool_share_prefix.argtypes = [pp, i64, i64, i64]
+    lib.pkv_pool_release.argtypes = [pp, i64]
+    lib.pkv_pool_sequence_length.argtypes = [pp, i64, i64p]
+    lib.pkv_pool_page_table.argtypes = [pp, i64, vp, i64, i64p]
+    lib.pkv_pool_block_tables.argtypes = [pp, vp, i64, vp, i64, vp]
+    lib.pkv_pool_get_stats.argtypes = [pp, ctypes.POINTER(PoolStats)]
+    lib.pkv_pool_validate.argtypes = [pp]
+    for name in ("pkv_pool_create", "pkv_pool_add_sequence", "pkv_pool_append", "pkv_pool_append_batch",
+                 "pkv_pool_share_prefix", "pkv_pool_release", "pkv_pool_sequence_length", "pkv_pool_page_table",
+                 "pkv_pool_block_tables", "pkv_pool_get_stats", "pkv_pool_validate"):
+        getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -235,3 +263,98 @@ def pkv_status_string(status: int) -> str:
 
 def pkv_version() -> int:
     return int(load_library().pkv_version())
+
+
+class BlockPool:
+    """Host-side page table of the paged cache (the library's pkv_pool_*).
+
+    Sequence ids are ints. Methods raise PkvError on a non-OK status; the
+    pool is unchanged after a failed call (an append batch keeps the appends
+    before the failing one, see ``append_batch``).
+    """
+
+    def __init__(self, total_blocks: int, block_size: int = 16, pop_order=None):
+        import numpy as np
+        self._lib = load_library()
+        self._np = np
+        handle = ctypes.c_void_p()
+        order = None if pop_order is None else np.ascontiguousarray(pop_order, dtype=np.int64)
+        _check("pkv_pool_create", self._lib.pkv_pool_create(
+            int(total_blocks), int(block_size), None if order is None else order.ctypes.data, ctypes.byref(handle)))
+        self._h = handle
+        self.total_blocks = int(total_blocks)
+        self.block_size = int(block_size)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.pkv_pool_destroy(h)
+            self._h = None
+
+    def add_sequence(self, seq: int) -> None:
+        _check("pkv_pool_add_sequence", self._lib.pkv_pool_add_sequence(self._h, int(seq)))
+
+    def append(self, seq: int, tokens: int):
+        """Returns (slot ids of the new tokens, copy pair (old, new) or None)."""
+        np = self._np
+        slots = np.empty(max(int(tokens), 0), dtype=np.int64)
+        pair = np.empty(2, dtype=np.int64)
+        n = ctypes.c_int32(0)
+        _check("pkv_pool_append", self._lib.pkv_pool_append(
+            self._h, int(seq), int(tokens), slots.ctypes.data if len(slots) else None, pair.ctypes.data,
+            ctypes.byref(n)))
+        return slots, (int(pair[0]), int(pair[1])) if n.value else None
+
+    def append_batch(self, seqs, tokens):
+        """One append per sequence, in order. Returns (slots, copy pairs [k][2])."""
+        np = self._np
+        seqs = np.ascontiguousarray(seqs, dtype=np.int64)
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        slots = np.empty(int(tokens.sum()), dtype=np.int64)
+        pairs = np.empty((len(seqs), 2), dtype=np.int64)
+        npairs, ndone = ctypes.c_int64(0), ctypes.c_int64(0)
+        _check("pkv_pool_append_batch", self._lib.pkv_pool_append_batch(
+            self._h, seqs.ctypes.data, tokens.ctypes.data, len(seqs), slots.ctypes.data if len(slots) else None,
+            pairs.ctypes.data, ctypes.byref(npairs), ctypes.byref(ndone)))
+        return slots, pairs[:npairs.value].copy()
+
+    def share_prefix(self, source: int, target: int, prefix_tokens: int) -> None:
+        _check("pkv_pool_share_prefix", self._lib.pkv_pool_share_prefix(self._h, int(source), int(target),
+                                                                         int(prefix_tokens)))
+
+    def release(self, seq: int) -> None:
+        _check("pkv_pool_release", self._lib.pkv_pool_release(self._h, int(seq)))
+
+    def sequence_length(self, seq: int) -> int:
+        n = ctypes.c_int64(0)
+        _check("pkv_pool_sequence_length", self._lib.pkv_pool_sequence_length(self._h, int(seq), ctypes.byref(n)))
+        return n.value
+
+    def page_table(self, seq: int):
+        np = self._np
+        n = ctypes.c_int64(0)
+        st = self._lib.pkv_pool_page_table(self._h, int(seq), None, 0, ctypes.byref(n))
+        if st not in (0, 2):
+            _check("pkv_pool_page_table", st)
+        out = np.empty(n.value, dtype=np.int32)
+        _check("pkv_pool_page_table", self._lib.pkv_pool_page_table(
+            self._h, int(seq), out.ctypes.data if n.value else None, n.value, ctypes.byref(n)))
+        return tuple(int(b) for b in out)
+
+    def block_tables(self, seqs, width: int):
+        """(int32 tables [n][width] padded with -1, int32 lengths [n])."""
+        np = self._np
+        seqs = np.ascontiguousarray(seqs, dtype=np.int64)
+        tables = np.empty((len(seqs), int(width)), dtype=np.int32)
+        lens = np.empty(len(seqs), dtype=np.int32)
+        _check("pkv_pool_block_tables", self._lib.pkv_pool_block_tables(
+            self._h, seqs.ctypes.data, len(seqs), tables.ctypes.data, int(width), lens.ctypes.data))
+        return tables, lens
+
+    def stats(self) -> dict:
+        st = PoolStats()
+        _check("pkv_pool_get_stats", self._lib.pkv_pool_get_stats(self._h, ctypes.byref(st)))
+        return {name: getattr(st, name) for name, _ in PoolStats._fields_}
+
+    def validate(self) -> None:
+        _check("pkv_pool_validate", self._lib.pkv_pool_validate(self._h))
