@@ -21,9 +21,13 @@ What it restates, in float64 (or exact integer / byte arithmetic):
 * ``attention``   -- gather K/V through a block table, then max-subtracted
   softmax attention (notebook project demo, Demo 2 ``attention``), with the
   grouped-query head mapping of notebook section 3.
+* ``prefix``      -- the two-phase (chunk-first over blocks shared by a group
+  of sequences, then sequence-first over each suffix) decode and its
+  log-sum-exp combination (paper-search page, ChunkAttention abstract;
+  notebook sections 5 and 7).
 
 Pins that tie these functions to the pages (not to themselves) live in
 ``tests/test_oracle_*.py`` and ``tests/golden/``.
 """
 
-from . import geometry, paged_pool, kv_ops, attention  # noqa: F401
+from . import geometry, paged_pool, kv_ops, attention, prefix  # noqa: F401
