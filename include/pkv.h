@@ -207,6 +207,68 @@ PKV_API pkv_status pkv_decode_attention(const void* q, const void* k_cache, cons
                                 const pkv_decode_opts* opts, void* stream);
 
 /*
+ * pkv_decode_prefixed_workspace_size -- bytes of device workspace
+ * pkv_decode_attention_prefixed needs (same zero-fill rule as above: zero it
+ * once before first use; completed calls leave their counters at zero).
+ * num_groups and max_group_blocks as in that call. Returns 0 for invalid sizes.
+ */
+PKV_API size_t pkv_decode_prefixed_workspace_size(int32_t batch, int32_t num_q_heads,
+                                                  int32_t max_blocks_per_seq, int32_t num_groups,
+                                                  int32_t max_group_blocks,
+                                                  const pkv_cache_desc* desc,
+                                                  const pkv_decode_opts* opts);
+
+/*
+ * pkv_decode_attention_prefixed -- pkv_decode_attention for a batch in which
+ * groups of sequences share leading blocks, computed in two phases.
+ * (paper-search page, ChunkAttention abstract: KV split into chunks that
+ * requests with a common prompt prefix share, and a "two-phase partition"
+ * kernel that reads a shared chunk once for all of them; notebook section 5
+ * `share_prefix`: the target's table begins with the source's first
+ * ceil(prefix/B) blocks, and section 7, prefix reuse.)
+ *
+ * Sequence i is a member of group g = prefix_group[i] when 0 <= g <
+ * num_groups, 0 <= group_blocks[g] <= max_group_blocks and its context holds
+ * group_blocks[g] whole blocks (16 * group_blocks[g] <= context_lens[i]).
+ * The caller guarantees that the first group_blocks[g] entries of every
+ * member's block table are the same physical blocks. Phase 1 attends the
+ * queries of all members of a group together over those shared blocks (each
+ * shared block is read once per 64 query rows: 64 / G members); phase 2
+ * attends each sequence over the rest of its context; the two partials are
+ * combined by their log-sum-exp weights. A sequence with prefix_group[i] < 0,
+ * or one that names a group but fails the membership rule (this also sets
+ * PKV_DEVERR_RANGE), is attended in one pass.
+ *
+ * The result equals pkv_decode_attention's on the same arguments, up to
+ * fp32 rounding order: the groups change the work, not the output. A shared
+ * partial last block is not shared here: its tokens belong to phase 2.
+ *
+ *   prefix_group      device, int32 [batch]: group of each sequence, or -1.
+ *   group_blocks      device, int32 [num_groups]: shared whole blocks per group.
+ *   num_groups        0..1024 (more: PKV_ERR_UNSUPPORTED); 0 = plain call.
+ *   max_group_blocks  host-side bound on group_blocks[], <= max_blocks_per_seq;
+ *                     sizes the split of the shared blocks over CTAs.
+ *   workspace         >= pkv_decode_prefixed_workspace_size(...) bytes,
+ *                     256-byte aligned, zero-filled before its first use.
+ * Other arguments, results and errors are pkv_decode_attention's. Phase 1
+ * runs on the tensor-core path (bf16, head_dim 64/128, G <= 8); elsewhere the
+ * groups are ignored and the call is pkv_decode_attention. With
+ * PKV_FLAG_CHECKED it also returns PKV_ERR_RANGE, writing nothing, when a
+ * sequence names a group but fails the membership rule or its table does not
+ * begin with the group's first member's group_blocks[g] entries. Two kernel
+ * launches per 1024 sequences.
+ */
+PKV_API pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, const void* v_cache,
+                                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                 const int32_t* context_lens, int32_t batch,
+                                                 int32_t num_q_heads, float scale,
+                                                 const int32_t* prefix_group, const int32_t* group_blocks,
+                                                 int32_t num_groups, int32_t max_group_blocks, void* out,
+                                                 void* workspace, size_t workspace_bytes,
+                                                 const pkv_cache_desc* desc, uint32_t flags,
+                                                 const pkv_decode_opts* opts, void* stream);
+
+/*
  * pkv_decode_attention_noalloc -- pkv_decode_attention without a
  * caller-provided workspace. The pages have no counterpart to this call; it
  * exists for callers that cannot allocate device memory: plugins running

@@ -204,7 +204,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
     const int64_t row = static_cast<int64_t>(num_q_heads) * desc->head_dim * elem;
     for (int32_t b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {
         const int32_t nb = batch - b0 < kMaxBatchPerLaunch ? batch - b0 : kMaxBatchPerLaunch;
-        DecodeArgs a;
+        DecodeArgs a{};
         a.q = static_cast<const char*>(q) + b0 * row;
         a.k_cache = k_cache;
         a.v_cache = v_cache;
@@ -227,6 +227,148 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
         a.test_stall = (flags & PKV_FLAG_TEST_STALL) ? 1 : 0;
         a.scale = scale;
         if (launch_decode(a, plan, s) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+size_t pkv_decode_prefixed_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                          int32_t num_groups, int32_t max_group_blocks, const pkv_cache_desc* desc,
+                                          const pkv_decode_opts* opts) {
+    if (check_desc(desc) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return 0;
+    if (num_groups < 0 || num_groups > kMaxBatchPerLaunch || max_group_blocks < 0) return 0;
+    DecodePlan plan;
+    if (decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan, true) != PKV_OK) return 0;
+    const int G = num_q_heads / desc->num_kv_heads;
+    const size_t base = decode_workspace_layout(batch, desc->num_kv_heads, plan.num_ctas, G, desc->head_dim).total;
+    if (plan.kernel != 2 || num_groups == 0) return base;
+    return prefix_plan(batch, num_groups, num_q_heads, desc->num_kv_heads, desc->head_dim, max_group_blocks, base)
+        .total;
+}
+
+pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                                         float scale, const int32_t* prefix_group, const int32_t* group_blocks,
+                                         int32_t num_groups, int32_t max_group_blocks, void* out, void* workspace,
+                                         size_t workspace_bytes, const pkv_cache_desc* desc, uint32_t flags,
+                                         const pkv_decode_opts* opts, void* stream) {
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (num_groups < 0 || max_group_blocks < 0 || max_group_blocks > max_blocks_per_seq) return PKV_ERR_SHAPE;
+    if (num_groups > kMaxBatchPerLaunch) return PKV_ERR_UNSUPPORTED;
+    if (flags & PKV_FLAG_TEST_STALL) return PKV_ERR_UNSUPPORTED;
+    if (num_groups > 0 && batch > 0) {
+        if (prefix_group == nullptr || group_blocks == nullptr) return PKV_ERR_NULL;
+        if ((reinterpret_cast<uintptr_t>(prefix_group) & 3u) || (reinterpret_cast<uintptr_t>(group_blocks) & 3u))
+            return PKV_ERR_ALIGN;
+    }
+    if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
+    DecodePlan plan;
+    int rc = decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan, true);
+    if (rc != PKV_OK) return static_cast<pkv_status>(rc);
+    // Without groups, or where only the CUDA-core kernel applies, the groups
+    // are only a hint: the plain call computes the same result.
+    if (num_groups == 0 || plan.kernel != 2 || batch == 0) {
+        if (num_groups > 0 && batch > 0 && (flags & PKV_FLAG_CHECKED)) {
+            cudaStream_t s = static_cast<cudaStream_t>(stream);
+            if (max_blocks_per_seq < 1) return PKV_ERR_SHAPE;
+            st = run_checked([&](unsigned int* verdict) {
+                return launch_check_groups(block_tables, max_blocks_per_seq, context_lens, prefix_group,
+                                           group_blocks, num_groups, max_group_blocks, batch, verdict, s);
+            }, s);
+            if (st != PKV_OK) return st;
+        }
+        return pkv_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                                    num_q_heads, scale, out, workspace, workspace_bytes, desc, flags, opts, stream);
+    }
+    if (!isfinite(scale)) return PKV_ERR_SHAPE;
+    if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
+    if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
+        return PKV_ERR_SHAPE;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace) return PKV_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_ALIGN;
+    const int G = num_q_heads / desc->num_kv_heads;
+    const WorkspaceLayout wl = decode_workspace_layout(batch, desc->num_kv_heads, plan.num_ctas, G, desc->head_dim);
+    const PrefixPlan pp =
+        prefix_plan(batch, num_groups, num_q_heads, desc->num_kv_heads, desc->head_dim, max_group_blocks, wl.total);
+    if (workspace_bytes < pp.total) return PKV_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    if (flags & PKV_FLAG_CHECKED) {
+        st = run_checked([&](unsigned int* verdict) {
+            cudaError_t e = launch_check_decode(block_tables, max_blocks_per_seq, context_lens, batch,
+                                                desc->num_blocks, verdict, s);
+            if (e != cudaSuccess) return e;
+            return launch_check_groups(block_tables, max_blocks_per_seq, context_lens, prefix_group, group_blocks,
+                                       num_groups, max_group_blocks, batch, verdict, s);
+        }, s);
+        if (st != PKV_OK) return st;
+    }
+    char* ws = static_cast<char*>(workspace);
+    const int64_t row = static_cast<int64_t>(num_q_heads) * desc->head_dim * 2;
+    for (int32_t b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {
+        const int32_t nb = batch - b0 < kMaxBatchPerLaunch ? batch - b0 : kMaxBatchPerLaunch;
+        DecodeArgs a{};
+        a.q = static_cast<const char*>(q) + b0 * row;
+        a.k_cache = k_cache;
+        a.v_cache = v_cache;
+        a.tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
+        a.lens = context_lens + b0;
+        a.out = static_cast<char*>(out) + b0 * row;
+        a.partials = reinterpret_cast<float*>(ws + wl.partials_offset);
+        a.counters = reinterpret_cast<int*>(ws + wl.counters_offset);
+        a.trace = wl.trace_offset ? ws + wl.trace_offset : nullptr;
+        a.status = status;
+        a.num_blocks = desc->num_blocks;
+        a.max_blocks = max_blocks_per_seq;
+        a.batch = nb;
+        a.q_heads = num_q_heads;
+        a.kv_heads = desc->num_kv_heads;
+        a.head_dim = desc->head_dim;
+        a.group = G;
+        a.dtype = desc->dtype;
+        a.num_ctas = plan.num_ctas;
+        a.test_stall = 0;
+        a.scale = scale;
+        a.prefix_group = prefix_group + b0;
+        a.group_blocks = group_blocks;
+        a.num_groups = num_groups;
+        a.max_group_blocks = max_group_blocks;
+        a.fold_o = reinterpret_cast<float*>(ws + pp.fold_o_offset);
+        a.fold_lse = reinterpret_cast<float*>(ws + pp.fold_lse_offset);
+        if (launch_decode(a, plan, s) != cudaSuccess) return PKV_ERR_CUDA;
+        PrefixArgs pa{};
+        pa.q = a.q;
+        pa.k_cache = k_cache;
+        pa.v_cache = v_cache;
+        pa.tables = a.tables;
+        pa.lens = a.lens;
+        pa.prefix_group = a.prefix_group;
+        pa.group_blocks = group_blocks;
+        pa.fold_o = a.fold_o;
+        pa.fold_lse = a.fold_lse;
+        pa.out = a.out;
+        pa.partials = reinterpret_cast<float*>(ws + pp.partials_offset);
+        pa.counters = reinterpret_cast<int*>(ws + pp.counters_offset);
+        pa.status = status;
+        pa.num_blocks = desc->num_blocks;
+        pa.max_blocks = max_blocks_per_seq;
+        pa.batch = nb;
+        pa.num_groups = num_groups;
+        pa.max_group_blocks = max_group_blocks;
+        pa.q_heads = num_q_heads;
+        pa.kv_heads = desc->num_kv_heads;
+        pa.head_dim = desc->head_dim;
+        pa.group = G;
+        pa.tiles = pp.tiles;
+        pa.chunks = pp.chunks;
+        pa.chunk_blocks = pp.chunk_blocks;
+        pa.scale = scale;
+        if (launch_prefix(pa, s) != cudaSuccess) return PKV_ERR_CUDA;
     }
     return PKV_OK;
 }

@@ -61,14 +61,26 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // ------------------------------------------------------------------ schedule
 // s_pre[i] = sum_{i' <= i} ceil(len_i' / 16) over this launch's sequences,
 // s_len[i] = len_i clamped to [0, max_blocks * 16].
-__device__ void build_prefix(int32_t* s_pre, int32_t* s_len, const int32_t* __restrict__ lens, int batch,
-                             int max_blocks, unsigned int* status) {
-    const int cap = max_blocks * 16;
-    for (int i = threadIdx.x; i < batch; i += blockDim.x) {
-        int n = lens[i];
+//
+// With shared-prefix groups (s_boff non-null) a member of a group (the rule
+// of prefix_member_blocks) attends here only its tokens past the group's
+// shared blocks: s_len[i] is that own-token count and s_boff[i] the block
+// offset at which they start, -1 for a plain sequence. A sequence that names
+// a group but fails the rule sets PKV_DEVERR_RANGE and is attended whole.
+__device__ void build_prefix(int32_t* s_pre, int32_t* s_len, int32_t* s_boff, const DecodeArgs& a) {
+    const int cap = a.max_blocks * 16;
+    for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
+        int n = a.lens[i];
         if (n < 0 || n > cap) {
-            if (blockIdx.x == 0) atomicOr(status, PKV_DEVERR_RANGE);
+            if (blockIdx.x == 0) atomicOr(a.status, PKV_DEVERR_RANGE);
             n = n < 0 ? 0 : cap;
+        }
+        if (s_boff != nullptr) {
+            const int nb =
+                prefix_member_blocks(a.prefix_group, a.group_blocks, a.num_groups, a.max_group_blocks, n, i);
+            if (nb < 0 && a.prefix_group[i] >= 0 && blockIdx.x == 0) atomicOr(a.status, PKV_DEVERR_RANGE);
+            s_boff[i] = nb;
+            if (nb > 0) n -= nb * 16;
         }
         s_len[i] = n;
         s_pre[i] = (n + 15) >> 4;
@@ -77,14 +89,14 @@ __device__ void build_prefix(int32_t* s_pre, int32_t* s_len, const int32_t* __re
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         int carry = 0;
-        for (int base = 0; base < batch; base += 32) {
-            int x = base + lane < batch ? s_pre[base + lane] : 0;
+        for (int base = 0; base < a.batch; base += 32) {
+            int x = base + lane < a.batch ? s_pre[base + lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, x, o);
                 if (lane >= o) x += y;
             }
-            if (base + lane < batch) s_pre[base + lane] = x + carry;
+            if (base + lane < a.batch) s_pre[base + lane] = x + carry;
             carry += __shfl_sync(0xffffffffu, x, 31);
         }
     }
@@ -208,13 +220,17 @@ __device__ __forceinline__ int pieces_of_segment(long long c0, long long c1, lon
 // shared memory (sm_o[(w*gstride + g)*D + d], sm_m/sm_l[w*gstride + g]).
 // A whole segment is normalised and written out directly. A cut segment's
 // piece goes to this CTA's slot in the workspace; it is announced later by
-// signal_pending. Returns true for a cut segment.
+// signal_pending. Returns true for a cut segment. With `fold` (a sequence of
+// a shared-prefix group) a whole segment's rows go to fold_o / fold_lse
+// instead of out.
 template <typename T, int D>
 __device__ bool write_piece(const float* sm_o, const float* sm_m, const float* sm_l, int gstride, int G,
-                            const Piece& pc, const DecodeArgs& a, long long cta, int warp, int lane) {
+                            const Piece& pc, const DecodeArgs& a, long long cta, int warp, int lane, bool fold) {
     const int S = G * D / 4;
     const int e0 = warp * S;
-    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
+    const long long row0 = static_cast<long long>(pc.seq) * a.q_heads + pc.head * G;
+    T* out_row = static_cast<T*>(a.out) + row0 * D;
+    float* fold_row = fold ? a.fold_o + row0 * D : nullptr;
     float* slice = nullptr;
     if (!pc.complete) slice = piece_slice(a.partials, cta, pc.first ? 0 : 1, warp, S, G);
     for (int e = e0 + lane; e < e0 + S; e += 32) {
@@ -230,12 +246,14 @@ __device__ bool write_piece(const float* sm_o, const float* sm_m, const float* s
             o += wt * sm_o[(w * gstride + g) * D + d];
             L += wt * sm_l[w * gstride + g];
         }
-        if (pc.complete)
-            store_out<T>(out_row + e, L > 0.f ? o / L : 0.f);
-        else
+        if (!pc.complete)
             slice[e - e0] = o;
+        else if (fold)
+            fold_row[e] = L > 0.f ? o / L : 0.f;
+        else
+            store_out<T>(out_row + e, L > 0.f ? o / L : 0.f);
     }
-    if (pc.complete) return false;
+    if (pc.complete && !(fold && warp == 0)) return false;
     if (lane < G) {
         float M = neg_inf();
         for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * gstride + lane]);
@@ -245,10 +263,14 @@ __device__ bool write_piece(const float* sm_o, const float* sm_m, const float* s
             const float mw = sm_m[w * gstride + lane];
             L += (mw == neg_inf()) ? 0.f : ex2(mw - base) * sm_l[w * gstride + lane];
         }
-        slice[S + lane] = M;
-        slice[S + G + lane] = L;
+        if (pc.complete) {
+            a.fold_lse[row0 + lane] = L > 0.f ? M + log2f(L) : neg_inf();
+        } else {
+            slice[S + lane] = M;
+            slice[S + G + lane] = L;
+        }
     }
-    return true;
+    return !pc.complete;
 }
 
 // CTA holding piece p (0-based) of the segment that starts at unit S0 and
@@ -289,7 +311,7 @@ __device__ __forceinline__ void load_piece(PieceVals<NPER, NG>& v, const float* 
 // the current two are combined (online log-sum-exp, per head).
 template <typename T, int D, int NPER, int NG>
 __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane,
-                            long long c0, int slot0, int npieces) {
+                            long long c0, int slot0, int npieces, bool fold) {
     const int S = G * D / 4;
     const int e0 = warp * S;
     const long long C = a.num_ctas;
@@ -344,7 +366,8 @@ __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long lo
 #pragma unroll
         for (int u = 0; u < 2; ++u) cur[u] = nxt[u];
     }
-    T* out_row = static_cast<T*>(a.out) + (static_cast<long long>(pc.seq) * a.q_heads + pc.head * G) * D;
+    const long long row0 = static_cast<long long>(pc.seq) * a.q_heads + pc.head * G;
+    T* out_row = static_cast<T*>(a.out) + row0 * D;
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
         const int e = lane + 32 * j;
@@ -352,7 +375,18 @@ __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long lo
         float Lj = 0.f;
 #pragma unroll
         for (int k = 0; k < NG; ++k) Lj = kj[j] == k ? L[k] : Lj;
-        store_out<T>(out_row + e0 + e, Lj > 0.f ? O[j] / Lj : 0.f);
+        if (fold)
+            a.fold_o[row0 * D + e0 + e] = Lj > 0.f ? O[j] / Lj : 0.f;
+        else
+            store_out<T>(out_row + e0 + e, Lj > 0.f ? O[j] / Lj : 0.f);
+    }
+    if (fold && lane == 0) {
+        // the log-sum-exp of each head whose first element is in this slice
+#pragma unroll
+        for (int k = 0; k < NG; ++k) {
+            const int g = g_first + k;
+            if (k < ng && g * D >= e0) a.fold_lse[row0 + g] = L[k] > 0.f ? M[k] + log2f(L[k]) : neg_inf();
+        }
     }
 }
 
@@ -363,7 +397,7 @@ __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long lo
 // next call.
 template <typename T, int D, int NPER, int NG>
 __device__ void signal_pending(const Piece* pending, int npending, int G, const DecodeArgs& a, long long U,
-                               int warp, int lane) {
+                               int warp, int lane, const int32_t* s_boff) {
     if (npending == 0) return;
     __threadfence();
     __syncwarp();
@@ -390,18 +424,28 @@ __device__ void signal_pending(const Piece* pending, int npending, int G, const 
         __threadfence();
         const Piece& pc = pending[i];
         const int slot0 = (pc.seg_start == range_start(c0s[i], U, C)) ? 0 : 1;
-        merge_slice<T, D, NPER, NG>(pc, G, a, U, warp, lane, c0s[i], slot0, nps[i]);
+        merge_slice<T, D, NPER, NG>(pc, G, a, U, warp, lane, c0s[i], slot0, nps[i],
+                                    s_boff != nullptr && s_boff[pc.seq] >= 0);
         if (lane == 0) *counters[i] = 0;
     }
 }
 
 // Rows of sequences with no tokens are zero; CTA c writes those of the
-// sequences i with i % num_ctas == c.
+// sequences i with i % num_ctas == c. A shared-prefix group member with no
+// own tokens gets the empty partial instead (zero output, -inf log-sum-exp).
 template <typename T>
-__device__ void zero_empty_rows(const int32_t* s_len, const DecodeArgs& a, int tid, int nthreads) {
+__device__ void zero_empty_rows(const int32_t* s_len, const int32_t* s_boff, const DecodeArgs& a, int tid,
+                                int nthreads) {
     const int row = a.q_heads * a.head_dim;
     for (int i = blockIdx.x; i < a.batch; i += a.num_ctas) {
         if (s_len[i] != 0) continue;
+        if (s_boff != nullptr && s_boff[i] >= 0) {
+            float* f = a.fold_o + static_cast<long long>(i) * row;
+            for (int e = tid; e < row; e += nthreads) f[e] = 0.f;
+            for (int e = tid; e < a.q_heads; e += nthreads)
+                a.fold_lse[static_cast<long long>(i) * a.q_heads + e] = neg_inf();
+            continue;
+        }
         T* out = static_cast<T*>(a.out) + static_cast<long long>(i) * row;
         for (int e = tid; e < row; e += nthreads) store_out<T>(out + e, 0.f);
     }
@@ -455,6 +499,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     const int buf_floats = C::kConsumers * G * (D + 2);
     int32_t* s_pre = reinterpret_cast<int32_t*>(scratch + 2 * buf_floats);
     int32_t* s_len = s_pre + a.batch;
+    int32_t* s_boff = a.prefix_group != nullptr ? s_len + a.batch : nullptr;  // shared-prefix mode only
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -480,7 +525,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     // the stream (typically the append) must be complete.
     grid_dependency_wait();
     allow_dependents();
-    build_prefix(s_pre, s_len, a.lens, a.batch, a.max_blocks, a.status);  // contains __syncthreads
+    build_prefix(s_pre, s_len, s_boff, a);  // contains __syncthreads
     if (threadIdx.x == 0) PKV_STAMP(a, blockIdx.x, 1);
 
     const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
@@ -500,7 +545,8 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         Piece pc;
         bool ok = true;
         while (ok && wk.next(pc)) {
-            const int32_t* trow = a.tables + static_cast<long long>(pc.seq) * a.max_blocks + pc.blk_from;
+            const int boff = s_boff != nullptr ? max(s_boff[pc.seq], 0) : 0;
+            const int32_t* trow = a.tables + static_cast<long long>(pc.seq) * a.max_blocks + boff + pc.blk_from;
             const int cnt_piece = pc.blk_to - pc.blk_from;
             int cur = lane < cnt_piece ? __ldg(trow + lane) : 0;
             for (int b0 = 0; ok && b0 < cnt_piece; b0 += 32) {
@@ -566,7 +612,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     const int v_row = r8 + 8 * (q8 >> 1);     // V: token row
     const int v_chunk = q8 & 1;               // V: +0 / +1 chunk within an m-tile
 
-    zero_empty_rows<__nv_bfloat16>(s_len, a, threadIdx.x, C::kConsumers * 32);
+    zero_empty_rows<__nv_bfloat16>(s_len, s_boff, a, threadIdx.x, C::kConsumers * 32);
     Walker wk;
     wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
     long long k = 0;
@@ -727,12 +773,14 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_bar);
         if (!mbar_wait(merge_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
-        if (write_piece<__nv_bfloat16, D>(sm_o, sm_m, sm_l, G, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
+        if (write_piece<__nv_bfloat16, D>(sm_o, sm_m, sm_l, G, G, pc, a, cta, warp, lane,
+                                          s_boff != nullptr && s_boff[pc.seq] >= 0))
+            pending[npending++] = pc;
         ++piece_idx;
     }
     // G <= 8: a warp's slice is G*D/4 <= 2*D elements, at most D/16 per lane
     // and at most three heads
-    signal_pending<__nv_bfloat16, D, D / 16, 3>(pending, npending, G, a, U, warp, lane);
+    signal_pending<__nv_bfloat16, D, D / 16, 3>(pending, npending, G, a, U, warp, lane, s_boff);
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 5);
 }
 
@@ -758,7 +806,7 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
     const int lane = threadIdx.x & 31;
     grid_dependency_wait();
     allow_dependents();
-    build_prefix(s_pre, s_len, a.lens, a.batch, a.max_blocks, a.status);
+    build_prefix(s_pre, s_len, nullptr, a);
 
     const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
     const long long cta = blockIdx.x;
@@ -770,7 +818,7 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
     const T* kc = static_cast<const T*>(a.k_cache);
     const T* vc = static_cast<const T*>(a.v_cache);
 
-    zero_empty_rows<T>(s_len, a, threadIdx.x, C::kThreads);
+    zero_empty_rows<T>(s_len, nullptr, a, threadIdx.x, C::kThreads);
     Walker wk;
     wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
     long long k = 0;
@@ -846,10 +894,10 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
             }
         }
         __syncthreads();
-        if (write_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, warp, lane)) pending[npending++] = pc;
+        if (write_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, warp, lane, false)) pending[npending++] = pc;
         __syncthreads();
     }
-    signal_pending<T, D, GMAX * D / 128, GMAX / 4 + 1>(pending, npending, G, a, U, warp, lane);
+    signal_pending<T, D, GMAX * D / 128, GMAX / 4 + 1>(pending, npending, G, a, U, warp, lane, nullptr);
 }
 
 // ------------------------------------------------------------------ host side
@@ -873,7 +921,7 @@ EncodeTiledFn encode_fn() {
 
 // 2-D view of a pool: rows of head_dim bf16 (one token of one head), boxes of
 // 16 rows x 64 columns with the 128-byte swizzle.
-bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim) {
+bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
@@ -949,7 +997,7 @@ template <int D, int NST>
 cudaError_t run_tc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
     CUtensorMap tmK, tmV;
     const int64_t rows = a.num_blocks * a.kv_heads * 16;
-    if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
+    if (!encode_pool_map(&tmK, a.k_cache, rows, D) || !encode_pool_map(&tmV, a.v_cache, rows, D))
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(decode_tc_kernel<D, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
@@ -957,6 +1005,10 @@ cudaError_t run_tc(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim) {
+    return encode_pool_map(map, pool, rows, head_dim);
+}
 
 WorkspaceLayout decode_workspace_layout(int batch, int kv_heads, int num_ctas, int group, int head_dim) {
     const int chunk = batch < kMaxBatchPerLaunch ? batch : kMaxBatchPerLaunch;
@@ -977,7 +1029,7 @@ WorkspaceLayout decode_workspace_layout(int batch, int kv_heads, int num_ctas, i
 }
 
 int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t max_blocks,
-                const pkv_decode_opts* opts, DecodePlan* plan) {
+                const pkv_decode_opts* opts, DecodePlan* plan, bool prefixed) {
     (void)max_blocks;
     const int G = q_heads / d.num_kv_heads;
     const int want = opts ? opts->kernel : 0;
@@ -997,14 +1049,14 @@ int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t
         const int want_st = opts ? opts->stages : 0;
         for (int st : {8, 12}) {
             if (want_st && want_st != st) continue;
-            size_t sm = 0;
+            size_t sm = prefixed ? static_cast<size_t>(chunk) * 4 : 0;  // per-sequence block offsets
             int n = 0;
             if (d.head_dim == 128) {
-                sm = st == 12 ? Tc<128, 12>::smem_bytes(G, chunk) : Tc<128, 8>::smem_bytes(G, chunk);
+                sm += st == 12 ? Tc<128, 12>::smem_bytes(G, chunk) : Tc<128, 8>::smem_bytes(G, chunk);
                 n = st == 12 ? cached_occupancy(2, 128 * 100 + st, sm, 160, nullptr, tc_query<128, 12>)
                              : cached_occupancy(2, 128 * 100 + st, sm, 160, nullptr, tc_query<128, 8>);
             } else {
-                sm = st == 12 ? Tc<64, 12>::smem_bytes(G, chunk) : Tc<64, 8>::smem_bytes(G, chunk);
+                sm += st == 12 ? Tc<64, 12>::smem_bytes(G, chunk) : Tc<64, 8>::smem_bytes(G, chunk);
                 n = st == 12 ? cached_occupancy(2, 64 * 100 + st, sm, 160, nullptr, tc_query<64, 12>)
                              : cached_occupancy(2, 64 * 100 + st, sm, 160, nullptr, tc_query<64, 8>);
             }

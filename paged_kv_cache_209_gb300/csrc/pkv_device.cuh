@@ -109,6 +109,14 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return policy;
 }
 
+// L2 policy for data that other CTAs read again soon (a shared prefix block
+// is read by every 64-row tile of its group): keep it over streamed data.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
+}
+
 // 2-D tiled bulk-tensor load into shared memory, completion counted in bytes
 // on `bar`, with an L2 cache policy. x is the innermost coordinate
 // (elements), y the row.
@@ -184,6 +192,22 @@ __device__ __forceinline__ float ex2(float x) {
 // lets the next kernel in the stream start its own prologue early.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Shared-prefix groups: the number of shared blocks sequence i attends in
+// the chunk-first pass, or -1 if it takes no part in one. Sequence i is a
+// member of group g = prefix_group[i] when 0 <= g < num_groups, the group's
+// block count nb = group_blocks[g] lies in [0, max_group_blocks] and the
+// sequence's context (n, already clamped to its table) holds nb whole blocks.
+// Anything else makes i a plain sequence; both passes use this one rule, so
+// a malformed group costs only the sharing, never the result.
+__device__ __forceinline__ int prefix_member_blocks(const int32_t* prefix_group, const int32_t* group_blocks,
+                                                    int num_groups, int max_group_blocks, int n, int i) {
+    const int g = prefix_group[i];
+    if (g < 0 || g >= num_groups) return -1;
+    const int nb = group_blocks[g];
+    if (nb < 0 || nb > max_group_blocks || nb > (n >> 4)) return -1;
+    return nb;
+}
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -2,6 +2,7 @@
 // translation units. Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -51,6 +52,16 @@ struct DecodeArgs {
     int32_t num_ctas;
     int32_t test_stall;  // PKV_FLAG_TEST_STALL: the producer issues nothing
     float scale;
+    // Shared-prefix groups (null for a plain call). A sequence with a group
+    // attends only its own blocks past the group's shared ones here, and its
+    // rows go to fold_o / fold_lse instead of out, for the chunk-first pass
+    // to combine with the shared part.
+    const int32_t* prefix_group;  // [batch]: group of sequence i, or -1
+    const int32_t* group_blocks;  // [num_groups]: whole blocks the group shares
+    int32_t num_groups;
+    int32_t max_group_blocks;     // host-side bound on group_blocks[]
+    float* fold_o;                // [batch][q_heads][head_dim]: normalised output over the own tokens
+    float* fold_lse;              // [batch][q_heads]: log2-sum-exp of the scaled logits, -inf if none
 };
 
 // Which kernel a decode call runs and on how many CTAs.
@@ -70,9 +81,61 @@ struct WorkspaceLayout {
     size_t counters_offset, partials_offset, trace_offset, total;
 };
 WorkspaceLayout decode_workspace_layout(int batch, int kv_heads, int num_ctas, int group, int head_dim);
+// `prefixed`: the call carries shared-prefix groups (a per-sequence block
+// offset in shared memory; the tensor-core kernel only).
 int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t max_blocks,
-                const pkv_decode_opts* opts, DecodePlan* plan);
+                const pkv_decode_opts* opts, DecodePlan* plan, bool prefixed = false);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+
+// 2-D TMA view of a bf16 pool: rows of head_dim elements (one token of one
+// KV head), 16-row x 64-column boxes, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim);
+
+// ---------------------------------------------------------------- shared-prefix decode
+// Chunk-first pass: for every group, the queries of all its members against
+// the group's shared blocks, combined with the members' own-token results
+// (fold_o / fold_lse, written by the decode kernel in prefixed mode).
+struct PrefixArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* tables;
+    const int32_t* lens;
+    const int32_t* prefix_group;
+    const int32_t* group_blocks;
+    const float* fold_o;
+    const float* fold_lse;
+    void* out;
+    float* partials;  // [tiles][kv_heads][chunks][64 rows][head_dim + 2]
+    int* counters;    // [tiles][kv_heads][4 warps]; zero between calls
+    unsigned int* status;
+    int64_t num_blocks;
+    int32_t max_blocks;
+    int32_t batch;
+    int32_t num_groups;
+    int32_t max_group_blocks;
+    int32_t q_heads;
+    int32_t kv_heads;
+    int32_t head_dim;
+    int32_t group;         // q_heads / kv_heads
+    int32_t tiles;         // grid x: upper bound on 64-row tiles over all groups
+    int32_t chunks;        // grid y: shared-block chunks per group
+    int32_t chunk_blocks;  // blocks per chunk
+    float scale;
+};
+
+// Grid and workspace of the chunk-first pass for a launch of `batch`
+// sequences (at most kMaxBatchPerLaunch).
+struct PrefixPlan {
+    int tiles, chunks, chunk_blocks;
+    size_t counters_offset, partials_offset, fold_o_offset, fold_lse_offset, total;
+};
+PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int head_dim, int max_group_blocks,
+                       size_t base_offset);
+cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t s);
+cudaError_t launch_check_groups(const int32_t* tables, int32_t max_blocks, const int32_t* lens,
+                                const int32_t* prefix_group, const int32_t* group_blocks, int32_t num_groups,
+                                int32_t max_group_blocks, int32_t batch, unsigned int* verdict, cudaStream_t s);
 
 int device_sm_count();
 

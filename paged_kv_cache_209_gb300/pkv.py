@@ -54,7 +54,7 @@ class DecodeOpts(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("pkv_append", "pkv_copy_blocks", "pkv_decode_workspace_size", "pkv_decode_attention",
-           "pkv_decode_attention_noalloc", "pkv_device_status", "pkv_status_string", "pkv_version",
+           "pkv_decode_prefixed_workspace_size", "pkv_decode_attention_prefixed", "pkv_decode_attention_noalloc", "pkv_device_status", "pkv_status_string", "pkv_version",
            "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_add_sequence", "pkv_pool_append", "pkv_pool_append_batch",
            "pkv_pool_share_prefix", "pkv_pool_release", "pkv_pool_sequence_length", "pkv_pool_page_table",
            "pkv_pool_block_tables", "pkv_pool_get_stats", "pkv_pool_validate")
@@ -82,6 +82,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_decode_attention.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp,
                                          ctypes.c_size_t, desc_p, u32, opts_p, vp]
     lib.pkv_decode_attention.restype = ctypes.c_int
+    lib.pkv_decode_prefixed_workspace_size.argtypes = [i32, i32, i32, i32, i32, desc_p, opts_p]
+    lib.pkv_decode_prefixed_workspace_size.restype = ctypes.c_size_t
+    lib.pkv_decode_attention_prefixed.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp, i32,
+                                                  i32, vp, vp, ctypes.c_size_t, desc_p, u32, opts_p, vp]
+    lib.pkv_decode_attention_prefixed.restype = ctypes.c_int
     lib.pkv_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp,
                                                  desc_p, u32, opts_p, vp]
     lib.pkv_decode_attention_noalloc.restype = ctypes.c_int
@@ -223,6 +228,56 @@ def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale:
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
         q_heads, ctypes.c_float(scale), _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags,
         _opts(kernel, num_ctas, stages), _stream(stream)))
+    return out
+
+
+def pkv_decode_prefixed_workspace_size(batch: int, num_q_heads: int, max_blocks_per_seq: int, num_groups: int,
+                                       max_group_blocks: int, k_cache, kernel: int = 0, num_ctas: int = 0,
+                                       stages: int = 0) -> int:
+    """Workspace bytes of the shared-prefix call; allocate them zero-filled and reuse them."""
+    lib = load_library()
+    desc = cache_desc(k_cache)
+    return int(lib.pkv_decode_prefixed_workspace_size(batch, num_q_heads, max_blocks_per_seq, num_groups,
+                                                      max_group_blocks, ctypes.byref(desc),
+                                                      _opts(kernel, num_ctas, stages)))
+
+
+def pkv_decode_attention_prefixed(q, k_cache, v_cache, block_tables, context_lens, scale: float, prefix_group,
+                                  group_blocks, max_group_blocks: int, out=None, workspace=None, flags: int = 0,
+                                  kernel: int = 0, num_ctas: int = 0, stages: int = 0, stream=None):
+    """Decode attention with shared-prefix groups (two phases); returns ``out``.
+
+    ``prefix_group`` is int32 [batch] (group of each sequence or -1),
+    ``group_blocks`` int32 [num_groups] (whole blocks each group shares),
+    ``max_group_blocks`` a host-side bound on ``group_blocks``.
+    """
+    lib = load_library()
+    _same_pools(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    batch, q_heads, d = q.shape
+    if d != desc.head_dim or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [batch][q_heads][head_dim] of the pool dtype")
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                    ("prefix_group", prefix_group), ("group_blocks", group_blocks)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} is int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != batch or context_lens.shape != (batch,):
+        raise ValueError("block_tables is [batch][max_blocks], context_lens [batch]")
+    if prefix_group.shape != (batch,) or group_blocks.dim() != 1:
+        raise ValueError("prefix_group is [batch], group_blocks [num_groups]")
+    max_blocks = int(block_tables.shape[1])
+    num_groups = int(group_blocks.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    need = pkv_decode_prefixed_workspace_size(batch, q_heads, max_blocks, num_groups, max_group_blocks, k_cache,
+                                              kernel, num_ctas, stages)
+    if workspace is None:
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check("pkv_decode_attention_prefixed", lib.pkv_decode_attention_prefixed(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
+        q_heads, ctypes.c_float(scale), _ptr(prefix_group), _ptr(group_blocks), num_groups, max_group_blocks,
+        _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags, _opts(kernel, num_ctas, stages),
+        _stream(stream)))
     return out
 
 

@@ -124,3 +124,32 @@ def attention_errors(got: torch.Tensor, want: np.ndarray):
     denom = float(np.linalg.norm(want))
     rel = float(np.linalg.norm(diff) / denom) if denom > 0 else float(np.linalg.norm(diff))
     return max_abs, rel
+
+
+def grouped_case(seed, member_of, group_blocks, suffix_lens, q_heads, kv_heads, head_dim, dtype,
+                 extra_blocks=3, width=None):
+    """Sequences in shared-prefix groups: sequence i is in group member_of[i]
+    (-1: none); the members of group p begin with the same group_blocks[p]
+    blocks; sequence i then holds suffix_lens[i] tokens of its own."""
+    rng = np.random.default_rng(seed)
+    member_of = [int(g) for g in member_of]
+    own_tokens = np.asarray(suffix_lens, dtype=np.int64)
+    heads = [int(group_blocks[g]) if g >= 0 else 0 for g in member_of]
+    own_blocks = (own_tokens + B - 1) // B
+    num_blocks = int(sum(group_blocks)) + int(own_blocks.sum()) + extra_blocks
+    perm = list(rng.permutation(num_blocks))
+    shared = [[int(perm.pop()) for _ in range(nb)] for nb in group_blocks]
+    lens = np.array([h * B + s for h, s in zip(heads, own_tokens)], dtype=np.int32)
+    w = width or max(1, int(max(h + o for h, o in zip(heads, own_blocks))))
+    tables = np.full((len(member_of), w), -1, dtype=np.int32)
+    for i, g in enumerate(member_of):
+        row = (shared[g] if g >= 0 else []) + [int(perm.pop()) for _ in range(int(own_blocks[i]))]
+        tables[i, :len(row)] = row
+    kp = W.numpy_normal((num_blocks, kv_heads, B, head_dim), seed * 11 + 1)
+    vp = W.numpy_normal((num_blocks, kv_heads, B, head_dim), seed * 11 + 2)
+    q = W.numpy_normal((len(member_of), q_heads, head_dim), seed * 11 + 3)
+    return dict(q=torch.from_numpy(q).to(dtype), k_pool=torch.from_numpy(kp).to(dtype),
+                v_pool=torch.from_numpy(vp).to(dtype), tables=tables, lens=lens,
+                prefix_group=np.array(member_of, dtype=np.int32),
+                group_blocks=np.array(group_blocks, dtype=np.int32), kv_heads=kv_heads,
+                scale=1.0 / np.sqrt(head_dim))

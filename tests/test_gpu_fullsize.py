@@ -119,3 +119,33 @@ def test_prefix_with_copy_on_write_pairs(pkv):
              pairs=torch.from_numpy(pairs).to(dev), tables=torch.from_numpy(tables).to(dev),
              lens=torch.from_numpy(lens).to(dev), tables_np=tables, lens_np=lens, scale=1.0 / np.sqrt(D))
     check_workload(pkv, w, 8)
+
+
+def test_prefix_workload_two_phase(pkv):
+    """The prefix workload through the shared-prefix call (all 64 sequences
+    in one group over the 256 shared blocks), in the benchmark's launch
+    configuration: sampled pairs against the float64 oracle, every row
+    against the plain decode."""
+    w = W.device_workload("prefix", torch.device("cuda", 0))
+    cfg = w["cfg"]
+    kv_heads = cfg["kv_heads"]
+    G = cfg["q_heads"] // kv_heads
+    nb = cfg["prefix"] // 16
+    hk, hv = cases.host_view(w["k_pool"]), cases.host_view(w["v_pool"])
+    OK.append_tokens(hk, hv, cases.host_view(w["k_new"]), cases.host_view(w["v_new"]), w["slots_np"])
+    pkv.pkv_copy_blocks(w["pairs"], w["k_pool"], w["v_pool"])
+    pkv.pkv_append(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"])
+    group = torch.zeros(cfg["batch"], dtype=torch.int32, device="cuda")
+    blocks = torch.tensor([nb], dtype=torch.int32, device="cuda")
+    out = pkv.pkv_decode_attention_prefixed(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"],
+                                            group, blocks, nb)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) == 0
+    q = cases.host_view(w["q"])
+    for (i, j) in sample_pairs(w["lens_np"], kv_heads, 6, 17):
+        want = OA.decode_attention_pair(q, hk, hv, w["tables_np"], w["lens_np"], w["scale"], i, j, kv_heads, "bf16")
+        ma, rl = cases.attention_errors(out[i, j * G:(j + 1) * G], want)
+        assert ma <= MAX_ABS and rl <= REL_L2, (i, j, ma, rl)
+    ref = pkv.pkv_decode_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"])
+    d = out.float() - ref.float()
+    assert (d.norm() / ref.float().norm()).item() <= 2e-3 and d.abs().max().item() <= 1e-2
