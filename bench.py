@@ -11,7 +11,14 @@ One step = the whole hot path for one decode token per sequence:
   -> pkv_decode_attention (one launch: split kernel with the merge fused).
 value = KV bytes read per step / device time per step (decimal GB/s).
 
+--workload prefix runs the shared-prefix call by default
+(pkv_decode_attention_prefixed: every sequence in one group over the 256
+shared blocks); --single-pass times pkv_decode_attention over the same tables.
+There value counts the K/V bytes attended (logical); unique_kv_gbs counts each
+stored byte once.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+                  [--workload NAME] [--single-pass]
 
 --impl reference times the float64 CPU oracle (the only other code here),
 on a bounded sample of the same workload per step. Under torchrun with
@@ -143,21 +150,24 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha():
-    src = os.path.join(ROOT, "paged_kv_cache_209_gb300", "csrc", "pkv_decode.cu")
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+def kernel_source_sha(files=("pkv_decode.cu",)):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_209_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+def profiled_traffic(summary, files=("pkv_decode.cu",)):
+    """DRAM bytes per decode call from the committed ncu summary
+    profiles/<summary>.md, if it was taken on the current kernel source
+    (else None)."""
+    p = os.path.join(ROOT, "profiles", f"{summary}.md")
     if not os.path.exists(p):
         return None
     text = open(p).read()
     m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"dram_bytes_per_call:\s*([0-9]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != kernel_source_sha():
+    if not m_sha or not m_tr or m_sha.group(1) != kernel_source_sha(files):
         return None
     return int(m_tr.group(1))
 
@@ -257,18 +267,31 @@ def run_pkv(args, cfg):
     tables_np, lens_np = w["tables_np"], w["lens_np"]
     MAXB = tables.shape[1]
     out = torch.empty((B, HQ, D), dtype=q.dtype, device=device)
-    ws_bytes = pkv.pkv_decode_workspace_size(B, HQ, MAXB, k_pool)
+    two_phase = args.workload == "prefix" and not args.single_pass
+    group, gblocks, mgb = w["prefix_group"], w["group_blocks"], w["max_group_blocks"]
+    if two_phase:
+        ws_bytes = pkv.pkv_decode_prefixed_workspace_size(B, HQ, MAXB, len(gblocks), mgb, k_pool)
+    else:
+        ws_bytes = pkv.pkv_decode_workspace_size(B, HQ, MAXB, k_pool)
     workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
     scale = w["scale"]
     stream = torch.cuda.current_stream()
 
+    def decode():
+        if two_phase:
+            pkv.pkv_decode_attention_prefixed(q, k_pool, v_pool, tables, lens, scale, group, gblocks, mgb, out=out,
+                                              workspace=workspace, stream=stream)
+        else:
+            pkv.pkv_decode_attention(q, k_pool, v_pool, tables, lens, scale, out=out, workspace=workspace,
+                                     stream=stream)
+
     def step():
         pkv.pkv_copy_blocks(pairs, k_pool, v_pool, stream=stream)
         pkv.pkv_append(kn, vn, slots, k_pool, v_pool, stream=stream)
-        pkv.pkv_decode_attention(q, k_pool, v_pool, tables, lens, scale, out=out, workspace=workspace,
-                                 stream=stream)
+        decode()
 
-    launches_per_step = 1 + (B + 1023) // 1024  # append + one decode launch per 1024 sequences
+    # append + per 1024 sequences one decode launch (two with the shared-prefix pass)
+    launches_per_step = 1 + (2 if two_phase else 1) * ((B + 1023) // 1024)
     gpu_id = str(torch.cuda.get_device_properties(device).uuid)
     gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
     sampler = ClockSampler(gpu_id) if rank == 0 else None
@@ -293,8 +316,7 @@ def run_pkv(args, cfg):
         ev = ev_dec.get(i)
         if ev:
             ev[0].record(stream)
-        pkv.pkv_decode_attention(q, k_pool, v_pool, tables, lens, scale, out=out, workspace=workspace,
-                                 stream=stream)
+        decode()
         if ev:
             ev[1].record(stream)
     end.record(stream)
@@ -307,8 +329,8 @@ def run_pkv(args, cfg):
     status_bits = pkv.pkv_device_status(clear=False)
 
     # -------- end-to-end: per-step inputs from pinned host memory, result back to the host
-    pins = [t.cpu().pin_memory() for t in (q, kn, vn, slots, tables, lens)]
-    devs = [q, kn, vn, slots, tables, lens]
+    devs = [q, kn, vn, slots, tables, lens] + ([group, gblocks] if two_phase else [])
+    pins = [t.cpu().pin_memory() for t in devs]
     out_pin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pins)
     d2h = out_pin.numel() * out_pin.element_size()
@@ -343,11 +365,18 @@ def run_pkv(args, cfg):
     value = total_kv / (ms_per_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     # algorithmic bytes of one decode call: K+V of every live token read once,
-    # q read, out written, block-table entries and lengths read
+    # q read, out written, block-table entries and lengths read. With the
+    # shared-prefix pass the shared blocks count once (the bytes a perfect
+    # kernel must move), not once per sequence.
     used_entries = int(((lens_np.astype(np.int64) + 15) // 16).sum())
-    alg_bytes = kvb + q.numel() * q.element_size() + out.numel() * out.element_size() + used_entries * 4 + B * 4
+    shared_tokens = int(mgb) * 16 * (B - 1) if two_phase else 0
+    unique_kvb = (kv_tokens - shared_tokens) * 2 * HKV * D * q.element_size()
+    alg_bytes = unique_kvb + q.numel() * q.element_size() + out.numel() * out.element_size() + used_entries * 4 + B * 4
     achieved = alg_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload)
+    if two_phase:
+        traffic = profiled_traffic("decode_prefix_two_phase", ("pkv_decode.cu", "pkv_prefix.cu"))
+    else:
+        traffic = profiled_traffic(f"decode_{args.workload}")
 
     # -------- CPU oracle baseline on a bounded sample of the same workload
     order = np.argsort(-lens_np)
@@ -363,13 +392,17 @@ def run_pkv(args, cfg):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(args.workload, cfg, lens_np),
                    "l2": L2_NOTE[args.workload],
-                   "step": f"copy_blocks ({int(pairs.shape[0])} pairs) + append ({B} tokens) + decode attention",
-                   "kernel": "tensor-core split-context kernel, merge fused"},
+                   "step": f"copy_blocks ({int(pairs.shape[0])} pairs) + append ({B} tokens) + "
+                           + ("shared-prefix decode attention (two phases)" if two_phase else "decode attention"),
+                   "kernel": "tensor-core split-context kernel, merge fused"
+                             + (", then the chunk-first pass over the shared blocks" if two_phase else "")},
         "hbm_frac": round(value / peak, 4),
+        "unique_kv_gbs": round(unique_kvb * ws / (ms_per_step * 1e-3) / 1e9, 2),
         "kv_tokens_per_s": round(kv_tokens * ws / (ms_per_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_tc_kernel<128> (one launch per pkv_decode_attention call)",
+                     "kernel": ("decode_tc_kernel<128> + prefix_umma_kernel<128> (one shared-prefix call)"
+                                if two_phase else "decode_tc_kernel<128> (one launch per pkv_decode_attention call)"),
                      "avg_launch_ms": round(dec_avg_ms, 5), "launches_timed": len(dec_ms),
                      "algorithmic_bytes": alg_bytes},
         "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -395,6 +428,8 @@ def main():
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_NAMES), default=WORKLOAD,
                     help="default: the 8K Llama-3-8B layer the headline metric is quoted on")
+    ap.add_argument("--single-pass", action="store_true",
+                    help="prefix workload: plain decode over the full tables instead of the shared-prefix call")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

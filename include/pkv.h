@@ -106,6 +106,9 @@ typedef struct {
     int32_t num_ctas;   /* 0 = one wave of resident CTAs; > 0 forces that
                            many CTAs (tests use it to force context splits) */
     int32_t stages;     /* tensor-core kernel ring depth: 0 = default (8), 8 or 12 */
+    int32_t prefix_kernel; /* shared-prefix pass of pkv_decode_attention_prefixed:
+                              0 = choose (2); 1 = mma.sync kernel, 64-row tiles;
+                              2 = tcgen05 kernel, 128-row tiles              */
 } pkv_decode_opts;
 
 /*

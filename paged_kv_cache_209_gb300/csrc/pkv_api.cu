@@ -241,7 +241,8 @@ size_t pkv_decode_prefixed_workspace_size(int32_t batch, int32_t num_q_heads, in
     const int G = num_q_heads / desc->num_kv_heads;
     const size_t base = decode_workspace_layout(batch, desc->num_kv_heads, plan.num_ctas, G, desc->head_dim).total;
     if (plan.kernel != 2 || num_groups == 0) return base;
-    return prefix_plan(batch, num_groups, num_q_heads, desc->num_kv_heads, desc->head_dim, max_group_blocks, base)
+    return prefix_plan(batch, num_groups, num_q_heads, desc->num_kv_heads, desc->head_dim, max_group_blocks, base,
+                       opts ? opts->prefix_kernel : 0)
         .total;
 }
 
@@ -292,8 +293,9 @@ pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, con
         return PKV_ERR_ALIGN;
     const int G = num_q_heads / desc->num_kv_heads;
     const WorkspaceLayout wl = decode_workspace_layout(batch, desc->num_kv_heads, plan.num_ctas, G, desc->head_dim);
-    const PrefixPlan pp =
-        prefix_plan(batch, num_groups, num_q_heads, desc->num_kv_heads, desc->head_dim, max_group_blocks, wl.total);
+    if (opts != nullptr && (opts->prefix_kernel < 0 || opts->prefix_kernel > 2)) return PKV_ERR_UNSUPPORTED;
+    const PrefixPlan pp = prefix_plan(batch, num_groups, num_q_heads, desc->num_kv_heads, desc->head_dim,
+                                      max_group_blocks, wl.total, opts ? opts->prefix_kernel : 0);
     if (workspace_bytes < pp.total) return PKV_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned int* status = device_info().status;
@@ -368,7 +370,7 @@ pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, con
         pa.chunks = pp.chunks;
         pa.chunk_blocks = pp.chunk_blocks;
         pa.scale = scale;
-        if (launch_prefix(pa, s) != cudaSuccess) return PKV_ERR_CUDA;
+        if (launch_prefix(pa, pp.kernel, s) != cudaSuccess) return PKV_ERR_CUDA;
     }
     return PKV_OK;
 }

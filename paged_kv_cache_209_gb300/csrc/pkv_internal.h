@@ -106,7 +106,7 @@ struct PrefixArgs {
     const float* fold_o;
     const float* fold_lse;
     void* out;
-    float* partials;  // [tiles][kv_heads][chunks][64 rows][head_dim + 2]
+    float* partials;  // [tiles][kv_heads][chunks][rows per tile][head_dim + 2]
     int* counters;    // [tiles][kv_heads][4 warps]; zero between calls
     unsigned int* status;
     int64_t num_blocks;
@@ -127,12 +127,14 @@ struct PrefixArgs {
 // Grid and workspace of the chunk-first pass for a launch of `batch`
 // sequences (at most kMaxBatchPerLaunch).
 struct PrefixPlan {
+    int kernel;  // 1 mma.sync (64-row tiles), 2 tcgen05 (128-row tiles)
+    int rows;    // query rows per tile
     int tiles, chunks, chunk_blocks;
     size_t counters_offset, partials_offset, fold_o_offset, fold_lse_offset, total;
 };
 PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int head_dim, int max_group_blocks,
-                       size_t base_offset);
-cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t s);
+                       size_t base_offset, int kernel);
+cudaError_t launch_prefix(const PrefixArgs& a, int kernel, cudaStream_t s);
 cudaError_t launch_check_groups(const int32_t* tables, int32_t max_blocks, const int32_t* lens,
                                 const int32_t* prefix_group, const int32_t* group_blocks, int32_t num_groups,
                                 int32_t max_group_blocks, int32_t batch, unsigned int* verdict, cudaStream_t s);

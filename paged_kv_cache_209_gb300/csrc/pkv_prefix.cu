@@ -5,31 +5,36 @@
 // target the source's leading blocks). The decode kernel, in prefixed mode,
 // has already attended every member over its own tokens past those blocks
 // and left the normalised result with its log2-sum-exp in fold_o / fold_lse.
-// This kernel attends the queries of all members of a group together over
-// the shared blocks -- each shared K/V block is read once per 64 query rows
-// instead of once per sequence -- and combines the two partials by their
-// log-sum-exp weights into the output rows (paper-search page, ChunkAttention
-// abstract: "two-phase partition", shared chunks first, then each sequence).
+// The kernels here attend the queries of all members of a group together
+// over the shared blocks -- each shared K/V block is read once per tile of
+// query rows instead of once per sequence -- and combine the two partials by
+// their log-sum-exp weights into the output rows (paper-search page,
+// ChunkAttention abstract: "two-phase partition", shared chunks first, then
+// each sequence).
 //
-// Work decomposition. The query rows of group p are (member m, query head g
-// of KV head h) in member order, row r = m * G + g. CTA (x, y, z) takes
-// 64-row tile x of the list of all groups' tiles (each group's rows padded to
-// a whole tile), chunk y of the group's shared blocks and KV head z. A group
-// whose shared blocks fit in one chunk is finished by its CTA directly;
-// otherwise each chunk leaves an fp32 partial (unnormalised O, running max m,
-// sum l) per row, and for each warp's 16 rows the last of the chunks' warps
-// to finish (an atomic counter per tile, head and warp) merges them.
+// Work decomposition (both kernels). The query rows of group p are (member
+// m, query head g of KV head h) in member order, row r = m * G + g. CTA
+// (x, y, z) takes row tile x of the list of all groups' tiles (each group's
+// rows padded to whole tiles), chunk y of the group's shared blocks and KV
+// head z. A group whose shared blocks fit in one chunk is finished by its CTA
+// directly; otherwise each chunk leaves an fp32 partial (unnormalised O,
+// running max m, sum l) per row, and the last of the chunks' warps to finish
+// a set of rows (an atomic counter per tile, head and warp) merges them.
 //
-// Inside a CTA one producer warp streams the chunk's K and V blocks of head
-// z through an NST-stage shared-memory ring with 2-D TMA loads (128-byte
-// swizzle, L2 evict-last: the other tiles of the group read the same
-// blocks). Four consumer warps own 16 query rows each and all consume every
-// block:
-//     S[16 rows][16 tokens] = Q[16][D] K^T           (mma m16n8k16, 2 n-tiles)
-//     online softmax on the S fragments in fp32, base 2
-//     O[16][D] += P[16][16] V[16][D]                  (mma m16n8k16)
-// The S accumulator fragments are already laid out as the A operand of P;
-// P is split into bf16 hi + lo as in the decode kernel.
+// prefix_umma_kernel (default): 128-row tiles on the 5th-generation tensor
+// cores. A TMA warp streams 64-token steps (four blocks) of K and V through a
+// shared-memory ring; one thread issues
+//     S[128][64]  = Q[128][D] K^T      (tcgen05.mma, accumulator in tensor memory,
+//                                        two S buffers so the next S overlaps)
+//     O[128][D]  += P[128][64] V[64][D] (P as bf16 hi + lo from shared memory,
+//                                        V read MN-major straight from the TMA layout)
+// and four softmax warps, one thread per query row, read S rows from tensor
+// memory, run the online softmax (base 2, lazy rescale of O in tensor
+// memory), and write P.
+//
+// prefix_mma_kernel: 64-row tiles, four warps of 16 rows each on mma.sync
+// (m16n8k16) with the S accumulator fragments reused as the A operand of P;
+// kept as a second implementation that the tests compare with.
 #include <math.h>
 #include <mutex>
 
@@ -40,70 +45,31 @@ namespace pkv {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kTileRows = 64;
 constexpr int kMaxChunks = 32;
 constexpr int kMaxGroups = kMaxBatchPerLaunch;
-constexpr int kMemberSlots = 72;  // members of one tile: at most 64 / G + 2
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 
-template <int D, int NST>
-struct Px {
-    static constexpr int kStages = NST;
-    static constexpr int kConsumers = 4;
-    static constexpr int kThreads = (kConsumers + 1) * 32;
-    static constexpr int kHalves = D / 64;
-    static constexpr int kPoolBytes = 16 * D * 2;
-    static constexpr int kStageBytes = 2 * kPoolBytes;  // K then V
-    // shared memory (offsets from a 1024-byte aligned base): the ring,
-    // full[NST] and empty[NST], stage flags and the abort flag, then
-    // info[8], the tile's members and the per-group member counts.
-    static constexpr int kOffBars = kStages * kStageBytes;
-    static constexpr int kOffFlags = kOffBars + 2 * kStages * 8;
-    static constexpr int kOffInts = kOffFlags + (kStages + 1) * 4;
-    static constexpr size_t kSmem = 1024 + kOffInts + (8 + kMemberSlots + kMaxGroups) * 4;
-};
+// Members of one tile: at most rows / G + 2.
+__host__ __device__ constexpr int member_slots(int rows) { return rows + 8; }
 
-template <int D, int NST>
-__global__ void __launch_bounds__(Px<D, NST>::kThreads)
-    prefix_tc_kernel(const PrefixArgs a, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV) {
-    using C = Px<D, NST>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-    uint64_t* empty = full + C::kStages;
-    int* stage_ok = reinterpret_cast<int*>(smem + C::kOffFlags);
-    volatile int* abort_flag = stage_ok + C::kStages;
-    int* info = reinterpret_cast<int*>(smem + C::kOffInts);  // [0] group, [1] tile in group, [2] first member
-    int* members = info + 8;
-    int* counts = members + kMemberSlots;
-
+// Shared prologue of both kernels (all threads; contains __syncthreads).
+// Counts the members of every group, finds the group and tile of this CTA's
+// x index and the tile's members in member order, and the chunk of shared
+// blocks of this CTA's y index. info[]: [0] group, [1] tile within the group,
+// [2] first member of the group, [3] shared blocks, [4] chunks of the group,
+// [5] rows of the tile, [6] first member of the tile. Returns false (for the
+// whole CTA) when the CTA has no work.
+template <int kRowsPerTile>
+__device__ bool locate_tile(const PrefixArgs& a, int* info, int* members, int* counts) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = a.group;
-    const int h = blockIdx.z;
-    const int chunk = blockIdx.y;
     const int cap = a.max_blocks * 16;
-
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], C::kConsumers);
-        }
-        *abort_flag = 0;
         info[0] = -1;
         info[2] = 0;
-        fence_barrier_init();
     }
-    if (threadIdx.x == 32) {
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-    }
-    // Inputs only until the fold: the kernel before this one (the decode
-    // kernel) lets it start once all its CTAs have passed their own wait on
-    // the kernels before them, so the K/V blocks are complete.
-    allow_dependents();
     for (int g = threadIdx.x; g < a.num_groups; g += blockDim.x) counts[g] = 0;
     __syncthreads();
     auto member_blocks = [&](int i) {
@@ -119,7 +85,7 @@ __global__ void __launch_bounds__(Px<D, NST>::kThreads)
         int carry = 0;
         for (int base = 0; base < a.num_groups; base += 32) {
             const int g = base + lane;
-            const int t = g < a.num_groups ? (counts[g] * G + kTileRows - 1) / kTileRows : 0;
+            const int t = g < a.num_groups ? (counts[g] * G + kRowsPerTile - 1) / kRowsPerTile : 0;
             int x = t;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -136,21 +102,12 @@ __global__ void __launch_bounds__(Px<D, NST>::kThreads)
     }
     __syncthreads();
     const int p = info[0];
-    // Every exit waits for the kernel before: this grid must not complete
-    // (and release the next kernel in the stream) before that one has.
-    if (p < 0) {
-        grid_dependency_wait();
-        return;
-    }
-    int nb = a.group_blocks[p];  // in [0, max_group_blocks]: p has members
+    if (p < 0) return false;
+    const int nb = a.group_blocks[p];  // in [0, max_group_blocks]: p has members
     const int nch = nb > 0 ? (nb + a.chunk_blocks - 1) / a.chunk_blocks : 1;
-    if (chunk >= nch) {
-        grid_dependency_wait();
-        return;
-    }
-    const int rows_total = counts[p] * G;
-    const int r0 = info[1] * kTileRows;
-    const int nrows = min(kTileRows, rows_total - r0);
+    if (static_cast<int>(blockIdx.y) >= nch) return false;
+    const int r0 = info[1] * kRowsPerTile;
+    const int nrows = min(kRowsPerTile, counts[p] * G - r0);
     const int m0 = r0 / G;
     const int m1 = (r0 + nrows - 1) / G + 1;
     if (warp == 0) {
@@ -166,8 +123,89 @@ __global__ void __launch_bounds__(Px<D, NST>::kThreads)
             }
             rank += __popc(bal);
         }
+        if (lane == 0) {
+            info[3] = nb;
+            info[4] = nch;
+            info[5] = nrows;
+            info[6] = m0;
+        }
     }
     __syncthreads();
+    return true;
+}
+
+// A CTA without work leaves at once, except CTA (0, 0, 0), which first waits
+// for the kernel before it: this grid must not complete (and release the next
+// kernel in the stream) before that one has.
+__device__ __forceinline__ void idle_exit() {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) grid_dependency_wait();
+}
+
+template <int D, int NST>
+struct Px {
+    static constexpr int kRows = 64;  // query rows per tile
+    static constexpr int kStages = NST;
+    static constexpr int kConsumers = 4;
+    static constexpr int kThreads = (kConsumers + 1) * 32;
+    static constexpr int kHalves = D / 64;
+    static constexpr int kPoolBytes = 16 * D * 2;
+    static constexpr int kStageBytes = 2 * kPoolBytes;  // K then V
+    // shared memory (offsets from a 1024-byte aligned base): the ring,
+    // full[NST] and empty[NST], stage flags and the abort flag, then
+    // info[8], the tile's members and the per-group member counts.
+    static constexpr int kOffBars = kStages * kStageBytes;
+    static constexpr int kOffFlags = kOffBars + 2 * kStages * 8;
+    static constexpr int kOffInts = kOffFlags + (kStages + 1) * 4;
+    static constexpr size_t kSmem = 1024 + kOffInts + (8 + member_slots(kRows) + kMaxGroups) * 4;
+};
+
+template <int D, int NST>
+__global__ void __launch_bounds__(Px<D, NST>::kThreads)
+    prefix_mma_kernel(const PrefixArgs a, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+    using C = Px<D, NST>;
+    constexpr int kTileRows = C::kRows;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+    uint64_t* empty = full + C::kStages;
+    int* stage_ok = reinterpret_cast<int*>(smem + C::kOffFlags);
+    volatile int* abort_flag = stage_ok + C::kStages;
+    int* info = reinterpret_cast<int*>(smem + C::kOffInts);
+    int* members = info + 8;
+    int* counts = members + member_slots(kTileRows);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+    const int h = blockIdx.z;
+    const int chunk = blockIdx.y;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::kConsumers);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    // Inputs only until the fold: the kernel before this one (the decode
+    // kernel) lets it start once all its CTAs have passed their own wait on
+    // the kernels before them, so the K/V blocks are complete.
+    allow_dependents();
+    if (!locate_tile<kTileRows>(a, info, members, counts)) {
+        idle_exit();
+        return;
+    }
+    const int nb = info[3];
+    const int nch = info[4];
+    const int nrows = info[5];
+    const int m0 = info[6];
+    const int r0 = info[1] * kTileRows;
     const int blk0 = chunk * a.chunk_blocks;
     const int nblk = nb > 0 ? min(a.chunk_blocks, nb - blk0) : 0;
 
@@ -448,6 +486,433 @@ __global__ void __launch_bounds__(Px<D, NST>::kThreads)
     }
 }
 
+// ------------------------------------------------------------------ tcgen05 kernel
+template <int D>
+struct Ux {
+    static constexpr int kRows = 128;                // M: query rows per tile = tensor-memory lanes
+    static constexpr int kTok = 64;                  // N of S = Q K^T: tokens per step
+    static constexpr int kBlk = kTok / 16;           // blocks per step
+    static constexpr int kHalves = D / 64;           // 64-column (128-byte) halves of a row
+    static constexpr int kStages = D == 128 ? 3 : 4;
+    static constexpr int kQBytes = kHalves * kRows * 128;
+    static constexpr int kHalfBytes = kTok * 128;    // one half of the 64 token rows of a step
+    static constexpr int kKBytes = kHalves * kHalfBytes;
+    static constexpr int kStageBytes = 2 * kKBytes;  // K then V
+    static constexpr int kPBytes = kRows * 128;      // 128 rows x 64 tokens, bf16
+    // Shared memory (offsets from a 1024-byte aligned base; every operand
+    // tile starts on a 1024-byte boundary, as the 128-byte swizzle wants):
+    // Q [halves][128 rows][128 B]; the K/V ring, each stage K then V as
+    // [halves][64 token rows][128 B] (the TMA layout of four 16-row boxes);
+    // P as two buffers of {hi, lo} [128 rows][128 B]; the mbarriers; then
+    // info[16], the tile's members and the per-group member counts.
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kQBytes;
+    static constexpr int kOffP = kOffKV + kStages * kStageBytes;
+    static constexpr int kOffBars = kOffP + 4 * kPBytes;
+    static constexpr int kNumBars = 2 * kStages + 7;  // kv_full, kv_empty, s_full[2], p_full[2], o_done[2], final
+    static constexpr int kOffInts = kOffBars + kNumBars * 8;
+    static constexpr size_t kSmem = 1024 + kOffInts + (16 + member_slots(kRows) + kMaxGroups) * 4;
+    static constexpr int kThreads = 192;   // warps 0-3 softmax (lanes 32w..32w+31), 4 TMA, 5 MMA
+    static constexpr uint32_t kTmemCols = 256;
+    static constexpr uint32_t kColS = 0;   // S buffers: columns [0, 64) and [64, 128)
+    static constexpr uint32_t kColO = 128; // O: columns [128, 128 + D)
+    static_assert(kColO + D <= kTmemCols, "tensor-memory columns");
+};
+
+template <int D>
+__global__ void __launch_bounds__(Ux<D>::kThreads, 1)
+    prefix_umma_kernel(const PrefixArgs a, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV) {
+    using C = Ux<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+    uint64_t* kv_empty = kv_full + C::kStages;
+    uint64_t* s_full = kv_empty + C::kStages;  // [2]: S buffer b holds a finished S
+    uint64_t* p_full = s_full + 2;             // [2]: P buffer b written (4 warp arrivals)
+    uint64_t* o_done = p_full + 2;             // [2]: the PV product of step j (buffer j % 2) has completed
+    uint64_t* final_bar = o_done + 2;          // every issued MMA has completed
+    int* info = reinterpret_cast<int*>(smem + C::kOffInts);
+    int* members = info + 16;
+    int* counts = members + member_slots(C::kRows);
+    volatile int* abort_flag = info + 14;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(info + 15);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+    const int h = blockIdx.z;
+    const int chunk = blockIdx.y;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 4);
+            mbar_init(&o_done[b], 1);
+        }
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32 * 4) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    allow_dependents();  // inputs only until the fold (see the mma.sync kernel)
+    if (!locate_tile<C::kRows>(a, info, members, counts)) {
+        idle_exit();
+        return;
+    }
+    // From here every thread of the CTA reaches the final __syncthreads, so
+    // the tensor memory allocated below is always freed.
+    const int nb = info[3];
+    const int nch = info[4];
+    const int nrows = info[5];
+    const int m0 = info[6];
+    const int r0 = info[1] * C::kRows;
+    const int blk0 = chunk * a.chunk_blocks;
+    const int nblk = nb > 0 ? min(a.chunk_blocks, nb - blk0) : 0;
+    const int nsteps = (nblk + C::kBlk - 1) / C::kBlk;
+
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    // Q rows into shared memory (K-major, 128-byte swizzle); thread r < 128 loads row r.
+    long long row_idx = 0;
+    bool row_ok = false;
+    if (warp < 4) {
+        const int r = threadIdx.x;
+        row_ok = r < nrows;
+        const int R = r0 + (row_ok ? r : 0);
+        const int m = R / G;
+        row_idx = static_cast<long long>(members[m - m0]) * a.q_heads + h * G + (R - m * G);
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + row_idx * D);
+        uint8_t* qs = smem + C::kOffQ;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(qs + (c >> 3) * (C::kRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        // Step j: blocks 4j .. 4j+3 of the chunk; lane b issues block b. A
+        // block past the chunk or with an invalid id is loaded from row -16
+        // (wholly out of range), which fills its box with zeros.
+        const uint64_t policy = l2_evict_last_policy();
+        const int32_t* trow = a.tables + static_cast<long long>(info[2]) * a.max_blocks + blk0;
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; j < nsteps; ++j) {
+            const int s = j % C::kStages;
+            int y = -16;
+            if (lane < C::kBlk && C::kBlk * j + lane < nblk) {
+                const int bid = __ldg(trow + C::kBlk * j + lane);
+                if (bid >= 0 && bid < a.num_blocks)
+                    y = (bid * a.kv_heads + h) * 16;
+                else
+                    atomicOr(a.status, PKV_DEVERR_RANGE);
+            }
+            int good = 1;
+            if (lane == 0) {
+                if (mbar_wait(&kv_empty[s], static_cast<uint32_t>((j / C::kStages) & 1) ^ 1u, a.status, abort_flag))
+                    mbar_arrive_expect_tx(&kv_full[s], C::kStageBytes);
+                else
+                    good = 0;
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+                ok = false;
+                break;
+            }
+            if (lane < C::kBlk) {
+                uint8_t* st = smem + C::kOffKV + s * C::kStageBytes + lane * 2048;
+#pragma unroll
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                    tma_load_2d(st + hf * C::kHalfBytes, &tmK, hf * 64, y, &kv_full[s], policy);
+                    tma_load_2d(st + C::kKBytes + hf * C::kHalfBytes, &tmV, hf * 64, y, &kv_full[s], policy);
+                }
+            }
+            ++issued;
+        }
+        if (!ok && lane == 0) {  // after an abort: wait (bounded) for the copies still in flight
+            const int first = issued > C::kStages ? issued - C::kStages : 0;
+            for (int u = first; u < issued; ++u)
+                mbar_wait(&kv_full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer (one thread)
+        if (lane == 0) {
+            constexpr uint32_t idS = umma_idesc_bf16(C::kRows, C::kTok, false, false);
+            constexpr uint32_t idO = umma_idesc_bf16(C::kRows, D, false, true);
+            const uint32_t q_base = smem_u32(smem + C::kOffQ);
+            bool ok = true;
+            // S_j = Q K_j^T into S buffer j % 2. Both operands K-major; a
+            // K-step of 16 elements is 32 bytes into the swizzled row.
+            auto issue_s = [&](int j) {
+                const int s = j % C::kStages;
+                if (!mbar_wait(&kv_full[s], static_cast<uint32_t>((j / C::kStages) & 1), a.status, abort_flag))
+                    return false;
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(smem + C::kOffKV + s * C::kStageBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ad = umma_desc_sw128(q_base + (kk >> 2) * (C::kRows * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = umma_desc_sw128(k_base + (kk >> 2) * C::kHalfBytes + (kk & 3) * 32, 16, 1024);
+                    umma_bf16(tmem + C::kColS + (j & 1) * C::kTok, ad, bd, idS, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&s_full[j & 1]);
+                return true;
+            };
+            for (int j = 0; ok && j < nsteps && j < 2; ++j) ok = issue_s(j);
+            for (int j = 0; ok && j < nsteps; ++j) {
+                if (!mbar_wait(&p_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // O += P_hi V + P_lo V. P is K-major (tokens along the row); V
+                // is MN-major straight from the TMA layout: 64 columns per
+                // 128-byte row, the two column halves kHalfBytes apart, 8
+                // token rows per 1024-byte atom.
+                const int s = j % C::kStages;
+                const uint32_t v_base = smem_u32(smem + C::kOffKV + s * C::kStageBytes + C::kKBytes);
+                const uint32_t p_base = smem_u32(smem + C::kOffP + (j & 1) * 2 * C::kPBytes);
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int kt = 0; kt < C::kTok / 16; ++kt) {
+                        const uint64_t ad = umma_desc_sw128(p_base + part * C::kPBytes + kt * 32, 16, 1024);
+                        const uint64_t bd = umma_desc_sw128(v_base + kt * 2048, C::kHalfBytes, 1024);
+                        umma_bf16(tmem + C::kColO, ad, bd, idO, (j > 0 || part > 0 || kt > 0) ? 1u : 0u);
+                    }
+                }
+                umma_commit(&kv_empty[s]);
+                umma_commit(&o_done[j & 1]);
+                if (j + 2 < nsteps) ok = issue_s(j + 2);
+            }
+            // nothing may still run on the tensor cores when the memory is freed
+            umma_commit(final_bar);
+            mbar_wait(final_bar, 0, a.status, nullptr);
+        }
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------- softmax warps
+    float m = ninf(), l = 0.f;  // running max (base 2, scaled) and sum of this thread's row
+    bool ok = true;
+    float acc[D];               // the row's output accumulator at the end
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    if (warp < 4) {
+        const int r = threadIdx.x;
+        const float scale_log2 = a.scale * kLog2e;
+        for (int j = 0; j < nsteps; ++j) {
+            if (!mbar_wait(&s_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.status, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[2][32];
+            tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok, sv[0]);
+            tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok + 32, sv[1]);
+            tmem_ld_wait();
+            const int valid = min(C::kTok, (nblk - C::kBlk * j) * 16);
+            float x[C::kTok];
+            float mx = ninf();
+#pragma unroll
+            for (int t = 0; t < C::kTok; ++t) {
+                x[t] = t < valid ? __uint_as_float(sv[t >> 5][t & 31]) * scale_log2 : ninf();
+                mx = fmaxf(mx, x[t]);
+            }
+            // lazy rescale: the running max moves only when a score exceeds it by more than 8
+            const bool resc = mx > m + 8.f;
+            float alpha = 1.f;
+            if (resc) {
+                const float mn = fmaxf(m, mx);
+                alpha = m == ninf() ? 0.f : ex2(m - mn);
+                m = mn;
+            }
+            uint32_t hi[C::kTok / 2], lo[C::kTok / 2];
+            float psum = 0.f;
+#pragma unroll
+            for (int t = 0; t < C::kTok; t += 2) {
+                const float p0 = ex2(x[t] - m), p1 = ex2(x[t + 1] - m);
+                psum += p0 + p1;
+                const uint32_t hv = pack_bf16x2(p0, p1);
+                hi[t / 2] = hv;
+                lo[t / 2] = pack_bf16x2(p0 - bf16lo_to_f32(hv), p1 - bf16hi_to_f32(hv));
+            }
+            l = l * alpha + psum;
+            // P buffer j % 2 was read by the PV product of step j - 2
+            if (j >= 2 && !mbar_wait(&o_done[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), a.status, abort_flag)) {
+                ok = false;
+                break;
+            }
+            // rescale O in tensor memory once the PV product of step j - 1 is in
+            if (__any_sync(0xffffffffu, resc && j > 0)) {
+                if (!mbar_wait(&o_done[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1), a.status,
+                               abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tmem + lane_base + C::kColO + c, ov);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(tmem + lane_base + C::kColO + c, ov);
+                }
+                tmem_st_wait();
+            }
+            uint8_t* prow = smem + C::kOffP + (j & 1) * 2 * C::kPBytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < C::kTok / 8; ++c) {
+                const int off = ((c ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+                *reinterpret_cast<uint4*>(prow + C::kPBytes + off) =
+                    make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[j & 1]);
+        }
+        // the row's O: the last PV product must be in
+#pragma unroll
+        for (int d = 0; d < D; ++d) acc[d] = 0.f;
+        if (ok && nsteps > 0) {
+            if (mbar_wait(&o_done[(nsteps - 1) & 1], static_cast<uint32_t>(((nsteps - 1) >> 1) & 1), a.status,
+                          abort_flag)) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tmem + lane_base + C::kColO + c, ov);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[c + e] = __uint_as_float(ov[e]);
+                }
+            } else {
+                ok = false;
+            }
+        }
+    }
+    // ---- tensor memory is no longer read: free it
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+    if (warp >= 4 || !ok || *abort_flag) {
+        grid_dependency_wait();
+        return;
+    }
+
+    // ---- merge the chunks' partials (several chunks) and fold in the own-token partial
+    const int r = threadIdx.x;
+    const long long tile_head = static_cast<long long>(h) * gridDim.x + blockIdx.x;
+    constexpr int kSlot = C::kRows * (D + 2);
+    if (nch > 1) {
+        float* slot = a.partials + (tile_head * a.chunks + chunk) * kSlot;
+#pragma unroll
+        for (int d = 0; d < D; d += 4)
+            __stcg(reinterpret_cast<float4*>(slot + r * D + d), make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]));
+        __stcg(slot + C::kRows * D + r, m);
+        __stcg(slot + C::kRows * D + C::kRows + r, l);
+        __threadfence();
+        __syncwarp();
+        int* counter = a.counters + tile_head * 4 + warp;
+        int old = 0;
+        if (lane == 0) old = atomicAdd(counter, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != nch - 1) {
+            grid_dependency_wait();
+            return;
+        }
+        __threadfence();
+        if (lane == 0) *counter = 0;  // ready for the next call
+    }
+    grid_dependency_wait();  // fold_o / fold_lse come from the decode kernel
+    if (!row_ok) return;
+    // Weights over the parts: every chunk's (m_c, l_c) and the own-token
+    // partial (lse_s, normalised o_s), all in base 2.
+    const float ls = __ldcg(a.fold_lse + row_idx);
+    float Mx = ls;
+    if (nch > 1) {
+        for (int c = 0; c < nch; ++c) {
+            const float* sl = a.partials + (tile_head * a.chunks + c) * kSlot;
+            const float lc = __ldcg(sl + C::kRows * D + C::kRows + r);
+            if (lc > 0.f) Mx = fmaxf(Mx, __ldcg(sl + C::kRows * D + r));
+        }
+    } else if (l > 0.f) {
+        Mx = fmaxf(Mx, m);
+    }
+    float den = 0.f, ws = 0.f;
+    if (Mx != ninf()) {
+        ws = ls == ninf() ? 0.f : ex2(ls - Mx);
+        den = ws;
+        if (nch > 1) {
+            for (int c = 0; c < nch; ++c) {
+                const float* sl = a.partials + (tile_head * a.chunks + c) * kSlot;
+                const float lc = __ldcg(sl + C::kRows * D + C::kRows + r);
+                if (lc > 0.f) den += lc * ex2(__ldcg(sl + C::kRows * D + r) - Mx);
+            }
+        } else if (l > 0.f) {
+            den += l * ex2(m - Mx);
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    ws *= inv;
+    if (nch > 1) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) acc[d] = 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const float* sl = a.partials + (tile_head * a.chunks + c) * kSlot;
+            const float lc = __ldcg(sl + C::kRows * D + C::kRows + r);
+            if (!(lc > 0.f)) continue;
+            const float w = ex2(__ldcg(sl + C::kRows * D + r) - Mx) * inv;
+#pragma unroll
+            for (int d = 0; d < D; d += 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(sl + r * D + d));
+                acc[d] += w * v.x;
+                acc[d + 1] += w * v.y;
+                acc[d + 2] += w * v.z;
+                acc[d + 3] += w * v.w;
+            }
+        }
+    } else {
+        const float w = l > 0.f ? ex2(m - Mx) * inv : 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) acc[d] *= w;
+    }
+    const float* fo = a.fold_o + row_idx * D;
+    uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row_idx * D);
+#pragma unroll
+    for (int d = 0; d < D; d += 8) {
+        const float4 f0 = __ldcg(reinterpret_cast<const float4*>(fo + d));
+        const float4 f1 = __ldcg(reinterpret_cast<const float4*>(fo + d + 4));
+        out[d / 8] = make_uint4(pack_bf16x2(acc[d] + ws * f0.x, acc[d + 1] + ws * f0.y),
+                                pack_bf16x2(acc[d + 2] + ws * f0.z, acc[d + 3] + ws * f0.w),
+                                pack_bf16x2(acc[d + 4] + ws * f1.x, acc[d + 5] + ws * f1.y),
+                                pack_bf16x2(acc[d + 6] + ws * f1.z, acc[d + 7] + ws * f1.w));
+    }
+}
+
 // ------------------------------------------------------------------ checked mode
 // One CTA per sequence: a member of a group must satisfy the membership rule
 // and its first group_blocks[g] table entries must equal those of the
@@ -477,38 +942,50 @@ __global__ void check_groups_kernel(const int32_t* tables, int32_t max_blocks, c
         if (mine[t] != theirs[t]) atomicOr(verdict, kVerdictRange);
 }
 
-template <int D, int NST>
-int prefix_occupancy() {
+// Resident CTAs per SM of a kernel (cached per device); sets its dynamic
+// shared-memory limit once.
+template <typename K>
+int kernel_occupancy(K kernel, int threads, size_t smem, int slot) {
     static std::mutex mu;
-    static int cache[64] = {0};
+    static int cache[4][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
     std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev] == 0) {
-        cudaFuncSetAttribute(prefix_tc_kernel<D, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Px<D, NST>::kSmem));
+    if (cache[slot][dev] == 0) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefix_tc_kernel<D, NST>, Px<D, NST>::kThreads,
-                                                          Px<D, NST>::kSmem) != cudaSuccess || n < 1)
-            n = 1;
-        cache[dev] = n;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+        cache[slot][dev] = n;
     }
-    return cache[dev];
+    return cache[slot][dev];
 }
 
-constexpr int kPrefixStages = 4;
+constexpr int kMmaStages = 4;
+
+int occupancy_of(int kernel, int head_dim) {
+    if (kernel == 1)
+        return head_dim == 128
+                   ? kernel_occupancy(prefix_mma_kernel<128, kMmaStages>, Px<128, kMmaStages>::kThreads,
+                                      Px<128, kMmaStages>::kSmem, 0)
+                   : kernel_occupancy(prefix_mma_kernel<64, kMmaStages>, Px<64, kMmaStages>::kThreads,
+                                      Px<64, kMmaStages>::kSmem, 1);
+    return head_dim == 128 ? kernel_occupancy(prefix_umma_kernel<128>, Ux<128>::kThreads, Ux<128>::kSmem, 2)
+                           : kernel_occupancy(prefix_umma_kernel<64>, Ux<64>::kThreads, Ux<64>::kSmem, 3);
+}
 
 template <int D>
-cudaError_t run_prefix(const PrefixArgs& a, cudaStream_t s) {
-    using C = Px<D, kPrefixStages>;
+cudaError_t run_prefix(const PrefixArgs& a, int kernel, cudaStream_t s) {
     CUtensorMap tmK, tmV;
     const int64_t rows = a.num_blocks * a.kv_heads * 16;
     if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
         return cudaErrorInvalidValue;
-    prefix_occupancy<D, kPrefixStages>();  // sets the shared-memory attribute once per device
-    return launch_pdl(prefix_tc_kernel<D, kPrefixStages>, dim3(a.tiles, a.chunks, a.kv_heads), dim3(C::kThreads),
-                      C::kSmem, s, a, tmK, tmV);
+    occupancy_of(kernel, D);  // sets the shared-memory limit once per device
+    const dim3 grid(a.tiles, a.chunks, a.kv_heads);
+    if (kernel == 1)
+        return launch_pdl(prefix_mma_kernel<D, kMmaStages>, grid, dim3(Px<D, kMmaStages>::kThreads),
+                          Px<D, kMmaStages>::kSmem, s, a, tmK, tmV);
+    return launch_pdl(prefix_umma_kernel<D>, grid, dim3(Ux<D>::kThreads), Ux<D>::kSmem, s, a, tmK, tmV);
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -516,26 +993,32 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 }  // namespace
 
 PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int head_dim, int max_group_blocks,
-                       size_t base_offset) {
+                       size_t base_offset, int kernel) {
     const int b = batch < 1 ? 1 : (batch < kMaxBatchPerLaunch ? batch : kMaxBatchPerLaunch);
     const int G = q_heads / kv_heads;
     PrefixPlan p;
-    const int full_tiles = (b * G + kTileRows - 1) / kTileRows;  // every sequence in one group
-    p.tiles = full_tiles + (num_groups < b ? num_groups : b);    // one partly filled tile per group at most
-    // Split the shared blocks so that a batch in one group fills the GPU:
-    // about two waves of resident CTAs.
-    const int per_sm = head_dim == 128 ? prefix_occupancy<128, kPrefixStages>() : prefix_occupancy<64, kPrefixStages>();
-    const int want = 2 * per_sm * device_sm_count();
+    p.kernel = kernel == 1 ? 1 : 2;
+    p.rows = p.kernel == 1 ? Px<128, kMmaStages>::kRows : Ux<128>::kRows;
+    // blocks per chunk: a multiple of the tcgen05 kernel's 4-block step
+    const int quantum = p.kernel == 1 ? 1 : Ux<128>::kBlk;
+    const int full_tiles = (b * G + p.rows - 1) / p.rows;  // every sequence in one group
+    p.tiles = full_tiles + (num_groups < b ? num_groups : b);  // one partly filled tile per group at most
+    // Split the shared blocks so that a batch in one group fills the GPU with
+    // one wave of resident CTAs (two for the mma.sync kernel, whose CTAs
+    // are small).
+    const int per_sm = occupancy_of(p.kernel, head_dim);
+    const int want = (p.kernel == 1 ? 2 : 1) * per_sm * device_sm_count();
     const int pairs = full_tiles * kv_heads;
-    int chunks = (want + pairs - 1) / pairs;
-    const size_t slot_bytes = static_cast<size_t>(kTileRows) * (head_dim + 2) * sizeof(float);
+    int chunks = want / pairs;
+    const size_t slot_bytes = static_cast<size_t>(p.rows) * (head_dim + 2) * sizeof(float);
     const size_t cap_chunks = (static_cast<size_t>(256) << 20) / (static_cast<size_t>(p.tiles) * kv_heads * slot_bytes);
     if (chunks > kMaxChunks) chunks = kMaxChunks;
     if (static_cast<size_t>(chunks) > cap_chunks) chunks = static_cast<int>(cap_chunks);
-    if (chunks > max_group_blocks) chunks = max_group_blocks;
     if (chunks < 1) chunks = 1;
-    p.chunk_blocks = max_group_blocks > 0 ? (max_group_blocks + chunks - 1) / chunks : 1;
-    p.chunks = max_group_blocks > 0 ? (max_group_blocks + p.chunk_blocks - 1) / p.chunk_blocks : 1;
+    int cb = max_group_blocks > 0 ? (max_group_blocks + chunks - 1) / chunks : 1;
+    cb = (cb + quantum - 1) / quantum * quantum;
+    p.chunk_blocks = cb;
+    p.chunks = max_group_blocks > 0 ? (max_group_blocks + cb - 1) / cb : 1;
     size_t off = align256(base_offset);
     p.counters_offset = off;
     off = align256(off + static_cast<size_t>(p.tiles) * kv_heads * 4 * sizeof(int));
@@ -549,8 +1032,8 @@ PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int
     return p;
 }
 
-cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t s) {
-    return a.head_dim == 128 ? run_prefix<128>(a, s) : run_prefix<64>(a, s);
+cudaError_t launch_prefix(const PrefixArgs& a, int kernel, cudaStream_t s) {
+    return a.head_dim == 128 ? run_prefix<128>(a, kernel, s) : run_prefix<64>(a, kernel, s);
 }
 
 cudaError_t launch_check_groups(const int32_t* tables, int32_t max_blocks, const int32_t* lens,

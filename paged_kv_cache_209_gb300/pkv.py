@@ -48,7 +48,8 @@ class PoolStats(ctypes.Structure):
 
 
 class DecodeOpts(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32)]
+    _fields_ = [("kernel", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("prefix_kernel", ctypes.c_int32)]
 
 
 _lib = None
@@ -189,10 +190,10 @@ def pkv_copy_blocks(src_dst_pairs, k_cache, v_cache, flags: int = 0, stream=None
                                                   _ptr(v_cache), ctypes.byref(desc), flags, _stream(stream)))
 
 
-def _opts(kernel: int, num_ctas: int, stages: int = 0):
-    if kernel == 0 and num_ctas == 0 and stages == 0:
+def _opts(kernel: int, num_ctas: int, stages: int = 0, prefix_kernel: int = 0):
+    if kernel == 0 and num_ctas == 0 and stages == 0 and prefix_kernel == 0:
         return None
-    return ctypes.byref(DecodeOpts(kernel, num_ctas, stages))
+    return ctypes.byref(DecodeOpts(kernel, num_ctas, stages, prefix_kernel))
 
 
 def pkv_decode_workspace_size(batch: int, num_q_heads: int, max_blocks_per_seq: int, k_cache,
@@ -233,18 +234,19 @@ def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale:
 
 def pkv_decode_prefixed_workspace_size(batch: int, num_q_heads: int, max_blocks_per_seq: int, num_groups: int,
                                        max_group_blocks: int, k_cache, kernel: int = 0, num_ctas: int = 0,
-                                       stages: int = 0) -> int:
+                                       stages: int = 0, prefix_kernel: int = 0) -> int:
     """Workspace bytes of the shared-prefix call; allocate them zero-filled and reuse them."""
     lib = load_library()
     desc = cache_desc(k_cache)
     return int(lib.pkv_decode_prefixed_workspace_size(batch, num_q_heads, max_blocks_per_seq, num_groups,
                                                       max_group_blocks, ctypes.byref(desc),
-                                                      _opts(kernel, num_ctas, stages)))
+                                                      _opts(kernel, num_ctas, stages, prefix_kernel)))
 
 
 def pkv_decode_attention_prefixed(q, k_cache, v_cache, block_tables, context_lens, scale: float, prefix_group,
                                   group_blocks, max_group_blocks: int, out=None, workspace=None, flags: int = 0,
-                                  kernel: int = 0, num_ctas: int = 0, stages: int = 0, stream=None):
+                                  kernel: int = 0, num_ctas: int = 0, stages: int = 0, prefix_kernel: int = 0,
+                                  stream=None):
     """Decode attention with shared-prefix groups (two phases); returns ``out``.
 
     ``prefix_group`` is int32 [batch] (group of each sequence or -1),
@@ -270,14 +272,14 @@ def pkv_decode_attention_prefixed(q, k_cache, v_cache, block_tables, context_len
     if out is None:
         out = torch.empty_like(q)
     need = pkv_decode_prefixed_workspace_size(batch, q_heads, max_blocks, num_groups, max_group_blocks, k_cache,
-                                              kernel, num_ctas, stages)
+                                              kernel, num_ctas, stages, prefix_kernel)
     if workspace is None:
         workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
     _check("pkv_decode_attention_prefixed", lib.pkv_decode_attention_prefixed(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
         q_heads, ctypes.c_float(scale), _ptr(prefix_group), _ptr(group_blocks), num_groups, max_group_blocks,
-        _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags, _opts(kernel, num_ctas, stages),
-        _stream(stream)))
+        _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags,
+        _opts(kernel, num_ctas, stages, prefix_kernel), _stream(stream)))
     return out
 
 

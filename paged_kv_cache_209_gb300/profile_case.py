@@ -1,9 +1,11 @@
 """Run decode steps of a named workload, for profiling under ncu.
 
     python -m paged_kv_cache_209_gb300.profile_case --workload llama8k --steps 5
+    python -m paged_kv_cache_209_gb300.profile_case --workload prefix --two-phase --steps 5
 
 One step is the hot path of the benchmark: block copy (no pairs in these
-workloads), slot-mapped append, decode attention. No timing, no CPU oracle:
+workloads), slot-mapped append, decode attention (with --two-phase, the
+shared-prefix call with the workload's groups). No timing, no CPU oracle:
 this only drives the kernels so that a profiler can capture them.
 """
 
@@ -19,18 +21,30 @@ def main():
     ap.add_argument("--workload", default="llama8k", choices=["llama8k", "long128k", "mixed", "prefix"])
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--kernel", type=int, default=0)
+    ap.add_argument("--prefix-kernel", type=int, default=0)
+    ap.add_argument("--two-phase", action="store_true", help="shared-prefix call (prefix workload)")
     args = ap.parse_args()
     torch.cuda.set_device(0)
     w = workloads.device_workload(args.workload, torch.device("cuda", 0))
     out = torch.empty_like(w["q"])
-    need = pkv.pkv_decode_workspace_size(w["q"].shape[0], w["q"].shape[1], w["tables"].shape[1], w["k_pool"],
-                                         kernel=args.kernel)
+    B, HQ, MAXB = w["q"].shape[0], w["q"].shape[1], w["tables"].shape[1]
+    if args.two_phase:
+        need = pkv.pkv_decode_prefixed_workspace_size(B, HQ, MAXB, len(w["group_blocks"]), w["max_group_blocks"],
+                                                      w["k_pool"], kernel=args.kernel,
+                                                      prefix_kernel=args.prefix_kernel)
+    else:
+        need = pkv.pkv_decode_workspace_size(B, HQ, MAXB, w["k_pool"], kernel=args.kernel)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     for _ in range(args.steps):
         pkv.pkv_copy_blocks(w["pairs"], w["k_pool"], w["v_pool"])
         pkv.pkv_append(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"])
-        pkv.pkv_decode_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"], out=out,
-                                 workspace=ws, kernel=args.kernel)
+        if args.two_phase:
+            pkv.pkv_decode_attention_prefixed(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"],
+                                              w["prefix_group"], w["group_blocks"], w["max_group_blocks"], out=out,
+                                              workspace=ws, kernel=args.kernel, prefix_kernel=args.prefix_kernel)
+        else:
+            pkv.pkv_decode_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"], out=out,
+                                     workspace=ws, kernel=args.kernel)
     torch.cuda.synchronize()
     bits = pkv.pkv_device_status()
     if bits:

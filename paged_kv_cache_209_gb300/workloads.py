@@ -164,6 +164,9 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
     seed = cfg["seed"] + seed_offset
     tables, lens, num_blocks = workload_index(name)
     slots = slot_of(tables, lens - 1)
+    # shared-prefix groups: the prefix workload is one group over its shared blocks
+    n_shared = cfg.get("prefix", 0) // BLOCK_SIZE
+    group = np.zeros(B, dtype=np.int32) if n_shared else np.full(B, -1, dtype=np.int32)
     return dict(
         name=name, cfg=cfg, num_blocks=num_blocks,
         k_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed, bf, device),
@@ -177,4 +180,7 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
         lens=torch.from_numpy(lens.astype(np.int32)).to(device),
         tables_np=tables, lens_np=lens.astype(np.int32), slots_np=slots,
         scale=1.0 / math.sqrt(D),
+        prefix_group=torch.from_numpy(group).to(device),
+        group_blocks=torch.tensor([n_shared] if n_shared else [], dtype=torch.int32, device=device),
+        max_group_blocks=n_shared,
     )

@@ -74,14 +74,15 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("prefix_kernel", [1, 2])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_prefixed_matches_oracle(pkv, name):
+def test_prefixed_matches_oracle(pkv, name, prefix_kernel):
     member_of, gb, smax, hq, hkv, d = CASES[name]
     rng = np.random.default_rng(len(name))
     suffix = rng.integers(0, smax + 1, len(member_of)) if smax else np.zeros(len(member_of), dtype=np.int64)
     c = cases.grouped_case(len(name) * 3 + 1, member_of, gb, suffix, hq, hkv, d, torch.bfloat16)
     dv = dev(c)
-    out = run(pkv, c, dv)
+    out = run(pkv, c, dv, prefix_kernel=prefix_kernel)
     assert pkv.pkv_device_status(clear=True) == 0
     want = oracle_rows(c)
     check(out, want)
@@ -91,9 +92,10 @@ def test_prefixed_matches_oracle(pkv, name):
     check(out, two)
 
 
+@pytest.mark.parametrize("prefix_kernel", [1, 2])
 @pytest.mark.parametrize("num_ctas", [3, 40, 5000])
 @pytest.mark.parametrize("max_group_blocks", [None, 60, 80])
-def test_split_counts_and_chunking(pkv, num_ctas, max_group_blocks):
+def test_split_counts_and_chunking(pkv, num_ctas, max_group_blocks, prefix_kernel):
     """Forced CTA counts cut the own-token segments across CTAs (their merge
     writes the fold); a looser bound on the shared blocks changes how they are
     chunked. Same rows every time."""
@@ -101,7 +103,7 @@ def test_split_counts_and_chunking(pkv, num_ctas, max_group_blocks):
     suffix = np.random.default_rng(5).integers(1, 300, len(member_of))
     c = cases.grouped_case(77, member_of, [45, 2], suffix, 32, 8, 128, torch.bfloat16, width=80)
     dv = dev(c)
-    out = run(pkv, c, dv, max_group_blocks=max_group_blocks, num_ctas=num_ctas)
+    out = run(pkv, c, dv, max_group_blocks=max_group_blocks, num_ctas=num_ctas, prefix_kernel=prefix_kernel)
     assert pkv.pkv_device_status(clear=True) == 0
     check(out, oracle_rows(c))
 
@@ -194,3 +196,19 @@ def test_host_rejections(pkv):
         pkv.pkv_decode_attention_prefixed(d["q"], d["k"], d["v"], d["tables"], d["lens"], c["scale"], d["group"],
                                           many, 2)
     assert e.value.name == "PKV_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (64, 16, 2)])
+def test_two_chunk_first_kernels_agree(pkv, d, hq, hkv):
+    """The tcgen05 and the mma.sync chunk-first kernels on the same rows:
+    two implementations of one pass (many members, a long shared run)."""
+    member_of = [0] * 40 + [1] * 9 + [-1] * 3
+    suffix = np.random.default_rng(3).integers(0, 90, len(member_of))
+    c = cases.grouped_case(91, member_of, [70, 13], suffix, hq, hkv, d, torch.bfloat16)
+    dv = dev(c)
+    a = run(pkv, c, dv, prefix_kernel=1)
+    b = run(pkv, c, dv, prefix_kernel=2)
+    assert pkv.pkv_device_status(clear=True) == 0
+    diff = (a.float() - b.float())
+    assert diff.abs().max().item() <= 1e-2 and (diff.norm() / a.float().norm()).item() <= 2e-3
+    check(b, oracle_rows(c))
