@@ -356,6 +356,7 @@ pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, con
         pa.out = a.out;
         pa.partials = reinterpret_cast<float*>(ws + pp.partials_offset);
         pa.counters = reinterpret_cast<int*>(ws + pp.counters_offset);
+        pa.trace = pp.trace_offset ? ws + pp.trace_offset : nullptr;
         pa.status = status;
         pa.num_blocks = desc->num_blocks;
         pa.max_blocks = max_blocks_per_seq;

@@ -108,6 +108,7 @@ struct PrefixArgs {
     void* out;
     float* partials;  // [tiles][kv_heads][chunks][rows per tile][head_dim + 2]
     int* counters;    // [tiles][kv_heads][4 warps]; zero between calls
+    void* trace;      // per-CTA timestamps (PKV_TRACE builds only)
     unsigned int* status;
     int64_t num_blocks;
     int32_t max_blocks;
@@ -130,7 +131,7 @@ struct PrefixPlan {
     int kernel;  // 1 mma.sync (64-row tiles), 2 tcgen05 (128-row tiles)
     int rows;    // query rows per tile
     int tiles, chunks, chunk_blocks;
-    size_t counters_offset, partials_offset, fold_o_offset, fold_lse_offset, total;
+    size_t counters_offset, partials_offset, fold_o_offset, fold_lse_offset, trace_offset, total;
 };
 PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int head_dim, int max_group_blocks,
                        size_t base_offset, int kernel);

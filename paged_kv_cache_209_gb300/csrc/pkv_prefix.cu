@@ -46,9 +46,21 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxChunks = 32;
+constexpr int kMaxCluster = 8;  // CTAs (chunks) per cluster of the tcgen05 kernel: the portable maximum
 constexpr int kMaxGroups = kMaxBatchPerLaunch;
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+
+// Build-time tracing (PKV_TRACE): each CTA of the tcgen05 kernel records
+// %globaltimer stamps in a row of 8 words: [0] entry, [1] tile located,
+// [2] tensor memory and Q ready, [3] softmax loop done, [4] tensor memory
+// freed, [5] exit of thread 0, [6] SM id, [7] 1 for a CTA with work.
+#ifdef PKV_TRACE
+#define PX_STAMP(a, i, v) \
+    (reinterpret_cast<unsigned long long*>((a).trace))[((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 8 + (i)] = (v)
+#else
+#define PX_STAMP(a, i, v) ((void)0)
+#endif
 
 // Members of one tile: at most rows / G + 2.
 __host__ __device__ constexpr int member_slots(int rows) { return rows + 8; }
@@ -58,10 +70,11 @@ __host__ __device__ constexpr int member_slots(int rows) { return rows + 8; }
 // x index and the tile's members in member order, and the chunk of shared
 // blocks of this CTA's y index. info[]: [0] group, [1] tile within the group,
 // [2] first member of the group, [3] shared blocks, [4] chunks of the group,
-// [5] rows of the tile, [6] first member of the tile. Returns false (for the
-// whole CTA) when the CTA has no work.
+// [5] rows of the tile, [6] first member of the tile. Returns (for the whole
+// CTA) 0 when x names no tile, 1 when the tile exists but its group has no
+// chunk y (info and members are set), 2 when the CTA has work.
 template <int kRowsPerTile>
-__device__ bool locate_tile(const PrefixArgs& a, int* info, int* members, int* counts) {
+__device__ int locate_tile(const PrefixArgs& a, int* info, int* members, int* counts) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = a.group;
@@ -102,10 +115,9 @@ __device__ bool locate_tile(const PrefixArgs& a, int* info, int* members, int* c
     }
     __syncthreads();
     const int p = info[0];
-    if (p < 0) return false;
+    if (p < 0) return 0;
     const int nb = a.group_blocks[p];  // in [0, max_group_blocks]: p has members
     const int nch = nb > 0 ? (nb + a.chunk_blocks - 1) / a.chunk_blocks : 1;
-    if (static_cast<int>(blockIdx.y) >= nch) return false;
     const int r0 = info[1] * kRowsPerTile;
     const int nrows = min(kRowsPerTile, counts[p] * G - r0);
     const int m0 = r0 / G;
@@ -131,7 +143,7 @@ __device__ bool locate_tile(const PrefixArgs& a, int* info, int* members, int* c
         }
     }
     __syncthreads();
-    return true;
+    return static_cast<int>(blockIdx.y) < nch ? 2 : 1;
 }
 
 // A CTA without work leaves at once, except CTA (0, 0, 0), which first waits
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(Px<D, NST>::kThreads)
     // kernel) lets it start once all its CTAs have passed their own wait on
     // the kernels before them, so the K/V blocks are complete.
     allow_dependents();
-    if (!locate_tile<kTileRows>(a, info, members, counts)) {
+    if (locate_tile<kTileRows>(a, info, members, counts) != 2) {
         idle_exit();
         return;
     }
@@ -512,11 +524,16 @@ struct Ux {
     static constexpr int kNumBars = 2 * kStages + 7;  // kv_full, kv_empty, s_full[2], p_full[2], o_done[2], final
     static constexpr int kOffInts = kOffBars + kNumBars * 8;
     static constexpr size_t kSmem = 1024 + kOffInts + (16 + member_slots(kRows) + kMaxGroups) * 4;
-    static constexpr int kThreads = 192;   // warps 0-3 softmax (lanes 32w..32w+31), 4 TMA, 5 MMA
-    static constexpr uint32_t kTmemCols = 256;
-    static constexpr uint32_t kColS = 0;   // S buffers: columns [0, 64) and [64, 128)
-    static constexpr uint32_t kColO = 128; // O: columns [128, 128 + D)
-    static_assert(kColO + D <= kTmemCols, "tensor-memory columns");
+    // warps 0-7 softmax: warp w takes rows 32 (w % 4) .. + 31 (its tensor-memory
+    // lanes) and token half w / 4 of every step; warp 8 TMA, warp 9 MMA
+    static constexpr int kSoftmaxWarps = 8;
+    static constexpr int kTmaWarp = 8;
+    static constexpr int kMmaWarp = 9;
+    static constexpr int kThreads = 320;
+    static constexpr uint32_t kColS = 0;    // S buffers: columns [0, 64) and [64, 128)
+    static constexpr uint32_t kColO = 128;  // O of token half 0: [128, 128 + D); half 1: [128 + D, 128 + 2D)
+    static constexpr uint32_t kTmemCols = kColO + 2 * D <= 256 ? 256 : 512;
+    static_assert(kColO + 2 * D <= kTmemCols, "tensor-memory columns");
 };
 
 template <int D>
@@ -529,7 +546,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
     uint64_t* kv_empty = kv_full + C::kStages;
     uint64_t* s_full = kv_empty + C::kStages;  // [2]: S buffer b holds a finished S
-    uint64_t* p_full = s_full + 2;             // [2]: P buffer b written (4 warp arrivals)
+    uint64_t* p_full = s_full + 2;             // [2]: P buffer b written (one arrival per softmax warp)
     uint64_t* o_done = p_full + 2;             // [2]: the PV product of step j (buffer j % 2) has completed
     uint64_t* final_bar = o_done + 2;          // every issued MMA has completed
     int* info = reinterpret_cast<int*>(smem + C::kOffInts);
@@ -545,40 +562,49 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     const int chunk = blockIdx.y;
 
     if (threadIdx.x == 0) {
+        PX_STAMP(a, 0, global_ns());
+        PX_STAMP(a, 6, sm_id());
+        PX_STAMP(a, 7, 0);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 4);
+            mbar_init(&p_full[b], C::kSoftmaxWarps);
             mbar_init(&o_done[b], 1);
         }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (threadIdx.x == 32 * 4) {
+    if (threadIdx.x == 32 * C::kTmaWarp) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
     allow_dependents();  // inputs only until the fold (see the mma.sync kernel)
-    if (!locate_tile<C::kRows>(a, info, members, counts)) {
+    const int where = locate_tile<C::kRows>(a, info, members, counts);
+    if (where == 0) {  // no tile: the same for every CTA of the cluster
         idle_exit();
         return;
     }
-    // From here every thread of the CTA reaches the final __syncthreads, so
-    // the tensor memory allocated below is always freed.
+    // From here every thread of the CTA reaches the final __syncthreads (so
+    // the tensor memory allocated below is always freed) and both cluster
+    // barriers. A CTA whose group has no chunk y streams nothing and only
+    // takes its share of the combine.
     const int nb = info[3];
-    const int nch = info[4];
     const int nrows = info[5];
     const int m0 = info[6];
     const int r0 = info[1] * C::kRows;
     const int blk0 = chunk * a.chunk_blocks;
-    const int nblk = nb > 0 ? min(a.chunk_blocks, nb - blk0) : 0;
+    const int nblk = (where == 2 && nb > 0) ? min(a.chunk_blocks, nb - blk0) : 0;
     const int nsteps = (nblk + C::kBlk - 1) / C::kBlk;
+    if (threadIdx.x == 0) {
+        PX_STAMP(a, 1, global_ns());
+        PX_STAMP(a, 7, 1);
+    }
 
-    if (warp == 5) {
+    if (warp == C::kMmaWarp) {
         tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
@@ -604,8 +630,9 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) PX_STAMP(a, 2, global_ns());
 
-    if (warp == 4) {
+    if (warp == C::kTmaWarp) {
         // ------------------------------------------------ TMA producer
         // Step j: blocks 4j .. 4j+3 of the chunk; lane b issues block b. A
         // block past the chunk or with an invalid id is loaded from row -16
@@ -651,7 +678,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             for (int u = first; u < issued; ++u)
                 mbar_wait(&kv_full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------ MMA issuer (one thread)
         if (lane == 0) {
             constexpr uint32_t idS = umma_idesc_bf16(C::kRows, C::kTok, false, false);
@@ -682,20 +709,25 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                // O += P_hi V + P_lo V. P is K-major (tokens along the row); V
-                // is MN-major straight from the TMA layout: 64 columns per
-                // 128-byte row, the two column halves kHalfBytes apart, 8
+                // O_t += P_hi V + P_lo V over token half t (tokens 32t .. 32t+31)
+                // into that half's accumulator. P is K-major (tokens along the
+                // row); V is MN-major straight from the TMA layout: 64 columns
+                // per 128-byte row, the two column halves kHalfBytes apart, 8
                 // token rows per 1024-byte atom.
                 const int s = j % C::kStages;
                 const uint32_t v_base = smem_u32(smem + C::kOffKV + s * C::kStageBytes + C::kKBytes);
                 const uint32_t p_base = smem_u32(smem + C::kOffP + (j & 1) * 2 * C::kPBytes);
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
+                for (int th = 0; th < 2; ++th) {
 #pragma unroll
-                    for (int kt = 0; kt < C::kTok / 16; ++kt) {
-                        const uint64_t ad = umma_desc_sw128(p_base + part * C::kPBytes + kt * 32, 16, 1024);
-                        const uint64_t bd = umma_desc_sw128(v_base + kt * 2048, C::kHalfBytes, 1024);
-                        umma_bf16(tmem + C::kColO, ad, bd, idO, (j > 0 || part > 0 || kt > 0) ? 1u : 0u);
+                    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                        for (int kt = 2 * th; kt < 2 * th + 2; ++kt) {
+                            const uint64_t ad = umma_desc_sw128(p_base + part * C::kPBytes + kt * 32, 16, 1024);
+                            const uint64_t bd = umma_desc_sw128(v_base + kt * 2048, C::kHalfBytes, 1024);
+                            umma_bf16(tmem + C::kColO + th * D, ad, bd, idO,
+                                      (j > 0 || part > 0 || kt > 2 * th) ? 1u : 0u);
+                        }
                     }
                 }
                 umma_commit(&kv_empty[s]);
@@ -710,12 +742,19 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     }
 
     // ---------------------------------------------------- softmax warps
-    float m = ninf(), l = 0.f;  // running max (base 2, scaled) and sum of this thread's row
+    // Thread (warp w < 8, lane i) keeps the online softmax of row 32 (w % 4) + i
+    // over token half w / 4 of every step, with its own running max, sum and O
+    // accumulator; the two halves of a row are combined once, at the end.
+    float m = ninf(), l = 0.f;  // running max (base 2, scaled) and sum
     bool ok = true;
-    float acc[D];               // the row's output accumulator at the end
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    if (warp < 4) {
-        const int r = threadIdx.x;
+    float acc[D];               // warps 0-3: the row's output accumulator at the end
+    const int q4 = warp & 3;
+    const int th = (warp >> 2) & 1;  // token half of this softmax warp
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t col_o = C::kColO + th * D;
+    float* xfer = reinterpret_cast<float*>(smem + C::kOffP);  // [3][128]: half 1's max, sum, status
+    if (warp < C::kSoftmaxWarps) {
+        const int r = q4 * 32 + lane;
         const float scale_log2 = a.scale * kLog2e;
         for (int j = 0; j < nsteps; ++j) {
             if (!mbar_wait(&s_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.status, abort_flag)) {
@@ -723,16 +762,15 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t sv[2][32];
-            tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok, sv[0]);
-            tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok + 32, sv[1]);
+            uint32_t sv[32];
+            tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok + th * 32, sv);
             tmem_ld_wait();
-            const int valid = min(C::kTok, (nblk - C::kBlk * j) * 16);
-            float x[C::kTok];
+            const int valid = min(C::kTok, (nblk - C::kBlk * j) * 16) - th * 32;
+            float x[32];
             float mx = ninf();
 #pragma unroll
-            for (int t = 0; t < C::kTok; ++t) {
-                x[t] = t < valid ? __uint_as_float(sv[t >> 5][t & 31]) * scale_log2 : ninf();
+            for (int t = 0; t < 32; ++t) {
+                x[t] = t < valid ? __uint_as_float(sv[t]) * scale_log2 : ninf();
                 mx = fmaxf(mx, x[t]);
             }
             // lazy rescale: the running max moves only when a score exceeds it by more than 8
@@ -743,11 +781,12 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 alpha = m == ninf() ? 0.f : ex2(m - mn);
                 m = mn;
             }
-            uint32_t hi[C::kTok / 2], lo[C::kTok / 2];
+            uint32_t hi[16], lo[16];
             float psum = 0.f;
+            const float base = m == ninf() ? 0.f : m;  // a half with no valid token yet
 #pragma unroll
-            for (int t = 0; t < C::kTok; t += 2) {
-                const float p0 = ex2(x[t] - m), p1 = ex2(x[t + 1] - m);
+            for (int t = 0; t < 32; t += 2) {
+                const float p0 = ex2(x[t] - base), p1 = ex2(x[t + 1] - base);
                 psum += p0 + p1;
                 const uint32_t hv = pack_bf16x2(p0, p1);
                 hi[t / 2] = hv;
@@ -759,7 +798,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 ok = false;
                 break;
             }
-            // rescale O in tensor memory once the PV product of step j - 1 is in
+            // rescale this half's O in tensor memory once the PV product of step j - 1 is in
             if (__any_sync(0xffffffffu, resc && j > 0)) {
                 if (!mbar_wait(&o_done[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1), a.status,
                                abort_flag)) {
@@ -770,18 +809,18 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < D; c += 32) {
                     uint32_t ov[32];
-                    tmem_ld32(tmem + lane_base + C::kColO + c, ov);
+                    tmem_ld32(tmem + lane_base + col_o + c, ov);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st32(tmem + lane_base + C::kColO + c, ov);
+                    tmem_st32(tmem + lane_base + col_o + c, ov);
                 }
                 tmem_st_wait();
             }
             uint8_t* prow = smem + C::kOffP + (j & 1) * 2 * C::kPBytes + r * 128;
 #pragma unroll
-            for (int c = 0; c < C::kTok / 8; ++c) {
-                const int off = ((c ^ (r & 7)) << 4);
+            for (int c = 0; c < 4; ++c) {
+                const int off = (((4 * th + c) ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
                 *reinterpret_cast<uint4*>(prow + C::kPBytes + off) =
                     make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
@@ -791,126 +830,149 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[j & 1]);
         }
-        // the row's O: the last PV product must be in
+        if (threadIdx.x == 0) PX_STAMP(a, 3, global_ns());
+        // the last PV product must be in before O is read or the P buffers reused
+        if (ok && nsteps > 0 &&
+            !mbar_wait(&o_done[(nsteps - 1) & 1], static_cast<uint32_t>(((nsteps - 1) >> 1) & 1), a.status,
+                       abort_flag))
+            ok = false;
+        tc_fence_after();
+        if (th == 1) {
+            xfer[r] = m;
+            xfer[C::kRows + r] = l;
+            xfer[2 * C::kRows + r] = ok ? 1.f : 0.f;
+        }
+        named_barrier_sync(1, 32 * C::kSoftmaxWarps);
+        if (th == 0) {
+            // combine the row's two halves
+            const float m1 = xfer[r], l1 = xfer[C::kRows + r];
+            const bool ok1 = xfer[2 * C::kRows + r] != 0.f;
+            const bool has0 = ok && l > 0.f, has1 = ok1 && l1 > 0.f;
+            const float M = fmaxf(has0 ? m : ninf(), has1 ? m1 : ninf());
+            const float w0 = has0 ? ex2(m - M) : 0.f, w1 = has1 ? ex2(m1 - M) : 0.f;
 #pragma unroll
-        for (int d = 0; d < D; ++d) acc[d] = 0.f;
-        if (ok && nsteps > 0) {
-            if (mbar_wait(&o_done[(nsteps - 1) & 1], static_cast<uint32_t>(((nsteps - 1) >> 1) & 1), a.status,
-                          abort_flag)) {
-                tc_fence_after();
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o0[32], o1[32];
+                tmem_ld32(tmem + lane_base + C::kColO + c, o0);
+                tmem_ld32(tmem + lane_base + C::kColO + D + c, o1);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t ov[32];
-                    tmem_ld32(tmem + lane_base + C::kColO + c, ov);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[c + e] = __uint_as_float(ov[e]);
-                }
-            } else {
-                ok = false;
+                for (int e = 0; e < 32; ++e)
+                    acc[c + e] = (has0 ? w0 * __uint_as_float(o0[e]) : 0.f) + (has1 ? w1 * __uint_as_float(o1[e]) : 0.f);
             }
+            l = (has0 ? w0 * l : 0.f) + (has1 ? w1 * l1 : 0.f);
+            m = M;
+            ok = true;  // a half that gave up contributes nothing; the status word records it
         }
     }
     // ---- tensor memory is no longer read: free it
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == C::kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
-    if (warp >= 4 || !ok || *abort_flag) {
-        grid_dependency_wait();
-        return;
-    }
+    if (threadIdx.x == 0) PX_STAMP(a, 4, global_ns());
 
-    // ---- merge the chunks' partials (several chunks) and fold in the own-token partial
-    const int r = threadIdx.x;
-    const long long tile_head = static_cast<long long>(h) * gridDim.x + blockIdx.x;
-    constexpr int kSlot = C::kRows * (D + 2);
-    if (nch > 1) {
-        float* slot = a.partials + (tile_head * a.chunks + chunk) * kSlot;
+    // ---- this chunk's partial of the tile's rows, in this CTA's shared memory
+    // (over the now idle K/V ring): O unnormalised [128][D + 4], the running
+    // maxima, the sums. A CTA without the chunk, or one that gave up, leaves
+    // empty rows (sum 0).
+    constexpr int kPS = D + 4;
+    float* part = reinterpret_cast<float*>(smem + C::kOffKV);
+    float* part_m = part + C::kRows * kPS;
+    float* part_l = part_m + C::kRows;
+    float* wts = part_l + C::kRows;  // [rows combined here][kMaxCluster + 1]
+    int* rowoff = reinterpret_cast<int*>(wts + C::kRows * (kMaxCluster + 1));
+    static_assert(C::kRows * (kPS + 2 + kMaxCluster + 2) * 4 <= C::kStages * C::kStageBytes, "partial fits the ring");
+    fence_proxy_async_smem();  // the ring was last written by TMA
+    if (warp < 4) {
+        const int r = threadIdx.x;
+        const bool live = ok && !*abort_flag && l > 0.f;
 #pragma unroll
         for (int d = 0; d < D; d += 4)
-            __stcg(reinterpret_cast<float4*>(slot + r * D + d), make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]));
-        __stcg(slot + C::kRows * D + r, m);
-        __stcg(slot + C::kRows * D + C::kRows + r, l);
-        __threadfence();
-        __syncwarp();
-        int* counter = a.counters + tile_head * 4 + warp;
-        int old = 0;
-        if (lane == 0) old = atomicAdd(counter, 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old != nch - 1) {
-            grid_dependency_wait();
-            return;
-        }
-        __threadfence();
-        if (lane == 0) *counter = 0;  // ready for the next call
+            *reinterpret_cast<float4*>(part + r * kPS + d) =
+                live ? make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        part_m[r] = live ? m : ninf();
+        part_l[r] = live ? l : 0.f;
     }
+    cluster_sync();
     grid_dependency_wait();  // fold_o / fold_lse come from the decode kernel
-    if (!row_ok) return;
-    // Weights over the parts: every chunk's (m_c, l_c) and the own-token
-    // partial (lse_s, normalised o_s), all in base 2.
-    const float ls = __ldcg(a.fold_lse + row_idx);
-    float Mx = ls;
-    if (nch > 1) {
-        for (int c = 0; c < nch; ++c) {
-            const float* sl = a.partials + (tile_head * a.chunks + c) * kSlot;
-            const float lc = __ldcg(sl + C::kRows * D + C::kRows + r);
-            if (lc > 0.f) Mx = fmaxf(Mx, __ldcg(sl + C::kRows * D + r));
-        }
-    } else if (l > 0.f) {
-        Mx = fmaxf(Mx, m);
-    }
-    float den = 0.f, ws = 0.f;
-    if (Mx != ninf()) {
-        ws = ls == ninf() ? 0.f : ex2(ls - Mx);
-        den = ws;
-        if (nch > 1) {
-            for (int c = 0; c < nch; ++c) {
-                const float* sl = a.partials + (tile_head * a.chunks + c) * kSlot;
-                const float lc = __ldcg(sl + C::kRows * D + C::kRows + r);
-                if (lc > 0.f) den += lc * ex2(__ldcg(sl + C::kRows * D + r) - Mx);
+
+    // ---- CTA k of the cluster combines rows [k R, (k + 1) R) of the tile: the
+    // chunks' partials (distributed shared memory) and the own-token partial
+    // (lse_s, normalised o_s), all weights in base 2
+    const int cn = gridDim.y;  // CTAs of the cluster = chunks
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int R = (C::kRows + cn - 1) / cn;
+    const int rb = rank * R;
+    const uint32_t part_addr = smem_u32(part);
+    if (static_cast<int>(threadIdx.x) < R) {
+        const int rr = threadIdx.x;
+        const int r = rb + rr;
+        int off = -1;
+        if (r < nrows) {
+            const int Rg = r0 + r;
+            const int mm = Rg / G;
+            off = members[mm - m0] * a.q_heads + h * G + (Rg - mm * G);
+            const float ls = __ldcg(a.fold_lse + off);
+            float mc[kMaxCluster], lc[kMaxCluster];
+            float Mx = ls;
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) {
+                mc[c] = ninf();
+                lc[c] = 0.f;
+                if (c < cn) {
+                    const uint32_t ad = mapa_shared(part_addr + (C::kRows * kPS + r) * 4, c);
+                    mc[c] = ld_cluster_f32(ad);
+                    lc[c] = ld_cluster_f32(ad + C::kRows * 4);
+                }
             }
-        } else if (l > 0.f) {
-            den += l * ex2(m - Mx);
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)
+                if (lc[c] > 0.f) Mx = fmaxf(Mx, mc[c]);
+            float den = 0.f, ws = 0.f;
+            if (Mx != ninf()) {
+                ws = ls == ninf() ? 0.f : ex2(ls - Mx);
+                den = ws;
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c)
+                    if (lc[c] > 0.f) den += lc[c] * ex2(mc[c] - Mx);
+            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)
+                wts[rr * (kMaxCluster + 1) + c] = lc[c] > 0.f ? ex2(mc[c] - Mx) * inv : 0.f;
+            wts[rr * (kMaxCluster + 1) + kMaxCluster] = ws * inv;
         }
+        rowoff[rr] = off;
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    ws *= inv;
-    if (nch > 1) {
+    __syncthreads();
+    for (int u = threadIdx.x; u < R * (D / 4); u += blockDim.x) {
+        const int rr = u / (D / 4);
+        const int c4 = u - rr * (D / 4);
+        const int off = rowoff[rr];
+        if (off < 0) continue;
+        const float* wr = wts + rr * (kMaxCluster + 1);
+        const float wsr = wr[kMaxCluster];
+        const float4 f = __ldcg(reinterpret_cast<const float4*>(a.fold_o + static_cast<long long>(off) * D + 4 * c4));
+        float4 o4 = make_float4(wsr * f.x, wsr * f.y, wsr * f.z, wsr * f.w);
+        const uint32_t la = part_addr + ((rb + rr) * kPS + 4 * c4) * 4;
 #pragma unroll
-        for (int d = 0; d < D; ++d) acc[d] = 0.f;
-        for (int c = 0; c < nch; ++c) {
-            const float* sl = a.partials + (tile_head * a.chunks + c) * kSlot;
-            const float lc = __ldcg(sl + C::kRows * D + C::kRows + r);
-            if (!(lc > 0.f)) continue;
-            const float w = ex2(__ldcg(sl + C::kRows * D + r) - Mx) * inv;
-#pragma unroll
-            for (int d = 0; d < D; d += 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(sl + r * D + d));
-                acc[d] += w * v.x;
-                acc[d + 1] += w * v.y;
-                acc[d + 2] += w * v.z;
-                acc[d + 3] += w * v.w;
+        for (int c = 0; c < kMaxCluster; ++c) {
+            if (c < cn && wr[c] != 0.f) {
+                const float4 v = ld_cluster_v4(mapa_shared(la, c));
+                o4.x += wr[c] * v.x;
+                o4.y += wr[c] * v.y;
+                o4.z += wr[c] * v.z;
+                o4.w += wr[c] * v.w;
             }
         }
-    } else {
-        const float w = l > 0.f ? ex2(m - Mx) * inv : 0.f;
-#pragma unroll
-        for (int d = 0; d < D; ++d) acc[d] *= w;
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + static_cast<long long>(off) * D + 4 * c4) =
+            make_uint2(pack_bf16x2(o4.x, o4.y), pack_bf16x2(o4.z, o4.w));
     }
-    const float* fo = a.fold_o + row_idx * D;
-    uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row_idx * D);
-#pragma unroll
-    for (int d = 0; d < D; d += 8) {
-        const float4 f0 = __ldcg(reinterpret_cast<const float4*>(fo + d));
-        const float4 f1 = __ldcg(reinterpret_cast<const float4*>(fo + d + 4));
-        out[d / 8] = make_uint4(pack_bf16x2(acc[d] + ws * f0.x, acc[d + 1] + ws * f0.y),
-                                pack_bf16x2(acc[d + 2] + ws * f0.z, acc[d + 3] + ws * f0.w),
-                                pack_bf16x2(acc[d + 4] + ws * f1.x, acc[d + 5] + ws * f1.y),
-                                pack_bf16x2(acc[d + 6] + ws * f1.z, acc[d + 7] + ws * f1.w));
-    }
+    cluster_sync();  // each CTA's partial stays in place until the whole cluster has read it
+    if (threadIdx.x == 0) PX_STAMP(a, 5, global_ns());
 }
 
 // ------------------------------------------------------------------ checked mode
@@ -974,6 +1036,41 @@ int occupancy_of(int kernel, int head_dim) {
                            : kernel_occupancy(prefix_umma_kernel<64>, Ux<64>::kThreads, Ux<64>::kSmem, 3);
 }
 
+// Clusters of `c` CTAs of the tcgen05 kernel that fit on the device at once
+// (cached per device and size).
+int active_clusters(int head_dim, int c) {
+    static std::mutex mu;
+    static int cache[2][kMaxCluster + 1][64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    const int hd = head_dim == 128 ? 1 : 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int& slot = cache[hd][c][dev];
+    if (slot == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, c, 1);
+        cfg.blockDim = dim3(hd ? Ux<128>::kThreads : Ux<64>::kThreads);
+        cfg.dynamicSmemBytes = hd ? Ux<128>::kSmem : Ux<64>::kSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = c;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        const cudaError_t e = hd ? cudaOccupancyMaxActiveClusters(&n, prefix_umma_kernel<128>, &cfg)
+                                 : cudaOccupancyMaxActiveClusters(&n, prefix_umma_kernel<64>, &cfg);
+        if (e != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = -1;  // not launchable at this size
+        }
+        slot = n;
+    }
+    return slot;
+}
+
 template <int D>
 cudaError_t run_prefix(const PrefixArgs& a, int kernel, cudaStream_t s) {
     CUtensorMap tmK, tmV;
@@ -985,7 +1082,8 @@ cudaError_t run_prefix(const PrefixArgs& a, int kernel, cudaStream_t s) {
     if (kernel == 1)
         return launch_pdl(prefix_mma_kernel<D, kMmaStages>, grid, dim3(Px<D, kMmaStages>::kThreads),
                           Px<D, kMmaStages>::kSmem, s, a, tmK, tmV);
-    return launch_pdl(prefix_umma_kernel<D>, grid, dim3(Ux<D>::kThreads), Ux<D>::kSmem, s, a, tmK, tmV);
+    return launch_pdl_cluster(prefix_umma_kernel<D>, grid, dim3(Ux<D>::kThreads), dim3(1, a.chunks, 1),
+                              Ux<D>::kSmem, s, a, tmK, tmV);
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1010,9 +1108,16 @@ PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int
     const int want = (p.kernel == 1 ? 2 : 1) * per_sm * device_sm_count();
     const int pairs = full_tiles * kv_heads;
     int chunks = want / pairs;
+    if (p.kernel == 2) {
+        // one cluster of `chunks` CTAs per (tile, KV head): the largest
+        // cluster size at which all of them fit on the device at once
+        int c = chunks < kMaxCluster ? (chunks < 1 ? 1 : chunks) : kMaxCluster;
+        while (c > 1 && active_clusters(head_dim, c) < pairs) --c;
+        chunks = c;
+    }
     const size_t slot_bytes = static_cast<size_t>(p.rows) * (head_dim + 2) * sizeof(float);
     const size_t cap_chunks = (static_cast<size_t>(256) << 20) / (static_cast<size_t>(p.tiles) * kv_heads * slot_bytes);
-    if (chunks > kMaxChunks) chunks = kMaxChunks;
+    if (chunks > (p.kernel == 1 ? kMaxChunks : kMaxCluster)) chunks = p.kernel == 1 ? kMaxChunks : kMaxCluster;
     if (static_cast<size_t>(chunks) > cap_chunks) chunks = static_cast<int>(cap_chunks);
     if (chunks < 1) chunks = 1;
     int cb = max_group_blocks > 0 ? (max_group_blocks + chunks - 1) / chunks : 1;
@@ -1023,11 +1128,19 @@ PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int
     p.counters_offset = off;
     off = align256(off + static_cast<size_t>(p.tiles) * kv_heads * 4 * sizeof(int));
     p.partials_offset = off;
-    if (p.chunks > 1) off = align256(off + static_cast<size_t>(p.tiles) * kv_heads * p.chunks * slot_bytes);
+    // the tcgen05 kernel combines its chunks through distributed shared memory
+    if (p.chunks > 1 && p.kernel == 1)
+        off = align256(off + static_cast<size_t>(p.tiles) * kv_heads * p.chunks * slot_bytes);
     p.fold_o_offset = off;
     off = align256(off + static_cast<size_t>(b) * q_heads * head_dim * sizeof(float));
     p.fold_lse_offset = off;
     off = align256(off + static_cast<size_t>(b) * q_heads * sizeof(float));
+#ifdef PKV_TRACE
+    p.trace_offset = off;
+    off = align256(off + static_cast<size_t>(p.tiles) * p.chunks * kv_heads * 64);
+#else
+    p.trace_offset = 0;
+#endif
     p.total = off;
     return p;
 }
