@@ -52,14 +52,22 @@ constexpr int kMaxGroups = kMaxBatchPerLaunch;
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 
 // Build-time tracing (PKV_TRACE): each CTA of the tcgen05 kernel records
-// %globaltimer stamps in a row of 8 words: [0] entry, [1] tile located,
+// %globaltimer stamps in a row of 16 words: [0] entry, [1] tile located,
 // [2] tensor memory and Q ready, [3] softmax loop done, [4] tensor memory
-// freed, [5] exit of thread 0, [6] SM id, [7] 1 for a CTA with work.
+// freed, [5] exit of thread 0, [6] SM id, [7] 1 for a CTA with work; sums over
+// the steps of: [8] softmax wait for S, [9] S load from tensor memory, [10]
+// softmax arithmetic, [11] softmax waits for PV products (and O rescale),
+// [12] P store and arrival, [13] MMA wait for P, [14] MMA wait for K/V,
+// [15] TMA wait for a free stage.
 #ifdef PKV_TRACE
 #define PX_STAMP(a, i, v) \
-    (reinterpret_cast<unsigned long long*>((a).trace))[((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 8 + (i)] = (v)
+    (reinterpret_cast<unsigned long long*>((a).trace))[((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 16 + (i)] = (v)
+#define PX_T(var) const unsigned long long var = global_ns()
+#define PX_ADD(acc, v) acc += (v)
 #else
 #define PX_STAMP(a, i, v) ((void)0)
+#define PX_T(var) ((void)0)
+#define PX_ADD(acc, v) ((void)0)
 #endif
 
 // Members of one tile: at most rows / G + 2.
@@ -73,25 +81,39 @@ __host__ __device__ constexpr int member_slots(int rows) { return rows + 8; }
 // [5] rows of the tile, [6] first member of the tile. Returns (for the whole
 // CTA) 0 when x names no tile, 1 when the tile exists but its group has no
 // chunk y (info and members are set), 2 when the CTA has work.
+//
+// `stage` holds 2 * kMaxBatchPerLaunch + kMaxGroups ints: the context lengths
+// (clamped to the tables), the group ids and the group block counts, read from
+// global memory once, side by side, so that nothing below waits on a chain of
+// dependent global loads.
 template <int kRowsPerTile>
-__device__ int locate_tile(const PrefixArgs& a, int* info, int* members, int* counts) {
+__device__ int locate_tile(const PrefixArgs& a, int* info, int* members, int* counts, int* stage) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = a.group;
     const int cap = a.max_blocks * 16;
+    int* s_len = stage;
+    int* s_grp = stage + kMaxBatchPerLaunch;
+    int* s_gb = stage + 2 * kMaxBatchPerLaunch;
     if (threadIdx.x == 0) {
         info[0] = -1;
         info[2] = 0;
     }
-    for (int g = threadIdx.x; g < a.num_groups; g += blockDim.x) counts[g] = 0;
+    for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
+        const int n = a.lens[i];
+        s_len[i] = n < 0 ? 0 : (n > cap ? cap : n);
+        s_grp[i] = a.prefix_group[i];
+    }
+    for (int g = threadIdx.x; g < a.num_groups; g += blockDim.x) {
+        counts[g] = 0;
+        s_gb[g] = a.group_blocks[g];
+    }
     __syncthreads();
     auto member_blocks = [&](int i) {
-        int n = a.lens[i];
-        n = n < 0 ? 0 : (n > cap ? cap : n);
-        return prefix_member_blocks(a.prefix_group, a.group_blocks, a.num_groups, a.max_group_blocks, n, i);
+        return prefix_member_blocks(s_grp, s_gb, a.num_groups, a.max_group_blocks, s_len[i], i);
     };
     for (int i = threadIdx.x; i < a.batch; i += blockDim.x)
-        if (member_blocks(i) >= 0) atomicAdd(&counts[a.prefix_group[i]], 1);
+        if (member_blocks(i) >= 0) atomicAdd(&counts[s_grp[i]], 1);
     __syncthreads();
     if (warp == 0) {
         // tile x -> (group, tile within the group): prefix sums of the groups' tile counts
@@ -116,7 +138,7 @@ __device__ int locate_tile(const PrefixArgs& a, int* info, int* members, int* co
     __syncthreads();
     const int p = info[0];
     if (p < 0) return 0;
-    const int nb = a.group_blocks[p];  // in [0, max_group_blocks]: p has members
+    const int nb = s_gb[p];  // in [0, max_group_blocks]: p has members
     const int nch = nb > 0 ? (nb + a.chunk_blocks - 1) / a.chunk_blocks : 1;
     const int r0 = info[1] * kRowsPerTile;
     const int nrows = min(kRowsPerTile, counts[p] * G - r0);
@@ -126,7 +148,7 @@ __device__ int locate_tile(const PrefixArgs& a, int* info, int* members, int* co
         int rank = 0;
         for (int base = 0; base < a.batch; base += 32) {
             const int i = base + lane;
-            const bool is = i < a.batch && a.prefix_group[i] == p && member_blocks(i) >= 0;
+            const bool is = i < a.batch && s_grp[i] == p && member_blocks(i) >= 0;
             const unsigned int bal = __ballot_sync(0xffffffffu, is);
             const int r = rank + __popc(bal & ((1u << lane) - 1u));
             if (is) {
@@ -168,7 +190,8 @@ struct Px {
     static constexpr int kOffBars = kStages * kStageBytes;
     static constexpr int kOffFlags = kOffBars + 2 * kStages * 8;
     static constexpr int kOffInts = kOffFlags + (kStages + 1) * 4;
-    static constexpr size_t kSmem = 1024 + kOffInts + (8 + member_slots(kRows) + kMaxGroups) * 4;
+    static constexpr size_t kSmem =
+        1024 + kOffInts + (8 + member_slots(kRows) + kMaxGroups + 2 * kMaxBatchPerLaunch + kMaxGroups) * 4;
 };
 
 template <int D, int NST>
@@ -186,6 +209,7 @@ __global__ void __launch_bounds__(Px<D, NST>::kThreads)
     int* info = reinterpret_cast<int*>(smem + C::kOffInts);
     int* members = info + 8;
     int* counts = members + member_slots(kTileRows);
+    int* stage = counts + kMaxGroups;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -209,7 +233,7 @@ __global__ void __launch_bounds__(Px<D, NST>::kThreads)
     // kernel) lets it start once all its CTAs have passed their own wait on
     // the kernels before them, so the K/V blocks are complete.
     allow_dependents();
-    if (locate_tile<kTileRows>(a, info, members, counts) != 2) {
+    if (locate_tile<kTileRows>(a, info, members, counts, stage) != 2) {
         idle_exit();
         return;
     }
@@ -505,25 +529,26 @@ struct Ux {
     static constexpr int kTok = 64;                  // N of S = Q K^T: tokens per step
     static constexpr int kBlk = kTok / 16;           // blocks per step
     static constexpr int kHalves = D / 64;           // 64-column (128-byte) halves of a row
-    static constexpr int kStages = D == 128 ? 3 : 4;
+    static constexpr int kStages = D == 128 ? 4 : 6;
     static constexpr int kQBytes = kHalves * kRows * 128;
     static constexpr int kHalfBytes = kTok * 128;    // one half of the 64 token rows of a step
     static constexpr int kKBytes = kHalves * kHalfBytes;
     static constexpr int kStageBytes = 2 * kKBytes;  // K then V
-    static constexpr int kPBytes = kRows * 128;      // 128 rows x 64 tokens, bf16
     // Shared memory (offsets from a 1024-byte aligned base; every operand
     // tile starts on a 1024-byte boundary, as the 128-byte swizzle wants):
     // Q [halves][128 rows][128 B]; the K/V ring, each stage K then V as
     // [halves][64 token rows][128 B] (the TMA layout of four 16-row boxes);
-    // P as two buffers of {hi, lo} [128 rows][128 B]; the mbarriers; then
-    // info[16], the tile's members and the per-group member counts.
+    // the exchange of the two token halves' row states; the mbarriers; then
+    // info[16], the tile's members, the per-group member counts and the
+    // staged lookup inputs.
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;
-    static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-    static constexpr int kOffBars = kOffP + 4 * kPBytes;
+    static constexpr int kOffX = kOffKV + kStages * kStageBytes;
+    static constexpr int kOffBars = kOffX + 3 * kRows * 4;
     static constexpr int kNumBars = 2 * kStages + 7;  // kv_full, kv_empty, s_full[2], p_full[2], o_done[2], final
     static constexpr int kOffInts = kOffBars + kNumBars * 8;
-    static constexpr size_t kSmem = 1024 + kOffInts + (16 + member_slots(kRows) + kMaxGroups) * 4;
+    static constexpr size_t kSmem =
+        1024 + kOffInts + (16 + member_slots(kRows) + kMaxGroups + 2 * kMaxBatchPerLaunch + kMaxGroups) * 4;
     // warps 0-7 softmax: warp w takes rows 32 (w % 4) .. + 31 (its tensor-memory
     // lanes) and token half w / 4 of every step; warp 8 TMA, warp 9 MMA
     static constexpr int kSoftmaxWarps = 8;
@@ -532,8 +557,11 @@ struct Ux {
     static constexpr int kThreads = 320;
     static constexpr uint32_t kColS = 0;    // S buffers: columns [0, 64) and [64, 128)
     static constexpr uint32_t kColO = 128;  // O of token half 0: [128, 128 + D); half 1: [128 + D, 128 + 2D)
-    static constexpr uint32_t kTmemCols = kColO + 2 * D <= 256 ? 256 : 512;
-    static_assert(kColO + 2 * D <= kTmemCols, "tensor-memory columns");
+    // P buffers b = 0, 1 at kColP + 64 b: bf16 pairs, hi in the first 32
+    // columns (token t in column t / 2), lo in the next 32
+    static constexpr uint32_t kColP = kColO + 2 * D;
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kColP + 128 <= kTmemCols, "tensor-memory columns");
 };
 
 template <int D>
@@ -552,6 +580,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     int* info = reinterpret_cast<int*>(smem + C::kOffInts);
     int* members = info + 16;
     int* counts = members + member_slots(C::kRows);
+    int* stage = counts + kMaxGroups;
     volatile int* abort_flag = info + 14;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(info + 15);
 
@@ -583,7 +612,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         tma_prefetch_desc(&tmV);
     }
     allow_dependents();  // inputs only until the fold (see the mma.sync kernel)
-    const int where = locate_tile<C::kRows>(a, info, members, counts);
+    const int where = locate_tile<C::kRows>(a, info, members, counts, stage);
     if (where == 0) {  // no tile: the same for every CTA of the cluster
         idle_exit();
         return;
@@ -608,7 +637,9 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
-    // Q rows into shared memory (K-major, 128-byte swizzle); thread r < 128 loads row r.
+    // Q rows into shared memory (K-major, 128-byte swizzle); thread r < 128
+    // loads row r. The TMA warp does not wait for this: it starts streaming
+    // K and V at once.
     long long row_idx = 0;
     bool row_ok = false;
     if (warp < 4) {
@@ -626,10 +657,13 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         }
         fence_proxy_async_smem();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    uint32_t tmem = 0;
+    if (warp != C::kTmaWarp) {
+        tc_fence_before();
+        named_barrier_sync(2, C::kThreads - 32);  // every warp but the TMA warp
+        tc_fence_after();
+        tmem = *tmem_slot;
+    }
     if (threadIdx.x == 0) PX_STAMP(a, 2, global_ns());
 
     if (warp == C::kTmaWarp) {
@@ -641,6 +675,9 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         const int32_t* trow = a.tables + static_cast<long long>(info[2]) * a.max_blocks + blk0;
         bool ok = true;
         int issued = 0;
+#ifdef PKV_TRACE
+        unsigned long long tr_tma = 0;
+#endif
         for (int j = 0; j < nsteps; ++j) {
             const int s = j % C::kStages;
             int y = -16;
@@ -653,10 +690,13 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             }
             int good = 1;
             if (lane == 0) {
+                PX_T(t0);
                 if (mbar_wait(&kv_empty[s], static_cast<uint32_t>((j / C::kStages) & 1) ^ 1u, a.status, abort_flag))
                     mbar_arrive_expect_tx(&kv_full[s], C::kStageBytes);
                 else
                     good = 0;
+                PX_T(t1);
+                PX_ADD(tr_tma, t1 - t0);
             }
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) {
@@ -678,6 +718,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             for (int u = first; u < issued; ++u)
                 mbar_wait(&kv_full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
         }
+        if (lane == 0) PX_STAMP(a, 15, tr_tma);
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------ MMA issuer (one thread)
         if (lane == 0) {
@@ -685,12 +726,18 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             constexpr uint32_t idO = umma_idesc_bf16(C::kRows, D, false, true);
             const uint32_t q_base = smem_u32(smem + C::kOffQ);
             bool ok = true;
+#ifdef PKV_TRACE
+            unsigned long long tr_p = 0, tr_kv = 0;
+#endif
             // S_j = Q K_j^T into S buffer j % 2. Both operands K-major; a
             // K-step of 16 elements is 32 bytes into the swizzled row.
             auto issue_s = [&](int j) {
                 const int s = j % C::kStages;
+                PX_T(t0);
                 if (!mbar_wait(&kv_full[s], static_cast<uint32_t>((j / C::kStages) & 1), a.status, abort_flag))
                     return false;
+                PX_T(t1);
+                PX_ADD(tr_kv, t1 - t0);
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(smem + C::kOffKV + s * C::kStageBytes);
 #pragma unroll
@@ -704,10 +751,13 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             };
             for (int j = 0; ok && j < nsteps && j < 2; ++j) ok = issue_s(j);
             for (int j = 0; ok && j < nsteps; ++j) {
+                PX_T(t0);
                 if (!mbar_wait(&p_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.status, abort_flag)) {
                     ok = false;
                     break;
                 }
+                PX_T(t1);
+                PX_ADD(tr_p, t1 - t0);
                 tc_fence_after();
                 // O_t += P_hi V + P_lo V over token half t (tokens 32t .. 32t+31)
                 // into that half's accumulator. P is K-major (tokens along the
@@ -716,17 +766,16 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 // token rows per 1024-byte atom.
                 const int s = j % C::kStages;
                 const uint32_t v_base = smem_u32(smem + C::kOffKV + s * C::kStageBytes + C::kKBytes);
-                const uint32_t p_base = smem_u32(smem + C::kOffP + (j & 1) * 2 * C::kPBytes);
+                const uint32_t p_col = tmem + C::kColP + (j & 1) * 64;
 #pragma unroll
                 for (int th = 0; th < 2; ++th) {
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
                         for (int kt = 2 * th; kt < 2 * th + 2; ++kt) {
-                            const uint64_t ad = umma_desc_sw128(p_base + part * C::kPBytes + kt * 32, 16, 1024);
                             const uint64_t bd = umma_desc_sw128(v_base + kt * 2048, C::kHalfBytes, 1024);
-                            umma_bf16(tmem + C::kColO + th * D, ad, bd, idO,
-                                      (j > 0 || part > 0 || kt > 2 * th) ? 1u : 0u);
+                            umma_bf16_ts(tmem + C::kColO + th * D, p_col + part * 32 + kt * 8, bd, idO,
+                                         (j > 0 || part > 0 || kt > 2 * th) ? 1u : 0u);
                         }
                     }
                 }
@@ -737,6 +786,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             // nothing may still run on the tensor cores when the memory is freed
             umma_commit(final_bar);
             mbar_wait(final_bar, 0, a.status, nullptr);
+            PX_STAMP(a, 13, tr_p);
+            PX_STAMP(a, 14, tr_kv);
         }
         __syncwarp();
     }
@@ -752,27 +803,43 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     const int th = (warp >> 2) & 1;  // token half of this softmax warp
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t col_o = C::kColO + th * D;
-    float* xfer = reinterpret_cast<float*>(smem + C::kOffP);  // [3][128]: half 1's max, sum, status
+    float* xfer = reinterpret_cast<float*>(smem + C::kOffX);  // [3][128]: half 1's max, sum, status
     if (warp < C::kSoftmaxWarps) {
         const int r = q4 * 32 + lane;
         const float scale_log2 = a.scale * kLog2e;
+#ifdef PKV_TRACE
+        unsigned long long tr_s = 0, tr_ld = 0, tr_math = 0, tr_o = 0, tr_w = 0;
+#endif
         for (int j = 0; j < nsteps; ++j) {
+            PX_T(t0);
             if (!mbar_wait(&s_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.status, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            PX_T(t1);
             uint32_t sv[32];
             tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok + th * 32, sv);
             tmem_ld_wait();
+            PX_T(t2);
             const int valid = min(C::kTok, (nblk - C::kBlk * j) * 16) - th * 32;
             float x[32];
-            float mx = ninf();
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                x[t] = t < valid ? __uint_as_float(sv[t]) * scale_log2 : ninf();
-                mx = fmaxf(mx, x[t]);
+            for (int t = 0; t < 32; ++t) x[t] = __uint_as_float(sv[t]) * scale_log2;
+            if (valid < 32) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    if (t >= valid) x[t] = ninf();
             }
+            // row maximum of the half, as a tree
+            float mt[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) mt[t] = fmaxf(x[t], x[t + 16]);
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                for (int t = 0; t < w; ++t) mt[t] = fmaxf(mt[t], mt[t + w]);
+            const float mx = mt[0];
             // lazy rescale: the running max moves only when a score exceeds it by more than 8
             const bool resc = mx > m + 8.f;
             float alpha = 1.f;
@@ -781,18 +848,25 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 alpha = m == ninf() ? 0.f : ex2(m - mn);
                 m = mn;
             }
+            // P = 2^(x - m) as bf16 hi + lo, both truncated: hi is the top half of
+            // p, lo the top half of p - hi (together ~16 significant bits)
             uint32_t hi[16], lo[16];
-            float psum = 0.f;
+            float ps[16];
             const float base = m == ninf() ? 0.f : m;  // a half with no valid token yet
 #pragma unroll
             for (int t = 0; t < 32; t += 2) {
                 const float p0 = ex2(x[t] - base), p1 = ex2(x[t + 1] - base);
-                psum += p0 + p1;
-                const uint32_t hv = pack_bf16x2(p0, p1);
-                hi[t / 2] = hv;
-                lo[t / 2] = pack_bf16x2(p0 - bf16lo_to_f32(hv), p1 - bf16hi_to_f32(hv));
+                ps[t / 2] = p0 + p1;
+                hi[t / 2] = pack_bf16x2_trunc(p0, p1);
+                lo[t / 2] = pack_bf16x2_trunc(p0 - bf16_trunc(p0), p1 - bf16_trunc(p1));
             }
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                for (int t = 0; t < w; ++t) ps[t] += ps[t + w];
+            const float psum = ps[0];
             l = l * alpha + psum;
+            PX_T(t3);
             // P buffer j % 2 was read by the PV product of step j - 2
             if (j >= 2 && !mbar_wait(&o_done[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), a.status, abort_flag)) {
                 ok = false;
@@ -817,20 +891,29 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 }
                 tmem_st_wait();
             }
-            uint8_t* prow = smem + C::kOffP + (j & 1) * 2 * C::kPBytes + r * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int off = (((4 * th + c) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-                *reinterpret_cast<uint4*>(prow + C::kPBytes + off) =
-                    make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
-            }
-            fence_proxy_async_smem();
+            PX_T(t4);
+            const uint32_t p_col = tmem + lane_base + C::kColP + (j & 1) * 64 + th * 16;
+            tmem_st16(p_col, hi);
+            tmem_st16(p_col + 32, lo);
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[j & 1]);
+            PX_T(t5);
+            PX_ADD(tr_s, t1 - t0);
+            PX_ADD(tr_ld, t2 - t1);
+            PX_ADD(tr_math, t3 - t2);
+            PX_ADD(tr_o, t4 - t3);
+            PX_ADD(tr_w, t5 - t4);
         }
-        if (threadIdx.x == 0) PX_STAMP(a, 3, global_ns());
+        if (threadIdx.x == 0) {
+            PX_STAMP(a, 3, global_ns());
+            PX_STAMP(a, 8, tr_s);
+            PX_STAMP(a, 9, tr_ld);
+            PX_STAMP(a, 10, tr_math);
+            PX_STAMP(a, 11, tr_o);
+            PX_STAMP(a, 12, tr_w);
+        }
         // the last PV product must be in before O is read or the P buffers reused
         if (ok && nsteps > 0 &&
             !mbar_wait(&o_done[(nsteps - 1) & 1], static_cast<uint32_t>(((nsteps - 1) >> 1) & 1), a.status,
@@ -1137,7 +1220,7 @@ PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int
     off = align256(off + static_cast<size_t>(b) * q_heads * sizeof(float));
 #ifdef PKV_TRACE
     p.trace_offset = off;
-    off = align256(off + static_cast<size_t>(p.tiles) * p.chunks * kv_heads * 64);
+    off = align256(off + static_cast<size_t>(p.tiles) * p.chunks * kv_heads * 128);
 #else
     p.trace_offset = 0;
 #endif
