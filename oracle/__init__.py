@@ -25,9 +25,12 @@ What it restates, in float64 (or exact integer / byte arithmetic):
   of sequences, then sequence-first over each suffix) decode and its
   log-sum-exp combination (paper-search page, ChunkAttention abstract;
   notebook sections 5 and 7).
+* ``multiquery``  -- several causal queries per sequence against its paged
+  context: speculative verification tokens or a prefill chunk (release page
+  Architectural Breakdown 2; notebook section 7).
 
 Pins that tie these functions to the pages (not to themselves) live in
 ``tests/test_oracle_*.py`` and ``tests/golden/``.
 """
 
-from . import geometry, paged_pool, kv_ops, attention, prefix  # noqa: F401
+from . import geometry, paged_pool, kv_ops, attention, prefix, multiquery  # noqa: F401
