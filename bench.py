@@ -55,6 +55,7 @@ WORKLOAD_NAMES = {
     "long128k": "70B-GQA decode layer, every context 131072 tokens",
     "mixed": "continuous-batching mix, contexts log-uniform on [16, 32768]",
     "prefix": "4096-token prefix shared by all sequences + private suffixes uniform in [1, 2048]",
+    "spec4": "Llama-3-8B decode layer verifying 4 draft tokens per sequence (causal multi-query), context 8192",
 }
 L2_NOTE = {
     "llama8k": "inputs larger than L2 (1 GiB K+V per step)",
@@ -62,6 +63,7 @@ L2_NOTE = {
     "mixed": "inputs larger than L2 (4.65 GB K+V per step)",
     "prefix": "unique K+V (0.33 GB) larger than L2; the 16 MiB shared prefix is re-read from L2 by every "
               "sequence, so logical GB/s can exceed HBM bandwidth",
+    "spec4": "inputs larger than L2 (1 GiB K+V per step, read once for the 4 queries of each sequence)",
 }
 
 
@@ -173,21 +175,31 @@ def profiled_traffic(summary, files=("pkv_decode.cu",)):
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
-def oracle_sample_rate(q, kp, vp, tables, lens, scale, kv_heads, pairs, time_budget_s=None):
-    """Run the float64 oracle on (seq, kv_head) pairs; returns (bytes, seconds, pairs done)."""
+def oracle_sample_rate(q, kp, vp, tables, lens, scale, kv_heads, pairs, time_budget_s=None, nq=1):
+    """Run the float64 oracle on (seq, kv_head) pairs; returns (bytes, seconds, pairs done).
+    With nq > 1 queries per sequence (rows i*nq .. i*nq+nq-1 of q), the
+    multi-query oracle runs on whole sequences (all KV heads) instead."""
     from oracle import attention as OA
+    from oracle import multiquery as OM
     done, nbytes = 0, 0
     t0 = time.perf_counter()
     for (i, j) in pairs:
-        OA.decode_attention_pair(q, kp, vp, tables, lens, scale, i, j, kv_heads, "bf16")
-        nbytes += int(lens[i]) * 2 * kp.shape[-1] * 2
+        if nq > 1:
+            if j:
+                continue
+            OM.multiquery_attention(q[i * nq:(i + 1) * nq], kp, vp, tables[i:i + 1], lens[i:i + 1],
+                                    np.array([0, nq]), scale, kv_heads, "bf16")
+            nbytes += int(lens[i]) * 2 * kv_heads * kp.shape[-1] * 2
+        else:
+            OA.decode_attention_pair(q, kp, vp, tables, lens, scale, i, j, kv_heads, "bf16")
+            nbytes += int(lens[i]) * 2 * kp.shape[-1] * 2
         done += 1
         if time_budget_s is not None and time.perf_counter() - t0 > time_budget_s:
             break
     return nbytes, time.perf_counter() - t0, done
 
 
-def cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, seqs):
+def cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, seqs, nq=1):
     import torch
     ids = np.unique(tables_np[seqs].reshape(-1))
     ids = ids[ids >= 0]
@@ -196,7 +208,8 @@ def cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, seqs):
     idx = torch.from_numpy(ids).to(k_pool.device)
     kp = k_pool.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
     vp = v_pool.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
-    qh = q[seqs].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    rows = np.concatenate([np.arange(s * nq, (s + 1) * nq) for s in seqs])
+    qh = q[torch.from_numpy(rows).to(q.device)].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     t = tables_np[seqs]
     t = np.where(t >= 0, remap[np.maximum(t, 0)], -1)
     return qh, kp, vp, t, lens_np[seqs]
@@ -266,11 +279,15 @@ def run_pkv(args, cfg):
     tables, lens, slots, pairs = w["tables"], w["lens"], w["slots"], w["pairs"]
     tables_np, lens_np = w["tables_np"], w["lens_np"]
     MAXB = tables.shape[1]
-    out = torch.empty((B, HQ, D), dtype=q.dtype, device=device)
+    out = torch.empty_like(q)
     two_phase = args.workload == "prefix" and not args.single_pass
+    nq = w["queries"]
+    qstart = w["query_start"]
     group, gblocks, mgb = w["prefix_group"], w["group_blocks"], w["max_group_blocks"]
     if two_phase:
         ws_bytes = pkv.pkv_decode_prefixed_workspace_size(B, HQ, MAXB, len(gblocks), mgb, k_pool)
+    elif nq > 1:
+        ws_bytes = pkv.pkv_multiquery_workspace_size(B, HQ, MAXB, nq, k_pool)
     else:
         ws_bytes = pkv.pkv_decode_workspace_size(B, HQ, MAXB, k_pool)
     workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
@@ -278,7 +295,10 @@ def run_pkv(args, cfg):
     stream = torch.cuda.current_stream()
 
     def decode():
-        if two_phase:
+        if nq > 1:
+            pkv.pkv_multiquery_attention(q, k_pool, v_pool, tables, lens, qstart, scale, nq, out=out,
+                                         workspace=workspace, stream=stream)
+        elif two_phase:
             pkv.pkv_decode_attention_prefixed(q, k_pool, v_pool, tables, lens, scale, group, gblocks, mgb, out=out,
                                               workspace=workspace, stream=stream)
         else:
@@ -329,7 +349,7 @@ def run_pkv(args, cfg):
     status_bits = pkv.pkv_device_status(clear=False)
 
     # -------- end-to-end: per-step inputs from pinned host memory, result back to the host
-    devs = [q, kn, vn, slots, tables, lens] + ([group, gblocks] if two_phase else [])
+    devs = [q, kn, vn, slots, tables, lens] + ([group, gblocks] if two_phase else []) + ([qstart] if nq > 1 else [])
     pins = [t.cpu().pin_memory() for t in devs]
     out_pin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pins)
@@ -381,9 +401,9 @@ def run_pkv(args, cfg):
     # -------- CPU oracle baseline on a bounded sample of the same workload
     order = np.argsort(-lens_np)
     sample_seqs = sorted({int(order[0]), int(order[len(order) // 2])})
-    qh, kph, vph, th, lh = cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, sample_seqs)
+    qh, kph, vph, th, lh = cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, sample_seqs, nq)
     pairs_list = [(i, j) for i in range(len(sample_seqs)) for j in range(HKV)]
-    cb, cs, cdone = oracle_sample_rate(qh, kph, vph, th, lh, scale, HKV, pairs_list, time_budget_s=20.0)
+    cb, cs, cdone = oracle_sample_rate(qh, kph, vph, th, lh, scale, HKV, pairs_list, time_budget_s=20.0, nq=nq)
     cpu_gbs = cb / cs / 1e9
 
     line = {
@@ -392,8 +412,10 @@ def run_pkv(args, cfg):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(args.workload, cfg, lens_np),
                    "l2": L2_NOTE[args.workload],
-                   "step": f"copy_blocks ({int(pairs.shape[0])} pairs) + append ({B} tokens) + "
-                           + ("shared-prefix decode attention (two phases)" if two_phase else "decode attention"),
+                   "step": f"copy_blocks ({int(pairs.shape[0])} pairs) + append ({B * nq} tokens) + "
+                           + ("shared-prefix decode attention (two phases)" if two_phase
+                              else f"causal multi-query attention ({nq} queries per sequence)" if nq > 1
+                              else "decode attention"),
                    "kernel": "tensor-core split-context kernel, merge fused"
                              + (", then the chunk-first pass over the shared blocks" if two_phase else "")},
         "hbm_frac": round(value / peak, 4),
@@ -402,12 +424,15 @@ def run_pkv(args, cfg):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": ("decode_tc_kernel<128> + prefix_umma_kernel<128> (one shared-prefix call)"
-                                if two_phase else "decode_tc_kernel<128> (one launch per pkv_decode_attention call)"),
+                                if two_phase else
+                                "mq_tc_kernel<128> (one launch per pkv_multiquery_attention call)" if nq > 1 else
+                                "decode_tc_kernel<128> (one launch per pkv_decode_attention call)"),
                      "avg_launch_ms": round(dec_avg_ms, 5), "launches_timed": len(dec_ms),
                      "algorithmic_bytes": alg_bytes},
         "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{cdone} (sequence, KV head) pairs of sequences {sample_seqs}, "
-                                   f"float64 NumPy oracle, one thread"},
+                         "sample": (f"{cdone} (sequence, KV head) pairs of sequences {sample_seqs}, "
+                                    if nq == 1 else f"{cdone} whole sequences of {sample_seqs} ({nq} queries each), ")
+                                   + "float64 NumPy oracle, one thread"},
         "e2e": {"value": round(total_kv / (e2e_s / args.steps) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

@@ -272,6 +272,53 @@ PKV_API pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_ca
                                                  const pkv_decode_opts* opts, void* stream);
 
 /*
+ * pkv_multiquery_workspace_size -- bytes of device workspace
+ * pkv_multiquery_attention needs (zero-fill once before first use; completed
+ * calls leave its counters at zero). Returns 0 for sizes the call rejects.
+ */
+PKV_API size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                             int32_t max_query_len, const pkv_cache_desc* desc,
+                                             const pkv_decode_opts* opts);
+
+/*
+ * pkv_multiquery_attention -- several causal queries per sequence against its
+ * paged context, in one pass over the cache.
+ * (release page, Architectural Breakdown 2: the target model verifies the K
+ * draft tokens in a single parallel pass; notebook section 7: a cached-prefix
+ * suffix attends to every cached position and causally within itself, and the
+ * chunks of a prefill together hold exactly the causal pairs of the prompt.)
+ *
+ * Sequence i holds n = context_lens[i] tokens, the last nq = query_start[i+1]
+ * - query_start[i] of which are this step's new tokens (appended before the
+ * call). Query t < nq, at row query_start[i] + t of q and out, attends to
+ * tokens 0 .. n - nq + t:
+ *     out[r][h] = sum_p softmax_p(scale * dot(q[r][h], K_j(p))) V_j(p),  p <= n - nq + t
+ * with K_j / V_j gathered through block_tables[i] as in pkv_decode_attention.
+ * One query per sequence is pkv_decode_attention. fp32 accumulation, one
+ * rounding to bf16.
+ *
+ *   q, out        device, bf16 [query_start[batch]][num_q_heads][head_dim].
+ *   query_start   device, int32 [batch + 1], non-decreasing row offsets.
+ *   max_query_len host bound on nq, 1 <= max_query_len and
+ *                 max_query_len * (num_q_heads / num_kv_heads) <= 32
+ *                 (else PKV_ERR_UNSUPPORTED).
+ *   workspace     >= pkv_multiquery_workspace_size(...) bytes, 256-byte
+ *                 aligned, zero-filled before its first use.
+ * Errors: as pkv_decode_attention; bf16 caches only (else PKV_ERR_DTYPE). A
+ * sequence whose query count lies outside [0, min(n, max_query_len)] gets no
+ * output rows and sets PKV_DEVERR_RANGE; with PKV_FLAG_CHECKED the call
+ * returns PKV_ERR_RANGE instead, having written nothing. The tensor-core path
+ * reads every K/V byte once for all the queries of its sequence.
+ */
+PKV_API pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const void* v_cache,
+                                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                            const int32_t* context_lens, const int32_t* query_start,
+                                            int32_t batch, int32_t num_q_heads, int32_t max_query_len,
+                                            float scale, void* out, void* workspace, size_t workspace_bytes,
+                                            const pkv_cache_desc* desc, uint32_t flags,
+                                            const pkv_decode_opts* opts, void* stream);
+
+/*
  * pkv_decode_attention_noalloc -- pkv_decode_attention without a
  * caller-provided workspace. The pages have no counterpart to this call; it
  * exists for callers that cannot allocate device memory: plugins running

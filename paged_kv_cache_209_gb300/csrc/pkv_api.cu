@@ -376,6 +376,89 @@ pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, con
     return PKV_OK;
 }
 
+size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                     int32_t max_query_len, const pkv_cache_desc* desc,
+                                     const pkv_decode_opts* opts) {
+    (void)max_blocks_per_seq;
+    if (check_desc(desc) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return 0;
+    const int G = num_q_heads / desc->num_kv_heads;
+    if (desc->dtype != PKV_BF16 || max_query_len < 1 || max_query_len * G > kMqMaxRows) return 0;
+    size_t co = 0, po = 0;
+    return mq_workspace_bytes(batch, desc->num_kv_heads, desc->head_dim, mq_num_ctas(desc->head_dim, batch, opts),
+                              &co, &po);
+}
+
+pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, const int32_t* query_start, int32_t batch,
+                                    int32_t num_q_heads, int32_t max_query_len, float scale, void* out,
+                                    void* workspace, size_t workspace_bytes, const pkv_cache_desc* desc,
+                                    uint32_t flags, const pkv_decode_opts* opts, void* stream) {
+    pkv_status st = check_desc(desc);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
+    if (!isfinite(scale) || max_query_len < 1) return PKV_ERR_SHAPE;
+    if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
+    const int G = num_q_heads / desc->num_kv_heads;
+    if (desc->dtype != PKV_BF16) return PKV_ERR_DTYPE;
+    if (max_query_len * G > kMqMaxRows) return PKV_ERR_UNSUPPORTED;
+    if (flags & PKV_FLAG_TEST_STALL) return PKV_ERR_UNSUPPORTED;
+    if (batch == 0) return PKV_OK;
+    if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
+        return PKV_ERR_SHAPE;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out || !workspace)
+        return PKV_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(query_start) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_ALIGN;
+    const int num_ctas = mq_num_ctas(desc->head_dim, batch, opts);
+    size_t co = 0, po = 0;
+    const size_t need = mq_workspace_bytes(batch, desc->num_kv_heads, desc->head_dim, num_ctas, &co, &po);
+    if (workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    if (flags & PKV_FLAG_CHECKED) {
+        st = run_checked([&](unsigned int* verdict) {
+            cudaError_t e = launch_check_decode(block_tables, max_blocks_per_seq, context_lens, batch,
+                                                desc->num_blocks, verdict, s);
+            if (e != cudaSuccess) return e;
+            return launch_check_queries(context_lens, query_start, batch, max_query_len, verdict, s);
+        }, s);
+        if (st != PKV_OK) return st;
+    }
+    char* ws = static_cast<char*>(workspace);
+    for (int32_t b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {
+        const int32_t nb = batch - b0 < kMaxBatchPerLaunch ? batch - b0 : kMaxBatchPerLaunch;
+        MqArgs a{};
+        a.q = q;
+        a.k_cache = k_cache;
+        a.v_cache = v_cache;
+        a.tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
+        a.lens = context_lens + b0;
+        a.qstart = query_start + b0;
+        a.out = out;
+        a.partials = reinterpret_cast<float*>(ws + po);
+        a.counters = reinterpret_cast<int*>(ws + co);
+        a.status = status;
+        a.num_blocks = desc->num_blocks;
+        a.max_blocks = max_blocks_per_seq;
+        a.batch = nb;
+        a.q_heads = num_q_heads;
+        a.kv_heads = desc->num_kv_heads;
+        a.head_dim = desc->head_dim;
+        a.group = G;
+        a.num_ctas = num_ctas;
+        a.max_query_len = max_query_len;
+        const int row_groups = (max_query_len * G + 7) / 8;
+        a.wpu = row_groups <= 1 ? 1 : (row_groups <= 2 ? 2 : 4);
+        a.scale = scale;
+        if (launch_multiquery(a, s) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
 pkv_status pkv_device_status(uint32_t* bits_out, int clear, void* stream) {
     unsigned int* status = device_info().status;
     if (status == nullptr) return PKV_ERR_CUDA;

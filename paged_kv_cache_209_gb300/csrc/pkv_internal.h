@@ -142,4 +142,37 @@ cudaError_t launch_check_groups(const int32_t* tables, int32_t max_blocks, const
 
 int device_sm_count();
 
+// ---------------------------------------------------------------- multi-query decode
+// Several causal queries per sequence; see pkv_multiquery.cu.
+struct MqArgs {
+    const void* q;          // [query_start[batch]][q_heads][head_dim] bf16
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* tables;
+    const int32_t* lens;
+    const int32_t* qstart;  // [batch + 1]: first query row of each sequence (absolute rows of q / out)
+    void* out;
+    float* partials;        // [num_ctas][2 slots][4 row groups][8 rows][head_dim + 2]
+    int* counters;          // [batch][kv_heads][4 row groups]; zero between calls
+    unsigned int* status;
+    int64_t num_blocks;
+    int32_t max_blocks;
+    int32_t batch;
+    int32_t q_heads;
+    int32_t kv_heads;
+    int32_t head_dim;
+    int32_t group;
+    int32_t num_ctas;
+    int32_t max_query_len;  // queries per sequence, at most (32 / group)
+    int32_t wpu;            // warps per unit: 1, 2 or 4 row groups of 8 (from max_query_len * group)
+    float scale;
+};
+constexpr int kMqMaxRows = 32;  // query rows per (sequence, KV head)
+int mq_num_ctas(int head_dim, int batch, const pkv_decode_opts* opts);
+size_t mq_workspace_bytes(int batch, int kv_heads, int head_dim, int num_ctas, size_t* counters_offset,
+                          size_t* partials_offset);
+cudaError_t launch_multiquery(const MqArgs& a, cudaStream_t s);
+cudaError_t launch_check_queries(const int32_t* lens, const int32_t* qstart, int32_t batch, int32_t max_query_len,
+                                 unsigned int* verdict, cudaStream_t s);
+
 }  // namespace pkv

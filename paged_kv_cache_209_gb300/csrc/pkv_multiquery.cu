@@ -1,0 +1,588 @@
+// Multi-query paged attention: several causal queries per sequence (the K
+// draft tokens a speculative step verifies in one pass, or a short prefill
+// chunk) against the sequence's paged context.
+//
+// Sequence i holds n = context_lens[i] tokens, the last nq of which are this
+// step's new tokens; its queries are rows query_start[i] .. query_start[i+1]-1
+// of q, and query t attends to tokens 0 .. n - nq + t (release page
+// "NeuralOps v1.3.4", Architectural Breakdown 2, single-pass verification of
+// the K candidates; notebook section 7: a suffix attends to every cached
+// position, causally within itself).
+//
+// Work decomposition: the stream-K split of the decode kernel over (sequence,
+// KV head, block) units, so K/V is read once per call for all query rows.
+// The query rows of one (sequence, KV head) are (query t, query head g),
+// row r = t G + g, at most 32, split into row groups of 8. With W = 1, 2 or 4
+// row groups (from max_query_len * G), the four consumer warps form 4 / W
+// unit lanes of W warps: warp w serves row group w % W and takes the blocks
+// k of its CTA's range with k % (4 / W) == w / W, so up to four blocks are in
+// flight per CTA whatever the row count:
+//     S^T[16 tokens][8 rows] = K[16][D] * Q^T[D][8]        (mma m16n8k16)
+//     causal mask per row, base-2 online softmax (lazy rescale)
+//     O^T[D][8] += V^T[D][16] * P^T[16][8]                  (P as bf16 hi + lo)
+// At the end of a segment piece the unit lanes' states of a row group are
+// combined through shared memory by the row group's first warp. A segment cut
+// by a CTA range boundary leaves one fp32 piece per CTA and row group; the
+// warp that completes a (segment, row group) counter merges them by
+// log-sum-exp.
+#include <math.h>
+#include <mutex>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+#include "pkv_schedule.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMqRows = 32;  // query rows per (sequence, KV head): 4 warps x 8
+
+__device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+
+template <int D, int NST>
+struct Mq {
+    static constexpr int kStages = NST;
+    static constexpr int kConsumers = 4;
+    static constexpr int kThreads = (kConsumers + 1) * 32;
+    static constexpr int kHalves = D / 64;
+    static constexpr int kPoolBytes = 16 * D * 2;
+    static constexpr int kStageBytes = 2 * kPoolBytes;  // K then V
+    // shared memory (offsets from a 1024-byte aligned base): the ring,
+    // full[NST], empty[NST] and the piece barrier, stage flags and the abort
+    // flag, the combine scratch (two buffers of 4 warps x 8 rows x (D + 2)
+    // floats, alternating between pieces), then per sequence: block prefix
+    // sums and context lengths.
+    static constexpr int kOffBars = kStages * kStageBytes;
+    static constexpr int kOffFlags = kOffBars + (2 * kStages + 1) * 8;
+    static constexpr int kOffScratch = ((kOffFlags + kStages * 4 + 4 + 15) / 16) * 16;
+    static constexpr int kScratchFloats = 2 * kConsumers * 8 * (D + 2);
+    static constexpr int kOffSeq = kOffScratch + kScratchFloats * 4;
+    static size_t smem_bytes(int batch) { return 1024 + kOffSeq + 2 * static_cast<size_t>(batch) * 4; }
+};
+
+// Workspace slice of one piece: CTA `cta`, slot (0: the piece that opens the
+// range, 1: the one that closes it), warp: 8 rows x D accumulators, 8 maxima,
+// 8 sums.
+__device__ __forceinline__ float* mq_slice(float* partials, long long cta, int slot, int warp, int D) {
+    return partials + ((cta * 2 + slot) * 4 + warp) * static_cast<long long>(8 * (D + 2));
+}
+
+// Merge every piece of warp `warp`'s rows of a cut segment and write the
+// output rows. Lane = 4 * row + quarter: row lane / 4 of the warp's 8, head-dim
+// quarter lane % 4.
+template <int D>
+__device__ void mq_merge(const Piece& pc, const MqArgs& a, long long U, int warp, int lane, long long c0, int slot0,
+                         int npieces, int rows, int q0) {
+    const long long C = a.num_ctas;
+    const int r8 = lane >> 2;
+    const int rr = warp * 8 + r8;
+    const int d0 = (lane & 3) * (D / 4);
+    float M = ninf(), L = 0.f;
+    float O[D / 4];
+#pragma unroll
+    for (int k = 0; k < D / 4; ++k) O[k] = 0.f;
+    for (int p = 0; p < npieces; ++p) {
+        const float* sl = mq_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, D);
+        const float mp = __ldcg(sl + 8 * D + r8);
+        const float lp = __ldcg(sl + 8 * D + 8 + r8);
+        const float Mn = fmaxf(M, mp);
+        const float base = Mn == ninf() ? 0.f : Mn;
+        const float sc = M == ninf() ? 0.f : ex2(M - base);
+        const float w = mp == ninf() ? 0.f : ex2(mp - base);
+        L = L * sc + w * lp;
+        M = Mn;
+#pragma unroll
+        for (int k = 0; k < D / 4; k += 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(sl + r8 * D + d0 + k));
+            O[k] = O[k] * sc + w * v.x;
+            O[k + 1] = O[k + 1] * sc + w * v.y;
+            O[k + 2] = O[k + 2] * sc + w * v.z;
+            O[k + 3] = O[k + 3] * sc + w * v.w;
+        }
+    }
+    if (rr >= rows) return;
+    const int G = a.group;
+    const int t = rr / G;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                          (static_cast<long long>(q0 + t) * a.q_heads + pc.head * G + (rr - t * G)) * D;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int k = 0; k < D / 4; k += 2)
+        *reinterpret_cast<uint32_t*>(orow + d0 + k) = pack_bf16x2(O[k] * inv, O[k + 1] * inv);
+}
+
+template <int D, int NST>
+__global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
+    mq_tc_kernel(const MqArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+    using C = Mq<D, NST>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* piece_bar = empty + C::kStages;  // every consumer warp published its piece state
+    int* stage_ok = reinterpret_cast<int*>(smem + C::kOffFlags);
+    volatile int* abort_flag = stage_ok + C::kStages;
+    float* scratch = reinterpret_cast<float*>(smem + C::kOffScratch);
+    int32_t* s_pre = reinterpret_cast<int32_t*>(smem + C::kOffSeq);
+    int32_t* s_len = s_pre + a.batch;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], a.wpu);  // the warps of one unit lane consume a stage
+        }
+        mbar_init(piece_bar, C::kConsumers);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    grid_dependency_wait();
+    allow_dependents();
+    // per sequence: context (clamped to the table), query count (clamped to
+    // [0, min(n, max_query_len)]), first query row, and block prefix sums
+    const int cap = a.max_blocks * 16;
+    for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
+        int n = a.lens[i];
+        const int q0 = a.qstart[i];
+        int nq = a.qstart[i + 1] - q0;
+        bool bad = n < 0 || n > cap;
+        n = n < 0 ? 0 : (n > cap ? cap : n);
+        if (q0 < 0 || nq < 0 || nq > n || nq > a.max_query_len) {
+            bad = true;
+            nq = 0;
+        }
+        if (bad && blockIdx.x == 0) atomicOr(a.status, PKV_DEVERR_RANGE);
+        s_len[i] = n;
+        s_pre[i] = nq > 0 ? (n + 15) >> 4 : 0;  // a sequence without queries streams nothing
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        int carry = 0;
+        for (int base = 0; base < a.batch; base += 32) {
+            int x = base + lane < a.batch ? s_pre[base + lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (base + lane < a.batch) s_pre[base + lane] = x + carry;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+    }
+    __syncthreads();
+
+    const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
+    const long long cta = blockIdx.x;
+    const long long ua = range_start(cta, U, a.num_ctas);
+    const long long ub = range_start(cta + 1, U, a.num_ctas);
+
+    if (warp == C::kConsumers) {
+        // ------------------------------------------------ producer warp (as in the decode kernel)
+        const uint64_t kv_policy = l2_evict_first_policy();
+        Walker wk;
+        wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
+        long long k = 0;
+        Piece pc;
+        bool ok = true;
+        while (ok && wk.next(pc)) {
+            const int32_t* trow = a.tables + static_cast<long long>(pc.seq) * a.max_blocks + pc.blk_from;
+            const int cnt_piece = pc.blk_to - pc.blk_from;
+            int cur = lane < cnt_piece ? __ldg(trow + lane) : 0;
+            for (int b0 = 0; ok && b0 < cnt_piece; b0 += 32) {
+                const int nidx = b0 + 32 + lane;
+                const int nxt = nidx < cnt_piece ? __ldg(trow + nidx) : 0;
+                const int cnt = min(32, cnt_piece - b0);
+                for (int e = 0; e < cnt; ++e, ++k) {
+                    const int bid = __shfl_sync(0xffffffffu, cur, e);
+                    int good = 1;
+                    if (lane == 0) {
+                        const int s = static_cast<int>(k % C::kStages);
+                        const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1) ^ 1u;
+                        if (!mbar_wait(&empty[s], par, a.status, abort_flag)) {
+                            good = 0;
+                        } else if (bid >= 0 && bid < a.num_blocks) {
+                            stage_ok[s] = 1;
+                            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                            uint8_t* st = smem + s * C::kStageBytes;
+                            const int y = (bid * a.kv_heads + pc.head) * 16;
+#pragma unroll
+                            for (int hf = 0; hf < C::kHalves; ++hf)
+                                tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
+#pragma unroll
+                            for (int hf = 0; hf < C::kHalves; ++hf)
+                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
+                        } else {
+                            stage_ok[s] = 0;
+                            atomicOr(a.status, PKV_DEVERR_RANGE);
+                            mbar_arrive(&full[s]);
+                        }
+                    }
+                    good = __shfl_sync(0xffffffffu, good, 0);
+                    if (!good) {
+                        ok = false;
+                        break;
+                    }
+                }
+                cur = nxt;
+            }
+        }
+        if (!ok && lane == 0) {  // after an abort: wait (bounded) for the copies still in flight
+            const long long first = k > C::kStages ? k - C::kStages : 0;
+            for (long long u = first; u < k; ++u)
+                mbar_wait(&full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    const int W = a.wpu;      // warps per unit (row groups)
+    const int UG = 4 / W;     // unit lanes
+    const int rg = warp % W;  // this warp's row group: rows 8 rg .. 8 rg + 7
+    const int ul = warp / W;  // this warp's unit lane
+    const int gid = lane >> 2;  // fragment row group
+    const int tig = lane & 3;   // thread in group
+    const float scale_log2 = a.scale * kLog2e;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+    const int q8 = lane >> 3, r8 = lane & 7;
+    const int k_row = r8 + 8 * (q8 & 1);
+    const int k_chunk = q8 >> 1;
+    const int v_row = r8 + 8 * (q8 >> 1);
+    const int v_chunk = q8 & 1;
+
+    Walker wk;
+    wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
+    long long k = 0;
+    int piece_idx = 0;
+    Piece pc;
+    Piece pending[2];
+    int npending = 0;
+    while (wk.next(pc)) {
+        const int n_ctx = s_len[pc.seq];
+        const int q0 = a.qstart[pc.seq];
+        const int nq = a.qstart[pc.seq + 1] - q0;  // valid: the sequence has units
+        const int rows = nq * G;
+        const bool active = rg * 8 < rows;
+        // Q^T fragments: column n = row 8 rg + gid of the row group
+        uint32_t qf[D / 16][2];
+        {
+            const int rr = rg * 8 + gid;
+            const bool live = rr < rows;
+            const int t = live ? rr / G : 0;
+            const __nv_bfloat16* qrow =
+                q + (static_cast<long long>(q0 + t) * a.q_heads + pc.head * G + (live ? rr - t * G : 0)) * D;
+            const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                qf[j][0] = live ? __ldg(q32 + (16 * j + 2 * tig) / 2) : 0u;
+                qf[j][1] = live ? __ldg(q32 + (16 * j + 2 * tig + 8) / 2) : 0u;
+            }
+        }
+        // last visible position of the lane's two columns (rows 2 tig, 2 tig + 1 of the group)
+        const int rc0 = rg * 8 + 2 * tig, rc1 = rc0 + 1;
+        const int lim0 = rc0 < rows ? n_ctx - nq + rc0 / G : -1;
+        const int lim1 = rc1 < rows ? n_ctx - nq + rc1 / G : -1;
+        float m0 = ninf(), m1 = ninf(), l0 = 0.f, l1 = 0.f;
+        float o[D / 16][4];
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+        for (int blk = pc.blk_from; blk < pc.blk_to; ++blk, ++k) {
+            if (static_cast<int>(k % UG) != ul) continue;
+            const int s = static_cast<int>(k % C::kStages);
+            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag)) return;
+            const int valid = min(16, n_ctx - blk * 16);
+            if (stage_ok[s] && active) {
+                const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
+                const uint32_t vbase = kbase + C::kPoolBytes;
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    const int gc = 2 * j + k_chunk;
+                    const uint32_t addr = kbase + (gc >> 3) * 2048 + k_row * 128 + (((gc & 7) ^ r8) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(addr, a0, a1, a2, a3);
+                    if (j & 1)
+                        mma_bf16_16816(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+                    else
+                        mma_bf16_16816(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+                }
+                // [0] (token gid, row 2tig) [1] (gid, 2tig+1) [2] (gid+8, 2tig) [3] (gid+8, 2tig+1)
+                const int p0 = blk * 16 + gid, p1 = p0 + 8;
+                const float x0 = p0 <= lim0 ? (sa[0] + sb[0]) * scale_log2 : ninf();
+                const float x1 = p0 <= lim1 ? (sa[1] + sb[1]) * scale_log2 : ninf();
+                const float x2 = p1 <= lim0 ? (sa[2] + sb[2]) * scale_log2 : ninf();
+                const float x3 = p1 <= lim1 ? (sa[3] + sb[3]) * scale_log2 : ninf();
+                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+                if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float nb0 = mn0 == ninf() ? 0.f : mn0;
+                    const float nb1 = mn1 == ninf() ? 0.f : mn1;
+                    const float al0 = m0 == ninf() ? 0.f : ex2(m0 - nb0);
+                    const float al1 = m1 == ninf() ? 0.f : ex2(m1 - nb1);
+                    l0 *= al0;
+                    l1 *= al1;
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        o[i][0] *= al0;
+                        o[i][1] *= al1;
+                        o[i][2] *= al0;
+                        o[i][3] *= al1;
+                    }
+                    m0 = mn0;
+                    m1 = mn1;
+                }
+                const float b0 = m0 == ninf() ? 0.f : m0;
+                const float b1 = m1 == ninf() ? 0.f : m1;
+                const float e0 = ex2(x0 - b0), e1 = ex2(x1 - b1), e2 = ex2(x2 - b0), e3 = ex2(x3 - b1);
+                l0 += e0 + e2;
+                l1 += e1 + e3;
+                const uint32_t h01 = pack_bf16x2(e0, e1), h23 = pack_bf16x2(e2, e3);
+                const uint32_t lo01 = pack_bf16x2(e0 - bf16lo_to_f32(h01), e1 - bf16hi_to_f32(h01));
+                const uint32_t lo23 = pack_bf16x2(e2 - bf16lo_to_f32(h23), e3 - bf16hi_to_f32(h23));
+                const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+                const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+                // rows past the context may hold anything: zero them in V
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (valid < 16) {
+                    mlo = (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
+                    mhi = (2 * tig + 8 < valid ? 0x0000ffffu : 0u) | (2 * tig + 9 < valid ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    const int gc = 2 * i + v_chunk;
+                    const uint32_t addr = vbase + (gc >> 3) * 2048 + v_row * 128 + (((gc & 7) ^ r8) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+                    a0 &= mlo;
+                    a1 &= mlo;
+                    a2 &= mhi;
+                    a3 &= mhi;
+                    mma_bf16_16816(o[i], a0, a1, a2, a3, bh0, bh1);
+                    mma_bf16_16816(o[i], a0, a1, a2, a3, bl0, bl1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        // ---- end of the piece: sums across the token rows of the fragments
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        const int c0 = 2 * tig, c1 = c0 + 1;  // the group's rows of the lane's columns
+        // The row group's state: the warp's own registers (one unit lane), or
+        // the combination of the unit lanes' states through shared memory.
+        float* buf = scratch + (piece_idx & 1) * (C::kConsumers * 8 * (D + 2));
+        if (UG > 1) {
+            float* so = buf + warp * 8 * (D + 2);  // [8 rows][D], then 8 maxima, 8 sums
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                so[c0 * D + 16 * i + gid] = o[i][0];
+                so[c1 * D + 16 * i + gid] = o[i][1];
+                so[c0 * D + 16 * i + gid + 8] = o[i][2];
+                so[c1 * D + 16 * i + gid + 8] = o[i][3];
+            }
+            if (gid == 0) {
+                so[8 * D + c0] = active ? m0 : ninf();
+                so[8 * D + c1] = active ? m1 : ninf();
+                so[8 * D + 8 + c0] = active ? l0 : 0.f;
+                so[8 * D + 8 + c1] = active ? l1 : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(piece_bar);
+            if (!mbar_wait(piece_bar, static_cast<uint32_t>(piece_idx & 1), a.status, abort_flag)) return;
+            ++piece_idx;
+            if (ul != 0 || !active) continue;
+            // combine the unit lanes of this row group: lane = 4 row + quarter
+            const int rw = lane >> 2;
+            const int d0 = (lane & 3) * (D / 4);
+            float M = ninf();
+            for (int u = 0; u < UG; ++u) M = fmaxf(M, buf[(u * W + rg) * 8 * (D + 2) + 8 * D + rw]);
+            const float base = M == ninf() ? 0.f : M;
+            float L = 0.f;
+            float O[D / 4];
+#pragma unroll
+            for (int e = 0; e < D / 4; ++e) O[e] = 0.f;
+            for (int u = 0; u < UG; ++u) {
+                const float* su = buf + (u * W + rg) * 8 * (D + 2);
+                const float mu = su[8 * D + rw];
+                const float wu = mu == ninf() ? 0.f : ex2(mu - base);
+                L += wu * su[8 * D + 8 + rw];
+#pragma unroll
+                for (int e = 0; e < D / 4; ++e) O[e] += wu * su[rw * D + d0 + e];
+            }
+            const int rr = rg * 8 + rw;
+            if (pc.complete) {
+                if (rr < rows) {
+                    const int t = rr / G;
+                    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                                          (static_cast<long long>(q0 + t) * a.q_heads + pc.head * G + (rr - t * G)) * D;
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+                    for (int e = 0; e < D / 4; e += 2)
+                        *reinterpret_cast<uint32_t*>(orow + d0 + e) = pack_bf16x2(O[e] * inv, O[e + 1] * inv);
+                }
+            } else {
+                float* sl = mq_slice(a.partials, cta, pc.first ? 0 : 1, rg, D);
+#pragma unroll
+                for (int e = 0; e < D / 4; ++e) sl[rw * D + d0 + e] = O[e];
+                if ((lane & 3) == 0) {
+                    sl[8 * D + rw] = M;
+                    sl[8 * D + 8 + rw] = L;
+                }
+                pending[npending++] = pc;
+            }
+            continue;
+        }
+        if (!active) continue;
+        if (pc.complete) {
+            const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int rr = rg * 8 + (c ? c1 : c0);
+                if (rr >= rows) continue;
+                const int t = rr / G;
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                                      (static_cast<long long>(q0 + t) * a.q_heads + pc.head * G + (rr - t * G)) * D;
+                const float inv = c ? i1 : i0;
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    orow[16 * i + gid] = __float2bfloat16_rn(o[i][c] * inv);
+                    orow[16 * i + gid + 8] = __float2bfloat16_rn(o[i][2 + c] * inv);
+                }
+            }
+        } else {
+            float* sl = mq_slice(a.partials, cta, pc.first ? 0 : 1, rg, D);
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                sl[c0 * D + 16 * i + gid] = o[i][0];
+                sl[c1 * D + 16 * i + gid] = o[i][1];
+                sl[c0 * D + 16 * i + gid + 8] = o[i][2];
+                sl[c1 * D + 16 * i + gid + 8] = o[i][3];
+            }
+            if (gid == 0) {
+                sl[8 * D + c0] = m0;
+                sl[8 * D + c1] = m1;
+                sl[8 * D + 8 + c0] = l0;
+                sl[8 * D + 8 + c1] = l1;
+            }
+            pending[npending++] = pc;
+        }
+    }
+    // announce this row group's cut pieces; the warp completing a count merges
+    if (npending == 0) return;
+    __threadfence();
+    __syncwarp();
+    const long long Cn = a.num_ctas;
+    for (int i = 0; i < npending; ++i) {
+        const Piece& pp = pending[i];
+        const long long c0s = cta_of(pp.seg_start, U, Cn);
+        const long long c1s = cta_of(pp.seg_start + pp.seg_len - 1, U, Cn);
+        const int np = pieces_of_segment(c0s, c1s, U, Cn);
+        int* counter = a.counters + (static_cast<long long>(pp.seq) * a.kv_heads + pp.head) * 4 + rg;
+        int old = 0;
+        if (lane == 0) old = atomicAdd(counter, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != np - 1) continue;
+        __threadfence();
+        const int slot0 = (pp.seg_start == range_start(c0s, U, Cn)) ? 0 : 1;
+        const int qq0 = a.qstart[pp.seq];
+        mq_merge<D>(pp, a, U, rg, lane, c0s, slot0, np, (a.qstart[pp.seq + 1] - qq0) * G, qq0);
+        if (lane == 0) *counter = 0;
+    }
+}
+
+template <typename K>
+int mq_occupancy(K kernel, int threads, size_t smem) {
+    int n = 0;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+    return n;
+}
+
+constexpr int kMqStages = 8;
+
+template <int D>
+cudaError_t run_mq(const MqArgs& a, int grid, cudaStream_t s) {
+    using C = Mq<D, kMqStages>;
+    CUtensorMap tmK, tmV;
+    const int64_t rows = a.num_blocks * a.kv_heads * 16;
+    if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
+        return cudaErrorInvalidValue;
+    const size_t smem = C::smem_bytes(a.batch);
+    cudaFuncSetAttribute(mq_tc_kernel<D, kMqStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    return launch_pdl(mq_tc_kernel<D, kMqStages>, dim3(grid), dim3(C::kThreads), smem, s, a, tmK, tmV);
+}
+
+}  // namespace
+
+int mq_num_ctas(int head_dim, int batch, const pkv_decode_opts* opts) {
+    if (opts && opts->num_ctas > 0) return opts->num_ctas;
+    static std::mutex mu;
+    static int cache[2][64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    const int b = batch < kMaxBatchPerLaunch ? (batch < 1 ? 1 : batch) : kMaxBatchPerLaunch;
+    std::lock_guard<std::mutex> lock(mu);
+    int& slot = cache[head_dim == 128 ? 1 : 0][dev];
+    if (slot == 0) {
+        // occupancy at the largest launch (the per-sequence arrays grow with the batch)
+        slot = head_dim == 128
+                   ? mq_occupancy(mq_tc_kernel<128, kMqStages>, Mq<128, kMqStages>::kThreads,
+                                  Mq<128, kMqStages>::smem_bytes(kMaxBatchPerLaunch))
+                   : mq_occupancy(mq_tc_kernel<64, kMqStages>, Mq<64, kMqStages>::kThreads,
+                                  Mq<64, kMqStages>::smem_bytes(kMaxBatchPerLaunch));
+    }
+    (void)b;
+    return slot * device_sm_count();
+}
+
+size_t mq_workspace_bytes(int batch, int kv_heads, int head_dim, int num_ctas, size_t* counters_offset,
+                          size_t* partials_offset) {
+    const int chunk = batch < kMaxBatchPerLaunch ? (batch < 1 ? 1 : batch) : kMaxBatchPerLaunch;
+    const size_t counters = static_cast<size_t>(chunk) * kv_heads * 4 * sizeof(int);
+    *counters_offset = 256;
+    *partials_offset = 256 + (counters + 255) / 256 * 256;
+    return *partials_offset + static_cast<size_t>(num_ctas) * 2 * 4 * 8 * (head_dim + 2) * sizeof(float);
+}
+
+namespace {
+// Checked mode: query counts must lie in [0, min(context, max_query_len)]
+// and the first query rows must be non-negative.
+__global__ void check_queries_kernel(const int32_t* lens, const int32_t* qstart, int32_t batch,
+                                     int32_t max_query_len, unsigned int* verdict) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < batch; i += gridDim.x * blockDim.x) {
+        const int n = lens[i], q0 = qstart[i], nq = qstart[i + 1] - q0;
+        if (q0 < 0 || nq < 0 || nq > n || nq > max_query_len) atomicOr(verdict, kVerdictRange);
+    }
+}
+}  // namespace
+
+cudaError_t launch_check_queries(const int32_t* lens, const int32_t* qstart, int32_t batch, int32_t max_query_len,
+                                 unsigned int* verdict, cudaStream_t s) {
+    if (batch <= 0) return cudaSuccess;
+    check_queries_kernel<<<(batch + 255) / 256, 256, 0, s>>>(lens, qstart, batch, max_query_len, verdict);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_multiquery(const MqArgs& a, cudaStream_t s) {
+    return a.head_dim == 128 ? run_mq<128>(a, a.num_ctas, s) : run_mq<64>(a, a.num_ctas, s);
+}
+
+}  // namespace pkv

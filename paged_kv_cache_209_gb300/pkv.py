@@ -55,7 +55,8 @@ class DecodeOpts(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("pkv_append", "pkv_copy_blocks", "pkv_decode_workspace_size", "pkv_decode_attention",
-           "pkv_decode_prefixed_workspace_size", "pkv_decode_attention_prefixed", "pkv_decode_attention_noalloc", "pkv_device_status", "pkv_status_string", "pkv_version",
+           "pkv_decode_prefixed_workspace_size", "pkv_decode_attention_prefixed", "pkv_decode_attention_noalloc",
+           "pkv_multiquery_workspace_size", "pkv_multiquery_attention", "pkv_device_status", "pkv_status_string", "pkv_version",
            "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_add_sequence", "pkv_pool_append", "pkv_pool_append_batch",
            "pkv_pool_share_prefix", "pkv_pool_release", "pkv_pool_sequence_length", "pkv_pool_page_table",
            "pkv_pool_block_tables", "pkv_pool_get_stats", "pkv_pool_validate")
@@ -88,6 +89,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_decode_attention_prefixed.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp, i32,
                                                   i32, vp, vp, ctypes.c_size_t, desc_p, u32, opts_p, vp]
     lib.pkv_decode_attention_prefixed.restype = ctypes.c_int
+    lib.pkv_multiquery_workspace_size.argtypes = [i32, i32, i32, i32, desc_p, opts_p]
+    lib.pkv_multiquery_workspace_size.restype = ctypes.c_size_t
+    lib.pkv_multiquery_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp,
+                                             ctypes.c_size_t, desc_p, u32, opts_p, vp]
+    lib.pkv_multiquery_attention.restype = ctypes.c_int
     lib.pkv_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp,
                                                  desc_p, u32, opts_p, vp]
     lib.pkv_decode_attention_noalloc.restype = ctypes.c_int
@@ -280,6 +286,45 @@ def pkv_decode_attention_prefixed(q, k_cache, v_cache, block_tables, context_len
         q_heads, ctypes.c_float(scale), _ptr(prefix_group), _ptr(group_blocks), num_groups, max_group_blocks,
         _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags,
         _opts(kernel, num_ctas, stages, prefix_kernel), _stream(stream)))
+    return out
+
+
+def pkv_multiquery_workspace_size(batch: int, num_q_heads: int, max_blocks_per_seq: int, max_query_len: int,
+                                  k_cache, num_ctas: int = 0) -> int:
+    """Workspace bytes of the multi-query call; allocate them zero-filled and reuse them."""
+    lib = load_library()
+    desc = cache_desc(k_cache)
+    return int(lib.pkv_multiquery_workspace_size(batch, num_q_heads, max_blocks_per_seq, max_query_len,
+                                                 ctypes.byref(desc), _opts(0, num_ctas)))
+
+
+def pkv_multiquery_attention(q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
+                             max_query_len: int, out=None, workspace=None, flags: int = 0, num_ctas: int = 0,
+                             stream=None):
+    """Causal multi-query attention; ``q``/``out`` are [query_start[-1]][q_heads][head_dim]
+    and ``query_start`` int32 [batch + 1]. Returns ``out``."""
+    lib = load_library()
+    _same_pools(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    rows, q_heads, d = q.shape
+    batch = int(context_lens.shape[0])
+    if d != desc.head_dim or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [rows][q_heads][head_dim] of the pool dtype")
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens), ("query_start", query_start)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} is int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != batch or query_start.shape != (batch + 1,):
+        raise ValueError("block_tables is [batch][max_blocks], query_start [batch + 1]")
+    max_blocks = int(block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        need = pkv_multiquery_workspace_size(batch, q_heads, max_blocks, max_query_len, k_cache, num_ctas)
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check("pkv_multiquery_attention", lib.pkv_multiquery_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens),
+        _ptr(query_start), batch, q_heads, max_query_len, ctypes.c_float(scale), _ptr(out), _ptr(workspace),
+        workspace.numel(), ctypes.byref(desc), flags, _opts(0, num_ctas), _stream(stream)))
     return out
 
 

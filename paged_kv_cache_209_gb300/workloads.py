@@ -18,6 +18,9 @@ Workloads (named by what they are; all use 16-token blocks):
   each, tables a permutation (seed 3) of a 32768-block pool.
 * ``prefix``       -- batch 64, Llama-3-8B heads, a 4096-token (256-block)
   shared prefix plus private suffixes uniform in [1, 2048] (seed 4).
+* ``spec4``        -- the ``llama8k`` layer verifying 4 draft tokens per
+  sequence: every context 8192 tokens including the 4 new ones, 4 causal
+  queries per sequence, tables a permutation (seed 5) of a 16384-block pool.
 
 Values are standard normal. Large tensors are drawn on the device with a
 seeded ``torch.Generator``; the oracle reads the same tensors back, so
@@ -43,6 +46,8 @@ CONFIGS = {
                      context=131072, num_blocks=32768, seed=3),
     "prefix": dict(batch=64, q_heads=32, kv_heads=8, head_dim=128, dtype="bf16",
                    prefix=4096, min_suffix=1, max_suffix=2048, seed=4),
+    "spec4": dict(batch=32, q_heads=32, kv_heads=8, head_dim=128, dtype="bf16",
+                  context=8192, num_blocks=16384, queries=4, seed=5),
 }
 
 
@@ -123,7 +128,7 @@ def workload_index(name: str):
     """
     cfg = CONFIGS[name]
     B = cfg["batch"]
-    if name in ("llama8k", "long128k"):
+    if name in ("llama8k", "long128k", "spec4"):
         lens = np.full(B, cfg["context"], dtype=np.int64)
         tables = permuted_tables(cfg["num_blocks"], B, cfg["context"] // BLOCK_SIZE, cfg["seed"])
         num_blocks = cfg["num_blocks"]
@@ -154,16 +159,21 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
 
     Returns the K/V pools, q, the step's new K/V rows with their slots, the
     copy pairs (none for these workloads), block tables and the context
-    lengths *after* the step's append (the new token is attended to).
+    lengths *after* the step's append (the new tokens are attended to). With
+    ``queries`` new tokens per sequence (``spec4``), q holds that many rows per
+    sequence in sequence order and ``query_start`` gives their offsets.
     """
     import torch
 
     cfg = CONFIGS[name]
     bf = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
     B, HQ, HKV, D = cfg["batch"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
+    nq = cfg.get("queries", 1)
     seed = cfg["seed"] + seed_offset
     tables, lens, num_blocks = workload_index(name)
-    slots = slot_of(tables, lens - 1)
+    # the step's new tokens: positions lens - nq .. lens - 1 of every sequence
+    pos = (lens[:, None] - nq + np.arange(nq)[None, :]).reshape(-1)
+    slots = slot_of(np.repeat(tables, nq, axis=0), pos)
     # shared-prefix groups: the prefix workload is one group over its shared blocks
     n_shared = cfg.get("prefix", 0) // BLOCK_SIZE
     group = np.zeros(B, dtype=np.int32) if n_shared else np.full(B, -1, dtype=np.int32)
@@ -171,9 +181,11 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
         name=name, cfg=cfg, num_blocks=num_blocks,
         k_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed, bf, device),
         v_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed + 1, bf, device),
-        q=torch_normal((B, HQ, D), seed + 2, bf, device),
-        k_new=torch_normal((B, HKV, D), seed + 3, bf, device),
-        v_new=torch_normal((B, HKV, D), seed + 4, bf, device),
+        q=torch_normal((B * nq, HQ, D), seed + 2, bf, device),
+        k_new=torch_normal((B * nq, HKV, D), seed + 3, bf, device),
+        v_new=torch_normal((B * nq, HKV, D), seed + 4, bf, device),
+        query_start=torch.arange(0, B * nq + 1, nq, dtype=torch.int32, device=device),
+        queries=nq,
         slots=torch.from_numpy(slots).to(device),
         pairs=torch.zeros((0, 2), dtype=torch.int64, device=device),
         tables=torch.from_numpy(tables).to(device),

@@ -153,3 +153,14 @@ def grouped_case(seed, member_of, group_blocks, suffix_lens, q_heads, kv_heads, 
                 prefix_group=np.array(member_of, dtype=np.int32),
                 group_blocks=np.array(group_blocks, dtype=np.int32), kv_heads=kv_heads,
                 scale=1.0 / np.sqrt(head_dim))
+
+
+def multiquery_case(seed, lens, nqs, q_heads, kv_heads, head_dim, dtype, extra_blocks=4, width=None):
+    """Sequences of the given lengths on a shuffled pool; sequence i's last
+    nqs[i] tokens are its queries (rows query_start[i] .. query_start[i+1]-1)."""
+    c = random_case(seed, lens, q_heads, kv_heads, head_dim, dtype, extra_blocks=extra_blocks, width=width)
+    qs = np.concatenate([[0], np.cumsum(np.asarray(nqs, dtype=np.int64))]).astype(np.int32)
+    q = W.numpy_normal((int(qs[-1]), q_heads, head_dim), seed * 7 + 5)
+    c["q"] = torch.from_numpy(q).to(dtype)
+    c["query_start"] = qs
+    return c

@@ -149,3 +149,37 @@ def test_prefix_workload_two_phase(pkv):
     ref = pkv.pkv_decode_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["scale"])
     d = out.float() - ref.float()
     assert (d.norm() / ref.float().norm()).item() <= 2e-3 and d.abs().max().item() <= 1e-2
+
+
+def test_spec4_workload_multiquery(pkv):
+    """The 8K Llama layer verifying 4 draft tokens per sequence: one append of
+    128 new tokens and one multi-query call, as the benchmark runs them.
+    Sampled (sequence, KV head) pairs against the float64 oracle; every row
+    against the decode kernel run once per query position (query t of each
+    sequence is a decode over the first 8192 - 4 + t + 1 tokens)."""
+    from oracle import multiquery as OM
+    w = W.device_workload("spec4", torch.device("cuda", 0))
+    cfg, nq = w["cfg"], w["queries"]
+    kv_heads = cfg["kv_heads"]
+    G = cfg["q_heads"] // kv_heads
+    hk, hv = cases.host_view(w["k_pool"]), cases.host_view(w["v_pool"])
+    OK.append_tokens(hk, hv, cases.host_view(w["k_new"]), cases.host_view(w["v_new"]), w["slots_np"])
+    pkv.pkv_append(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"])
+    out = pkv.pkv_multiquery_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["query_start"],
+                                       w["scale"], nq)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert np.array_equal(cases.host_view(w["k_pool"]), hk) and np.array_equal(cases.host_view(w["v_pool"]), hv)
+    qh = cases.host_view(w["q"])
+    qs = np.arange(0, cfg["batch"] * nq + 1, nq)
+    for (i, j) in sample_pairs(w["lens_np"], kv_heads, 4, 23):
+        sub_q = qh[qs[i]:qs[i + 1]]
+        want = OM.multiquery_attention(sub_q, hk, hv, w["tables_np"][i:i + 1], w["lens_np"][i:i + 1],
+                                       np.array([0, nq]), w["scale"], kv_heads, "bf16")
+        ma, rl = cases.attention_errors(out[qs[i]:qs[i + 1], j * G:(j + 1) * G], want[:, j * G:(j + 1) * G])
+        assert ma <= MAX_ABS and rl <= REL_L2, (i, j, ma, rl)
+    for t in range(nq):
+        ref = pkv.pkv_decode_attention(w["q"][t::nq].contiguous(), w["k_pool"], w["v_pool"], w["tables"],
+                                       w["lens"] - (nq - 1 - t), w["scale"])
+        d = out[t::nq].float() - ref.float()
+        assert d.abs().max().item() <= 1e-2 and (d.norm() / ref.float().norm()).item() <= 2e-3, t

@@ -1,0 +1,143 @@
+"""Multi-query (causal) paged attention through the C ABI against the oracle.
+
+Every output row is compared with the float64 oracle (query t of a sequence
+with n tokens and nq queries attends to tokens 0 .. n - nq + t). Cases cover
+group sizes 1-8, head_dim 64 and 128, query counts 0 to max_query_len per
+sequence, contexts that are all queries (a whole prompt), contexts inside
+one block, ragged lengths, forced CTA counts that cut segments (their merge),
+batches above one launch, workspace reuse, malformed query ranges (flagged,
+other rows right) and checked mode; one query per sequence is also checked
+against the decode kernel.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import cases
+from oracle import multiquery as OM
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, REL_L2 = 1e-2, 2e-3
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_209_gb300 import pkv as P
+    P.load_library()
+    return P
+
+
+def dev(c):
+    d = torch.device("cuda", 0)
+    return dict(q=c["q"].to(d), k=c["k_pool"].to(d), v=c["v_pool"].to(d),
+                tables=torch.from_numpy(c["tables"]).to(d), lens=torch.from_numpy(c["lens"]).to(d),
+                qs=torch.from_numpy(c["query_start"]).to(d))
+
+
+def want(c):
+    return OM.multiquery_attention(cases.host_view(c["q"]), cases.host_view(c["k_pool"]),
+                                   cases.host_view(c["v_pool"]), c["tables"], c["lens"], c["query_start"],
+                                   c["scale"], c["kv_heads"], "bf16")
+
+
+def run(pkv, c, d, mql, **kw):
+    out = pkv.pkv_multiquery_attention(d["q"], d["k"], d["v"], d["tables"], d["lens"], d["qs"], c["scale"], mql, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def check(out, ref):
+    ma, rl = cases.attention_errors(out, ref)
+    assert ma <= MAX_ABS and rl <= REL_L2, (ma, rl)
+
+
+CASES = {
+    # name: (lens, query counts, q_heads, kv_heads, head_dim, max_query_len)
+    "spec4_llama": ([300, 17, 64, 1000, 5], [4, 4, 4, 4, 4], 32, 8, 128, 4),
+    "ragged_counts_g4": ([40, 33, 16, 200, 7, 90], [0, 3, 8, 1, 7, 5], 8, 2, 128, 8),
+    "g8_d64": ([129, 48, 500, 3], [2, 4, 3, 3], 16, 2, 64, 4),
+    "g1_whole_prompts": ([20, 32, 31], [20, 32, 31], 2, 2, 64, 32),
+    "g3": ([77, 64, 12, 400], [10, 1, 10, 6], 6, 2, 128, 10),
+    "single_block_contexts": ([1, 2, 15, 16], [1, 2, 8, 8], 8, 2, 128, 8),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_multiquery_matches_oracle(pkv, name):
+    lens, nqs, hq, hkv, d, mql = CASES[name]
+    c = cases.multiquery_case(len(name), lens, nqs, hq, hkv, d, torch.bfloat16)
+    out = run(pkv, c, dev(c), mql)
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want(c))
+
+
+@pytest.mark.parametrize("num_ctas", [3, 40, 5000])
+def test_cut_segments(pkv, num_ctas):
+    """Forced CTA counts cut (sequence, KV head) segments across CTAs; every
+    warp's pieces are merged by the last one to finish."""
+    lens, nqs = [1200, 333, 40, 2048], [4, 2, 4, 3]
+    c = cases.multiquery_case(9, lens, nqs, 32, 8, 128, torch.bfloat16)
+    out = run(pkv, c, dev(c), 4, num_ctas=num_ctas)
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want(c))
+
+
+def test_one_query_per_sequence_is_decode(pkv):
+    c = cases.multiquery_case(10, [70, 1, 512, 33], [1, 1, 1, 1], 32, 8, 128, torch.bfloat16)
+    d = dev(c)
+    mq = run(pkv, c, d, 1)
+    dec = pkv.pkv_decode_attention(d["q"], d["k"], d["v"], d["tables"], d["lens"], c["scale"])
+    diff = (mq.float() - dec.float())
+    assert diff.abs().max().item() <= 1e-2 and (diff.norm() / dec.float().norm()).item() <= 2e-3
+    check(mq, want(c))
+
+
+def test_batch_above_one_launch_and_reuse(pkv):
+    rng = np.random.default_rng(11)
+    lens = rng.integers(1, 120, 1100)
+    nqs = np.minimum(lens, rng.integers(0, 5, 1100))
+    c = cases.multiquery_case(12, lens, nqs, 8, 2, 64, torch.bfloat16)
+    d = dev(c)
+    need = pkv.pkv_multiquery_workspace_size(1100, 8, c["tables"].shape[1], 4, d["k"])
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ref = want(c)
+    for _ in range(2):
+        out = run(pkv, c, d, 4, workspace=ws)
+        assert pkv.pkv_device_status(clear=True) == 0
+        check(out, ref)
+
+
+def test_malformed_query_ranges(pkv):
+    """A sequence asking for more queries than it has tokens (or than
+    max_query_len) gets no rows and sets PKV_DEVERR_RANGE; the other rows are
+    right. Checked mode rejects the call and writes nothing."""
+    c = cases.multiquery_case(13, [30, 3, 50], [2, 4, 2], 8, 2, 128, torch.bfloat16)   # 4 > 3 tokens
+    d = dev(c)
+    out = torch.full_like(d["q"], 5.0)
+    run(pkv, c, d, 4, out=out)
+    assert pkv.pkv_device_status(clear=True) & 2
+    good = np.r_[0:2, 6:8]
+    ref = want(dict(c, lens=np.array([30, 3, 50]), query_start=np.array([0, 2, 2, 4]),
+                    q=torch.cat([c["q"][0:2], c["q"][6:8]])))
+    check(out[torch.from_numpy(good).cuda()], ref)
+    out2 = torch.full_like(d["q"], 5.0)
+    with pytest.raises(pkv.PkvError) as e:
+        run(pkv, c, d, 4, out=out2, flags=pkv.PKV_FLAG_CHECKED)
+    assert e.value.name == "PKV_ERR_RANGE"
+    assert bool((out2 == 5.0).all())
+
+
+def test_host_rejections(pkv):
+    c = cases.multiquery_case(14, [30, 40], [2, 2], 32, 8, 128, torch.bfloat16)
+    d = dev(c)
+    with pytest.raises(pkv.PkvError) as e:
+        run(pkv, c, d, 9)            # 9 queries x 4 heads > 32 rows
+    assert e.value.name == "PKV_ERR_UNSUPPORTED"
+    cf = cases.multiquery_case(14, [30, 40], [2, 2], 8, 2, 64, torch.float32)
+    with pytest.raises(pkv.PkvError) as e:
+        run(pkv, cf, dev(cf), 2)
+    assert e.value.name == "PKV_ERR_DTYPE"
