@@ -25,6 +25,9 @@ What it restates, in float64 (or exact integer / byte arithmetic):
   of sequences, then sequence-first over each suffix) decode and its
   log-sum-exp combination (paper-search page, ChunkAttention abstract;
   notebook sections 5 and 7).
+* ``quant``       -- per-row symmetric low-bit quantization of K/V rows (the
+  notebook's ``fake_quantize_rows`` with the scale stored as float32), the
+  quantizing append and attention over the quantized cache (section 8).
 * ``multiquery``  -- several causal queries per sequence against its paged
   context: speculative verification tokens or a prefill chunk (release page
   Architectural Breakdown 2; notebook section 7).
@@ -33,4 +36,4 @@ Pins that tie these functions to the pages (not to themselves) live in
 ``tests/test_oracle_*.py`` and ``tests/golden/``.
 """
 
-from . import geometry, paged_pool, kv_ops, attention, prefix, multiquery  # noqa: F401
+from . import geometry, paged_pool, kv_ops, attention, prefix, multiquery, quant  # noqa: F401

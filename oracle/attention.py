@@ -35,11 +35,13 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Widen a cache or query array given as float32 or bf16 bits."""
+    """Widen a cache or query array given as float32, bf16 bits or float64."""
     if dtype == "bf16":
         return bf16_bits_to_f64(x)
     if dtype == "f32":
         return np.asarray(x, dtype=np.float32).astype(np.float64)
+    if dtype == "f64":
+        return np.asarray(x, dtype=np.float64)
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
