@@ -56,6 +56,7 @@ WORKLOAD_NAMES = {
     "mixed": "continuous-batching mix, contexts log-uniform on [16, 32768]",
     "prefix": "4096-token prefix shared by all sequences + private suffixes uniform in [1, 2048]",
     "spec4": "Llama-3-8B decode layer verifying 4 draft tokens per sequence (causal multi-query), context 8192",
+    "llama8k_q8": "Llama-3-8B decode layer over an int8 KV cache (per-row float32 scales), every context 8192 tokens",
 }
 L2_NOTE = {
     "llama8k": "inputs larger than L2 (1 GiB K+V per step)",
@@ -64,12 +65,21 @@ L2_NOTE = {
     "prefix": "unique K+V (0.33 GB) larger than L2; the 16 MiB shared prefix is re-read from L2 by every "
               "sequence, so logical GB/s can exceed HBM bandwidth",
     "spec4": "inputs larger than L2 (1 GiB K+V per step, read once for the 4 queries of each sequence)",
+    "llama8k_q8": "inputs larger than L2 (0.55 GB of K+V codes and scales per step)",
 }
 
 
 def workload_desc(name, cfg, lens):
+    kind = "int8 K/V codes + float32 row scales, bf16 q" if cfg["dtype"] == "int8" else cfg["dtype"]
     return (f"{WORKLOAD_NAMES[name]}: batch {cfg['batch']}, {cfg['q_heads']} q / {cfg['kv_heads']} kv heads, "
-            f"head_dim {cfg['head_dim']}, 16-token blocks, shuffled pool, bf16, {int(lens.sum())} KV tokens")
+            f"head_dim {cfg['head_dim']}, 16-token blocks, shuffled pool, {kind}, {int(lens.sum())} KV tokens")
+
+
+def kv_bytes_per_token(cfg):
+    """Bytes of one token's K and V over all KV heads (codes + scales for int8)."""
+    if cfg["dtype"] == "int8":
+        return 2 * cfg["kv_heads"] * (cfg["head_dim"] + 4)
+    return 2 * cfg["kv_heads"] * cfg["head_dim"] * (4 if cfg["dtype"] == "f32" else 2)
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -199,6 +209,40 @@ def oracle_sample_rate(q, kp, vp, tables, lens, scale, kv_heads, pairs, time_bud
     return nbytes, time.perf_counter() - t0, done
 
 
+def oracle_sample_rate_q8(q, kc, vc, ks, vs, tables, lens, scale, kv_heads, time_budget_s=None):
+    """The int8-cache oracle on whole sequences (all KV heads), one at a time;
+    returns (bytes, seconds, sequences done). ``vc`` is in the oracle's
+    token-row layout."""
+    from oracle import quant as OQ
+    done, nbytes = 0, 0
+    t0 = time.perf_counter()
+    for i in range(len(lens)):
+        OQ.decode_attention_q8(q[i:i + 1], kc, vc, ks, vs, tables[i:i + 1], lens[i:i + 1], scale, kv_heads, "bf16")
+        nbytes += int(lens[i]) * 2 * kv_heads * (kc.shape[-1] + 4)
+        done += 1
+        if time_budget_s is not None and time.perf_counter() - t0 > time_budget_s:
+            break
+    return nbytes, time.perf_counter() - t0, done
+
+
+def cpu_sample_data_q8(w, q, tables_np, lens_np, seqs):
+    """Host copies of the sampled sequences' int8 blocks (V codes turned to token rows)."""
+    import torch
+    ids = np.unique(tables_np[seqs].reshape(-1))
+    ids = ids[ids >= 0]
+    remap = -np.ones(w["k_pool"].shape[0], dtype=np.int64)
+    remap[ids] = np.arange(len(ids))
+    idx = torch.from_numpy(ids).to(q.device)
+    kc = w["k_pool"].index_select(0, idx).cpu().numpy()
+    vc = np.ascontiguousarray(w["v_pool"].index_select(0, idx).cpu().numpy().transpose(0, 1, 3, 2))
+    ks = w["k_scales"].index_select(0, idx).cpu().numpy()
+    vs = w["v_scales"].index_select(0, idx).cpu().numpy()
+    qh = q[torch.tensor(seqs, device=q.device)].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    t = tables_np[seqs]
+    t = np.where(t >= 0, remap[np.maximum(t, 0)], -1)
+    return qh, kc, vc, ks, vs, t, lens_np[seqs]
+
+
 def cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, seqs, nq=1):
     import torch
     ids = np.unique(tables_np[seqs].reshape(-1))
@@ -238,15 +282,31 @@ def run_reference(args, cfg):
     assert len(np.unique(ids)) == n_used
     scale = 1.0 / np.sqrt(cfg["head_dim"])
     pairs = [(0, 0)]
+    if cfg["dtype"] == "int8":
+        # int8 codes and float32 scales of the sampled sequence's blocks (token-row layout)
+        rng = np.random.default_rng(cfg["seed"])
+        qshape = shape[:3]
+        kc = np.clip(np.rint(rng.standard_normal(shape) * 42), -127, 127).astype(np.int8)
+        vc = np.clip(np.rint(rng.standard_normal(shape) * 42), -127, 127).astype(np.int8)
+        ks = rng.uniform(0.02, 0.03, qshape).astype(np.float32)
+        vs = rng.uniform(0.02, 0.03, qshape).astype(np.float32)
+
+        def one_step():
+            return oracle_sample_rate_q8(q, kc, vc, ks, vs, t, lens, scale, cfg["kv_heads"])[:2]
+        what = f"1 sequence x {cfg['kv_heads']} KV heads ({int(lens[0])} tokens, int8 K+V codes, float32 scales)"
+    else:
+        def one_step():
+            return oracle_sample_rate(q, kp, vp, t, lens, scale, cfg["kv_heads"], pairs)[:2]
+        what = f"1 sequence x 1 KV head ({int(lens[0])} tokens, bf16 K+V)"
     for _ in range(args.warmup):
-        oracle_sample_rate(q, kp, vp, t, lens, scale, cfg["kv_heads"], pairs)
+        one_step()
     tot_b, tot_s = 0, 0.0
     for _ in range(args.steps):
-        b, s_, _ = oracle_sample_rate(q, kp, vp, t, lens, scale, cfg["kv_heads"], pairs)
+        b, s_ = one_step()
         tot_b += b
         tot_s += s_
     gbs = tot_b / tot_s / 1e9
-    sample = f"1 sequence x 1 KV head ({int(lens[0])} tokens, bf16 K+V) per step"
+    sample = f"{what} per step"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3),
@@ -254,7 +314,7 @@ def run_reference(args, cfg):
         "config": {"workload": workload_desc(args.workload, cfg, lens_all), "sample": sample},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "kv_tokens_per_s": round(tot_b / (2 * cfg["kv_heads"] * cfg["head_dim"] * 2) / tot_s, 1),
+        "kv_tokens_per_s": round(tot_b / kv_bytes_per_token(cfg) / tot_s, 1),
     }
     print(json.dumps(line), flush=True)
 
@@ -281,10 +341,14 @@ def run_pkv(args, cfg):
     MAXB = tables.shape[1]
     out = torch.empty_like(q)
     two_phase = args.workload == "prefix" and not args.single_pass
+    q8 = cfg["dtype"] == "int8"
     nq = w["queries"]
     qstart = w["query_start"]
     group, gblocks, mgb = w["prefix_group"], w["group_blocks"], w["max_group_blocks"]
-    if two_phase:
+    if q8:
+        ks_pool, vs_pool = w["k_scales"], w["v_scales"]
+        ws_bytes = pkv.pkv_decode_q8_workspace_size(B, HQ, MAXB, k_pool)
+    elif two_phase:
         ws_bytes = pkv.pkv_decode_prefixed_workspace_size(B, HQ, MAXB, len(gblocks), mgb, k_pool)
     elif nq > 1:
         ws_bytes = pkv.pkv_multiquery_workspace_size(B, HQ, MAXB, nq, k_pool)
@@ -295,7 +359,10 @@ def run_pkv(args, cfg):
     stream = torch.cuda.current_stream()
 
     def decode():
-        if nq > 1:
+        if q8:
+            pkv.pkv_decode_attention_q8(q, k_pool, v_pool, ks_pool, vs_pool, tables, lens, scale, out=out,
+                                        workspace=workspace, stream=stream)
+        elif nq > 1:
             pkv.pkv_multiquery_attention(q, k_pool, v_pool, tables, lens, qstart, scale, nq, out=out,
                                          workspace=workspace, stream=stream)
         elif two_phase:
@@ -305,9 +372,16 @@ def run_pkv(args, cfg):
             pkv.pkv_decode_attention(q, k_pool, v_pool, tables, lens, scale, out=out, workspace=workspace,
                                      stream=stream)
 
+    def copy_and_append():
+        if q8:
+            pkv.pkv_copy_blocks_q8(pairs, k_pool, v_pool, ks_pool, vs_pool, stream=stream)
+            pkv.pkv_append_q8(kn, vn, slots, k_pool, v_pool, ks_pool, vs_pool, stream=stream)
+        else:
+            pkv.pkv_copy_blocks(pairs, k_pool, v_pool, stream=stream)
+            pkv.pkv_append(kn, vn, slots, k_pool, v_pool, stream=stream)
+
     def step():
-        pkv.pkv_copy_blocks(pairs, k_pool, v_pool, stream=stream)
-        pkv.pkv_append(kn, vn, slots, k_pool, v_pool, stream=stream)
+        copy_and_append()
         decode()
 
     # append + per 1024 sequences one decode launch (two with the shared-prefix pass)
@@ -331,8 +405,7 @@ def run_pkv(args, cfg):
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(args.steps):
-        pkv.pkv_copy_blocks(pairs, k_pool, v_pool, stream=stream)
-        pkv.pkv_append(kn, vn, slots, k_pool, v_pool, stream=stream)
+        copy_and_append()
         ev = ev_dec.get(i)
         if ev:
             ev[0].record(stream)
@@ -379,7 +452,8 @@ def run_pkv(args, cfg):
         return
 
     kv_tokens = int(lens_np.sum())
-    kvb = kv_tokens * 2 * HKV * D * q.element_size()
+    tok_bytes = kv_bytes_per_token(cfg)
+    kvb = kv_tokens * tok_bytes
     total_kv = kvb * ws
     ms_per_step = ms_total / args.steps
     value = total_kv / (ms_per_step * 1e-3) / 1e9
@@ -390,49 +464,62 @@ def run_pkv(args, cfg):
     # kernel must move), not once per sequence.
     used_entries = int(((lens_np.astype(np.int64) + 15) // 16).sum())
     shared_tokens = int(mgb) * 16 * (B - 1) if two_phase else 0
-    unique_kvb = (kv_tokens - shared_tokens) * 2 * HKV * D * q.element_size()
+    unique_kvb = (kv_tokens - shared_tokens) * tok_bytes
     alg_bytes = unique_kvb + q.numel() * q.element_size() + out.numel() * out.element_size() + used_entries * 4 + B * 4
     achieved = alg_bytes / (dec_avg_ms * 1e-3) / 1e9
     if two_phase:
         traffic = profiled_traffic("decode_prefix_two_phase", ("pkv_decode.cu", "pkv_prefix.cu"))
+    elif q8 or nq > 1:
+        traffic = profiled_traffic(f"decode_{args.workload}", ("pkv_multiquery.cu",))
     else:
         traffic = profiled_traffic(f"decode_{args.workload}")
 
     # -------- CPU oracle baseline on a bounded sample of the same workload
     order = np.argsort(-lens_np)
     sample_seqs = sorted({int(order[0]), int(order[len(order) // 2])})
-    qh, kph, vph, th, lh = cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, sample_seqs, nq)
-    pairs_list = [(i, j) for i in range(len(sample_seqs)) for j in range(HKV)]
-    cb, cs, cdone = oracle_sample_rate(qh, kph, vph, th, lh, scale, HKV, pairs_list, time_budget_s=20.0, nq=nq)
+    if q8:
+        qh, kch, vch, ksh, vsh, th, lh = cpu_sample_data_q8(w, q, tables_np, lens_np, sample_seqs)
+        cb, cs, cdone = oracle_sample_rate_q8(qh, kch, vch, ksh, vsh, th, lh, scale, HKV, time_budget_s=20.0)
+        cpu_what = f"{cdone} whole sequences of {sample_seqs} (int8 cache, all KV heads), "
+    else:
+        qh, kph, vph, th, lh = cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, sample_seqs, nq)
+        pairs_list = [(i, j) for i in range(len(sample_seqs)) for j in range(HKV)]
+        cb, cs, cdone = oracle_sample_rate(qh, kph, vph, th, lh, scale, HKV, pairs_list, time_budget_s=20.0, nq=nq)
+        cpu_what = (f"{cdone} (sequence, KV head) pairs of sequences {sample_seqs}, " if nq == 1
+                    else f"{cdone} whole sequences of {sample_seqs} ({nq} queries each), ")
     cpu_gbs = cb / cs / 1e9
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8" if q8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": workload_desc(args.workload, cfg, lens_np),
                    "l2": L2_NOTE[args.workload],
-                   "step": f"copy_blocks ({int(pairs.shape[0])} pairs) + append ({B * nq} tokens) + "
-                           + ("shared-prefix decode attention (two phases)" if two_phase
+                   "step": f"copy_blocks{'_q8' if q8 else ''} ({int(pairs.shape[0])} pairs) + "
+                           + f"{'quantizing append' if q8 else 'append'} ({B * nq} tokens) + "
+                           + ("decode attention over the int8 cache" if q8
+                              else "shared-prefix decode attention (two phases)" if two_phase
                               else f"causal multi-query attention ({nq} queries per sequence)" if nq > 1
                               else "decode attention"),
-                   "kernel": "tensor-core split-context kernel, merge fused"
-                             + (", then the chunk-first pass over the shared blocks" if two_phase else "")},
+                   "kernel": ("tensor-core split-context kernel on int8 codes (exact in f16), per-row scales "
+                              "applied to S and folded into P, merge fused" if q8 else
+                              "tensor-core split-context kernel, merge fused"
+                              + (", then the chunk-first pass over the shared blocks" if two_phase else ""))},
         "hbm_frac": round(value / peak, 4),
         "unique_kv_gbs": round(unique_kvb * ws / (ms_per_step * 1e-3) / 1e9, 2),
         "kv_tokens_per_s": round(kv_tokens * ws / (ms_per_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("decode_tc_kernel<128> + prefix_umma_kernel<128> (one shared-prefix call)"
+                     "kernel": ("mq_tc_kernel<128, int8> (one launch per pkv_decode_attention_q8 call)" if q8
+                                else "decode_tc_kernel<128> + prefix_umma_kernel<128> (one shared-prefix call)"
                                 if two_phase else
                                 "mq_tc_kernel<128> (one launch per pkv_multiquery_attention call)" if nq > 1 else
                                 "decode_tc_kernel<128> (one launch per pkv_decode_attention call)"),
                      "avg_launch_ms": round(dec_avg_ms, 5), "launches_timed": len(dec_ms),
                      "algorithmic_bytes": alg_bytes},
         "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": (f"{cdone} (sequence, KV head) pairs of sequences {sample_seqs}, "
-                                    if nq == 1 else f"{cdone} whole sequences of {sample_seqs} ({nq} queries each), ")
-                                   + "float64 NumPy oracle, one thread"},
+                         "sample": cpu_what + "float64 NumPy oracle, one thread"},
         "e2e": {"value": round(total_kv / (e2e_s / args.steps) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

@@ -74,7 +74,9 @@ typedef enum {
     PKV_ERR_INVARIANT = 14    /* block pool: an internal invariant is broken     */
 } pkv_status;
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+/* PKV_INT8: the low-bit pools of pkv_append_q8 / pkv_decode_attention_q8
+ * (int8 codes plus one float32 scale per token row of a KV head). */
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_INT8 = 2 } pkv_dtype;
 
 /* Geometry of one layer's K and V pools. */
 typedef struct {
@@ -317,6 +319,76 @@ PKV_API pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, 
                                             float scale, void* out, void* workspace, size_t workspace_bytes,
                                             const pkv_cache_desc* desc, uint32_t flags,
                                             const pkv_decode_opts* opts, void* stream);
+
+/*
+ * Low-bit (int8) paged KV.
+ * (notebook section 8: fewer bits per coordinate shrink the bytes per token in
+ * proportion; notebook project demo `fake_quantize_rows`: per row, limit =
+ * 2^(bits-1) - 1, scale = max|x| / limit (1 for a zero row), codes =
+ * clip(rint(x / scale), -limit, limit), value = code * scale.)
+ *
+ * A row is one token of one KV head (head_dim coordinates); bits = 8, limit =
+ * 127. The scale is stored as a float32, computed as float32(max|x|) / 127 in
+ * float32; each code is rint(x / scale) in float64 (half to even) against that
+ * stored scale, clipped to [-127, 127]. The cached row stands for code * scale.
+ * Pools (desc->dtype = PKV_INT8, head_dim 64 or 128 for the append, 128 for
+ * the attention, block_size 16), caller-allocated, device:
+ *   k_codes   int8  [num_blocks][num_kv_heads][16][head_dim]   (token rows)
+ *   v_codes   int8  [num_blocks][num_kv_heads][head_dim][16]   (coordinate rows)
+ *   k_scales,
+ *   v_scales  float [num_blocks][num_kv_heads][16]
+ * 132 bytes per (token, KV head, pool) at head_dim 128, against 256 for bf16.
+ */
+
+/*
+ * pkv_append_q8 -- slot-mapped quantizing append: for each token t with
+ * s = slot_mapping[t] >= 0 and each KV head h, row (t, h) of k (bf16
+ * [num_tokens][num_kv_heads][head_dim]) is quantized into k_codes / k_scales at
+ * block s/16, slot s%16, and the same for v. Arguments and errors as
+ * pkv_append (PKV_FLAG_CHECKED validates the slots first).
+ */
+PKV_API pkv_status pkv_append_q8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                                 void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                                 const pkv_cache_desc* desc, uint32_t flags, void* stream);
+
+/*
+ * pkv_copy_blocks_q8 -- copy-on-write block copy of the low-bit pools: codes
+ * and scales of every pair {src, dst}, with pkv_copy_blocks's rules.
+ */
+PKV_API pkv_status pkv_copy_blocks_q8(const int64_t* src_dst_pairs, int64_t num_pairs, void* k_codes,
+                                      void* v_codes, float* k_scales, float* v_scales,
+                                      const pkv_cache_desc* desc, uint32_t flags, void* stream);
+
+/*
+ * pkv_decode_q8_workspace_size -- bytes of workspace pkv_decode_attention_q8
+ * needs (zero-fill once before first use; completed calls leave its counters at
+ * zero). max_query_len as in pkv_multiquery_attention (1 for plain decode).
+ */
+PKV_API size_t pkv_decode_q8_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                            int32_t max_query_len, const pkv_cache_desc* desc,
+                                            const pkv_decode_opts* opts);
+
+/*
+ * pkv_decode_attention_q8 -- decode (or causal multi-query) attention over the
+ * low-bit pools: the result pkv_multiquery_attention (query_start non-NULL) or
+ * pkv_decode_attention (query_start NULL: one query per sequence, a sequence
+ * with no tokens gets a zero row) would give over the values the cached rows
+ * stand for (code * scale). q and out are bf16 as in those calls; fp32
+ * accumulation, one rounding to bf16. The products run on f16 tensor cores:
+ * the codes and q (each row scaled by a power of two) are exact there, the
+ * softmax weights times the V scale are rounded to f16. head_dim 128, at most
+ * 32 query rows per (sequence, KV head). Errors, checked mode and the device
+ * status bits as in pkv_multiquery_attention; query_start NULL with
+ * max_query_len != 1 is PKV_ERR_SHAPE.
+ */
+PKV_API pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes,
+                                           const float* k_scales, const float* v_scales,
+                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                           const int32_t* context_lens, const int32_t* query_start,
+                                           int32_t batch, int32_t num_q_heads, int32_t max_query_len,
+                                           float scale, void* out, void* workspace, size_t workspace_bytes,
+                                           const pkv_cache_desc* desc, uint32_t flags,
+                                           const pkv_decode_opts* opts, void* stream);
 
 /*
  * pkv_decode_attention_noalloc -- pkv_decode_attention without a

@@ -72,6 +72,15 @@ pkv_status run_checked(F launch, cudaStream_t s) {
     return PKV_OK;
 }
 
+pkv_status check_desc_q8(const pkv_cache_desc* d, bool attention) {
+    if (d == nullptr) return PKV_ERR_NULL;
+    if (d->block_size != 16 || d->num_blocks < 1 || d->num_kv_heads < 1) return PKV_ERR_SHAPE;
+    if (d->head_dim != 128 && (attention || d->head_dim != 64)) return PKV_ERR_SHAPE;
+    if (d->dtype != PKV_INT8) return PKV_ERR_DTYPE;
+    if (d->num_blocks * d->num_kv_heads * d->head_dim >= (int64_t(1) << 31)) return PKV_ERR_SHAPE;
+    return PKV_OK;
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -439,6 +448,148 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
         a.lens = context_lens + b0;
         a.qstart = query_start + b0;
         a.out = out;
+        a.partials = reinterpret_cast<float*>(ws + po);
+        a.counters = reinterpret_cast<int*>(ws + co);
+        a.status = status;
+        a.num_blocks = desc->num_blocks;
+        a.max_blocks = max_blocks_per_seq;
+        a.batch = nb;
+        a.q_heads = num_q_heads;
+        a.kv_heads = desc->num_kv_heads;
+        a.head_dim = desc->head_dim;
+        a.group = G;
+        a.num_ctas = num_ctas;
+        a.max_query_len = max_query_len;
+        const int row_groups = (max_query_len * G + 7) / 8;
+        a.wpu = row_groups <= 1 ? 1 : (row_groups <= 2 ? 2 : 4);
+        a.scale = scale;
+        if (launch_multiquery(a, s) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_append_q8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_codes,
+                         void* v_codes, float* k_scales, float* v_scales, const pkv_cache_desc* desc, uint32_t flags,
+                         void* stream) {
+    pkv_status st = check_desc_q8(desc, false);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return PKV_ERR_SHAPE;
+    if (!k_codes || !v_codes || !k_scales || !v_scales) return PKV_ERR_NULL;
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales))
+        return PKV_ERR_ALIGN;
+    if (num_tokens == 0) return PKV_OK;
+    if (k == nullptr || v == nullptr || slot_mapping == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)) return PKV_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    if (flags & PKV_FLAG_CHECKED) {
+        if (num_tokens > 16384) return PKV_ERR_UNSUPPORTED;
+        const int64_t num_slots = desc->num_blocks * 16;
+        st = run_checked([&](unsigned int* verdict) { return launch_check_slots(slot_mapping, num_tokens, num_slots, verdict, s); }, s);
+        if (st != PKV_OK) return st;
+    }
+    return launch_append_q8(k, v, slot_mapping, num_tokens, k_codes, v_codes, k_scales, v_scales, *desc, status, s) ==
+                   cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks_q8(const int64_t* pairs, int64_t num_pairs, void* k_codes, void* v_codes, float* k_scales,
+                              float* v_scales, const pkv_cache_desc* desc, uint32_t flags, void* stream) {
+    pkv_status st = check_desc_q8(desc, false);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0) return PKV_ERR_SHAPE;
+    if (!k_codes || !v_codes || !k_scales || !v_scales) return PKV_ERR_NULL;
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales))
+        return PKV_ERR_ALIGN;
+    if (num_pairs == 0) return PKV_OK;
+    if (pairs == nullptr) return PKV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(pairs) & 7u) return PKV_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    if (flags & PKV_FLAG_CHECKED) {
+        if (num_pairs > 16384) return PKV_ERR_UNSUPPORTED;
+        st = run_checked([&](unsigned int* verdict) { return launch_check_pairs(pairs, num_pairs, desc->num_blocks, verdict, s); }, s);
+        if (st != PKV_OK) return st;
+    }
+    // the code pools move as whole blocks of num_kv_heads * 16 * head_dim bytes (either layout)
+    if (launch_copy_blocks(pairs, num_pairs, k_codes, v_codes, *desc, status, s) != cudaSuccess) return PKV_ERR_CUDA;
+    return launch_copy_scales(pairs, num_pairs, k_scales, v_scales, *desc, status, s) == cudaSuccess ? PKV_OK
+                                                                                                    : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_q8_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                    int32_t max_query_len, const pkv_cache_desc* desc, const pkv_decode_opts* opts) {
+    (void)max_blocks_per_seq;
+    if (check_desc_q8(desc, true) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
+        return 0;
+    const int G = num_q_heads / desc->num_kv_heads;
+    if (max_query_len < 1 || max_query_len * G > kMqMaxRows) return 0;
+    size_t co = 0, po = 0;
+    return mq_workspace_bytes(batch, desc->num_kv_heads, desc->head_dim,
+                              mq_num_ctas(desc->head_dim, batch, opts, true), &co, &po);
+}
+
+pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                                   const float* v_scales, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, const int32_t* query_start, int32_t batch,
+                                   int32_t num_q_heads, int32_t max_query_len, float scale, void* out,
+                                   void* workspace, size_t workspace_bytes, const pkv_cache_desc* desc,
+                                   uint32_t flags, const pkv_decode_opts* opts, void* stream) {
+    pkv_status st = check_desc_q8(desc, true);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
+    if (!isfinite(scale) || max_query_len < 1) return PKV_ERR_SHAPE;
+    if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
+    const int G = num_q_heads / desc->num_kv_heads;
+    if (max_query_len * G > kMqMaxRows) return PKV_ERR_UNSUPPORTED;
+    if (query_start == nullptr && max_query_len != 1) return PKV_ERR_SHAPE;
+    if (flags & PKV_FLAG_TEST_STALL) return PKV_ERR_UNSUPPORTED;
+    if (batch == 0) return PKV_OK;
+    if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
+        return PKV_ERR_SHAPE;
+    if (!q || !k_codes || !v_codes || !k_scales || !v_scales || !block_tables || !context_lens || !out ||
+        !workspace)
+        return PKV_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) ||
+        !aligned16(v_scales) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(context_lens) & 3u) || (reinterpret_cast<uintptr_t>(query_start) & 3u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_ALIGN;
+    const int num_ctas = mq_num_ctas(desc->head_dim, batch, opts, true);
+    size_t co = 0, po = 0;
+    const size_t need = mq_workspace_bytes(batch, desc->num_kv_heads, desc->head_dim, num_ctas, &co, &po);
+    if (workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* status = device_info().status;
+    if (status == nullptr) return PKV_ERR_CUDA;
+    if (flags & PKV_FLAG_CHECKED) {
+        st = run_checked([&](unsigned int* verdict) {
+            cudaError_t e = launch_check_decode(block_tables, max_blocks_per_seq, context_lens, batch,
+                                                desc->num_blocks, verdict, s);
+            if (e != cudaSuccess || query_start == nullptr) return e;
+            return launch_check_queries(context_lens, query_start, batch, max_query_len, verdict, s);
+        }, s);
+        if (st != PKV_OK) return st;
+    }
+    char* ws = static_cast<char*>(workspace);
+    const int64_t row = static_cast<int64_t>(num_q_heads) * desc->head_dim * 2;
+    for (int32_t b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {
+        const int32_t nb = batch - b0 < kMaxBatchPerLaunch ? batch - b0 : kMaxBatchPerLaunch;
+        MqArgs a{};
+        // with query offsets the rows are absolute; without, row i of this launch is sequence b0 + i
+        a.q = query_start ? q : static_cast<const char*>(q) + b0 * row;
+        a.out = query_start ? out : static_cast<char*>(out) + b0 * row;
+        a.qstart = query_start ? query_start + b0 : nullptr;
+        a.k_cache = k_codes;
+        a.v_cache = v_codes;
+        a.k_scales = k_scales;
+        a.v_scales = v_scales;
+        a.q8 = 1;
+        a.tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
+        a.lens = context_lens + b0;
         a.partials = reinterpret_cast<float*>(ws + po);
         a.counters = reinterpret_cast<int*>(ws + co);
         a.status = status;

@@ -923,6 +923,20 @@ bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_di
     return encode_pool_map(map, pool, rows, head_dim);
 }
 
+bool make_map_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                 uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType t = dtype == PKV_INT8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(map, t, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 WorkspaceLayout decode_workspace_layout(int batch, int kv_heads, int num_ctas, int group, int head_dim) {
     const int chunk = batch < kMaxBatchPerLaunch ? batch : kMaxBatchPerLaunch;
     WorkspaceLayout w;

@@ -90,6 +90,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
 // 2-D TMA view of a bf16 pool: rows of head_dim elements (one token of one
 // KV head), 16-row x 64-column boxes, 128-byte swizzle.
 bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim);
+// 2-D TMA view of `rows` rows of `inner` elements (PKV_INT8: uint8, else
+// float32) `row_bytes` apart; boxes of box_inner x box_rows.
+bool make_map_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                 uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 
 // ---------------------------------------------------------------- shared-prefix decode
 // Chunk-first pass: for every group, the queries of all its members against
@@ -142,6 +146,13 @@ cudaError_t launch_check_groups(const int32_t* tables, int32_t max_blocks, const
 
 int device_sm_count();
 
+// ---------------------------------------------------------------- low-bit KV
+cudaError_t launch_append_q8(const void* k, const void* v, const int64_t* slots, int64_t num_tokens, void* k_codes,
+                             void* v_codes, float* k_scales, float* v_scales, const pkv_cache_desc& d,
+                             unsigned int* status, cudaStream_t s);
+cudaError_t launch_copy_scales(const int64_t* pairs, int64_t num_pairs, float* k_scales, float* v_scales,
+                               const pkv_cache_desc& d, unsigned int* status, cudaStream_t s);
+
 // ---------------------------------------------------------------- multi-query decode
 // Several causal queries per sequence; see pkv_multiquery.cu.
 struct MqArgs {
@@ -150,7 +161,8 @@ struct MqArgs {
     const void* v_cache;
     const int32_t* tables;
     const int32_t* lens;
-    const int32_t* qstart;  // [batch + 1]: first query row of each sequence (absolute rows of q / out)
+    const int32_t* qstart;  // [batch + 1]: first query row of each sequence (absolute rows of q / out);
+                            // null: one query per sequence at row i (decode)
     void* out;
     float* partials;        // [num_ctas][2 slots][4 row groups][8 rows][head_dim + 2]
     int* counters;          // [batch][kv_heads][4 row groups]; zero between calls
@@ -166,9 +178,13 @@ struct MqArgs {
     int32_t max_query_len;  // queries per sequence, at most (32 / group)
     int32_t wpu;            // warps per unit: 1, 2 or 4 row groups of 8 (from max_query_len * group)
     float scale;
+    // int8 pools (q8 != 0): k_cache / v_cache are the code pools, with these scales
+    const float* k_scales;
+    const float* v_scales;
+    int32_t q8;
 };
 constexpr int kMqMaxRows = 32;  // query rows per (sequence, KV head)
-int mq_num_ctas(int head_dim, int batch, const pkv_decode_opts* opts);
+int mq_num_ctas(int head_dim, int batch, const pkv_decode_opts* opts, bool q8 = false);
 size_t mq_workspace_bytes(int batch, int kv_heads, int head_dim, int num_ctas, size_t* counters_offset,
                           size_t* partials_offset);
 cudaError_t launch_multiquery(const MqArgs& a, cudaStream_t s);

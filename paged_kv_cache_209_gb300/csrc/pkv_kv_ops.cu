@@ -121,7 +121,7 @@ __global__ void check_decode_kernel(const int32_t* __restrict__ tables, int32_t 
     }
 }
 
-int elem_bytes(int dtype) { return dtype == PKV_BF16 ? 2 : 4; }
+int elem_bytes(int dtype) { return dtype == PKV_BF16 ? 2 : (dtype == PKV_INT8 ? 1 : 4); }
 
 }  // namespace
 

@@ -40,20 +40,44 @@ constexpr int kMqRows = 32;  // query rows per (sequence, KV head): 4 warps x 8
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 
-template <int D, int NST>
+// Blocks whose copies the producer warp issues together (one per lane), a
+// build-time knob per cache type. A TMA instruction costs the issuing warp
+// about a hundred cycles whether one lane or eight issue it, so a producer
+// that issued one block at a time could not keep up with 4 KB int8 blocks.
+#ifndef PKV_MQ_ISSUE_LANES
+#define PKV_MQ_ISSUE_LANES 4
+#endif
+#ifndef PKV_MQ8_ISSUE_LANES
+#define PKV_MQ8_ISSUE_LANES 8
+#endif
+
+template <int D, int NST, bool Q8 = false>
 struct Mq {
+    static constexpr int kIssueLanes = Q8 ? PKV_MQ8_ISSUE_LANES : PKV_MQ_ISSUE_LANES;
     static constexpr int kStages = NST;
     static constexpr int kConsumers = 4;
     static constexpr int kThreads = (kConsumers + 1) * 32;
     static constexpr int kHalves = D / 64;
     static constexpr int kPoolBytes = 16 * D * 2;
-    static constexpr int kStageBytes = 2 * kPoolBytes;  // K then V
+    // bf16: K then V (16 rows x D each). int8: K codes [16][D] at 0, V codes
+    // [D][16] at 16 D; the 16 K scales (at 0) and the 16 V scales (at 128) of
+    // the stage sit in a ring of their own after the stages, 256 bytes per
+    // stage. Every TMA destination is 128-byte aligned (a smaller alignment
+    // faults); stages are 1024-byte aligned (the K swizzle).
+    static constexpr int kStageBytes = Q8 ? 2 * 16 * D : 2 * kPoolBytes;
+    static constexpr int kScaleBytes = Q8 ? 256 : 0;
+    static constexpr int kVScaleOff = 128;
+    static constexpr int kTxBytes = Q8 ? 2 * 16 * D + 128 : kStageBytes;
+    static constexpr int kOffScales = kStages * kStageBytes;
+    static_assert(kStages >= 2 * kIssueLanes && kIssueLanes <= 32, "two groups of issued blocks must fit the ring");
+    static_assert(kOffScales % 1024 == 0 && kScaleBytes % 128 == 0 && kVScaleOff % 128 == 0,
+                  "TMA destinations must stay 128-byte aligned");
     // shared memory (offsets from a 1024-byte aligned base): the ring,
     // full[NST], empty[NST] and the piece barrier, stage flags and the abort
     // flag, the combine scratch (two buffers of 4 warps x 8 rows x (D + 2)
     // floats, alternating between pieces), then per sequence: block prefix
     // sums and context lengths.
-    static constexpr int kOffBars = kStages * kStageBytes;
+    static constexpr int kOffBars = kOffScales + kStages * kScaleBytes;
     static constexpr int kOffFlags = kOffBars + (2 * kStages + 1) * 8;
     static constexpr int kOffScratch = ((kOffFlags + kStages * 4 + 4 + 15) / 16) * 16;
     static constexpr int kScratchFloats = 2 * kConsumers * 8 * (D + 2);
@@ -112,10 +136,56 @@ __device__ void mq_merge(const Piece& pc, const MqArgs& a, long long U, int warp
         *reinterpret_cast<uint32_t*>(orow + d0 + k) = pack_bf16x2(O[k] * inv, O[k + 1] * inv);
 }
 
-template <int D, int NST>
-__global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
-    mq_tc_kernel(const MqArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
-    using C = Mq<D, NST>;
+// Token order of the int8 path: row m of S^T = K Q^T holds token sigma(m), so
+// that the four codes a lane reads from a V coordinate row (tokens 4 tig ..
+// 4 tig + 3) are the P^T k-slots 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 it
+// meets in the PV product.
+__device__ __forceinline__ int sigma(int m) {
+    return m < 8 ? 4 * (m >> 1) + (m & 1) : 4 * ((m - 8) >> 1) + 2 + (m & 1);
+}
+
+// Four int8 codes c (one 32-bit word, lowest byte first) -> two f16x2 pairs
+// (bytes 0, 1) and (bytes 2, 3) holding c + 1152 exactly: the code offset by
+// 128 becomes the low mantissa byte of the f16 1024 + u. Used for K, whose
+// scores are formed afresh for every block: S = S' - 1152 * (query sum), one
+// subtraction per score instead of one per code; the rounding of S' stays
+// within a few fp32 steps of 1152 * sum |q|, below 2^-16 of the largest
+// score the row could reach.
+constexpr float kCodeBias = 1152.f;
+__device__ __forceinline__ void codes_to_f16x2_biased(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    const uint32_t u = w ^ 0x80808080u;
+    p01 = __byte_perm(u, 0x64646464u, 0x5140);
+    p23 = __byte_perm(u, 0x64646464u, 0x5342);
+}
+
+// The same, exact codes c (the bias subtracted in f16). Used for V: the
+// output accumulates over the whole context, so a bias there would let the
+// accumulator's rounding grow with the context length times 1152.
+__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    uint32_t h01, h23;
+    codes_to_f16x2_biased(w, h01, h23);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const __half2 r01 = __hsub2(*reinterpret_cast<const __half2*>(&h01), bias);
+    const __half2 r23 = __hsub2(*reinterpret_cast<const __half2*>(&h23), bias);
+    p01 = *reinterpret_cast<const uint32_t*>(&r01);
+    p23 = *reinterpret_cast<const uint32_t*>(&r23);
+}
+
+__device__ __forceinline__ float f16x2_sum(uint32_t h) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    return f.x + f.y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int D, int NST, bool Q8>
+__global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
+    mq_tc_kernel(const MqArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs) {
+    using C = Mq<D, NST, Q8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
@@ -143,6 +213,10 @@ __global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
     if (threadIdx.x == 32) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        if (Q8) {
+            tma_prefetch_desc(&tmKs);
+            tma_prefetch_desc(&tmVs);
+        }
     }
     grid_dependency_wait();
     allow_dependents();
@@ -151,10 +225,11 @@ __global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
     const int cap = a.max_blocks * 16;
     for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
         int n = a.lens[i];
-        const int q0 = a.qstart[i];
-        int nq = a.qstart[i + 1] - q0;
         bool bad = n < 0 || n > cap;
         n = n < 0 ? 0 : (n > cap ? cap : n);
+        // without query offsets: one query per sequence (row i), none for an empty context
+        const int q0 = a.qstart != nullptr ? a.qstart[i] : i;
+        int nq = a.qstart != nullptr ? a.qstart[i + 1] - q0 : (n > 0 ? 1 : 0);
         if (q0 < 0 || nq < 0 || nq > n || nq > a.max_query_len) {
             bad = true;
             nq = 0;
@@ -179,6 +254,15 @@ __global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
     }
     __syncthreads();
 
+    if (a.qstart == nullptr) {
+        // one query per sequence: an empty context gives a zero row
+        const int row = a.q_heads * D;
+        for (int i = blockIdx.x; i < a.batch; i += a.num_ctas) {
+            if (s_len[i] != 0) continue;
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + static_cast<long long>(i) * row;
+            for (int e = threadIdx.x; e < row; e += blockDim.x) o[e] = __float2bfloat16_rn(0.f);
+        }
+    }
     const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
     const long long cta = blockIdx.x;
     const long long ua = range_start(cta, U, a.num_ctas);
@@ -200,36 +284,55 @@ __global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
                 const int nidx = b0 + 32 + lane;
                 const int nxt = nidx < cnt_piece ? __ldg(trow + nidx) : 0;
                 const int cnt = min(32, cnt_piece - b0);
-                for (int e = 0; e < cnt; ++e, ++k) {
-                    const int bid = __shfl_sync(0xffffffffu, cur, e);
-                    int good = 1;
-                    if (lane == 0) {
-                        const int s = static_cast<int>(k % C::kStages);
-                        const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1) ^ 1u;
-                        if (!mbar_wait(&empty[s], par, a.status, abort_flag)) {
-                            good = 0;
-                        } else if (bid >= 0 && bid < a.num_blocks) {
-                            stage_ok[s] = 1;
-                            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                            uint8_t* st = smem + s * C::kStageBytes;
-                            const int y = (bid * a.kv_heads + pc.head) * 16;
+                // kIssueLanes consecutive blocks at a time, one per lane: each
+                // lane waits for its own stage, then the lanes issue their
+                // copies with the same (non-divergent) instructions, so the
+                // issue cost of a TMA instruction is shared by the group
+                for (int e0 = 0; e0 < cnt; e0 += C::kIssueLanes) {
+                    const int e = e0 + lane;
+                    const bool mine = lane < C::kIssueLanes && e < cnt;
+                    const int bid = __shfl_sync(0xffffffffu, cur, e & 31);
+                    const long long kk = k + lane;
+                    const int s = static_cast<int>(kk % C::kStages);
+                    bool waited = true;
+                    if (mine) {
+                        const uint32_t par = static_cast<uint32_t>((kk / C::kStages) & 1) ^ 1u;
+                        waited = mbar_wait(&empty[s], par, a.status, abort_flag);
+                    }
+                    if (!__all_sync(0xffffffffu, waited)) {  // nothing of this group was issued
+                        ok = false;
+                        break;
+                    }
+                    const bool load = mine && bid >= 0 && bid < a.num_blocks;
+                    if (mine) {
+                        stage_ok[s] = load ? 1 : 0;
+                        if (load) {
+                            mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+                        } else {
+                            atomicOr(a.status, PKV_DEVERR_RANGE);
+                            mbar_arrive(&full[s]);
+                        }
+                    }
+                    if (load) {
+                        uint8_t* st = smem + s * C::kStageBytes;
+                        const int hb = bid * a.kv_heads + pc.head;
+                        if (Q8) {
+                            tma_load_2d(st, &tmK, 0, hb * 16, &full[s], kv_policy);
+                            tma_load_2d(st + 16 * D, &tmV, 0, hb * 16, &full[s], kv_policy);
+                            uint8_t* sc = smem + C::kOffScales + s * C::kScaleBytes;
+                            tma_load_2d(sc, &tmKs, 0, hb, &full[s], kv_policy);
+                            tma_load_2d(sc + C::kVScaleOff, &tmVs, 0, hb, &full[s], kv_policy);
+                        } else {
+                            const int y = hb * 16;
 #pragma unroll
                             for (int hf = 0; hf < C::kHalves; ++hf)
                                 tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
 #pragma unroll
                             for (int hf = 0; hf < C::kHalves; ++hf)
                                 tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
-                        } else {
-                            stage_ok[s] = 0;
-                            atomicOr(a.status, PKV_DEVERR_RANGE);
-                            mbar_arrive(&full[s]);
                         }
                     }
-                    good = __shfl_sync(0xffffffffu, good, 0);
-                    if (!good) {
-                        ok = false;
-                        break;
-                    }
+                    k += min(C::kIssueLanes, cnt - e0);
                 }
                 cur = nxt;
             }
@@ -266,25 +369,66 @@ __global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
     int npending = 0;
     while (wk.next(pc)) {
         const int n_ctx = s_len[pc.seq];
-        const int q0 = a.qstart[pc.seq];
-        const int nq = a.qstart[pc.seq + 1] - q0;  // valid: the sequence has units
+        const int q0 = a.qstart != nullptr ? a.qstart[pc.seq] : pc.seq;
+        const int nq = a.qstart != nullptr ? a.qstart[pc.seq + 1] - q0 : 1;  // valid: the sequence has units
         const int rows = nq * G;
         const bool active = rg * 8 < rows;
         // Q^T fragments: column n = row 8 rg + gid of the row group
         uint32_t qf[D / 16][2];
+        float cf0 = scale_log2, cf1 = scale_log2;  // int8 path: per-column score factors
+        float kb0 = 0.f, kb1 = 0.f;                // int8 path: the code bias times the column's query sum
         {
             const int rr = rg * 8 + gid;
             const bool live = rr < rows;
             const int t = live ? rr / G : 0;
             const __nv_bfloat16* qrow =
                 q + (static_cast<long long>(q0 + t) * a.q_heads + pc.head * G + (live ? rr - t * G : 0)) * D;
-            const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
+            if (!Q8) {
+                const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
 #pragma unroll
-            for (int j = 0; j < D / 16; ++j) {
-                qf[j][0] = live ? __ldg(q32 + (16 * j + 2 * tig) / 2) : 0u;
-                qf[j][1] = live ? __ldg(q32 + (16 * j + 2 * tig + 8) / 2) : 0u;
+                for (int j = 0; j < D / 16; ++j) {
+                    qf[j][0] = live ? __ldg(q32 + (16 * j + 2 * tig) / 2) : 0u;
+                    qf[j][1] = live ? __ldg(q32 + (16 * j + 2 * tig + 8) / 2) : 0u;
+                }
+            } else {
+                // f16 operands: coordinates 4 tig .. 4 tig + 3 of each 16 (the
+                // contraction order of the int8 K fragments), the row scaled by
+                // 2^-e so that its largest magnitude stays below 2^15
+                float qv[D / 16][4];
+                float qmax = 0.f;
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    const uint2 w = live ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * j + 4 * tig)) : make_uint2(0u, 0u);
+                    qv[j][0] = bf16lo_to_f32(w.x);
+                    qv[j][1] = bf16hi_to_f32(w.x);
+                    qv[j][2] = bf16lo_to_f32(w.y);
+                    qv[j][3] = bf16hi_to_f32(w.y);
+                    qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(qv[j][0]), fabsf(qv[j][1])), fmaxf(fabsf(qv[j][2]), fabsf(qv[j][3]))));
+                }
+                qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+                qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+                const int ex = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xffu) - 127;
+                const int e = ex > 14 ? ex - 14 : 0;
+                const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+                const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+                float qsum = 0.f;  // of the f16 operands as rounded
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    qf[j][0] = pack_f16x2(qv[j][0] * down, qv[j][1] * down);
+                    qf[j][1] = pack_f16x2(qv[j][2] * down, qv[j][3] * down);
+                    qsum += f16x2_sum(qf[j][0]) + f16x2_sum(qf[j][1]);
+                }
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+                // S^T columns 2 tig, 2 tig + 1 are the rows held by lanes 8 tig and 8 tig + 4
+                cf0 = __shfl_sync(0xffffffffu, up, 8 * tig) * scale_log2;
+                cf1 = __shfl_sync(0xffffffffu, up, 8 * tig + 4) * scale_log2;
+                kb0 = kCodeBias * __shfl_sync(0xffffffffu, qsum, 8 * tig);
+                kb1 = kCodeBias * __shfl_sync(0xffffffffu, qsum, 8 * tig + 4);
             }
         }
+        const int tokA = sigma(gid), tokB = sigma(gid + 8);  // int8 path: tokens of S^T rows gid, gid + 8
+        const int kq_tok = sigma(r8 + 8 * (q8 & 1));         // int8 path: K token row of this lane's address
         // last visible position of the lane's two columns (rows 2 tig, 2 tig + 1 of the group)
         const int rc0 = rg * 8 + 2 * tig, rc1 = rc0 + 1;
         const int lim0 = rc0 < rows ? n_ctx - nq + rc0 / G : -1;
@@ -294,12 +438,15 @@ __global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-        for (int blk = pc.blk_from; blk < pc.blk_to; ++blk, ++k) {
-            if (static_cast<int>(k % UG) != ul) continue;
+        // this unit lane's blocks of the piece: running block index k = ul (mod UG)
+        const long long k_end = k + (pc.blk_to - pc.blk_from);
+        const int skip = (ul - static_cast<int>(k & (UG - 1))) & (UG - 1);
+        k += skip;
+        for (int blk = pc.blk_from + skip; blk < pc.blk_to; blk += UG, k += UG) {
             const int s = static_cast<int>(k % C::kStages);
             if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag)) return;
             const int valid = min(16, n_ctx - blk * 16);
-            if (stage_ok[s] && active) {
+            if (!Q8 && stage_ok[s] && active) {
                 const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
                 const uint32_t vbase = kbase + C::kPoolBytes;
                 float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -374,9 +521,85 @@ __global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
                     mma_bf16_16816(o[i], a0, a1, a2, a3, bl0, bl1);
                 }
             }
+            if (Q8 && stage_ok[s] && active) {
+                const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
+                const uint32_t vb = kb + 16 * D;
+                const float* ksc = reinterpret_cast<const float*>(smem + C::kOffScales + s * C::kScaleBytes);
+                const float* vsc = ksc + C::kVScaleOff / 4;
+                // ---- S^T = K Q^T on f16 codes: one ldmatrix gives two k-steps
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int jj = 0; jj < D / 32; ++jj) {
+                    const int gc = 2 * jj + (q8 >> 1);
+                    const uint32_t addr = kb + kq_tok * 128 + (((gc & 7) ^ (kq_tok & 7)) << 4);
+                    uint32_t w0, w1, w2, w3;
+                    ldmatrix_x4(addr, w0, w1, w2, w3);
+                    uint32_t a0, a1, a2, a3;
+                    codes_to_f16x2_biased(w0, a0, a2);
+                    codes_to_f16x2_biased(w1, a1, a3);
+                    mma_f16_16816(sa, a0, a1, a2, a3, qf[2 * jj][0], qf[2 * jj][1]);
+                    codes_to_f16x2_biased(w2, a0, a2);
+                    codes_to_f16x2_biased(w3, a1, a3);
+                    mma_f16_16816(sb, a0, a1, a2, a3, qf[2 * jj + 1][0], qf[2 * jj + 1][1]);
+                }
+                // [0] (token tokA, row 2tig) [1] (tokA, 2tig+1) [2] (tokB, 2tig) [3] (tokB, 2tig+1)
+                const int pA = blk * 16 + tokA, pB = blk * 16 + tokB;
+                const float kA = ksc[tokA], kB = ksc[tokB];
+                const float x0 = pA <= lim0 ? (sa[0] + sb[0] - kb0) * kA * cf0 : ninf();
+                const float x1 = pA <= lim1 ? (sa[1] + sb[1] - kb1) * kA * cf1 : ninf();
+                const float x2 = pB <= lim0 ? (sa[2] + sb[2] - kb0) * kB * cf0 : ninf();
+                const float x3 = pB <= lim1 ? (sa[3] + sb[3] - kb1) * kB * cf1 : ninf();
+                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+                if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float nb0 = mn0 == ninf() ? 0.f : mn0;
+                    const float nb1 = mn1 == ninf() ? 0.f : mn1;
+                    const float al0 = m0 == ninf() ? 0.f : ex2(m0 - nb0);
+                    const float al1 = m1 == ninf() ? 0.f : ex2(m1 - nb1);
+                    l0 *= al0;
+                    l1 *= al1;
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        o[i][0] *= al0;
+                        o[i][1] *= al1;
+                        o[i][2] *= al0;
+                        o[i][3] *= al1;
+                    }
+                    m0 = mn0;
+                    m1 = mn1;
+                }
+                const float b0 = m0 == ninf() ? 0.f : m0;
+                const float b1 = m1 == ninf() ? 0.f : m1;
+                const float e0 = ex2(x0 - b0), e1 = ex2(x1 - b1), e2 = ex2(x2 - b0), e3 = ex2(x3 - b1);
+                l0 += e0 + e2;
+                l1 += e1 + e3;
+                // P' = P times the V scale of its token (zero past the context), as f16
+                const float vA = pA < n_ctx ? vsc[tokA] : 0.f, vB = pB < n_ctx ? vsc[tokB] : 0.f;
+                const uint32_t bh0 = movmatrix_trans(pack_f16x2(e0 * vA, e1 * vA));
+                const uint32_t bh1 = movmatrix_trans(pack_f16x2(e2 * vB, e3 * vB));
+                // ---- O^T += V^T P'^T: V coordinate rows of 16 token codes
+#pragma unroll
+                for (int ii = 0; ii < D / 32; ++ii) {
+                    uint32_t w0, w1, w2, w3;
+                    ldmatrix_x4(vb + (32 * ii + 8 * q8 + r8) * 16, w0, w1, w2, w3);
+                    uint32_t a0, a1, a2, a3;
+                    codes_to_f16x2(w0, a0, a2);
+                    codes_to_f16x2(w1, a1, a3);
+                    mma_f16_16816(o[2 * ii], a0, a1, a2, a3, bh0, bh1);
+                    codes_to_f16x2(w2, a0, a2);
+                    codes_to_f16x2(w3, a1, a3);
+                    mma_f16_16816(o[2 * ii + 1], a0, a1, a2, a3, bh0, bh1);
+                }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
+        k = k_end;
         // ---- end of the piece: sums across the token rows of the fragments
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -500,8 +723,10 @@ __global__ void __launch_bounds__(Mq<D, NST>::kThreads, 2)
         if (old != np - 1) continue;
         __threadfence();
         const int slot0 = (pp.seg_start == range_start(c0s, U, Cn)) ? 0 : 1;
-        const int qq0 = a.qstart[pp.seq];
-        mq_merge<D>(pp, a, U, rg, lane, c0s, slot0, np, (a.qstart[pp.seq + 1] - qq0) * G, qq0);
+        // without query offsets: sequence i has its one query in row i
+        const int qq0 = a.qstart != nullptr ? a.qstart[pp.seq] : pp.seq;
+        const int nqq = a.qstart != nullptr ? a.qstart[pp.seq + 1] - qq0 : 1;
+        mq_merge<D>(pp, a, U, rg, lane, c0s, slot0, np, nqq * G, qq0);
         if (lane == 0) *counter = 0;
     }
 }
@@ -514,42 +739,71 @@ int mq_occupancy(K kernel, int threads, size_t smem) {
     return n;
 }
 
-constexpr int kMqStages = 8;
+// Ring depth (a build-time knob): stages of 2 * 16 * D bytes (bf16) or 16 * D
+// bytes (int8 codes) per CTA.
+#ifndef PKV_MQ_STAGES
+#define PKV_MQ_STAGES 8
+#endif
+#ifndef PKV_MQ8_STAGES
+#define PKV_MQ8_STAGES 16
+#endif
+constexpr int kMqStages = PKV_MQ_STAGES;
+constexpr int kMq8Stages = PKV_MQ8_STAGES;
+template <bool Q8>
+constexpr int mq_stages() { return Q8 ? kMq8Stages : kMqStages; }
 
-template <int D>
+template <int D, bool Q8>
 cudaError_t run_mq(const MqArgs& a, int grid, cudaStream_t s) {
-    using C = Mq<D, kMqStages>;
-    CUtensorMap tmK, tmV;
-    const int64_t rows = a.num_blocks * a.kv_heads * 16;
-    if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
-        return cudaErrorInvalidValue;
+    using C = Mq<D, mq_stages<Q8>(), Q8>;
+    CUtensorMap tmK, tmV, tmKs, tmVs;
+    if (Q8) {
+        const uint64_t hb = static_cast<uint64_t>(a.num_blocks) * a.kv_heads;
+        if (!make_map_2d(&tmK, PKV_INT8, a.k_cache, D, hb * 16, D, D, 16, true) ||
+            // the V codes of one (block, head) are D x 16 contiguous bytes: described as 16 rows of D
+            // bytes, one TMA box moves them with 16 row requests instead of D requests of 16 bytes
+            !make_map_2d(&tmV, PKV_INT8, a.v_cache, D, hb * 16, D, D, 16, false) ||
+            !make_map_2d(&tmKs, PKV_F32, a.k_scales, 16, hb, 64, 16, 1, false) ||
+            !make_map_2d(&tmVs, PKV_F32, a.v_scales, 16, hb, 64, 16, 1, false))
+            return cudaErrorInvalidValue;
+    } else {
+        const int64_t rows = a.num_blocks * a.kv_heads * 16;
+        if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
+            return cudaErrorInvalidValue;
+        tmKs = tmK;  // unused by the bf16 path
+        tmVs = tmV;
+    }
     const size_t smem = C::smem_bytes(a.batch);
-    cudaFuncSetAttribute(mq_tc_kernel<D, kMqStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(mq_tc_kernel<D, mq_stages<Q8>(), Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
-    return launch_pdl(mq_tc_kernel<D, kMqStages>, dim3(grid), dim3(C::kThreads), smem, s, a, tmK, tmV);
+    return launch_pdl(mq_tc_kernel<D, mq_stages<Q8>(), Q8>, dim3(grid), dim3(C::kThreads), smem, s, a, tmK, tmV, tmKs,
+                      tmVs);
 }
 
 }  // namespace
 
-int mq_num_ctas(int head_dim, int batch, const pkv_decode_opts* opts) {
+int mq_num_ctas(int head_dim, int batch, const pkv_decode_opts* opts, bool q8) {
     if (opts && opts->num_ctas > 0) return opts->num_ctas;
     static std::mutex mu;
-    static int cache[2][64] = {};
+    static int cache[3][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    const int b = batch < kMaxBatchPerLaunch ? (batch < 1 ? 1 : batch) : kMaxBatchPerLaunch;
+    (void)batch;
     std::lock_guard<std::mutex> lock(mu);
-    int& slot = cache[head_dim == 128 ? 1 : 0][dev];
+    const int which = q8 ? 2 : (head_dim == 128 ? 1 : 0);
+    int& slot = cache[which][dev];
     if (slot == 0) {
         // occupancy at the largest launch (the per-sequence arrays grow with the batch)
-        slot = head_dim == 128
-                   ? mq_occupancy(mq_tc_kernel<128, kMqStages>, Mq<128, kMqStages>::kThreads,
-                                  Mq<128, kMqStages>::smem_bytes(kMaxBatchPerLaunch))
-                   : mq_occupancy(mq_tc_kernel<64, kMqStages>, Mq<64, kMqStages>::kThreads,
-                                  Mq<64, kMqStages>::smem_bytes(kMaxBatchPerLaunch));
+        if (q8)
+            slot = mq_occupancy(mq_tc_kernel<128, kMq8Stages, true>, Mq<128, kMq8Stages, true>::kThreads,
+                                Mq<128, kMq8Stages, true>::smem_bytes(kMaxBatchPerLaunch));
+        else if (head_dim == 128)
+            slot = mq_occupancy(mq_tc_kernel<128, kMqStages, false>, Mq<128, kMqStages>::kThreads,
+                                Mq<128, kMqStages>::smem_bytes(kMaxBatchPerLaunch));
+        else
+            slot = mq_occupancy(mq_tc_kernel<64, kMqStages, false>, Mq<64, kMqStages>::kThreads,
+                                Mq<64, kMqStages>::smem_bytes(kMaxBatchPerLaunch));
     }
-    (void)b;
     return slot * device_sm_count();
 }
 
@@ -582,7 +836,8 @@ cudaError_t launch_check_queries(const int32_t* lens, const int32_t* qstart, int
 }
 
 cudaError_t launch_multiquery(const MqArgs& a, cudaStream_t s) {
-    return a.head_dim == 128 ? run_mq<128>(a, a.num_ctas, s) : run_mq<64>(a, a.num_ctas, s);
+    if (a.q8) return run_mq<128, true>(a, a.num_ctas, s);
+    return a.head_dim == 128 ? run_mq<128, false>(a, a.num_ctas, s) : run_mq<64, false>(a, a.num_ctas, s);
 }
 
 }  // namespace pkv

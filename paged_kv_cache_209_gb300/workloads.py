@@ -21,6 +21,11 @@ Workloads (named by what they are; all use 16-token blocks):
 * ``spec4``        -- the ``llama8k`` layer verifying 4 draft tokens per
   sequence: every context 8192 tokens including the 4 new ones, 4 causal
   queries per sequence, tables a permutation (seed 5) of a 16384-block pool.
+* ``llama8k_q8``   -- the ``llama8k`` layer over an int8 cache: K codes
+  ``[blocks][8][16][128]``, V codes ``[blocks][8][128][16]``, float32 scales
+  ``[blocks][8][16]`` per pool; codes a rounded normal of standard deviation
+  42 clipped to +-127, scales uniform on [0.02, 0.03] (the range per-row
+  scales of standard-normal rows fall in), tables a permutation (seed 6).
 
 Values are standard normal. Large tensors are drawn on the device with a
 seeded ``torch.Generator``; the oracle reads the same tensors back, so
@@ -48,6 +53,8 @@ CONFIGS = {
                    prefix=4096, min_suffix=1, max_suffix=2048, seed=4),
     "spec4": dict(batch=32, q_heads=32, kv_heads=8, head_dim=128, dtype="bf16",
                   context=8192, num_blocks=16384, queries=4, seed=5),
+    "llama8k_q8": dict(batch=32, q_heads=32, kv_heads=8, head_dim=128, dtype="int8",
+                       context=8192, num_blocks=16384, seed=6),
 }
 
 
@@ -120,6 +127,21 @@ def torch_normal(shape, seed: int, dtype, device):
     return torch.randn(tuple(shape), generator=gen, device=device, dtype=torch.float32).to(dtype)
 
 
+def int8_codes(shape, seed: int, device):
+    """Rounded normal draws of standard deviation 42, clipped to [-127, 127], as int8."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(seed)
+    x = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32) * 42.0
+    return x.round().clamp_(-127, 127).to(torch.int8)
+
+
+def uniform(shape, lo: float, hi: float, seed: int, device):
+    """float32 draws uniform on [lo, hi)."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(seed)
+    return torch.rand(tuple(shape), generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
+
+
 def workload_index(name: str):
     """Index metadata of a named workload: ``(tables int32, lens int64, num_blocks)``.
 
@@ -128,7 +150,7 @@ def workload_index(name: str):
     """
     cfg = CONFIGS[name]
     B = cfg["batch"]
-    if name in ("llama8k", "long128k", "spec4"):
+    if name in ("llama8k", "long128k", "spec4", "llama8k_q8"):
         lens = np.full(B, cfg["context"], dtype=np.int64)
         tables = permuted_tables(cfg["num_blocks"], B, cfg["context"] // BLOCK_SIZE, cfg["seed"])
         num_blocks = cfg["num_blocks"]
@@ -166,7 +188,7 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
     import torch
 
     cfg = CONFIGS[name]
-    bf = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    bf = torch.float32 if cfg["dtype"] == "f32" else torch.bfloat16   # int8 pools take bf16 q and new rows
     B, HQ, HKV, D = cfg["batch"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
     nq = cfg.get("queries", 1)
     seed = cfg["seed"] + seed_offset
@@ -177,10 +199,16 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
     # shared-prefix groups: the prefix workload is one group over its shared blocks
     n_shared = cfg.get("prefix", 0) // BLOCK_SIZE
     group = np.zeros(B, dtype=np.int32) if n_shared else np.full(B, -1, dtype=np.int32)
+    if cfg["dtype"] == "int8":
+        pools = dict(k_pool=int8_codes((num_blocks, HKV, BLOCK_SIZE, D), seed, device),
+                     v_pool=int8_codes((num_blocks, HKV, D, BLOCK_SIZE), seed + 1, device),
+                     k_scales=uniform((num_blocks, HKV, BLOCK_SIZE), 0.02, 0.03, seed + 5, device),
+                     v_scales=uniform((num_blocks, HKV, BLOCK_SIZE), 0.02, 0.03, seed + 6, device))
+    else:
+        pools = dict(k_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed, bf, device),
+                     v_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed + 1, bf, device))
     return dict(
-        name=name, cfg=cfg, num_blocks=num_blocks,
-        k_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed, bf, device),
-        v_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed + 1, bf, device),
+        name=name, cfg=cfg, num_blocks=num_blocks, **pools,
         q=torch_normal((B * nq, HQ, D), seed + 2, bf, device),
         k_new=torch_normal((B * nq, HKV, D), seed + 3, bf, device),
         v_new=torch_normal((B * nq, HKV, D), seed + 4, bf, device),

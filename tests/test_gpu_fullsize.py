@@ -183,3 +183,38 @@ def test_spec4_workload_multiquery(pkv):
                                        w["lens"] - (nq - 1 - t), w["scale"])
         d = out[t::nq].float() - ref.float()
         assert d.abs().max().item() <= 1e-2 and (d.norm() / ref.float().norm()).item() <= 2e-3, t
+
+
+def test_llama8k_q8_workload(pkv):
+    """The 8K Llama layer over an int8 cache, as the benchmark runs it: the
+    quantizing append of the step's 32 tokens (whole pools bit-exact against
+    the oracle's append) and one decode call; sampled (sequence, KV head)
+    pairs against the float64 oracle over the values the cache stands for."""
+    from oracle import quant as OQ
+    w = W.device_workload("llama8k_q8", torch.device("cuda", 0))
+    cfg = w["cfg"]
+    kv_heads = cfg["kv_heads"]
+    G = cfg["q_heads"] // kv_heads
+    hkc, hvc = w["k_pool"].cpu().numpy(), w["v_pool"].cpu().numpy()
+    hks, hvs = w["k_scales"].cpu().numpy(), w["v_scales"].cpu().numpy()
+    kn = OA.bf16_bits_to_f64(cases.host_view(w["k_new"]))
+    vn = OA.bf16_bits_to_f64(cases.host_view(w["v_new"]))
+    # the V pool is stored [block][head][d][16]; the oracle writes token rows through a transposed view
+    OQ.append_tokens_q8(hkc, hvc.transpose(0, 1, 3, 2), hks, hvs, kn, vn, w["slots_np"])
+    pkv.pkv_append_q8(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"], w["k_scales"], w["v_scales"])
+    out = pkv.pkv_decode_attention_q8(w["q"], w["k_pool"], w["v_pool"], w["k_scales"], w["v_scales"], w["tables"],
+                                      w["lens"], w["scale"])
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert np.array_equal(w["k_pool"].cpu().numpy(), hkc) and np.array_equal(w["v_pool"].cpu().numpy(), hvc)
+    assert np.array_equal(w["k_scales"].cpu().numpy(), hks) and np.array_equal(w["v_scales"].cpu().numpy(), hvs)
+    qh = cases.host_view(w["q"])
+    for (i, j) in sample_pairs(w["lens_np"], kv_heads, 4, 29):
+        n = int(w["lens_np"][i])
+        blocks = w["tables_np"][i, :(n + 15) // 16]
+        sub = np.arange(len(blocks))[None, :]
+        want = OQ.decode_attention_q8(qh[i:i + 1], hkc[blocks], hvc[blocks].transpose(0, 1, 3, 2), hks[blocks],
+                                      hvs[blocks], sub, w["lens_np"][i:i + 1], w["scale"], kv_heads, "bf16")
+        ma, rl = cases.attention_errors(out[i:i + 1, j * G:(j + 1) * G], want[:, j * G:(j + 1) * G])
+        assert ma <= MAX_ABS and rl <= REL_L2, (i, j, ma, rl)
+    assert bool(torch.isfinite(out.float()).all())
