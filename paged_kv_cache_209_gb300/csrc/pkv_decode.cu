@@ -368,6 +368,12 @@ __device__ void zero_empty_rows(const int32_t* s_len, const int32_t* s_boff, con
 // Tensor-core kernel configuration. NST is the depth of the shared-memory ring
 // (blocks in flight per CTA); the host picks the deepest ring that still fits
 // two CTAs per SM.
+// Most blocks the producer warp issues in one batch (one per lane).
+#ifndef PKV_TC_ISSUE_LANES
+#define PKV_TC_ISSUE_LANES 4
+#endif
+constexpr int kTcIssueLanes = PKV_TC_ISSUE_LANES;
+
 template <int D, int NST>
 struct Tc {
     static constexpr int kStages = NST;
@@ -377,6 +383,7 @@ struct Tc {
     // stage two phases ahead of its last use, and a parity wait cannot tell
     // those phases apart.
     static_assert(kStages % kConsumers == 0, "ring depth must be a multiple of the consumer warps");
+    static_assert(kStages >= kTcIssueLanes && kTcIssueLanes < 32, "a batch of issued blocks must fit the ring");
     static constexpr int kThreads = (kConsumers + 1) * 32;
     static constexpr int kHalves = D / 64;                  // 64-column TMA boxes per row
     static constexpr int kPoolBytes = 16 * D * 2;           // one block, one head, one pool
@@ -466,37 +473,53 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
                 const int nidx = b0 + 32 + lane;
                 const int nxt = nidx < cnt_piece ? __ldg(trow + nidx) : 0;
                 const int cnt = min(32, cnt_piece - b0);
-                for (int e = 0; e < cnt; ++e, ++k) {
-                    const int bid = __shfl_sync(0xffffffffu, cur, e);
-                    int good = 1;
-                    if (lane == 0) {
-                        const int s = static_cast<int>(k % C::kStages);
-                        const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1) ^ 1u;
-                        if (!mbar_wait(&empty[s], par, a.status, abort_flag)) {
-                            good = 0;
-                        } else if (bid >= 0 && bid < a.num_blocks) {
-                            stage_ok[s] = 1;
+                // In order, in batches: lane i probes (without blocking) the
+                // stage of block e0 + i; the run of free stages from the first
+                // is issued at once, one block per lane with the same
+                // instructions (a TMA instruction costs the warp about the
+                // same for one lane as for several). Only when the first
+                // stage is busy does the warp wait (bounded), for that one.
+                for (int e0 = 0; e0 < cnt;) {
+                    const int e = e0 + lane;
+                    const long long kk = k + lane;
+                    const int s = static_cast<int>(kk % C::kStages);
+                    const uint32_t par = static_cast<uint32_t>((kk / C::kStages) & 1) ^ 1u;
+                    const bool probe = lane < kTcIssueLanes && e < cnt && mbar_test_wait(&empty[s], par);
+                    int n = __ffs(~__ballot_sync(0xffffffffu, probe)) - 1;
+                    if (n == 0) {
+                        bool waited = true;
+                        if (lane == 0) waited = mbar_wait(&empty[s], par, a.status, abort_flag);
+                        if (!__shfl_sync(0xffffffffu, waited, 0)) {  // nothing of this batch was issued
+                            ok = false;
+                            break;
+                        }
+                        n = 1;
+                    }
+                    const int bid = __shfl_sync(0xffffffffu, cur, e & 31);
+                    const bool mine = lane < n;
+                    const bool load = mine && bid >= 0 && bid < a.num_blocks;
+                    if (mine) {
+                        stage_ok[s] = load ? 1 : 0;
+                        if (load) {
                             mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                            uint8_t* st = smem + s * C::kStageBytes;
-                            const int y = (bid * a.kv_heads + pc.head) * 16;
-#pragma unroll
-                            for (int hf = 0; hf < C::kHalves; ++hf)
-                                tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
-#pragma unroll
-                            for (int hf = 0; hf < C::kHalves; ++hf)
-                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
-                            if (k == 0) PKV_STAMP(a, blockIdx.x, 2);
                         } else {
-                            stage_ok[s] = 0;
                             atomicOr(a.status, PKV_DEVERR_RANGE);
                             mbar_arrive(&full[s]);
                         }
                     }
-                    good = __shfl_sync(0xffffffffu, good, 0);
-                    if (!good) {
-                        ok = false;
-                        break;
+                    if (load) {
+                        uint8_t* st = smem + s * C::kStageBytes;
+                        const int y = (bid * a.kv_heads + pc.head) * 16;
+#pragma unroll
+                        for (int hf = 0; hf < C::kHalves; ++hf)
+                            tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
+#pragma unroll
+                        for (int hf = 0; hf < C::kHalves; ++hf)
+                            tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
+                        if (kk == 0) PKV_STAMP(a, blockIdx.x, 2);
                     }
+                    k += n;
+                    e0 += n;
                 }
                 cur = nxt;
             }

@@ -40,8 +40,8 @@ constexpr int kMqRows = 32;  // query rows per (sequence, KV head): 4 warps x 8
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 
-// Blocks whose copies the producer warp issues together (one per lane), a
-// build-time knob per cache type. A TMA instruction costs the issuing warp
+// Most blocks whose copies the producer warp issues together (one per lane),
+// a build-time knob per cache type. A TMA instruction costs the issuing warp
 // about a hundred cycles whether one lane or eight issue it, so a producer
 // that issued one block at a time could not keep up with 4 KB int8 blocks.
 #ifndef PKV_MQ_ISSUE_LANES
@@ -69,7 +69,7 @@ struct Mq {
     static constexpr int kVScaleOff = 128;
     static constexpr int kTxBytes = Q8 ? 2 * 16 * D + 128 : kStageBytes;
     static constexpr int kOffScales = kStages * kStageBytes;
-    static_assert(kStages >= 2 * kIssueLanes && kIssueLanes <= 32, "two groups of issued blocks must fit the ring");
+    static_assert(kStages >= kIssueLanes && kIssueLanes < 32, "a batch of issued blocks must fit the ring");
     static_assert(kOffScales % 1024 == 0 && kScaleBytes % 128 == 0 && kVScaleOff % 128 == 0,
                   "TMA destinations must stay 128-byte aligned");
     // shared memory (offsets from a 1024-byte aligned base): the ring,
@@ -284,25 +284,31 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                 const int nidx = b0 + 32 + lane;
                 const int nxt = nidx < cnt_piece ? __ldg(trow + nidx) : 0;
                 const int cnt = min(32, cnt_piece - b0);
-                // kIssueLanes consecutive blocks at a time, one per lane: each
-                // lane waits for its own stage, then the lanes issue their
-                // copies with the same (non-divergent) instructions, so the
-                // issue cost of a TMA instruction is shared by the group
-                for (int e0 = 0; e0 < cnt; e0 += C::kIssueLanes) {
+                // In order, but in batches: each lane probes (without
+                // blocking) the stage of one of the next kIssueLanes blocks,
+                // and the longest run of free stages from the first is issued
+                // at once, one block per lane with the same instructions (a
+                // TMA instruction costs the warp about the same whether one
+                // lane issues it or eight). Only when the first stage is busy
+                // does the warp wait (bounded), for that one.
+                for (int e0 = 0; e0 < cnt;) {
                     const int e = e0 + lane;
-                    const bool mine = lane < C::kIssueLanes && e < cnt;
-                    const int bid = __shfl_sync(0xffffffffu, cur, e & 31);
                     const long long kk = k + lane;
                     const int s = static_cast<int>(kk % C::kStages);
-                    bool waited = true;
-                    if (mine) {
-                        const uint32_t par = static_cast<uint32_t>((kk / C::kStages) & 1) ^ 1u;
-                        waited = mbar_wait(&empty[s], par, a.status, abort_flag);
+                    const uint32_t par = static_cast<uint32_t>((kk / C::kStages) & 1) ^ 1u;
+                    const bool probe = lane < C::kIssueLanes && e < cnt && mbar_test_wait(&empty[s], par);
+                    int n = __ffs(~__ballot_sync(0xffffffffu, probe)) - 1;  // free stages from the first on
+                    if (n == 0) {
+                        bool waited = true;
+                        if (lane == 0) waited = mbar_wait(&empty[s], par, a.status, abort_flag);
+                        if (!__shfl_sync(0xffffffffu, waited, 0)) {  // nothing of this batch was issued
+                            ok = false;
+                            break;
+                        }
+                        n = 1;
                     }
-                    if (!__all_sync(0xffffffffu, waited)) {  // nothing of this group was issued
-                        ok = false;
-                        break;
-                    }
+                    const int bid = __shfl_sync(0xffffffffu, cur, e & 31);
+                    const bool mine = lane < n;
                     const bool load = mine && bid >= 0 && bid < a.num_blocks;
                     if (mine) {
                         stage_ok[s] = load ? 1 : 0;
@@ -332,7 +338,8 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                                 tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
                         }
                     }
-                    k += min(C::kIssueLanes, cnt - e0);
+                    k += n;
+                    e0 += n;
                 }
                 cur = nxt;
             }
