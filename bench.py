@@ -421,16 +421,38 @@ def run_pkv(args, cfg):
     dec_avg_ms = max_over_ranks(sum(dec_ms) / len(dec_ms), ws, device)
     status_bits = pkv.pkv_device_status(clear=False)
 
-    # -------- end-to-end: per-step inputs from pinned host memory, result back to the host
-    devs = [q, kn, vn, slots, tables, lens] + ([group, gblocks] if two_phase else []) + ([qstart] if nq > 1 else [])
-    pins = [t.cpu().pin_memory() for t in devs]
+    # -------- end-to-end: per-step inputs from pinned host memory, result back to the host.
+    # The step's inputs live in one pinned host buffer and one device buffer
+    # (256-byte aligned slices), so a step costs one host-to-device copy, the
+    # kernels (which read the device slices) and one device-to-host copy.
+    names = ["q", "kn", "vn", "slots", "tables", "lens"] + (["group", "gblocks"] if two_phase else []) \
+        + (["qstart"] if nq > 1 else [])
+    srcs = {"q": q, "kn": kn, "vn": vn, "slots": slots, "tables": tables, "lens": lens, "group": group,
+            "gblocks": gblocks, "qstart": qstart}
+    offs, total = {}, 0
+    for n in names:
+        offs[n] = total
+        total += (srcs[n].numel() * srcs[n].element_size() + 255) // 256 * 256
+    pack_dev = torch.zeros(total, dtype=torch.uint8, device=device)
+    pack_host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    views = {}
+    for n in names:
+        t = srcs[n]
+        nb = t.numel() * t.element_size()
+        views[n] = pack_dev[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+        views[n].copy_(t)
+        pack_host[offs[n]:offs[n] + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+    q, kn, vn, slots, tables, lens = (views[n] for n in ["q", "kn", "vn", "slots", "tables", "lens"])
+    if two_phase:
+        group, gblocks = views["group"], views["gblocks"]
+    if nq > 1:
+        qstart = views["qstart"]
     out_pin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in pins)
+    h2d = total
     d2h = out_pin.numel() * out_pin.element_size()
 
     def e2e_step():
-        for dst, src in zip(devs, pins):
-            dst.copy_(src, non_blocking=True)
+        pack_dev.copy_(pack_host, non_blocking=True)
         step()
         out_pin.copy_(out, non_blocking=True)
 

@@ -456,17 +456,21 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
             if (!Q8 && stage_ok[s] && active) {
                 const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
                 const uint32_t vbase = kbase + C::kPoolBytes;
-                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                // four independent accumulator chains over the k-steps
+                float sc4[4][4] = {};
 #pragma unroll
                 for (int j = 0; j < D / 16; ++j) {
                     const int gc = 2 * j + k_chunk;
                     const uint32_t addr = kbase + (gc >> 3) * 2048 + k_row * 128 + (((gc & 7) ^ r8) << 4);
                     uint32_t a0, a1, a2, a3;
                     ldmatrix_x4(addr, a0, a1, a2, a3);
-                    if (j & 1)
-                        mma_bf16_16816(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
-                    else
-                        mma_bf16_16816(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+                    mma_bf16_16816(sc4[j & 3], a0, a1, a2, a3, qf[j][0], qf[j][1]);
+                }
+                float sa[4], sb[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sa[e] = sc4[0][e] + sc4[2][e];
+                    sb[e] = sc4[1][e] + sc4[3][e];
                 }
                 // [0] (token gid, row 2tig) [1] (gid, 2tig+1) [2] (gid+8, 2tig) [3] (gid+8, 2tig+1)
                 const int p0 = blk * 16 + gid, p1 = p0 + 8;
@@ -534,7 +538,8 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                 const float* ksc = reinterpret_cast<const float*>(smem + C::kOffScales + s * C::kScaleBytes);
                 const float* vsc = ksc + C::kVScaleOff / 4;
                 // ---- S^T = K Q^T on f16 codes: one ldmatrix gives two k-steps
-                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                // four independent accumulator chains over the k-steps
+                float sc4[4][4] = {};
 #pragma unroll
                 for (int jj = 0; jj < D / 32; ++jj) {
                     const int gc = 2 * jj + (q8 >> 1);
@@ -544,10 +549,16 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                     uint32_t a0, a1, a2, a3;
                     codes_to_f16x2_biased(w0, a0, a2);
                     codes_to_f16x2_biased(w1, a1, a3);
-                    mma_f16_16816(sa, a0, a1, a2, a3, qf[2 * jj][0], qf[2 * jj][1]);
+                    mma_f16_16816(sc4[(2 * jj) & 3], a0, a1, a2, a3, qf[2 * jj][0], qf[2 * jj][1]);
                     codes_to_f16x2_biased(w2, a0, a2);
                     codes_to_f16x2_biased(w3, a1, a3);
-                    mma_f16_16816(sb, a0, a1, a2, a3, qf[2 * jj + 1][0], qf[2 * jj + 1][1]);
+                    mma_f16_16816(sc4[(2 * jj + 1) & 3], a0, a1, a2, a3, qf[2 * jj + 1][0], qf[2 * jj + 1][1]);
+                }
+                float sa[4], sb[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sa[e] = sc4[0][e] + sc4[2][e];
+                    sb[e] = sc4[1][e] + sc4[3][e];
                 }
                 // [0] (token tokA, row 2tig) [1] (tokA, 2tig+1) [2] (tokB, 2tig) [3] (tokB, 2tig+1)
                 const int pA = blk * 16 + tokA, pB = blk * 16 + tokB;
