@@ -183,3 +183,24 @@ def test_host_rejections(pkv):
     with pytest.raises(pkv.PkvError) as e:
         run_q8(pkv, c64)                                      # the attention is head_dim 128 only
     assert e.value.name == "PKV_ERR_SHAPE"
+
+
+def test_bad_block_id_and_checked_mode(pkv):
+    """A block id outside the pool is never loaded: the call sets
+    PKV_DEVERR_RANGE and the rows of the other sequences stay right; checked
+    mode rejects the call before anything is written."""
+    c = q8_case(21, [60, 45, 100], 32, 8)
+    nb = c["kc"].shape[0]
+    bad = dict(c, tables=c["tables"].copy())
+    bad["tables"][1, 1] = nb + 7                               # sequence 1, its second block
+    out = run_q8(pkv, bad)
+    assert pkv.pkv_device_status(clear=True) & 2
+    ref = want_q8(c)
+    check(out[[0, 2]], ref[[0, 2]])
+    dev = torch.device("cuda", 0)
+    out2 = torch.full((3, 32, 128), 5.0, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pkv.PkvError) as e:
+        run_q8(pkv, bad, out=out2, flags=pkv.PKV_FLAG_CHECKED)
+    assert e.value.name == "PKV_ERR_RANGE"
+    assert bool((out2 == 5.0).all())
+    assert pkv.pkv_device_status(clear=True) == 0
