@@ -61,6 +61,7 @@ WORKLOAD_NAMES = {
     "prefix": "4096-token prefix shared by all sequences + private suffixes uniform in [1, 2048]",
     "spec4": "Llama-3-8B decode layer verifying 4 draft tokens per sequence (causal multi-query), context 8192",
     "llama8k_q8": "Llama-3-8B decode layer over an int8 KV cache (per-row float32 scales), every context 8192 tokens",
+    "prefill512": "chunked prefill on the Llama-3-8B layer: 512 causal queries per sequence, context 8192",
 }
 L2_NOTE = {
     "llama8k": "inputs larger than L2 (1 GiB K+V per step)",
@@ -70,6 +71,7 @@ L2_NOTE = {
               "sequence, so logical GB/s can exceed HBM bandwidth",
     "spec4": "inputs larger than L2 (1 GiB K+V per step, read once for the 4 queries of each sequence)",
     "llama8k_q8": "inputs larger than L2 (0.55 GB of K+V codes and scales per step)",
+    "prefill512": "K+V 0.27 GB (larger than L2); the 16 query tiles of a sequence re-read its K/V, mostly from L2",
 }
 
 
@@ -189,10 +191,12 @@ def profiled_traffic(summary, files=("pkv_decode.cu",)):
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
-def oracle_sample_rate(q, kp, vp, tables, lens, scale, kv_heads, pairs, time_budget_s=None, nq=1):
+def oracle_sample_rate(q, kp, vp, tables, lens, scale, kv_heads, pairs, time_budget_s=None, nq=1, q_sample=None):
     """Run the float64 oracle on (seq, kv_head) pairs; returns (bytes, seconds, pairs done).
     With nq > 1 queries per sequence (rows i*nq .. i*nq+nq-1 of q), the
-    multi-query oracle runs on whole sequences (all KV heads) instead."""
+    multi-query oracle runs on whole sequences (all KV heads) instead; with
+    q_sample, on the last q_sample queries of each (they see the same tokens as
+    in the full call), credited with that fraction of the sequence's bytes."""
     from oracle import attention as OA
     from oracle import multiquery as OM
     done, nbytes = 0, 0
@@ -201,9 +205,10 @@ def oracle_sample_rate(q, kp, vp, tables, lens, scale, kv_heads, pairs, time_bud
         if nq > 1:
             if j:
                 continue
-            OM.multiquery_attention(q[i * nq:(i + 1) * nq], kp, vp, tables[i:i + 1], lens[i:i + 1],
-                                    np.array([0, nq]), scale, kv_heads, "bf16")
-            nbytes += int(lens[i]) * 2 * kv_heads * kp.shape[-1] * 2
+            ns = nq if q_sample is None else min(q_sample, nq)
+            OM.multiquery_attention(q[(i + 1) * nq - ns:(i + 1) * nq], kp, vp, tables[i:i + 1], lens[i:i + 1],
+                                    np.array([0, ns]), scale, kv_heads, "bf16")
+            nbytes += int(lens[i]) * 2 * kv_heads * kp.shape[-1] * 2 * ns // nq
         else:
             OA.decode_attention_pair(q, kp, vp, tables, lens, scale, i, j, kv_heads, "bf16")
             nbytes += int(lens[i]) * 2 * kp.shape[-1] * 2
@@ -508,7 +513,22 @@ def run_pkv(args, cfg):
     unique_kvb = (kv_tokens - shared_tokens) * tok_bytes
     alg_bytes = unique_kvb + q.numel() * q.element_size() + out.numel() * out.element_size() + used_entries * 4 + B * 4
     achieved = alg_bytes / (dec_avg_ms * 1e-3) / 1e9
-    if two_phase:
+    # chunked prefill (more than 32 query rows per KV head) runs on the
+    # tensor-core tile kernel: a dense contraction, so its roofline is tensor
+    # throughput. Algorithmic FLOPs: 4 D per (query row, visible token)
+    # (2 D for q.k, 2 D for p.v), summed over the causal triangle.
+    prefill = nq * (HQ // HKV) > 32
+    if prefill:
+        vis = sum(int(n) * nq - nq * (nq - 1) // 2 for n in lens_np)   # sum over t of (n - nq + t + 1)
+        alg_flops = vis * HQ * D * 4
+        tflops = alg_flops / (dec_avg_ms * 1e-3) / 1e12
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+            os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        t_peak = float(peaks.get("bf16_tflops", 1900.0))
+        t_kind = "measured (cuBLAS bf16 burst)" if "bf16_tflops" in peaks else "fallback"
+    if prefill:
+        traffic = profiled_traffic(f"decode_{args.workload}", ("pkv_prefix.cu",))
+    elif two_phase:
         traffic = profiled_traffic("decode_prefix_two_phase", ("pkv_decode.cu", "pkv_prefix.cu"))
     elif q8 or nq > 1:
         traffic = profiled_traffic(f"decode_{args.workload}", ("pkv_multiquery.cu",))
@@ -525,8 +545,12 @@ def run_pkv(args, cfg):
     else:
         qh, kph, vph, th, lh = cpu_sample_data(k_pool, v_pool, q, tables_np, lens_np, sample_seqs, nq)
         pairs_list = [(i, j) for i in range(len(sample_seqs)) for j in range(HKV)]
-        cb, cs, cdone = oracle_sample_rate(qh, kph, vph, th, lh, scale, HKV, pairs_list, time_budget_s=20.0, nq=nq)
+        qsamp = 8 if prefill else None
+        cb, cs, cdone = oracle_sample_rate(qh, kph, vph, th, lh, scale, HKV, pairs_list, time_budget_s=20.0, nq=nq,
+                                           q_sample=qsamp)
         cpu_what = (f"{cdone} (sequence, KV head) pairs of sequences {sample_seqs}, " if nq == 1
+                    else f"the last {qsamp} of the {nq} queries of {cdone} sequences of {sample_seqs} "
+                         "(bytes credited in proportion), " if prefill
                     else f"{cdone} whole sequences of {sample_seqs} ({nq} queries each), ")
     cpu_gbs = cb / cs / 1e9
 
@@ -543,14 +567,22 @@ def run_pkv(args, cfg):
                               else "shared-prefix decode attention (two phases)" if two_phase
                               else f"causal multi-query attention ({nq} queries per sequence)" if nq > 1
                               else "decode attention"),
-                   "kernel": ("tensor-core split-context kernel on int8 codes (exact in f16), per-row scales "
+                   "kernel": ("tcgen05 tile kernel: 128 query rows per tile, S and O in tensor memory, the "
+                              "context split over a thread-block cluster combined through distributed shared "
+                              "memory" if prefill else
+                              "tensor-core split-context kernel on int8 codes (exact in f16), per-row scales "
                               "applied to S and folded into P, merge fused" if q8 else
                               "tensor-core split-context kernel, merge fused"
                               + (", then the chunk-first pass over the shared blocks" if two_phase else ""))},
         "hbm_frac": round(value / peak, 4),
         "unique_kv_gbs": round(unique_kvb * ws / (ms_per_step * 1e-3) / 1e9, 2),
         "kv_tokens_per_s": round(kv_tokens * ws / (ms_per_step * 1e-3), 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+        "roofline": ({"bound": "tensor", "achieved": round(tflops, 2), "peak": t_peak, "peak_kind": t_kind,
+                      "unit": "TFLOP/s", "frac": round(tflops / t_peak, 4), "traffic": traffic,
+                      "kernel": "prefix_umma_kernel<128, prefill> (one launch per pkv_multiquery_attention call)",
+                      "avg_launch_ms": round(dec_avg_ms, 5), "launches_timed": len(dec_ms),
+                      "algorithmic_flops": alg_flops, "algorithmic_bytes": alg_bytes} if prefill else
+                     {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": ("mq_tc_kernel<128, int8> (one launch per pkv_decode_attention_q8 call)" if q8
                                 else "decode_tc_kernel<128> + prefix_umma_kernel<128> (one shared-prefix call)"
@@ -558,7 +590,7 @@ def run_pkv(args, cfg):
                                 "mq_tc_kernel<128> (one launch per pkv_multiquery_attention call)" if nq > 1 else
                                 "decode_tc_kernel<128> (one launch per pkv_decode_attention call)"),
                      "avg_launch_ms": round(dec_avg_ms, 5), "launches_timed": len(dec_ms),
-                     "algorithmic_bytes": alg_bytes},
+                     "algorithmic_bytes": alg_bytes}),
         "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": cpu_what + "float64 NumPy oracle, one thread"},
         "e2e": {"value": round(total_kv / (e2e_s / args.steps) / 1e9, 2), "unit": "GB/s",

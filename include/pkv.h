@@ -301,16 +301,22 @@ PKV_API size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads,
  *
  *   q, out        device, bf16 [query_start[batch]][num_q_heads][head_dim].
  *   query_start   device, int32 [batch + 1], non-decreasing row offsets.
- *   max_query_len host bound on nq, 1 <= max_query_len and
- *                 max_query_len * (num_q_heads / num_kv_heads) <= 32
- *                 (else PKV_ERR_UNSUPPORTED).
+ *   max_query_len host bound on nq, 1 <= max_query_len <= 65536 (else
+ *                 PKV_ERR_UNSUPPORTED). Up to 32 query rows per (sequence,
+ *                 KV head) (max_query_len * num_q_heads / num_kv_heads) run
+ *                 on the split decode kernel; more (a chunked prefill) run on
+ *                 the 5th-generation tensor cores: 128-row query tiles, the
+ *                 context split over a thread-block cluster whose CTAs combine
+ *                 their partials on chip (that path uses only 256 bytes of the
+ *                 workspace).
  *   workspace     >= pkv_multiquery_workspace_size(...) bytes, 256-byte
  *                 aligned, zero-filled before its first use.
  * Errors: as pkv_decode_attention; bf16 caches only (else PKV_ERR_DTYPE). A
  * sequence whose query count lies outside [0, min(n, max_query_len)] gets no
  * output rows and sets PKV_DEVERR_RANGE; with PKV_FLAG_CHECKED the call
- * returns PKV_ERR_RANGE instead, having written nothing. The tensor-core path
- * reads every K/V byte once for all the queries of its sequence.
+ * returns PKV_ERR_RANGE instead, having written nothing. The split decode
+ * kernel reads every K/V byte once for all the queries of its sequence; the
+ * prefill path reads a sequence's K/V once per 128-row query tile.
  */
 PKV_API pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const void* v_cache,
                                             const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -391,7 +391,8 @@ size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
     (void)max_blocks_per_seq;
     if (check_desc(desc) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return 0;
     const int G = num_q_heads / desc->num_kv_heads;
-    if (desc->dtype != PKV_BF16 || max_query_len < 1 || max_query_len * G > kMqMaxRows) return 0;
+    if (desc->dtype != PKV_BF16 || max_query_len < 1 || max_query_len > kMaxQueryLen) return 0;
+    if (max_query_len * G > kMqMaxRows) return 256;  // tensor-core prefill path: combines on chip
     size_t co = 0, po = 0;
     return mq_workspace_bytes(batch, desc->num_kv_heads, desc->head_dim, mq_num_ctas(desc->head_dim, batch, opts),
                               &co, &po);
@@ -410,7 +411,8 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
     if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
     const int G = num_q_heads / desc->num_kv_heads;
     if (desc->dtype != PKV_BF16) return PKV_ERR_DTYPE;
-    if (max_query_len * G > kMqMaxRows) return PKV_ERR_UNSUPPORTED;
+    if (max_query_len > kMaxQueryLen) return PKV_ERR_UNSUPPORTED;
+    const bool prefill = max_query_len * G > kMqMaxRows;  // many query rows: the tcgen05 kernel
     if (flags & PKV_FLAG_TEST_STALL) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
     if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
@@ -421,9 +423,10 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
         (reinterpret_cast<uintptr_t>(query_start) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PKV_ERR_ALIGN;
-    const int num_ctas = mq_num_ctas(desc->head_dim, batch, opts);
+    const int num_ctas = prefill ? 0 : mq_num_ctas(desc->head_dim, batch, opts);
     size_t co = 0, po = 0;
-    const size_t need = mq_workspace_bytes(batch, desc->num_kv_heads, desc->head_dim, num_ctas, &co, &po);
+    const size_t need =
+        prefill ? 256 : mq_workspace_bytes(batch, desc->num_kv_heads, desc->head_dim, num_ctas, &co, &po);
     if (workspace_bytes < need) return PKV_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned int* status = device_info().status;
@@ -436,6 +439,30 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
             return launch_check_queries(context_lens, query_start, batch, max_query_len, verdict, s);
         }, s);
         if (st != PKV_OK) return st;
+    }
+    if (prefill) {
+        for (int32_t b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {
+            PrefixArgs pa{};
+            pa.q = q;
+            pa.k_cache = k_cache;
+            pa.v_cache = v_cache;
+            pa.tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
+            pa.lens = context_lens + b0;
+            pa.qstart = query_start + b0;
+            pa.out = out;
+            pa.status = status;
+            pa.num_blocks = desc->num_blocks;
+            pa.max_blocks = max_blocks_per_seq;
+            pa.batch = batch - b0 < kMaxBatchPerLaunch ? batch - b0 : kMaxBatchPerLaunch;
+            pa.q_heads = num_q_heads;
+            pa.kv_heads = desc->num_kv_heads;
+            pa.head_dim = desc->head_dim;
+            pa.group = G;
+            pa.max_query_len = max_query_len;
+            pa.scale = scale;
+            if (launch_prefill(pa, s) != cudaSuccess) return PKV_ERR_CUDA;
+        }
+        return PKV_OK;
     }
     char* ws = static_cast<char*>(workspace);
     for (int32_t b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {

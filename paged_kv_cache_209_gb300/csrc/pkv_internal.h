@@ -127,6 +127,10 @@ struct PrefixArgs {
     int32_t chunks;        // grid y: shared-block chunks per group
     int32_t chunk_blocks;  // blocks per chunk
     float scale;
+    // causal multi-query (chunked prefill) mode of the tcgen05 kernel: the
+    // queries of sequence i are rows qstart[i] .. qstart[i+1]-1 of q / out
+    const int32_t* qstart;
+    int32_t max_query_len;
 };
 
 // Grid and workspace of the chunk-first pass for a launch of `batch`
@@ -140,6 +144,10 @@ struct PrefixPlan {
 PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int head_dim, int max_group_blocks,
                        size_t base_offset, int kernel);
 cudaError_t launch_prefix(const PrefixArgs& a, int kernel, cudaStream_t s);
+// Causal multi-query attention with many query rows per (sequence, KV head)
+// on the tcgen05 kernel: 128-row query tiles, the context split over a
+// cluster; fills a.tiles / a.chunks / a.chunk_blocks.
+cudaError_t launch_prefill(PrefixArgs& a, cudaStream_t s);
 cudaError_t launch_check_groups(const int32_t* tables, int32_t max_blocks, const int32_t* lens,
                                 const int32_t* prefix_group, const int32_t* group_blocks, int32_t num_groups,
                                 int32_t max_group_blocks, int32_t batch, unsigned int* verdict, cudaStream_t s);
@@ -183,7 +191,8 @@ struct MqArgs {
     const float* v_scales;
     int32_t q8;
 };
-constexpr int kMqMaxRows = 32;  // query rows per (sequence, KV head)
+constexpr int kMqMaxRows = 32;      // query rows per (sequence, KV head) of the mma.sync kernel
+constexpr int kMaxQueryLen = 65536;  // queries per sequence in one multi-query call
 int mq_num_ctas(int head_dim, int batch, const pkv_decode_opts* opts, bool q8 = false);
 size_t mq_workspace_bytes(int batch, int kv_heads, int head_dim, int num_ctas, size_t* counters_offset,
                           size_t* partials_offset);

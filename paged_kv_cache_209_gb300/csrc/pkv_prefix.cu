@@ -168,6 +168,77 @@ __device__ int locate_tile(const PrefixArgs& a, int* info, int* members, int* co
     return static_cast<int>(blockIdx.y) < nch ? 2 : 1;
 }
 
+// Prologue of the causal multi-query (chunked prefill) mode (all threads;
+// contains __syncthreads). The query rows of sequence i are (query t, query
+// head g of KV head h), row r = t G + g, in 128-row tiles; query t of a
+// sequence with n tokens and nq queries sees tokens 0 .. n - nq + t. Finds
+// the sequence and tile of this CTA's x index. info[]: [1] tile within the
+// sequence, [2] sequence, [3] blocks the tile's last row sees, [4] chunks of
+// them, [5] rows of the tile, [7] n, [8] nq, [9] first query row of the
+// sequence. Returns 0 when x names no tile, 1 when the tile has no chunk y,
+// 2 when the CTA has work. A sequence whose query range is malformed
+// (negative, more queries than tokens or than max_query_len) gets no tiles
+// and sets PKV_DEVERR_RANGE.
+template <int kRowsPerTile>
+__device__ int locate_prefill_tile(const PrefixArgs& a, int* info, int* stage) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+    const int cap = a.max_blocks * 16;
+    int* s_tiles = stage;  // tiles of each sequence
+    if (threadIdx.x == 0) info[0] = -1;
+    for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
+        const int n = a.lens[i];
+        const int q0 = a.qstart[i];
+        const int nq = a.qstart[i + 1] - q0;
+        const bool bad = n < 0 || n > cap || q0 < 0 || nq < 0 || nq > n || nq > a.max_query_len;
+        if (bad && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(a.status, PKV_DEVERR_RANGE);
+        s_tiles[i] = bad ? 0 : (nq * G + kRowsPerTile - 1) / kRowsPerTile;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < a.batch; base += 32) {
+            const int i = base + lane;
+            const int t = i < a.batch ? s_tiles[i] : 0;
+            int x = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int excl = carry + x - t;
+            if (t > 0 && static_cast<int>(blockIdx.x) >= excl && static_cast<int>(blockIdx.x) < excl + t) {
+                info[0] = i;
+                info[1] = static_cast<int>(blockIdx.x) - excl;
+            }
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+    }
+    __syncthreads();
+    const int i = info[0];
+    if (i < 0) return 0;
+    if (threadIdx.x == 0) {
+        const int n = a.lens[i];
+        const int q0 = a.qstart[i];
+        const int nq = a.qstart[i + 1] - q0;
+        const int r0 = info[1] * kRowsPerTile;
+        const int nrows = min(kRowsPerTile, nq * G - r0);
+        const int seen = n - nq + (r0 + nrows - 1) / G + 1;  // tokens the tile's last row sees, >= 1
+        const int nb = (seen + 15) / 16;
+        info[2] = i;
+        info[3] = nb;
+        info[4] = (nb + a.chunk_blocks - 1) / a.chunk_blocks;
+        info[5] = nrows;
+        info[6] = 0;
+        info[7] = n;
+        info[8] = nq;
+        info[9] = q0;
+    }
+    __syncthreads();
+    return static_cast<int>(blockIdx.y) < info[4] ? 2 : 1;
+}
+
 // A CTA without work leaves at once, except CTA (0, 0, 0), which first waits
 // for the kernel before it: this grid must not complete (and release the next
 // kernel in the stream) before that one has.
@@ -564,7 +635,9 @@ struct Ux {
     static_assert(kColP + 128 <= kTmemCols, "tensor-memory columns");
 };
 
-template <int D>
+// PF (chunked prefill): the queries of one sequence over its own context
+// with a causal limit per row, written straight to the output (no fold).
+template <int D, bool PF>
 __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     prefix_umma_kernel(const PrefixArgs a, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
@@ -612,7 +685,10 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         tma_prefetch_desc(&tmV);
     }
     allow_dependents();  // inputs only until the fold (see the mma.sync kernel)
-    const int where = locate_tile<C::kRows>(a, info, members, counts, stage);
+    // chunked prefill reads the K/V rows the append before it wrote
+    if constexpr (PF) grid_dependency_wait();
+    const int where = PF ? locate_prefill_tile<C::kRows>(a, info, stage)
+                         : locate_tile<C::kRows>(a, info, members, counts, stage);
     if (where == 0) {  // no tile: the same for every CTA of the cluster
         idle_exit();
         return;
@@ -646,8 +722,13 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         const int r = threadIdx.x;
         row_ok = r < nrows;
         const int R = r0 + (row_ok ? r : 0);
-        const int m = R / G;
-        row_idx = static_cast<long long>(members[m - m0]) * a.q_heads + h * G + (R - m * G);
+        if constexpr (PF) {
+            const int t = R / G;
+            row_idx = static_cast<long long>(info[9] + t) * a.q_heads + h * G + (R - t * G);
+        } else {
+            const int m = R / G;
+            row_idx = static_cast<long long>(members[m - m0]) * a.q_heads + h * G + (R - m * G);
+        }
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + row_idx * D);
         uint8_t* qs = smem + C::kOffQ;
 #pragma unroll
@@ -807,6 +888,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     if (warp < C::kSoftmaxWarps) {
         const int r = q4 * 32 + lane;
         const float scale_log2 = a.scale * kLog2e;
+        // prefill: the last token position this row sees (-1 for a padding row)
+        const int lim = PF ? (r < nrows ? info[7] - info[8] + (r0 + r) / G : -1) : 0;
 #ifdef PKV_TRACE
         unsigned long long tr_s = 0, tr_ld = 0, tr_math = 0, tr_o = 0, tr_w = 0;
 #endif
@@ -822,7 +905,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok + th * 32, sv);
             tmem_ld_wait();
             PX_T(t2);
-            const int valid = min(C::kTok, (nblk - C::kBlk * j) * 16) - th * 32;
+            int valid = min(C::kTok, (nblk - C::kBlk * j) * 16) - th * 32;
+            if constexpr (PF) valid = min(valid, lim - ((blk0 + C::kBlk * j) * 16 + th * 32) + 1);
             float x[32];
 #pragma unroll
             for (int t = 0; t < 32; ++t) x[t] = __uint_as_float(sv[t]) * scale_log2;
@@ -996,9 +1080,14 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         int off = -1;
         if (r < nrows) {
             const int Rg = r0 + r;
-            const int mm = Rg / G;
-            off = members[mm - m0] * a.q_heads + h * G + (Rg - mm * G);
-            const float ls = __ldcg(a.fold_lse + off);
+            if constexpr (PF) {
+                const int t = Rg / G;
+                off = (info[9] + t) * a.q_heads + h * G + (Rg - t * G);
+            } else {
+                const int mm = Rg / G;
+                off = members[mm - m0] * a.q_heads + h * G + (Rg - mm * G);
+            }
+            const float ls = PF ? ninf() : __ldcg(a.fold_lse + off);  // no own-token partial in prefill
             float mc[kMaxCluster], lc[kMaxCluster];
             float Mx = ls;
 #pragma unroll
@@ -1038,8 +1127,12 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         if (off < 0) continue;
         const float* wr = wts + rr * (kMaxCluster + 1);
         const float wsr = wr[kMaxCluster];
-        const float4 f = __ldcg(reinterpret_cast<const float4*>(a.fold_o + static_cast<long long>(off) * D + 4 * c4));
-        float4 o4 = make_float4(wsr * f.x, wsr * f.y, wsr * f.z, wsr * f.w);
+        (void)wsr;
+        float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (!PF) {
+            const float4 f = __ldcg(reinterpret_cast<const float4*>(a.fold_o + static_cast<long long>(off) * D + 4 * c4));
+            o4 = make_float4(wsr * f.x, wsr * f.y, wsr * f.z, wsr * f.w);
+        }
         const uint32_t la = part_addr + ((rb + rr) * kPS + 4 * c4) * 4;
 #pragma unroll
         for (int c = 0; c < kMaxCluster; ++c) {
@@ -1092,7 +1185,7 @@ __global__ void check_groups_kernel(const int32_t* tables, int32_t max_blocks, c
 template <typename K>
 int kernel_occupancy(K kernel, int threads, size_t smem, int slot) {
     static std::mutex mu;
-    static int cache[4][64] = {};
+    static int cache[6][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
@@ -1115,21 +1208,24 @@ int occupancy_of(int kernel, int head_dim) {
                                       Px<128, kMmaStages>::kSmem, 0)
                    : kernel_occupancy(prefix_mma_kernel<64, kMmaStages>, Px<64, kMmaStages>::kThreads,
                                       Px<64, kMmaStages>::kSmem, 1);
-    return head_dim == 128 ? kernel_occupancy(prefix_umma_kernel<128>, Ux<128>::kThreads, Ux<128>::kSmem, 2)
-                           : kernel_occupancy(prefix_umma_kernel<64>, Ux<64>::kThreads, Ux<64>::kSmem, 3);
+    if (kernel == 3)  // the prefill mode of the tcgen05 kernel
+        return head_dim == 128 ? kernel_occupancy(prefix_umma_kernel<128, true>, Ux<128>::kThreads, Ux<128>::kSmem, 4)
+                               : kernel_occupancy(prefix_umma_kernel<64, true>, Ux<64>::kThreads, Ux<64>::kSmem, 5);
+    return head_dim == 128 ? kernel_occupancy(prefix_umma_kernel<128, false>, Ux<128>::kThreads, Ux<128>::kSmem, 2)
+                           : kernel_occupancy(prefix_umma_kernel<64, false>, Ux<64>::kThreads, Ux<64>::kSmem, 3);
 }
 
-// Clusters of `c` CTAs of the tcgen05 kernel that fit on the device at once
-// (cached per device and size).
-int active_clusters(int head_dim, int c) {
+// Clusters of `c` CTAs of the tcgen05 kernel (pf: its prefill mode) that fit
+// on the device at once (cached per device and size).
+int active_clusters(int head_dim, int c, bool pf = false) {
     static std::mutex mu;
-    static int cache[2][kMaxCluster + 1][64] = {};
+    static int cache[2][2][kMaxCluster + 1][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
     const int hd = head_dim == 128 ? 1 : 0;
     std::lock_guard<std::mutex> lock(mu);
-    int& slot = cache[hd][c][dev];
+    int& slot = cache[pf ? 1 : 0][hd][c][dev];
     if (slot == 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, c, 1);
@@ -1143,8 +1239,13 @@ int active_clusters(int head_dim, int c) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        const cudaError_t e = hd ? cudaOccupancyMaxActiveClusters(&n, prefix_umma_kernel<128>, &cfg)
-                                 : cudaOccupancyMaxActiveClusters(&n, prefix_umma_kernel<64>, &cfg);
+        cudaError_t e;
+        if (pf)
+            e = hd ? cudaOccupancyMaxActiveClusters(&n, prefix_umma_kernel<128, true>, &cfg)
+                   : cudaOccupancyMaxActiveClusters(&n, prefix_umma_kernel<64, true>, &cfg);
+        else
+            e = hd ? cudaOccupancyMaxActiveClusters(&n, prefix_umma_kernel<128, false>, &cfg)
+                   : cudaOccupancyMaxActiveClusters(&n, prefix_umma_kernel<64, false>, &cfg);
         if (e != cudaSuccess || n < 1) {
             cudaGetLastError();
             n = -1;  // not launchable at this size
@@ -1165,8 +1266,34 @@ cudaError_t run_prefix(const PrefixArgs& a, int kernel, cudaStream_t s) {
     if (kernel == 1)
         return launch_pdl(prefix_mma_kernel<D, kMmaStages>, grid, dim3(Px<D, kMmaStages>::kThreads),
                           Px<D, kMmaStages>::kSmem, s, a, tmK, tmV);
-    return launch_pdl_cluster(prefix_umma_kernel<D>, grid, dim3(Ux<D>::kThreads), dim3(1, a.chunks, 1),
+    return launch_pdl_cluster(prefix_umma_kernel<D, false>, grid, dim3(Ux<D>::kThreads), dim3(1, a.chunks, 1),
                               Ux<D>::kSmem, s, a, tmK, tmV);
+}
+
+// Chunked prefill: tiles of 128 query rows (every sequence padded to whole
+// tiles, at most max_query_len queries each); each (tile, KV head) is one
+// cluster whose CTAs split the context into chunks of whole 64-token steps,
+// as many as fill the device with one wave when the tiles are few.
+template <int D>
+cudaError_t run_prefill(PrefixArgs& a, cudaStream_t s) {
+    CUtensorMap tmK, tmV;
+    const int64_t rows = a.num_blocks * a.kv_heads * 16;
+    if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
+        return cudaErrorInvalidValue;
+    occupancy_of(3, D);  // sets the shared-memory limit once per device
+    const int per_seq = (a.max_query_len * a.group + Ux<D>::kRows - 1) / Ux<D>::kRows;
+    a.tiles = a.batch * per_seq;
+    const int pairs = a.tiles * a.kv_heads;
+    int c = device_sm_count() / (pairs > 0 ? pairs : 1);
+    c = c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c);
+    while (c > 1 && active_clusters(D, c, true) < 1) --c;
+    int cb = (a.max_blocks + c - 1) / c;
+    cb = (cb + Ux<D>::kBlk - 1) / Ux<D>::kBlk * Ux<D>::kBlk;
+    a.chunk_blocks = cb;
+    a.chunks = (a.max_blocks + cb - 1) / cb;
+    if (a.tiles == 0) return cudaSuccess;
+    return launch_pdl_cluster(prefix_umma_kernel<D, true>, dim3(a.tiles, a.chunks, a.kv_heads), dim3(Ux<D>::kThreads),
+                              dim3(1, a.chunks, 1), Ux<D>::kSmem, s, a, tmK, tmV);
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1230,6 +1357,10 @@ PrefixPlan prefix_plan(int batch, int num_groups, int q_heads, int kv_heads, int
 
 cudaError_t launch_prefix(const PrefixArgs& a, int kernel, cudaStream_t s) {
     return a.head_dim == 128 ? run_prefix<128>(a, kernel, s) : run_prefix<64>(a, kernel, s);
+}
+
+cudaError_t launch_prefill(PrefixArgs& a, cudaStream_t s) {
+    return a.head_dim == 128 ? run_prefill<128>(a, s) : run_prefill<64>(a, s);
 }
 
 cudaError_t launch_check_groups(const int32_t* tables, int32_t max_blocks, const int32_t* lens,

@@ -21,6 +21,10 @@ Workloads (named by what they are; all use 16-token blocks):
 * ``spec4``        -- the ``llama8k`` layer verifying 4 draft tokens per
   sequence: every context 8192 tokens including the 4 new ones, 4 causal
   queries per sequence, tables a permutation (seed 5) of a 16384-block pool.
+* ``prefill512``   -- chunked prefill on the Llama-3-8B layer: batch 8,
+  32 q / 8 kv heads, head_dim 128, bf16, every context 8192 tokens of which
+  the last 512 are this step's chunk (512 causal queries per sequence),
+  tables a permutation (seed 7) of a 4096-block pool.
 * ``llama8k_q8``   -- the ``llama8k`` layer over an int8 cache: K codes
   ``[blocks][8][16][128]``, V codes ``[blocks][8][128][16]``, float32 scales
   ``[blocks][8][16]`` per pool; codes a rounded normal of standard deviation
@@ -55,6 +59,8 @@ CONFIGS = {
                   context=8192, num_blocks=16384, queries=4, seed=5),
     "llama8k_q8": dict(batch=32, q_heads=32, kv_heads=8, head_dim=128, dtype="int8",
                        context=8192, num_blocks=16384, seed=6),
+    "prefill512": dict(batch=8, q_heads=32, kv_heads=8, head_dim=128, dtype="bf16",
+                       context=8192, num_blocks=4096, queries=512, seed=7),
 }
 
 
@@ -150,7 +156,7 @@ def workload_index(name: str):
     """
     cfg = CONFIGS[name]
     B = cfg["batch"]
-    if name in ("llama8k", "long128k", "spec4", "llama8k_q8"):
+    if name in ("llama8k", "long128k", "spec4", "llama8k_q8", "prefill512"):
         lens = np.full(B, cfg["context"], dtype=np.int64)
         tables = permuted_tables(cfg["num_blocks"], B, cfg["context"] // BLOCK_SIZE, cfg["seed"])
         num_blocks = cfg["num_blocks"]

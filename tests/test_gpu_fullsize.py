@@ -218,3 +218,33 @@ def test_llama8k_q8_workload(pkv):
         ma, rl = cases.attention_errors(out[i:i + 1, j * G:(j + 1) * G], want[:, j * G:(j + 1) * G])
         assert ma <= MAX_ABS and rl <= REL_L2, (i, j, ma, rl)
     assert bool(torch.isfinite(out.float()).all())
+
+
+def test_prefill512_workload(pkv):
+    """Chunked prefill on the 8K Llama layer (512 causal queries per sequence,
+    the tensor-core tile path), as the benchmark runs it: the append of the
+    chunk's 4096 tokens (pools bit-exact), then one multi-query call; sampled
+    (sequence, KV head) pairs, all 512 queries, against the float64 oracle."""
+    from oracle import multiquery as OM
+    w = W.device_workload("prefill512", torch.device("cuda", 0))
+    cfg, nq = w["cfg"], w["queries"]
+    kv_heads = cfg["kv_heads"]
+    G = cfg["q_heads"] // kv_heads
+    hk, hv = cases.host_view(w["k_pool"]), cases.host_view(w["v_pool"])
+    OK.append_tokens(hk, hv, cases.host_view(w["k_new"]), cases.host_view(w["v_new"]), w["slots_np"])
+    pkv.pkv_append(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"])
+    out = pkv.pkv_multiquery_attention(w["q"], w["k_pool"], w["v_pool"], w["tables"], w["lens"], w["query_start"],
+                                       w["scale"], nq)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert np.array_equal(cases.host_view(w["k_pool"]), hk) and np.array_equal(cases.host_view(w["v_pool"]), hv)
+    qh = cases.host_view(w["q"])
+    for (i, j) in sample_pairs(w["lens_np"], kv_heads, 2, 31):
+        rows = slice(i * nq, (i + 1) * nq)
+        sub_q = qh[rows][:, j * G:(j + 1) * G]
+        # one KV head: the oracle over a single-head view of the pools
+        want = OM.multiquery_attention(sub_q, hk[:, j:j + 1], hv[:, j:j + 1], w["tables_np"][i:i + 1],
+                                       w["lens_np"][i:i + 1], np.array([0, nq]), w["scale"], 1, "bf16")
+        ma, rl = cases.attention_errors(out[rows, j * G:(j + 1) * G], want)
+        assert ma <= MAX_ABS and rl <= REL_L2, (i, j, ma, rl)
+    assert bool(torch.isfinite(out.float()).all())

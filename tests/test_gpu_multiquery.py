@@ -1,5 +1,8 @@
 """Multi-query (causal) paged attention through the C ABI against the oracle.
 
+Calls with up to 32 query rows per (sequence, KV head) run on the split
+decode kernel; more rows (a chunked prefill) on the tensor-core tile kernel.
+
 Every output row is compared with the float64 oracle (query t of a sequence
 with n tokens and nq queries attends to tokens 0 .. n - nq + t). Cases cover
 group sizes 1-8, head_dim 64 and 128, query counts 0 to max_query_len per
@@ -135,9 +138,62 @@ def test_host_rejections(pkv):
     c = cases.multiquery_case(14, [30, 40], [2, 2], 32, 8, 128, torch.bfloat16)
     d = dev(c)
     with pytest.raises(pkv.PkvError) as e:
-        run(pkv, c, d, 9)            # 9 queries x 4 heads > 32 rows
+        run(pkv, c, d, 65537, workspace=torch.zeros(256, dtype=torch.uint8, device="cuda"))
     assert e.value.name == "PKV_ERR_UNSUPPORTED"
     cf = cases.multiquery_case(14, [30, 40], [2, 2], 8, 2, 64, torch.float32)
     with pytest.raises(pkv.PkvError) as e:
         run(pkv, cf, dev(cf), 2)
     assert e.value.name == "PKV_ERR_DTYPE"
+
+
+PREFILL = {
+    # name: (lens, query counts, q_heads, kv_heads, head_dim, max_query_len) -- more than 32 rows
+    "llama_ragged": ([300, 129, 1000, 64], [40, 129, 300, 64], 32, 8, 128, 300),
+    "g8_d64": ([500, 77], [200, 77], 16, 2, 64, 200),
+    "g1_whole_prompts": ([90, 33, 1], [90, 33, 1], 8, 8, 128, 90),
+    "zero_queries": ([256, 40, 700], [100, 0, 37], 32, 8, 128, 100),
+    "long_context_two_tiles": ([4000, 2500], [64, 33], 32, 8, 128, 64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL))
+def test_prefill_matches_oracle(pkv, name):
+    """Chunked prefill (tensor-core tiles): every output row against the
+    float64 oracle."""
+    lens, nqs, hq, hkv, d, mql = PREFILL[name]
+    c = cases.multiquery_case(len(name) + 50, lens, nqs, hq, hkv, d, torch.bfloat16)
+    out = run(pkv, c, dev(c), mql)
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want(c))
+
+
+def test_prefill_path_agrees_with_split_kernel(pkv):
+    """The same 16-row call through both paths: max_query_len 4 (16 rows,
+    split decode kernel) and 9 (36 rows, tensor-core tiles)."""
+    c = cases.multiquery_case(61, [700, 40, 129, 2000], [4, 4, 3, 4], 32, 8, 128, torch.bfloat16)
+    d = dev(c)
+    a = run(pkv, c, d, 4)
+    b = run(pkv, c, d, 9)
+    assert pkv.pkv_device_status(clear=True) == 0
+    diff = a.float() - b.float()
+    assert diff.abs().max().item() <= 1e-2 and (diff.norm() / a.float().norm()).item() <= 2e-3
+    check(b, want(c))
+
+
+def test_prefill_malformed_query_ranges(pkv):
+    """A sequence asking for more queries than it has tokens gets no rows and
+    sets PKV_DEVERR_RANGE; the other rows are right; checked mode rejects."""
+    c = cases.multiquery_case(62, [80, 30, 90], [40, 50, 33], 8, 2, 128, torch.bfloat16)   # 50 > 30 tokens
+    d = dev(c)
+    out = torch.full_like(d["q"], 5.0)
+    run(pkv, c, d, 50, out=out)
+    assert pkv.pkv_device_status(clear=True) & 2
+    keep = np.r_[0:40, 90:123]
+    ref = want(dict(c, lens=np.array([80, 90]), query_start=np.array([0, 40, 73]),
+                    q=torch.cat([c["q"][0:40], c["q"][90:123]]), tables=c["tables"][[0, 2]]))
+    check(out[torch.from_numpy(keep).cuda()], ref)
+    out2 = torch.full_like(d["q"], 5.0)
+    with pytest.raises(pkv.PkvError) as e:
+        run(pkv, c, d, 50, out=out2, flags=pkv.PKV_FLAG_CHECKED)
+    assert e.value.name == "PKV_ERR_RANGE"
+    assert bool((out2 == 5.0).all())
