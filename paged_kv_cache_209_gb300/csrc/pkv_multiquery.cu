@@ -9,6 +9,10 @@
 // the K candidates; notebook section 7: a suffix attends to every cached
 // position, causally within itself).
 //
+// This kernel takes calls with up to 32 query rows per (sequence, KV head)
+// (max_query_len * G); more rows (a chunked prefill) run on the tcgen05 tile
+// kernel's prefill mode in pkv_prefix.cu.
+//
 // Work decomposition: the stream-K split of the decode kernel over (sequence,
 // KV head, block) units, so K/V is read once per call for all query rows.
 // The query rows of one (sequence, KV head) are (query t, query head g),

@@ -197,3 +197,15 @@ def test_prefill_malformed_query_ranges(pkv):
         run(pkv, c, d, 50, out=out2, flags=pkv.PKV_FLAG_CHECKED)
     assert e.value.name == "PKV_ERR_RANGE"
     assert bool((out2 == 5.0).all())
+
+
+def test_prefill_batch_above_one_launch(pkv):
+    """More than 1024 sequences on the tile path: the call runs one launch per
+    1024 sequences, with absolute query rows."""
+    rng = np.random.default_rng(63)
+    lens = rng.integers(9, 60, 1030)
+    nqs = np.minimum(lens, rng.integers(0, 10, 1030))
+    c = cases.multiquery_case(64, lens, nqs, 8, 2, 64, torch.bfloat16)
+    out = run(pkv, c, dev(c), 9)          # 9 queries x 4 heads = 36 rows: the tile path
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want(c))
