@@ -115,3 +115,19 @@ def test_workspace_size_rejects_bad_geometry(lib):
     # the tensor-core kernel takes bf16 only
     assert lib.pkv_decode_workspace_size(2, 32, 4, ctypes.byref(_desc(dtype=0)),
                                          ctypes.byref(DecodeOpts(2, 0))) == 0
+
+
+def test_multiquery_workspace_routing(lib):
+    """Calls with more than 32 query rows per (sequence, KV head) take the
+    tensor-core tile path, which combines on chip: a 256-byte workspace.
+    Query counts above 65536 are rejected (size 0), as are float32 caches."""
+    d = _desc()                                   # bf16, 8 KV heads
+    assert lib.pkv_multiquery_workspace_size(4, 32, 16, 9, ctypes.byref(d), None) == 256    # 36 rows
+    assert lib.pkv_multiquery_workspace_size(4, 32, 16, 65537, ctypes.byref(d), None) == 0
+    assert lib.pkv_multiquery_workspace_size(4, 32, 16, 9, ctypes.byref(_desc(dtype=0)), None) == 0
+    # rejected before anything is enqueued: more than 65536 queries, float32 caches
+    args = [FAKE, FAKE, FAKE, FAKE, 16, FAKE, FAKE, 4, 32]
+    tail = [ctypes.c_float(0.1), FAKE, FAKE, 256, ctypes.byref(d), 0, None, None]
+    assert lib.pkv_multiquery_attention(*args, 65537, *tail) == 10          # PKV_ERR_UNSUPPORTED
+    tail32 = [ctypes.c_float(0.1), FAKE, FAKE, 256, ctypes.byref(_desc(dtype=0)), 0, None, None]
+    assert lib.pkv_multiquery_attention(*args, 9, *tail32) == 3             # PKV_ERR_DTYPE
