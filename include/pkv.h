@@ -89,11 +89,13 @@ typedef struct {
 
 /* flags */
 #define PKV_FLAG_CHECKED 1u    /* validate device-resident indices first (syncs) */
-/* Test hook for failure detection, pkv_decode_attention with the tensor-core
- * kernel only (opts->kernel == 2): the kernel's producer warp issues no copies,
- * so every consumer wait runs out after 20 ms instead of 2 s. The call itself
- * returns PKV_OK; the sticky device status then reports PKV_DEVERR_TIMEOUT and
- * `out` holds no result. Nothing is in flight when the kernel returns. */
+/* Test hook for failure detection, on pkv_decode_attention with the
+ * tensor-core kernel (opts->kernel == 2), on pkv_multiquery_attention up to 32
+ * query rows per (sequence, KV head) and on pkv_decode_attention_q8: the
+ * kernel's producer warp issues no copies, so every consumer wait runs out
+ * after 20 ms instead of 2 s. The call itself returns PKV_OK; the sticky device
+ * status then reports PKV_DEVERR_TIMEOUT and `out` holds no result. Nothing is
+ * in flight when the kernel returns. Elsewhere the flag is PKV_ERR_UNSUPPORTED. */
 #define PKV_FLAG_TEST_STALL 0x80000000u
 
 /* Bits of the sticky device status (pkv_device_status). */

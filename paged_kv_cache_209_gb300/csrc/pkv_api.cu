@@ -413,7 +413,7 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
     if (desc->dtype != PKV_BF16) return PKV_ERR_DTYPE;
     if (max_query_len > kMaxQueryLen) return PKV_ERR_UNSUPPORTED;
     const bool prefill = max_query_len * G > kMqMaxRows;  // many query rows: the tcgen05 kernel
-    if (flags & PKV_FLAG_TEST_STALL) return PKV_ERR_UNSUPPORTED;
+    if (prefill && (flags & PKV_FLAG_TEST_STALL)) return PKV_ERR_UNSUPPORTED;  // the hook is the split kernel's
     if (batch == 0) return PKV_OK;
     if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
         return PKV_ERR_SHAPE;
@@ -489,6 +489,7 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
         a.max_query_len = max_query_len;
         const int row_groups = (max_query_len * G + 7) / 8;
         a.wpu = row_groups <= 1 ? 1 : (row_groups <= 2 ? 2 : 4);
+        a.test_stall = (flags & PKV_FLAG_TEST_STALL) ? 1 : 0;
         a.scale = scale;
         if (launch_multiquery(a, s) != cudaSuccess) return PKV_ERR_CUDA;
     }
@@ -573,7 +574,6 @@ pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const voi
     const int G = num_q_heads / desc->num_kv_heads;
     if (max_query_len * G > kMqMaxRows) return PKV_ERR_UNSUPPORTED;
     if (query_start == nullptr && max_query_len != 1) return PKV_ERR_SHAPE;
-    if (flags & PKV_FLAG_TEST_STALL) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
     if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
         return PKV_ERR_SHAPE;
@@ -631,6 +631,7 @@ pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const voi
         a.max_query_len = max_query_len;
         const int row_groups = (max_query_len * G + 7) / 8;
         a.wpu = row_groups <= 1 ? 1 : (row_groups <= 2 ? 2 : 4);
+        a.test_stall = (flags & PKV_FLAG_TEST_STALL) ? 1 : 0;
         a.scale = scale;
         if (launch_multiquery(a, s) != cudaSuccess) return PKV_ERR_CUDA;
     }

@@ -190,6 +190,7 @@ struct MqArgs {
     const float* k_scales;
     const float* v_scales;
     int32_t q8;
+    int32_t test_stall;  // PKV_FLAG_TEST_STALL: the producer issues nothing
 };
 constexpr int kMqMaxRows = 32;      // query rows per (sequence, KV head) of the mma.sync kernel
 constexpr int kMaxQueryLen = 65536;  // queries per sequence in one multi-query call

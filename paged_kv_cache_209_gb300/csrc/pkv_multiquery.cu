@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
 
     if (warp == C::kConsumers) {
         // ------------------------------------------------ producer warp (as in the decode kernel)
+        if (a.test_stall) return;  // test hook: nothing is ever issued, so every consumer wait runs out
         const uint64_t kv_policy = l2_evict_first_policy();
         Walker wk;
         wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
@@ -455,7 +456,9 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
         k += skip;
         for (int blk = pc.blk_from + skip; blk < pc.blk_to; blk += UG, k += UG) {
             const int s = static_cast<int>(k % C::kStages);
-            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag)) return;
+            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag,
+                           a.test_stall ? kTestWaitLimitNs : kWaitLimitNs))
+                return;
             const int valid = min(16, n_ctx - blk * 16);
             if (!Q8 && stage_ok[s] && active) {
                 const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);

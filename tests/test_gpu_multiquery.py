@@ -209,3 +209,23 @@ def test_prefill_batch_above_one_launch(pkv):
     out = run(pkv, c, dev(c), 9)          # 9 queries x 4 heads = 36 rows: the tile path
     assert pkv.pkv_device_status(clear=True) == 0
     check(out, want(c))
+
+
+def test_bounded_wait_runs_out_and_is_reported(pkv):
+    """Failure detection in the split kernel: with the stall hook its producer
+    issues nothing, every consumer wait runs out (20 ms), the kernel returns
+    and the sticky status says so; the next call on the same context and
+    workspace is right. The tile path has no hook and rejects the flag."""
+    c = cases.multiquery_case(65, [300, 40, 900], [4, 4, 2], 32, 8, 128, torch.bfloat16)
+    d = dev(c)
+    ws = torch.zeros(pkv.pkv_multiquery_workspace_size(3, 32, c["tables"].shape[1], 4, d["k"]), dtype=torch.uint8,
+                     device="cuda")
+    pkv.pkv_device_status(clear=True)
+    run(pkv, c, d, 4, workspace=ws, flags=pkv.PKV_FLAG_TEST_STALL)
+    assert pkv.pkv_device_status(clear=True) & pkv.PKV_DEVERR_TIMEOUT
+    out = run(pkv, c, d, 4, workspace=ws)
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want(c))
+    with pytest.raises(pkv.PkvError) as e:
+        run(pkv, c, d, 9, flags=pkv.PKV_FLAG_TEST_STALL)
+    assert e.value.name == "PKV_ERR_UNSUPPORTED"

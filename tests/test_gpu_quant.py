@@ -204,3 +204,15 @@ def test_bad_block_id_and_checked_mode(pkv):
     assert e.value.name == "PKV_ERR_RANGE"
     assert bool((out2 == 5.0).all())
     assert pkv.pkv_device_status(clear=True) == 0
+
+
+def test_bounded_wait_runs_out_and_is_reported(pkv):
+    """The stall hook on the int8 attention: every wait runs out, the status
+    reports it, and the next call is right."""
+    c = q8_case(66, [200, 33, 700], 32, 8)
+    pkv.pkv_device_status(clear=True)
+    run_q8(pkv, c, flags=pkv.PKV_FLAG_TEST_STALL)
+    assert pkv.pkv_device_status(clear=True) & pkv.PKV_DEVERR_TIMEOUT
+    out = run_q8(pkv, c)
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want_q8(c))
