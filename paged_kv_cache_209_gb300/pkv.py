@@ -312,7 +312,11 @@ def pkv_multiquery_attention(q, k_cache, v_cache, block_tables, context_lens, qu
                              max_query_len: int, out=None, workspace=None, flags: int = 0, num_ctas: int = 0,
                              stream=None):
     """Causal multi-query attention; ``q``/``out`` are [query_start[-1]][q_heads][head_dim]
-    and ``query_start`` int32 [batch + 1]. Returns ``out``."""
+    and ``query_start`` int32 [batch + 1]. Returns ``out``.
+
+    Up to 32 query rows per (sequence, KV head) (``max_query_len * q_heads / kv_heads``)
+    run on the split decode kernel (``num_ctas`` applies there); more, a chunked
+    prefill, on the tcgen05 tile kernel, which needs only 256 bytes of workspace."""
     lib = load_library()
     _same_pools(k_cache, v_cache)
     desc = cache_desc(k_cache)
