@@ -216,3 +216,14 @@ def test_bounded_wait_runs_out_and_is_reported(pkv):
     out = run_q8(pkv, c)
     assert pkv.pkv_device_status(clear=True) == 0
     check(out, want_q8(c))
+
+
+def test_batch_above_one_launch(pkv):
+    """More than 1024 sequences: one launch per 1024, decode rows at their
+    absolute positions."""
+    rng = np.random.default_rng(67)
+    lens = rng.integers(0, 80, 1030)
+    c = q8_case(67, lens, 8, 2)
+    out = run_q8(pkv, c)
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want_q8(c))
