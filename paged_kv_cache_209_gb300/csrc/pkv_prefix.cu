@@ -830,6 +830,17 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 umma_commit(&s_full[j & 1]);
                 return true;
             };
+            // prefill: the step and stage row of the first slot past the
+            // sequence's end, when that slot lies in a block this CTA streams
+            int tail_step = -1, tail_row = 0;
+            if constexpr (PF) {
+                const int n_end = info[7];
+                const int bl = n_end >> 4;
+                if ((n_end & 15) != 0 && bl >= blk0 && bl < blk0 + nblk) {
+                    tail_step = (bl - blk0) / C::kBlk;
+                    tail_row = ((bl - blk0) % C::kBlk) * 16 + (n_end & 15);
+                }
+            }
             for (int j = 0; ok && j < nsteps && j < 2; ++j) ok = issue_s(j);
             for (int j = 0; ok && j < nsteps; ++j) {
                 PX_T(t0);
@@ -846,6 +857,22 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 // per 128-byte row, the two column halves kHalfBytes apart, 8
                 // token rows per 1024-byte atom.
                 const int s = j % C::kStages;
+                if constexpr (PF) {
+                    // The slots of the sequence's last block past its length may
+                    // hold anything, NaN included. P is zero there, but 0 * NaN
+                    // is not, so those V rows are zeroed before the product
+                    // (their copy has landed: S_j waited for it).
+                    if (j == tail_step) {
+                        uint8_t* vt = smem + C::kOffKV + s * C::kStageBytes + C::kKBytes;
+                        for (int hf = 0; hf < C::kHalves; ++hf)
+                            for (int row = tail_row; row < (tail_row | 15) + 1; ++row)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    *reinterpret_cast<uint4*>(vt + hf * C::kHalfBytes + row * 128 + c * 16) =
+                                        make_uint4(0u, 0u, 0u, 0u);
+                        fence_proxy_async_smem();
+                    }
+                }
                 const uint32_t v_base = smem_u32(smem + C::kOffKV + s * C::kStageBytes + C::kKBytes);
                 const uint32_t p_col = tmem + C::kColP + (j & 1) * 64;
 #pragma unroll

@@ -155,10 +155,12 @@ def grouped_case(seed, member_of, group_blocks, suffix_lens, q_heads, kv_heads, 
                 scale=1.0 / np.sqrt(head_dim))
 
 
-def multiquery_case(seed, lens, nqs, q_heads, kv_heads, head_dim, dtype, extra_blocks=4, width=None):
+def multiquery_case(seed, lens, nqs, q_heads, kv_heads, head_dim, dtype, extra_blocks=4, width=None, poison=False):
     """Sequences of the given lengths on a shuffled pool; sequence i's last
-    nqs[i] tokens are its queries (rows query_start[i] .. query_start[i+1]-1)."""
-    c = random_case(seed, lens, q_heads, kv_heads, head_dim, dtype, extra_blocks=extra_blocks, width=width)
+    nqs[i] tokens are its queries (rows query_start[i] .. query_start[i+1]-1).
+    poison: every slot no sequence holds is K = NaN, V = -inf."""
+    c = random_case(seed, lens, q_heads, kv_heads, head_dim, dtype, extra_blocks=extra_blocks, width=width,
+                    poison=poison)
     qs = np.concatenate([[0], np.cumsum(np.asarray(nqs, dtype=np.int64))]).astype(np.int32)
     q = W.numpy_normal((int(qs[-1]), q_heads, head_dim), seed * 7 + 5)
     c["q"] = torch.from_numpy(q).to(dtype)

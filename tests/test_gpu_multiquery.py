@@ -180,6 +180,21 @@ def test_prefill_path_agrees_with_split_kernel(pkv):
     check(b, want(c))
 
 
+@pytest.mark.parametrize("mql", [4, 40])
+def test_poisoned_tail_slots(pkv, mql):
+    """Slots past every context (the rest of each last block, spare blocks)
+    hold K = NaN and V = -inf: a masked token must contribute nothing, not
+    0 * NaN. 4 queries per sequence run on the split kernel, 40 on the tiles;
+    no length is a multiple of 16."""
+    lens = [300, 17, 1001, 45, 130]
+    c = cases.multiquery_case(66 + mql, lens, [min(mql, n) for n in lens], 32, 8, 128, torch.bfloat16,
+                              poison=True)
+    out = run(pkv, c, dev(c), mql)
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert bool(torch.isfinite(out).all())
+    check(out, want(c))
+
+
 def test_prefill_malformed_query_ranges(pkv):
     """A sequence asking for more queries than it has tokens gets no rows and
     sets PKV_DEVERR_RANGE; the other rows are right; checked mode rejects."""
