@@ -4,7 +4,9 @@ oracle (every output element, decode bars: max-abs 1e-2, relative L2 2e-3).
 For each path 24 cases draw the batch, the context lengths (including empty
 contexts and contexts inside one block), the query-head group size, head_dim
 and, where the call takes them, forced CTA counts, query counts and prefix
-groups. A failing case prints its seed, so it can be rerun alone.
+groups; about half of the decode and multi-query cases hold K = NaN and
+V = -inf in every slot no sequence holds. A failing case prints its seed, so
+it can be rerun alone.
 """
 
 import numpy as np
@@ -55,11 +57,11 @@ def test_decode_random(pkv, seed):
     hq, hkv = heads(rng)
     d = int(rng.choice([64, 128]))
     lens = lengths(rng, int(rng.integers(1, 40)), int(rng.choice([64, 700, 3000])))
-    c = cases.random_case(1000 + seed, lens, hq, hkv, d, torch.bfloat16)
-    dev = torch.device("cuda", 0)
     kw = {}
     if rng.random() < 0.5:
         kw["num_ctas"] = int(rng.integers(1, 400))          # cut segments at arbitrary places
+    c = cases.random_case(1000 + seed, lens, hq, hkv, d, torch.bfloat16, poison=bool(rng.random() < 0.5))
+    dev = torch.device("cuda", 0)
     out = pkv.pkv_decode_attention(c["q"].to(dev), c["k_pool"].to(dev), c["v_pool"].to(dev),
                                    torch.from_numpy(c["tables"]).to(dev), torch.from_numpy(c["lens"]).to(dev),
                                    c["scale"], **kw)
@@ -81,7 +83,7 @@ def test_multiquery_random(pkv, seed):
     lens = np.maximum(lengths(rng, int(rng.integers(1, 12)), int(rng.choice([40, 300, 1500]))), 1)
     mql = int(rng.choice([1, 2, 4, 8, 40, 130]))
     nqs = np.minimum(lens, rng.integers(0, mql + 1, len(lens)))
-    c = cases.multiquery_case(2000 + seed, lens, nqs, hq, hkv, d, torch.bfloat16)
+    c = cases.multiquery_case(2000 + seed, lens, nqs, hq, hkv, d, torch.bfloat16, poison=bool(rng.random() < 0.5))
     dev = torch.device("cuda", 0)
     out = pkv.pkv_multiquery_attention(c["q"].to(dev), c["k_pool"].to(dev), c["v_pool"].to(dev),
                                        torch.from_numpy(c["tables"]).to(dev), torch.from_numpy(c["lens"]).to(dev),
