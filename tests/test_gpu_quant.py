@@ -155,6 +155,25 @@ def test_multiquery_q8_matches_oracle(pkv, nqs, hq, mql):
     check(out, want_q8(c))
 
 
+@pytest.mark.parametrize("multi", [False, True])
+def test_poisoned_scales_of_unused_slots(pkv, multi):
+    """Slots no sequence holds (the rest of each last block, spare blocks)
+    carry NaN K scales and +inf V scales: a masked token must contribute
+    nothing, not 0 * inf. Decode and 4 queries per sequence."""
+    lens = [300, 17, 1001, 45, 130]
+    c = q8_case(78 + multi, lens, 32, 8, nqs=[4] * len(lens) if multi else None)
+    live = np.zeros(c["ks"].shape[0::2], dtype=bool)         # [blocks][slots]
+    for i, n in enumerate(c["lens"]):
+        for t in range(int(n)):
+            live[c["tables"][i, t // 16], t % 16] = True
+    c["ks"].transpose(0, 2, 1)[~live] = np.nan
+    c["vs"].transpose(0, 2, 1)[~live] = np.inf
+    out = run_q8(pkv, c, max_query_len=4 if multi else 1)
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert bool(torch.isfinite(out).all())
+    check(out, want_q8(c))
+
+
 def test_wide_scales_and_large_queries(pkv):
     """Row scales spanning four orders of magnitude, and queries far outside
     the f16 range (the kernel rescales each query row by a power of two before
