@@ -171,7 +171,9 @@ def test_poisoned_scales_of_unused_slots(pkv, multi):
     out = run_q8(pkv, c, max_query_len=4 if multi else 1)
     assert pkv.pkv_device_status(clear=True) == 0
     assert bool(torch.isfinite(out).all())
-    check(out, want_q8(c))
+    with np.errstate(invalid="ignore"):                      # the oracle dequantizes the poisoned rows too
+        ref = want_q8(c)
+    check(out, ref)
 
 
 def test_wide_scales_and_large_queries(pkv):
