@@ -39,6 +39,10 @@
  *        nothing written.
  *  - Every wait inside a kernel is bounded; if one runs out the kernel stops,
  *    sets PKV_DEVERR_TIMEOUT in the sticky device status and returns.
+ *  - Attention calls take num_q_heads, a positive multiple of the pool's
+ *    num_kv_heads and at most PKV_MAX_Q_HEADS (else PKV_ERR_SHAPE; the
+ *    workspace-size queries return 0), so that row and tile counts such as
+ *    max_query_len * num_q_heads / num_kv_heads stay 32-bit.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -99,6 +103,9 @@ typedef struct {
 #define PKV_FLAG_TEST_STALL 0x80000000u
 
 /* Bits of the sticky device status (pkv_device_status). */
+/* Largest num_q_heads an attention call accepts. */
+#define PKV_MAX_Q_HEADS 1024
+
 #define PKV_DEVERR_TIMEOUT 1u
 #define PKV_DEVERR_RANGE 2u
 

@@ -45,6 +45,12 @@ DeviceInfo& device_info() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Query heads of an attention call: a positive multiple of the KV heads, at
+// most PKV_MAX_Q_HEADS (query-row counts per (sequence, KV head) stay 32-bit).
+bool q_heads_ok(int32_t num_q_heads, const pkv_cache_desc* d) {
+    return num_q_heads >= 1 && num_q_heads <= PKV_MAX_Q_HEADS && num_q_heads % d->num_kv_heads == 0;
+}
+
 pkv_status check_desc(const pkv_cache_desc* d) {
     if (d == nullptr) return PKV_ERR_NULL;
     if (d->block_size != 16 || d->num_blocks < 1 || d->num_kv_heads < 1) return PKV_ERR_SHAPE;
@@ -165,7 +171,7 @@ pkv_status pkv_copy_blocks(const int64_t* pairs, int64_t num_pairs, void* k_cach
 
 size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                  const pkv_cache_desc* desc, const pkv_decode_opts* opts) {
-    if (check_desc(desc) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
+    if (check_desc(desc) != PKV_OK || batch < 0 || !q_heads_ok(num_q_heads, desc))
         return 0;
     DecodePlan plan;
     if (decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan) != PKV_OK) return 0;
@@ -181,7 +187,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
                                 const pkv_decode_opts* opts, void* stream) {
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
-    if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
+    if (batch < 0 || !q_heads_ok(num_q_heads, desc)) return PKV_ERR_SHAPE;
     if (!isfinite(scale)) return PKV_ERR_SHAPE;
     if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
     if ((flags & PKV_FLAG_TEST_STALL) && !(opts != nullptr && opts->kernel == 2)) return PKV_ERR_UNSUPPORTED;
@@ -243,7 +249,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
 size_t pkv_decode_prefixed_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                           int32_t num_groups, int32_t max_group_blocks, const pkv_cache_desc* desc,
                                           const pkv_decode_opts* opts) {
-    if (check_desc(desc) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return 0;
+    if (check_desc(desc) != PKV_OK || batch < 0 || !q_heads_ok(num_q_heads, desc)) return 0;
     if (num_groups < 0 || num_groups > kMaxBatchPerLaunch || max_group_blocks < 0) return 0;
     DecodePlan plan;
     if (decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan, true) != PKV_OK) return 0;
@@ -272,7 +278,7 @@ pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, con
         if ((reinterpret_cast<uintptr_t>(prefix_group) & 3u) || (reinterpret_cast<uintptr_t>(group_blocks) & 3u))
             return PKV_ERR_ALIGN;
     }
-    if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
+    if (batch < 0 || !q_heads_ok(num_q_heads, desc)) return PKV_ERR_SHAPE;
     DecodePlan plan;
     int rc = decode_plan(*desc, batch, num_q_heads, max_blocks_per_seq, opts, &plan, true);
     if (rc != PKV_OK) return static_cast<pkv_status>(rc);
@@ -389,7 +395,7 @@ size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
                                      int32_t max_query_len, const pkv_cache_desc* desc,
                                      const pkv_decode_opts* opts) {
     (void)max_blocks_per_seq;
-    if (check_desc(desc) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return 0;
+    if (check_desc(desc) != PKV_OK || batch < 0 || !q_heads_ok(num_q_heads, desc)) return 0;
     const int G = num_q_heads / desc->num_kv_heads;
     if (desc->dtype != PKV_BF16 || max_query_len < 1 || max_query_len > kMaxQueryLen) return 0;
     if (max_query_len * G > kMqMaxRows) return 256;  // tensor-core prefill path: combines on chip
@@ -406,7 +412,7 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
                                     uint32_t flags, const pkv_decode_opts* opts, void* stream) {
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
-    if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
+    if (batch < 0 || !q_heads_ok(num_q_heads, desc)) return PKV_ERR_SHAPE;
     if (!isfinite(scale) || max_query_len < 1) return PKV_ERR_SHAPE;
     if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
     const int G = num_q_heads / desc->num_kv_heads;
@@ -551,7 +557,7 @@ pkv_status pkv_copy_blocks_q8(const int64_t* pairs, int64_t num_pairs, void* k_c
 size_t pkv_decode_q8_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                     int32_t max_query_len, const pkv_cache_desc* desc, const pkv_decode_opts* opts) {
     (void)max_blocks_per_seq;
-    if (check_desc_q8(desc, true) != PKV_OK || batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
+    if (check_desc_q8(desc, true) != PKV_OK || batch < 0 || !q_heads_ok(num_q_heads, desc))
         return 0;
     const int G = num_q_heads / desc->num_kv_heads;
     if (max_query_len < 1 || max_query_len * G > kMqMaxRows) return 0;
@@ -568,7 +574,7 @@ pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const voi
                                    uint32_t flags, const pkv_decode_opts* opts, void* stream) {
     pkv_status st = check_desc_q8(desc, true);
     if (st != PKV_OK) return st;
-    if (batch < 0 || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return PKV_ERR_SHAPE;
+    if (batch < 0 || !q_heads_ok(num_q_heads, desc)) return PKV_ERR_SHAPE;
     if (!isfinite(scale) || max_query_len < 1) return PKV_ERR_SHAPE;
     if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
     const int G = num_q_heads / desc->num_kv_heads;

@@ -91,6 +91,8 @@ def test_decode_argument_checks(lib):
         kw.get("qh", 32), f(kw.get("scale", 0.1)), FAKE, kw.get("ws", FAKE), 1 << 30, ctypes.byref(d), 0, None,
         None)
     assert call(qh=30) == 2                      # not a multiple of the KV heads
+    assert call(qh=1032) == 2                    # above PKV_MAX_Q_HEADS (1024)
+    assert call(qh=0) == 2
     assert call(scale=float("inf")) == 2
     assert call(maxb=0) == 2
     assert call(batch=-1) == 2
@@ -125,6 +127,9 @@ def test_multiquery_workspace_routing(lib):
     assert lib.pkv_multiquery_workspace_size(4, 32, 16, 9, ctypes.byref(d), None) == 256    # 36 rows
     assert lib.pkv_multiquery_workspace_size(4, 32, 16, 65537, ctypes.byref(d), None) == 0
     assert lib.pkv_multiquery_workspace_size(4, 32, 16, 9, ctypes.byref(_desc(dtype=0)), None) == 0
+    # more query heads than PKV_MAX_Q_HEADS: query-row counts would leave 32 bits
+    assert lib.pkv_multiquery_workspace_size(4, 2048, 16, 65536, ctypes.byref(d), None) == 0
+    assert lib.pkv_decode_workspace_size(4, 2048, 16, ctypes.byref(d), None) == 0
     # rejected before anything is enqueued: more than 65536 queries, float32 caches
     args = [FAKE, FAKE, FAKE, FAKE, 16, FAKE, FAKE, 4, 32]
     tail = [ctypes.c_float(0.1), FAKE, FAKE, 256, ctypes.byref(d), 0, None, None]
