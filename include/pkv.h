@@ -42,7 +42,9 @@
  *  - Attention calls take num_q_heads, a positive multiple of the pool's
  *    num_kv_heads and at most PKV_MAX_Q_HEADS (else PKV_ERR_SHAPE; the
  *    workspace-size queries return 0), so that row and tile counts such as
- *    max_query_len * num_q_heads / num_kv_heads stay 32-bit.
+ *    max_query_len * num_q_heads / num_kv_heads stay 32-bit. Likewise
+ *    max_blocks_per_seq * 16 and max_blocks_per_seq * min(batch, 1024) must
+ *    stay below 2^31 (else PKV_ERR_SHAPE).
  */
 #ifndef PKV_H
 #define PKV_H

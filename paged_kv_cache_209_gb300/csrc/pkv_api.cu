@@ -51,6 +51,15 @@ bool q_heads_ok(int32_t num_q_heads, const pkv_cache_desc* d) {
     return num_q_heads >= 1 && num_q_heads <= PKV_MAX_Q_HEADS && num_q_heads % d->num_kv_heads == 0;
 }
 
+// Block-table width of an attention call: the tokens of one sequence
+// (max_blocks * 16) and the blocks of one launch's sequences (at most
+// kMaxBatchPerLaunch of them, prefix-summed on the device) are 32-bit counts.
+bool table_width_ok(int32_t batch, int32_t max_blocks) {
+    const int64_t per_launch = batch < kMaxBatchPerLaunch ? batch : kMaxBatchPerLaunch;
+    return max_blocks >= 1 && static_cast<int64_t>(max_blocks) * 16 < (int64_t(1) << 31) &&
+           per_launch * max_blocks < (int64_t(1) << 31);
+}
+
 pkv_status check_desc(const pkv_cache_desc* d) {
     if (d == nullptr) return PKV_ERR_NULL;
     if (d->block_size != 16 || d->num_blocks < 1 || d->num_kv_heads < 1) return PKV_ERR_SHAPE;
@@ -192,8 +201,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
     if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
     if ((flags & PKV_FLAG_TEST_STALL) && !(opts != nullptr && opts->kernel == 2)) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
-    if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
-        return PKV_ERR_SHAPE;
+    if (!table_width_ok(batch, max_blocks_per_seq)) return PKV_ERR_SHAPE;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace) return PKV_ERR_NULL;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
@@ -299,8 +307,7 @@ pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, con
     }
     if (!isfinite(scale)) return PKV_ERR_SHAPE;
     if (opts != nullptr && opts->num_ctas < 0) return PKV_ERR_SHAPE;
-    if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
-        return PKV_ERR_SHAPE;
+    if (!table_width_ok(batch, max_blocks_per_seq)) return PKV_ERR_SHAPE;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace) return PKV_ERR_NULL;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
@@ -421,8 +428,7 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
     const bool prefill = max_query_len * G > kMqMaxRows;  // many query rows: the tcgen05 kernel
     if (prefill && (flags & PKV_FLAG_TEST_STALL)) return PKV_ERR_UNSUPPORTED;  // the hook is the split kernel's
     if (batch == 0) return PKV_OK;
-    if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
-        return PKV_ERR_SHAPE;
+    if (!table_width_ok(batch, max_blocks_per_seq)) return PKV_ERR_SHAPE;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out || !workspace)
         return PKV_ERR_NULL;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
@@ -581,8 +587,7 @@ pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const voi
     if (max_query_len * G > kMqMaxRows) return PKV_ERR_UNSUPPORTED;
     if (query_start == nullptr && max_query_len != 1) return PKV_ERR_SHAPE;
     if (batch == 0) return PKV_OK;
-    if (max_blocks_per_seq < 1 || static_cast<int64_t>(max_blocks_per_seq) * 16 >= (int64_t(1) << 31))
-        return PKV_ERR_SHAPE;
+    if (!table_width_ok(batch, max_blocks_per_seq)) return PKV_ERR_SHAPE;
     if (!q || !k_codes || !v_codes || !k_scales || !v_scales || !block_tables || !context_lens || !out ||
         !workspace)
         return PKV_ERR_NULL;

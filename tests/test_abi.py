@@ -95,6 +95,9 @@ def test_decode_argument_checks(lib):
     assert call(qh=0) == 2
     assert call(scale=float("inf")) == 2
     assert call(maxb=0) == 2
+    assert call(maxb=1 << 27) == 2               # max_blocks * 16 reaches 2^31
+    assert call(maxb=1 << 21, batch=1024) == 2   # the launch's blocks reach 2^31
+    assert call(maxb=1 << 21, batch=0) == 0
     assert call(batch=-1) == 2
     assert call(q=None) == 1
     assert call(ws=None) == 1
