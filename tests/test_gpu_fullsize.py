@@ -248,3 +248,29 @@ def test_prefill512_workload(pkv):
         ma, rl = cases.attention_errors(out[rows, j * G:(j + 1) * G], want)
         assert ma <= MAX_ABS and rl <= REL_L2, (i, j, ma, rl)
     assert bool(torch.isfinite(out.float()).all())
+
+
+def test_prefill_at_the_query_limit(pkv):
+    """The largest query count the multi-query call accepts: one sequence
+    whose last 65536 tokens (max_query_len) are queries, after a 100-token
+    prefix; 8 q / 2 KV heads, head_dim 64, i.e. 2048 tiles of 128 rows per KV
+    head on the tensor-core path. Every output finite; the first, second,
+    last and one middle query row against the float64 oracle."""
+    from oracle import multiquery as OM
+    nq, prefix = 65536, 100
+    c = cases.random_case(71, [prefix + nq], 8, 2, 64, torch.bfloat16)
+    q = torch.from_numpy(W.numpy_normal((nq, 8, 64), 72)).to(torch.bfloat16)
+    dev = torch.device("cuda", 0)
+    out = pkv.pkv_multiquery_attention(q.to(dev), c["k_pool"].to(dev), c["v_pool"].to(dev),
+                                       torch.from_numpy(c["tables"]).to(dev), torch.from_numpy(c["lens"]).to(dev),
+                                       torch.tensor([0, nq], dtype=torch.int32, device=dev), c["scale"], nq)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert bool(torch.isfinite(out.float()).all())
+    qh, hk, hv = cases.host_view(q), cases.host_view(c["k_pool"]), cases.host_view(c["v_pool"])
+    for t in (0, 1, 40000, nq - 1):
+        # query t sees tokens 0 .. prefix + t: the same as a one-query call on that many tokens
+        want = OM.multiquery_attention(qh[t:t + 1], hk, hv, c["tables"], np.array([prefix + t + 1], dtype=np.int32),
+                                       np.array([0, 1]), c["scale"], 2, "bf16")
+        ma, rl = cases.attention_errors(out[t:t + 1], want)
+        assert ma <= MAX_ABS and rl <= REL_L2, (t, ma, rl)
