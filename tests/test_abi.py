@@ -132,6 +132,7 @@ def test_multiquery_workspace_routing(lib):
     assert lib.pkv_multiquery_workspace_size(4, 32, 16, 9, ctypes.byref(_desc(dtype=0)), None) == 0
     # more query heads than PKV_MAX_Q_HEADS: query-row counts would leave 32 bits
     assert lib.pkv_multiquery_workspace_size(4, 2048, 16, 65536, ctypes.byref(d), None) == 0
+    assert lib.pkv_multiquery_workspace_size(4, 1024, 16, 65536, ctypes.byref(d), None) == 256   # both limits
     assert lib.pkv_decode_workspace_size(4, 2048, 16, ctypes.byref(d), None) == 0
     # rejected before anything is enqueued: more than 65536 queries, float32 caches
     args = [FAKE, FAKE, FAKE, FAKE, 16, FAKE, FAKE, 4, 32]
