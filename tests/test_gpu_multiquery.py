@@ -167,6 +167,17 @@ def test_prefill_matches_oracle(pkv, name):
     check(out, want(c))
 
 
+@pytest.mark.parametrize("hq,hkv,mql", [(64, 2, 1), (64, 2, 3), (128, 1, 2)])
+def test_large_query_groups(pkv, hq, hkv, mql):
+    """32 and 128 query heads per KV head: 32 rows per (sequence, KV head)
+    still run on the split kernel, more on the tile kernel, where one query's
+    heads fill whole tiles."""
+    c = cases.multiquery_case(90 + hq + mql, [300, 17, 900], [mql] * 3, hq, hkv, 128, torch.bfloat16, poison=True)
+    out = run(pkv, c, dev(c), mql)
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want(c))
+
+
 def test_prefill_path_agrees_with_split_kernel(pkv):
     """The same 16-row call through both paths: max_query_len 4 (16 rows,
     split decode kernel) and 9 (36 rows, tensor-core tiles)."""
