@@ -1,214 +1,198 @@
-"""Page-table simulator: ref-counted physical blocks, prefix sharing, copy-on-write.
+"""Page-table simulator: reference-counted physical blocks, prefix sharing and
+copy-on-write. Test infrastructure: only the tests, the smoke check and the
+benchmark's CPU legs use it.
 
-Restates the behaviour of the page pool of "Notebook 10. KV cache and serving:
-bytes, pages, and ceilings", section 5 ("Page pool: prefix sharing and
-copy-on-write") and its section 6 trace, in code written for this oracle. The
-pool stores no tensors: it tracks, per physical block, a reference count and a
-fill (live slots), and per sequence a logical length and a page table (list of
-physical block ids; logical token ``t`` lives in ``table[t // B]`` at slot
-``t % B``).
+Behaviour follows "Notebook 10. KV cache and serving: bytes, pages, and
+ceilings": the page pool of section 5 (prefix sharing and copy-on-write), the
+eight-block trace of section 6 and the negative tests of section 9. The pool
+holds no tensor data. Logical token ``t`` of a sequence lives in physical
+block ``table[t // B]`` at slot ``t % B``.
 
-Behaviour that the pages fix and that the pins check:
+How this simulator is organised (its own design, not the notebook's code):
 
-* Free blocks form a stack. A fresh pool hands out ids in ascending order
-  (the stack starts as ``N-1 ... 0`` and pops from the end); released blocks
-  are pushed on top, so the most recently freed block is reused first.
-* ``append`` first counts the blocks it needs (one copy-on-write replacement
-  if the last block is partial *and* shared, plus enough new blocks for the
-  overflow) and raises ``MemoryError`` before touching anything if the free
-  stack is too short ("Allocation is preflighted, so OOM cannot leave a
-  partially mutated pool").
-* Copy-on-write happens only for a shared partial final block: the old block
-  loses one reference and a fresh block with the same number of filled slots
-  replaces it in the writer's table. A full shared block is never copied,
-  since appends start a new block.
-* ``share_prefix`` gives the target the source's first ``ceil(prefix/B)``
-  blocks and adds one reference to each.
-* A block's fill is the largest number of its slots that any sharer still
-  covers (sharers of unequal length, notebook section 5).
+* State is only what cannot be derived: each sequence's length and page
+  table, each block's reference count, and the free-id stack. How full a
+  block is, the payload, the waste and the sharing savings are derived from
+  the tables whenever they are asked for.
+* Every mutation is first turned into a plan (the number of ids it takes
+  from the stack and whether the last block must be privatised), the plan
+  is checked, and only then applied. A refused plan changes nothing, which is
+  the section 5 guarantee that running out of blocks never leaves a
+  half-applied append.
 
-The single addition for a real cache: every copy-on-write records the pair
-``(old_block, new_block)`` in ``copy_pairs``. The block-copy kernel must copy
-those blocks before the append writes into ``new_block``.
+Rules the pages fix, and the pins check:
+
+* The free ids are a last-in first-out stack. A fresh pool hands out
+  ``0, 1, 2, ...`` in that order; a released block goes on top and is the
+  next one handed out.
+* Appending to a sequence whose last block is partly filled *and* held by
+  another sequence first gives the writer a private replacement holding the
+  same filled slots (copy-on-write). A full shared block is never copied:
+  new tokens start a new block.
+* ``share_prefix`` hands the target the source's first ``ceil(prefix / B)``
+  blocks, one more reference each.
+* A block's fill is the largest number of its slots that any of its
+  sharers covers (sharers may have different lengths).
+
+Addition for a real cache: each copy-on-write records ``(old, new)`` in
+``copy_pairs``; the block-copy kernel must move those blocks before the step's
+append writes into ``new``.
 """
 
 from __future__ import annotations
 
-import math
 from typing import Hashable, Iterable
 
 
 def _count(name: str, value, minimum: int) -> int:
-    """Integer check that refuses bools (notebook section 1 validators)."""
+    """A plain ``int`` no smaller than ``minimum`` (bools are refused)."""
     if isinstance(value, bool) or not isinstance(value, int) or value < minimum:
-        raise ValueError(f"{name} must be an integer >= {minimum}")
+        raise ValueError(f"{name}: expected an int >= {minimum}, got {value!r}")
     return value
 
 
+def blocks_for(tokens: int, block_size: int) -> int:
+    """Blocks that hold ``tokens`` tokens: ceil(tokens / B) (0 for none)."""
+    return -(-tokens // block_size)
+
+
 class PagedKVPool:
-    """Ref-counted block pool with prefix sharing and copy-on-write.
+    """Reference-counted block pool with prefix sharing and copy-on-write.
 
     ``pop_order`` (optional) is the order in which a fresh pool hands out
-    block ids; by default ``0, 1, 2, ...`` exactly as the notebook's pool.
-    Passing a permutation relabels the physical ids without changing any
-    other behaviour (the invariance the decode kernel must respect).
+    block ids; by default ``0, 1, 2, ...`` as in the notebook. Another
+    permutation only renames the physical ids (the invariance the attention
+    kernels must respect).
     """
 
     def __init__(self, total_blocks: int, block_size: int = 16,
                  pop_order: Iterable[int] | None = None) -> None:
         self.total_blocks = _count("total_blocks", total_blocks, 1)
         self.block_size = _count("block_size", block_size, 1)
-        order = list(range(self.total_blocks)) if pop_order is None else [int(b) for b in pop_order]
-        if sorted(order) != list(range(self.total_blocks)):
-            raise ValueError("pop_order must be a permutation of the block ids")
-        # The stack pops from its end, so store the hand-out order reversed.
-        self._free: list[int] = order[::-1]
-        self._refs = [0] * self.total_blocks
-        self._fill = [0] * self.total_blocks
-        self._len: dict[Hashable, int] = {}
-        self._table: dict[Hashable, list[int]] = {}
+        hand_out = list(range(total_blocks)) if pop_order is None else [int(b) for b in pop_order]
+        if sorted(hand_out) != list(range(total_blocks)):
+            raise ValueError("pop_order: expected a permutation of 0 .. total_blocks - 1")
+        # top of the stack (the next id handed out) is the end of the list
+        self._stack: list[int] = hand_out[::-1]
+        self._refcount = [0] * total_blocks
+        self._length: dict[Hashable, int] = {}
+        self._pages: dict[Hashable, list[int]] = {}
         self.copy_pairs: list[tuple[int, int]] = []
 
-    # ------------------------------------------------------------ helpers
-    def _state(self, seq: Hashable) -> tuple[int, list[int]]:
-        if seq not in self._len:
-            raise KeyError(f"unknown sequence: {seq!r}")
-        return self._len[seq], self._table[seq]
+    # ------------------------------------------------------------ internals
+    def _lookup(self, seq: Hashable) -> tuple[int, list[int]]:
+        try:
+            return self._length[seq], self._pages[seq]
+        except KeyError:
+            raise KeyError(f"no sequence {seq!r} in this pool") from None
 
-    def _pop_block(self, filled: int) -> int:
-        block = self._free.pop()
-        self._refs[block] = 1
-        self._fill[block] = filled
-        return block
+    def _tail_needs_copy(self, length: int, pages: list[int]) -> bool:
+        """Whether writing past ``length`` must first privatise the last block."""
+        return length % self.block_size != 0 and self._refcount[pages[-1]] > 1
 
-    def _needed_blocks(self, length: int, table: list[int], count: int) -> int:
-        """Blocks an append of ``count`` tokens must take from the free stack."""
-        if count == 0:
-            return 0
+    def _take_ids(self, n: int) -> list[int]:
+        """Pop ``n`` ids off the stack (the caller has checked there are enough)."""
+        taken = [self._stack.pop() for _ in range(n)]
+        for b in taken:
+            self._refcount[b] += 1
+        return taken
+
+    def _fills(self) -> dict[int, int]:
+        """Derived fill of every referenced block: max over its sharers."""
         B = self.block_size
-        used_in_last = length % B
-        room = 0
-        need = 0
-        if table and used_in_last:
-            room = B - used_in_last
-            if self._refs[table[-1]] > 1:
-                need += 1  # private replacement for the shared partial block
-        overflow = max(0, count - room)
-        return need + (overflow + B - 1) // B
-
-    def _recount_fills(self) -> None:
-        """Fill of a block = max over its sharers of the slots they cover."""
-        B = self.block_size
-        fills = [0] * self.total_blocks
-        for seq, table in self._table.items():
-            n = self._len[seq]
-            for j, block in enumerate(table):
-                covered = min(B, n - j * B)
-                if covered > fills[block]:
-                    fills[block] = covered
-        self._fill = fills
+        fill: dict[int, int] = {}
+        for seq, pages in self._pages.items():
+            n = self._length[seq]
+            for j, b in enumerate(pages):
+                fill[b] = max(fill.get(b, 0), min(B, n - j * B))
+        return fill
 
     # ------------------------------------------------------------ mutators
     def create(self, seq: Hashable) -> None:
-        """Register an empty sequence; ids must be hashable and unique."""
+        """Register an empty sequence (hashable, not yet registered)."""
         hash(seq)
-        if seq in self._len:
-            raise ValueError(f"sequence already exists: {seq!r}")
-        self._len[seq] = 0
-        self._table[seq] = []
+        if seq in self._length:
+            raise ValueError(f"sequence {seq!r} is already registered")
+        self._length[seq] = 0
+        self._pages[seq] = []
 
     def append(self, seq: Hashable, token_count: int) -> None:
-        """Grow ``seq`` by ``token_count`` logical tokens.
+        """Grow ``seq`` by ``token_count`` tokens.
 
-        Raises ``MemoryError`` with the pool unchanged when the free stack
-        cannot cover the copy-on-write replacement plus the new blocks.
+        Raises ``MemoryError``, with nothing changed, when the stack holds
+        fewer ids than the plan needs (a private copy of a shared partial
+        last block, plus the blocks the new length adds).
         """
         count = _count("token_count", token_count, 0)
-        length, table = self._state(seq)
-        need = self._needed_blocks(length, table, count)
-        if need > len(self._free):
-            raise MemoryError(f"need {need} free blocks, {len(self._free)} remain")
-        if count == 0:
-            return
-        B = self.block_size
-        used_in_last = length % B
-        if table and used_in_last:
-            last = table[-1]
-            if self._refs[last] > 1:
-                self._refs[last] -= 1
-                fresh = self._pop_block(filled=used_in_last)
-                table[-1] = fresh
-                self.copy_pairs.append((last, fresh))
-                last = fresh
-            take = min(count, B - used_in_last)
-            self._fill[last] = used_in_last + take
-            length += take
-            count -= take
-        while count > 0:
-            take = min(count, B)
-            table.append(self._pop_block(filled=take))
-            length += take
-            count -= take
-        self._len[seq] = length
-        self._recount_fills()
-        self.validate()
+        length, pages = self._lookup(seq)
+        # plan
+        privatise = count > 0 and self._tail_needs_copy(length, pages)
+        grow = blocks_for(length + count, self.block_size) - len(pages)
+        cost = grow + int(privatise)
+        if cost > len(self._stack):
+            raise MemoryError(f"appending {count} tokens to {seq!r} takes {cost} blocks; "
+                              f"only {len(self._stack)} are free")
+        # apply
+        if privatise:
+            shared = pages[-1]
+            self._refcount[shared] -= 1
+            (pages[-1],) = self._take_ids(1)
+            self.copy_pairs.append((shared, pages[-1]))
+        pages.extend(self._take_ids(grow))
+        self._length[seq] = length + count
 
     def share_prefix(self, source: Hashable, target: Hashable, prefix_tokens: int) -> None:
-        """Create ``target`` whose first ``prefix_tokens`` tokens are ``source``'s."""
-        src_len, src_table = self._state(source)
+        """Register ``target`` holding the first ``prefix_tokens`` tokens of ``source``."""
+        src_len, src_pages = self._lookup(source)
         prefix = _count("prefix_tokens", prefix_tokens, 0)
         if prefix > src_len:
-            raise ValueError("prefix_tokens exceeds source length")
-        if target in self._len:
-            raise ValueError(f"target sequence already exists: {target!r}")
+            raise ValueError(f"{source!r} holds {src_len} tokens; cannot share {prefix}")
         hash(target)
-        shared = src_table[: -(-prefix // self.block_size)] if prefix else []
-        for block in shared:
-            self._refs[block] += 1
-        self._len[target] = prefix
-        self._table[target] = list(shared)
-        self.validate()
+        if target in self._length:
+            raise ValueError(f"sequence {target!r} is already registered")
+        pages = src_pages[:blocks_for(prefix, self.block_size)]
+        for b in pages:
+            self._refcount[b] += 1
+        self._length[target] = prefix
+        self._pages[target] = list(pages)
 
     def release(self, seq: Hashable) -> None:
-        """Drop ``seq``; blocks whose last reference goes are cleared and pushed."""
-        _, table = self._state(seq)
-        for block in table:
-            self._refs[block] -= 1
-            if self._refs[block] == 0:
-                self._fill[block] = 0
-                self._free.append(block)
-        del self._len[seq]
-        del self._table[seq]
-        self._recount_fills()
-        self.validate()
+        """Forget ``seq``; every block it held last goes back on the stack, in
+        table order (so its last such block is handed out next)."""
+        _, pages = self._lookup(seq)
+        del self._length[seq], self._pages[seq]
+        for b in pages:
+            self._refcount[b] -= 1
+            if self._refcount[b] == 0:
+                self._stack.append(b)
 
     def take_copy_pairs(self) -> list[tuple[int, int]]:
-        """Return and clear the copy-on-write pairs recorded so far."""
+        """The copy-on-write pairs recorded since the last call (then cleared)."""
         pairs, self.copy_pairs = self.copy_pairs, []
         return pairs
 
     # ------------------------------------------------------------ queries
     def sequence_length(self, seq: Hashable) -> int:
-        return self._state(seq)[0]
+        return self._lookup(seq)[0]
 
     def page_table(self, seq: Hashable) -> tuple[int, ...]:
-        return tuple(self._state(seq)[1])
+        return tuple(self._lookup(seq)[1])
 
     def slots(self, seq: Hashable, start: int, count: int) -> list[int]:
-        """Physical slot ids ``block * B + offset`` of logical tokens [start, start+count)."""
-        length, table = self._state(seq)
-        if start < 0 or start + count > length:
-            raise ValueError("token range outside the sequence")
+        """Slot ids ``block * B + offset`` of logical tokens ``start .. start+count-1``."""
+        length, pages = self._lookup(seq)
+        if start < 0 or count < 0 or start + count > length:
+            raise ValueError(f"tokens {start} .. {start + count - 1} are not all inside {seq!r}")
         B = self.block_size
-        return [table[t // B] * B + t % B for t in range(start, start + count)]
+        return [pages[t // B] * B + t % B for t in range(start, start + count)]
 
     @property
     def free_blocks(self) -> int:
-        return len(self._free)
+        return len(self._stack)
 
     @property
     def allocated_blocks(self) -> int:
-        return self.total_blocks - len(self._free)
+        return self.total_blocks - len(self._stack)
 
     @property
     def physical_capacity_tokens(self) -> int:
@@ -216,11 +200,11 @@ class PagedKVPool:
 
     @property
     def physical_payload_tokens(self) -> int:
-        return sum(f for f, r in zip(self._fill, self._refs) if r)
+        return sum(self._fills().values())
 
     @property
     def logical_tokens(self) -> int:
-        return sum(self._len.values())
+        return sum(self._length.values())
 
     @property
     def internal_waste_tokens(self) -> int:
@@ -231,66 +215,60 @@ class PagedKVPool:
         return self.logical_tokens - self.physical_payload_tokens
 
     def snapshot(self) -> dict:
-        """Deterministic summary with the notebook's field names."""
-        seqs = sorted(self._len, key=repr)
+        """Summary with the field names of the notebook's recorded trace."""
+        payload = self.physical_payload_tokens
         return {
-            "sequences": {str(s): {"length": self._len[s], "blocks": list(self._table[s])}
-                          for s in seqs},
+            "sequences": {str(s): {"length": self._length[s], "blocks": list(self._pages[s])}
+                          for s in sorted(self._length, key=repr)},
             "allocated_blocks": self.allocated_blocks,
             "free_blocks": self.free_blocks,
             "physical_capacity_tokens": self.physical_capacity_tokens,
-            "physical_payload_tokens": self.physical_payload_tokens,
+            "physical_payload_tokens": payload,
             "logical_tokens": self.logical_tokens,
-            "internal_waste_tokens": self.internal_waste_tokens,
-            "sharing_savings_tokens": self.sharing_savings_tokens,
+            "internal_waste_tokens": self.physical_capacity_tokens - payload,
+            "sharing_savings_tokens": self.logical_tokens - payload,
         }
 
     def validate(self) -> None:
-        """Invariants of notebook section 5: tables, references, fills, free stack."""
-        if len(set(self._free)) != len(self._free):
-            raise AssertionError("free stack holds a block twice")
-        if any(not 0 <= b < self.total_blocks for b in self._free):
-            raise AssertionError("free stack holds an invalid id")
-        refs = [0] * self.total_blocks
-        for seq, table in self._table.items():
-            n = self._len[seq]
-            if n < 0:
-                raise AssertionError("negative sequence length")
-            if len(table) != -(-n // self.block_size):
-                raise AssertionError("page table length disagrees with sequence length")
-            if len(set(table)) != len(table):
-                raise AssertionError("a sequence maps one block twice")
-            for b in table:
-                if not 0 <= b < self.total_blocks:
-                    raise AssertionError("page table holds an invalid id")
-                refs[b] += 1
-        free = set(self._free)
-        for b in range(self.total_blocks):
-            if refs[b] != self._refs[b]:
-                raise AssertionError("reference count disagrees with page tables")
-            if refs[b] == 0:
-                if b not in free or self._fill[b] != 0:
-                    raise AssertionError("unreferenced block is not clean and free")
-            else:
-                if b in free:
-                    raise AssertionError("referenced block sits on the free stack")
-                if not 1 <= self._fill[b] <= self.block_size:
-                    raise AssertionError("referenced block has an invalid fill")
+        """Check the pool's invariants; raises ``AssertionError`` on the first broken one."""
+        N, B = self.total_blocks, self.block_size
+        on_stack = [0] * N
+        for b in self._stack:
+            if not 0 <= b < N:
+                raise AssertionError(f"free stack holds id {b}, outside the pool")
+            on_stack[b] += 1
+        held = [0] * N
+        for seq, pages in self._pages.items():
+            n = self._length[seq]
+            if n < 0 or len(pages) != blocks_for(n, B):
+                raise AssertionError(f"{seq!r}: {len(pages)} blocks for {n} tokens")
+            if len(set(pages)) != len(pages):
+                raise AssertionError(f"{seq!r} maps one block twice")
+            for b in pages:
+                if not 0 <= b < N:
+                    raise AssertionError(f"{seq!r} maps id {b}, outside the pool")
+                held[b] += 1
+        for b in range(N):
+            if held[b] != self._refcount[b]:
+                raise AssertionError(f"block {b}: reference count {self._refcount[b]}, held by {held[b]}")
+            if on_stack[b] != (held[b] == 0):
+                raise AssertionError(f"block {b}: held by {held[b]} tables, {on_stack[b]} times on the stack")
+        for b, f in self._fills().items():
+            if not 1 <= f <= B:
+                raise AssertionError(f"block {b}: fill {f} outside 1 .. {B}")
         if self.logical_tokens < self.physical_payload_tokens:
-            raise AssertionError("physical payload exceeds logical payload")
+            raise AssertionError("more tokens stored than the sequences hold")
 
 
 class PrivatePagedKV:
-    """Private pages only (notebook "Lecture-level core"): no sharing, no copy.
-
-    ``append_to(seq, total)`` grows a sequence to ``total`` tokens, taking
-    ``ceil(total/B) - len(table)`` blocks from the free stack, all or none.
-    """
+    """Private pages only (the notebook's lecture-level core): no sharing, no
+    copy. ``append_to(seq, total)`` grows a sequence to ``total`` tokens with
+    all the blocks it needs from the stack, or none of them."""
 
     def __init__(self, n_blocks: int, block_size: int = 16) -> None:
         self.n_blocks = _count("n_blocks", n_blocks, 1)
         self.block_size = _count("block_size", block_size, 1)
-        self.free = list(range(self.n_blocks))[::-1]
+        self.free = list(range(n_blocks - 1, -1, -1))
         self.tables: dict[Hashable, list[int]] = {}
         self.lengths: dict[Hashable, int] = {}
 
@@ -298,21 +276,14 @@ class PrivatePagedKV:
         total = _count("total_tokens", total_tokens, 0)
         hash(seq)
         if total < self.lengths.get(seq, 0):
-            raise ValueError("append_to cannot shorten a sequence")
-        table = self.tables.get(seq, [])
-        need = -(-total // self.block_size) - len(table)
-        if need > len(self.free):
-            raise MemoryError("not enough free blocks")
-        self.tables[seq] = table
-        for _ in range(need):
-            table.append(self.free.pop())
+            raise ValueError(f"{seq!r} already holds more than {total} tokens")
+        pages = self.tables.get(seq, [])
+        extra = blocks_for(total, self.block_size) - len(pages)
+        if extra > len(self.free):
+            raise MemoryError(f"{seq!r} needs {extra} more blocks; only {len(self.free)} are free")
+        self.tables[seq] = pages + [self.free.pop() for _ in range(extra)]
         self.lengths[seq] = total
 
     def release(self, seq: Hashable) -> None:
         self.free.extend(self.tables.pop(seq))
         del self.lengths[seq]
-
-
-def blocks_for(tokens: int, block_size: int) -> int:
-    """Number of blocks that hold ``tokens`` tokens: ceil(tokens / B)."""
-    return math.ceil(tokens / block_size) if tokens else 0

@@ -186,3 +186,39 @@ def test_random_operations_keep_invariants_and_fill_accounting():
                     covered.add(pool.slots(n, t, 1)[0])
             assert pool.physical_payload_tokens == len(covered)
             assert pool.logical_tokens == sum(pool.sequence_length(n) for n in names)
+
+
+def test_released_blocks_are_handed_out_last_in_first_out():
+    """Section 5: released blocks go back on top of the free stack, so the
+    block freed last is the next one handed out."""
+    pool = PagedKVPool(6, 4)
+    for s, n in (("a", 4), ("b", 8), ("c", 4)):   # a: [0], b: [1, 2], c: [3]
+        pool.create(s)
+        pool.append(s, n)
+    pool.release("b")                            # pushes 1, then 2
+    pool.create("d")
+    pool.append("d", 12)
+    assert pool.page_table("d") == (2, 1, 4)
+    pool.release("a")
+    pool.release("c")
+    pool.create("e")
+    pool.append("e", 5)
+    assert pool.page_table("e") == (3, 0)
+
+
+def test_full_shared_block_is_never_copied():
+    """Section 5: copy-on-write applies only to a shared *partial* last block;
+    appending after a shared full block starts a new block and copies nothing
+    (the 4096-token shared prefix is 256 full blocks: zero copy pairs)."""
+    pool = PagedKVPool(8, 4)
+    pool.create("root")
+    pool.append("root", 8)
+    pool.share_prefix("root", "x", 8)
+    pool.append("x", 1)
+    assert pool.take_copy_pairs() == []
+    assert pool.page_table("x") == (0, 1, 2)
+    pool.share_prefix("x", "y", 9)               # shares x's partial last block 2
+    pool.append("y", 1)
+    assert pool.take_copy_pairs() == [(2, 3)]
+    assert pool.page_table("y") == (0, 1, 3) and pool.page_table("x") == (0, 1, 2)
+    pool.validate()
