@@ -24,12 +24,18 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import gather_tokens, softmax_attention, to_f64
+from .attention import gather_tokens, softmax_attention, to_f64  # noqa: F401  (softmax_attention: used by tests)
 
 
 def multiquery_attention(q, k_pool, v_pool, block_tables, context_lens, query_start, scale,
                          kv_heads: int, dtype: str, block_size: int = 16) -> np.ndarray:
-    """Float64 ``[total_queries][query_heads][d]``."""
+    """Float64 ``[total_queries][query_heads][d]``.
+
+    Per (sequence, KV head) the queries' logits against all ``n`` gathered
+    tokens are formed at once; a token a query may not see (position past
+    ``n - nq + t``) gets logit ``-inf``, i.e. weight exactly 0, so each row is
+    the softmax over its visible tokens only.
+    """
     total, query_heads, d = q.shape
     if query_heads % kv_heads:
         raise ValueError("query_heads must be a multiple of kv_heads")
@@ -40,11 +46,18 @@ def multiquery_attention(q, k_pool, v_pool, block_tables, context_lens, query_st
         n, nq = int(context_lens[i]), q1 - q0
         if nq > n:
             raise ValueError(f"sequence {i}: {nq} queries but {n} tokens")
-        for t in range(nq):
-            visible = n - nq + t + 1
-            for j in range(kv_heads):
-                K = to_f64(gather_tokens(k_pool, block_tables[i], visible, j, block_size), dtype)
-                V = to_f64(gather_tokens(v_pool, block_tables[i], visible, j, block_size), dtype)
-                qg = to_f64(q[q0 + t, j * G:(j + 1) * G], dtype)
-                out[q0 + t, j * G:(j + 1) * G] = softmax_attention(qg, K, V, scale)
+        if nq == 0:
+            continue
+        last_visible = n - nq + np.arange(nq)                       # query t sees tokens 0 .. last_visible[t]
+        visible = np.arange(n)[None, :] <= last_visible[:, None]   # [nq][n]
+        visible = np.repeat(visible, G, axis=0)                    # rows (t, g)
+        for j in range(kv_heads):
+            K = to_f64(gather_tokens(k_pool, block_tables[i], n, j, block_size), dtype)
+            V = to_f64(gather_tokens(v_pool, block_tables[i], n, j, block_size), dtype)
+            Q = to_f64(q[q0:q1, j * G:(j + 1) * G], dtype).reshape(nq * G, d)
+            logits = np.where(visible, scale * (Q @ K.T), -np.inf)
+            logits = logits - logits.max(axis=1, keepdims=True)
+            weights = np.exp(logits)
+            weights = weights / weights.sum(axis=1, keepdims=True)
+            out[q0:q1, j * G:(j + 1) * G] = (weights @ V).reshape(nq, G, d)
     return out
