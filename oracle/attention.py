@@ -18,7 +18,8 @@ So one output row is ``softmax(scale * K q) V`` with ``K``/``V`` the first
 ``context_lens[i]`` logical tokens gathered through the block table. bf16
 inputs widen to float64 exactly (a bf16 value is the top 16 bits of a
 float32). A sequence with no tokens has no keys to attend to; its output is
-defined as zeros (the pages call a zero-key decode "not a real decode query").
+defined as zeros (notebook section 3 notes that a decode with no keys is not
+a decode query that occurs in practice).
 
 Nothing here splits the context, reorders the sum or fuses steps.
 """

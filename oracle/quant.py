@@ -11,8 +11,8 @@ Sources:
   ``codes = clip(rint(x / scale), -limit, limit)``, dequantized value
   ``codes * scale``.
 
-Reading (the notebook dequantizes in float64 as "a numerical experiment, not
-a packed kernel"): a row is the ``head_dim`` coordinates of one token of one
+Reading (the notebook dequantizes in float64 and says the demo is an
+experiment on the numbers, not a storage format): a row is the ``head_dim`` coordinates of one token of one
 KV head. A packed cache stores the codes as int8 and the scale as a float32:
 ``scale = float32(max|x|) / float32(limit)`` rounded to float32 (max|x| of
 bf16 or float32 inputs is exact in float32); the code decision divides in
