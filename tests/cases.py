@@ -43,6 +43,54 @@ def padded_tables(pool: PagedKVPool, seqs, width: int | None = None) -> np.ndarr
     return out
 
 
+def simulate_workload_step(tables, lens_after, queries, num_blocks, shared_blocks=0):
+    """Rebuild a full-size workload's cache state with the oracle's page pool
+    and run the step's appends there.
+
+    Before the step sequence i holds ``lens_after[i] - queries`` tokens; the
+    step appends ``queries`` tokens to each sequence in index order. With
+    ``shared_blocks`` > 0 a root sequence holds that many full blocks and
+    every sequence starts as a copy of it (``share_prefix``). The pool hands
+    out ids in the order these operations request them, read off ``tables``,
+    so the simulator must end with exactly ``tables`` (asserted: the
+    workload's tables are a state the pool's rules can reach).
+
+    Returns ``(slots int64 [batch * queries] in sequence order, copy pairs
+    int64 [n][2])`` as the oracle's pool produces them.
+    """
+    tables = np.asarray(tables)
+    lens_after = np.asarray(lens_after, dtype=np.int64)
+    before = lens_after - queries
+    nb_before, nb_after = W.blocks_needed(before), W.blocks_needed(lens_after)
+    order = [int(b) for b in tables[0, :shared_blocks]] if shared_blocks else []
+    for i in range(len(lens_after)):
+        order += [int(b) for b in tables[i, shared_blocks:nb_before[i]]]
+    for i in range(len(lens_after)):
+        order += [int(b) for b in tables[i, nb_before[i]:nb_after[i]]]
+    taken = set(order)
+    assert len(taken) == len(order), "a block id is requested twice"
+    order += [b for b in range(num_blocks) if b not in taken]
+    pool = PagedKVPool(num_blocks, B, pop_order=order)
+    if shared_blocks:
+        pool.create("root")
+        pool.append("root", shared_blocks * B)
+    for i in range(len(lens_after)):
+        if shared_blocks:
+            pool.share_prefix("root", i, shared_blocks * B)
+        else:
+            pool.create(i)
+        pool.append(i, int(before[i]) - shared_blocks * B)
+    slots = []
+    for i in range(len(lens_after)):
+        start = pool.sequence_length(i)
+        pool.append(i, queries)
+        slots += pool.slots(i, start, queries)
+    pairs = np.array(pool.take_copy_pairs(), dtype=np.int64).reshape(-1, 2)
+    got = padded_tables(pool, range(len(lens_after)), width=tables.shape[1])
+    assert np.array_equal(got, tables), "the page pool does not reach the workload's tables"
+    return np.array(slots, dtype=np.int64), pairs
+
+
 def tiny_case(dtype=torch.float32, head_dim=64, q_heads=4, kv_heads=2, poison=False):
     """The 3-sequence workload: seq 1 holds 9 tokens, seq 0 shares its first 6
     (a shared partial block), seq 2 holds 33; then one step appends one token
