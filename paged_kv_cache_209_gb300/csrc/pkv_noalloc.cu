@@ -13,6 +13,8 @@
 // The array below lives in device memory on every GPU that loads the library,
 // from module load until the process exits. Its size is the hard limit of
 // this entry point.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "pkv.h"
@@ -27,20 +29,54 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Process-unique id of the context current on this thread (0 if the driver
+// cannot say). A cudaDeviceReset destroys the device's primary context, and
+// the array with it; the runtime's next call creates a new context with a new
+// id, where the array has a new address.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 // Device address of the scratch array for the current device. In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached. Returns nullptr if
-// the lookup fails.
+// (with the device current) at set-up: on the first call on a device, and
+// again on the first call after the device's context was replaced (a
+// cudaDeviceReset). Returns nullptr if the lookup fails.
 unsigned char* scratch_address() {
     static std::mutex mu;
     static unsigned char* addr[kMaxDevices] = {};
+    static unsigned long long ctx_of[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned long long ctx = current_context_id();
+    if (ctx == 0 && cudaSetDevice(dev) == cudaSuccess) ctx = current_context_id();  // make the primary context current
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    if (addr[dev] == nullptr || ctx != ctx_of[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_pkv_noalloc_scratch) != cudaSuccess) return nullptr;
         addr[dev] = static_cast<unsigned char*>(p);
+        ctx_of[dev] = ctx;
     }
     return addr[dev];
 }
@@ -53,6 +89,7 @@ extern "C" pkv_status pkv_decode_attention_noalloc(const void* q, const void* k_
                                                    int32_t num_q_heads, float scale, void* out,
                                                    const pkv_cache_desc* desc, uint32_t flags,
                                                    const pkv_decode_opts* opts, void* stream) {
+    pkv::NvtxRange nvtx_range("pkv_decode_attention_noalloc");
     if (desc == nullptr) return PKV_ERR_NULL;
     if (batch == 0) return pkv_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                                 context_lens, batch, num_q_heads, scale, out, nullptr, 0, desc,

@@ -189,6 +189,23 @@ def test_split_count_invariance(pkv, num_ctas):
     assert diff <= 2 ** -7, diff   # one bf16 ulp of an O(1) value at most
 
 
+@pytest.mark.parametrize("num_ctas", [2, 3, 7, 64, 1000, 5000])
+def test_split_count_invariance_fp32(pkv, num_ctas):
+    """fp32 caches and fp32 output (CUDA-core kernel): cutting the contexts
+    at any CTA count changes the result only by fp32 reassociation of the
+    pieces' log-sum-exp merge, ~1e-6 relative against the one-CTA run (no
+    output rounding hides a merge error here)."""
+    c = cases.random_case(32, [1, 17, 200, 1024, 4097, 33], 32, 8, 128, torch.float32)
+    args = (dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]), c["tables"], c["lens"], c["scale"])
+    ref = run_attention(pkv, *args, kernel=1, num_ctas=1)
+    got = run_attention(pkv, *args, kernel=1, num_ctas=num_ctas)
+    check_close(got, oracle_attention(c, c["tables"], c["lens"]), rel=2e-5)
+    rel = ((got - ref).norm() / ref.norm()).item()
+    ma = (got - ref).abs().max().item()
+    print(f"num_ctas={num_ctas}: relative L2 {rel:.2e}, max-abs {ma:.2e} against one CTA")
+    assert rel <= 1e-6 and ma <= 1e-5, (rel, ma)
+
+
 def test_block_relabelling_gives_identical_output(pkv):
     c = cases.random_case(31, [3, 18, 35, 700], 32, 8, 128, torch.bfloat16, extra_blocks=11)
     nb = c["k_pool"].shape[0]
@@ -366,3 +383,46 @@ def test_bounded_wait_runs_out_and_is_reported(pkv):
     with pytest.raises(pkv.PkvError) as e:      # the hook exists for the tensor-core kernel only
         run_attention(pkv, *args, kernel=1, flags=pkv.PKV_FLAG_TEST_STALL)
     assert e.value.name == "PKV_ERR_UNSUPPORTED"
+
+
+def test_checked_decode_rejects_a_zero_length_context(pkv):
+    """A context of length 0 is no decode query: checked mode rejects it with
+    PKV_ERR_RANGE and writes nothing; the default mode writes a zero row."""
+    c = cases.random_case(37, [20, 0, 40], 8, 2, 128, torch.bfloat16)
+    args = (dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]), c["tables"], c["lens"], c["scale"])
+    out = torch.full((3, 8, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        run_attention(pkv, *args, out=out, flags=pkv.PKV_FLAG_CHECKED)
+    assert e.value.name == "PKV_ERR_RANGE"
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
+    got = run_attention(pkv, *args, out=out)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert torch.all(got[1] == 0)
+    check_close(got, oracle_attention(c, c["tables"], c["lens"]))
+
+
+def test_device_status_is_shared_by_streams_and_sticky(pkv):
+    """The sticky status is one word per device: a bit set by a call on one
+    stream is seen from another stream, no later call clears it (successful
+    or not), and only an explicit clear resets it."""
+    c = cases.random_case(38, [20, 40], 4, 2, 64, torch.bfloat16)
+    bad = c["tables"].copy()
+    bad[1, 2] = 10 ** 6
+    a, b = torch.cuda.Stream(), torch.cuda.Stream()
+    args = (dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]))
+    torch.cuda.synchronize()
+    pkv.pkv_device_status(clear=True)
+    with torch.cuda.stream(a):
+        run_attention(pkv, *args, bad, c["lens"], c["scale"], stream=a)
+    a.synchronize()
+    with torch.cuda.stream(b):
+        good = run_attention(pkv, *args, c["tables"], c["lens"], c["scale"], stream=b)
+    assert pkv.pkv_device_status(clear=False, stream=b) & pkv.PKV_DEVERR_RANGE
+    with torch.cuda.stream(b):
+        run_attention(pkv, *args, c["tables"], c["lens"], c["scale"], stream=b)
+    assert pkv.pkv_device_status(clear=False, stream=a) & pkv.PKV_DEVERR_RANGE
+    assert pkv.pkv_device_status(clear=True, stream=b) & pkv.PKV_DEVERR_RANGE
+    assert pkv.pkv_device_status(clear=False, stream=a) == 0
+    check_close(good, oracle_attention(c, c["tables"], c["lens"]))
