@@ -25,9 +25,9 @@
  *    stream) and returns without waiting, except in PKV_FLAG_CHECKED mode.
  *  - Host-visible arguments are validated before anything is enqueued. A call
  *    that returns an error status has written no byte of any output buffer
- *    ("validate first; keep old state intact if an input is rejected",
- *    notebook "PyTorch bridge - B17"; "OOM cannot leave a partially mutated
- *    pool", notebook section 5).
+ *    (notebook "PyTorch bridge - B17": inputs are checked before any state
+ *    changes, and a rejected input leaves the old state as it was; notebook
+ *    section 5: running out of blocks never leaves a half-updated pool).
  *  - Indices that live in device memory (slot ids, block ids, context
  *    lengths, copy pairs) are checked on the device:
  *      * default (fast) mode: an out-of-range entry is never dereferenced; it
@@ -196,23 +196,29 @@ PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
  *     s_t = scale * dot(q[i][h], K_j(t)),  t < n
  *     out[i][h] = sum_t softmax(s)_t * V_j(t)
  * where K_j(t) / V_j(t) is row t % 16 of KV head j in block
- * block_tables[i][t / 16]. n == 0 gives a zero row. Accumulation is fp32;
+ * block_tables[i][t / 16]. n == 0 gives a zero row in the default mode (a
+ * query with no keys; notebook section 3 notes it does not occur in a real
+ * decode, so PKV_FLAG_CHECKED rejects it, below). Accumulation is fp32;
  * out is written once, rounded to nearest-even into desc->dtype. One kernel
  * launch per 1024 sequences.
  *
  *   q             device, [batch][num_q_heads][head_dim], desc->dtype.
  *   block_tables  device, int32 [batch][max_blocks_per_seq]; entries at
  *                 index >= ceil(n/16) are never read.
- *   context_lens  device, int32 [batch], 0 <= n <= max_blocks_per_seq*16.
+ *   context_lens  device, int32 [batch], 0 <= n <= max_blocks_per_seq*16
+ *                 (1 <= n with PKV_FLAG_CHECKED).
  *   out           device, [batch][num_q_heads][head_dim], desc->dtype.
  *   workspace     device, >= pkv_decode_workspace_size(...) bytes, 256-byte
  *                 aligned, zero-filled before its first use (see above).
  *   opts          NULL or tuning (above).
  * Errors: host-side checks as above plus num_q_heads % num_kv_heads != 0
  * (PKV_ERR_SHAPE) and a short workspace (PKV_ERR_WORKSPACE); with
- * PKV_FLAG_CHECKED a context length outside [0, max_blocks_per_seq*16] or a
+ * PKV_FLAG_CHECKED a context length outside [1, max_blocks_per_seq*16] or a
  * block id outside [0, num_blocks) among the blocks a sequence uses gives
  * PKV_ERR_RANGE. batch may exceed any internal limit: the call splits it.
+ * `opts` is an addition to the pages' argument list (q, caches, tables,
+ * lengths, scale, out): kernel choice and CTA count for tests and tuning;
+ * NULL keeps the defaults.
  */
 PKV_API pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -430,7 +436,9 @@ PKV_API pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, c
  *    wrong results. Order them, e.g. issue them on one stream.
  *  - The first call on each device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
- *    stream capture begins.
+ *    stream capture begins. cudaDeviceReset destroys the array with the
+ *    device's context; the first call after it (in the new context) looks the
+ *    address up again, so it too belongs before any capture.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
 PKV_API pkv_status pkv_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
@@ -521,6 +529,15 @@ PKV_API pkv_status pkv_pool_validate(const pkv_pool* pool);
  * pkv_device_status -- read (and with clear != 0, reset) the sticky device
  * status of the current device: an OR of PKV_DEVERR_* bits set by kernels
  * since the last clear. Waits for `stream`. Returns PKV_OK or PKV_ERR_CUDA.
+ *
+ * The status is one word per device, shared by every caller, stream and
+ * thread of the process that uses the library on that device: a bit set by
+ * any call's kernel stays set (no later call clears it, successful or not)
+ * until some caller clears it here. A clear therefore also clears bits that
+ * other callers' kernels set; a caller that needs its own verdict should
+ * read without clearing, or use PKV_FLAG_CHECKED, whose verdict is returned
+ * by the call itself. Reading waits only for `stream`: kernels still running
+ * on other streams may set bits after the read.
  */
 PKV_API pkv_status pkv_device_status(uint32_t* bits_out, int clear, void* stream);
 

@@ -70,9 +70,13 @@ pkv_status check_desc(const pkv_cache_desc* d) {
     return PKV_OK;
 }
 
-// Runs one validation launch in checked mode and waits for its verdict.
+// Runs one validation launch in checked mode and waits for its verdict. The
+// verdict word is one per device, so checked calls from different host
+// threads take turns (each waits for its verdict before releasing it).
 template <typename F>
 pkv_status run_checked(F launch, cudaStream_t s) {
+    static std::mutex verdict_mu;
+    std::lock_guard<std::mutex> lock(verdict_mu);
     unsigned int* status = device_info().status;
     if (status == nullptr) return PKV_ERR_CUDA;
     unsigned int* verdict = status + 1;
@@ -134,6 +138,7 @@ int32_t pkv_version(void) { return 100; }
 
 pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                       void* v_cache, const pkv_cache_desc* desc, uint32_t flags, void* stream) {
+    NvtxRange nvtx_range("pkv_append");
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
     if (num_tokens < 0) return PKV_ERR_SHAPE;
@@ -158,6 +163,7 @@ pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping,
 
 pkv_status pkv_copy_blocks(const int64_t* pairs, int64_t num_pairs, void* k_cache, void* v_cache,
                            const pkv_cache_desc* desc, uint32_t flags, void* stream) {
+    NvtxRange nvtx_range("pkv_copy_blocks");
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
     if (num_pairs < 0) return PKV_ERR_SHAPE;
@@ -194,6 +200,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
                                 int32_t num_q_heads, float scale, void* out, void* workspace,
                                 size_t workspace_bytes, const pkv_cache_desc* desc, uint32_t flags,
                                 const pkv_decode_opts* opts, void* stream) {
+    NvtxRange nvtx_range("pkv_decode_attention");
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
     if (batch < 0 || !q_heads_ok(num_q_heads, desc)) return PKV_ERR_SHAPE;
@@ -219,7 +226,7 @@ pkv_status pkv_decode_attention(const void* q, const void* k_cache, const void* 
     if (flags & PKV_FLAG_CHECKED) {
         st = run_checked([&](unsigned int* verdict) {
             return launch_check_decode(block_tables, max_blocks_per_seq, context_lens, batch, desc->num_blocks,
-                                       verdict, s);
+                                       1, verdict, s);
         }, s);
         if (st != PKV_OK) return st;
     }
@@ -276,6 +283,7 @@ pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, con
                                          int32_t num_groups, int32_t max_group_blocks, void* out, void* workspace,
                                          size_t workspace_bytes, const pkv_cache_desc* desc, uint32_t flags,
                                          const pkv_decode_opts* opts, void* stream) {
+    NvtxRange nvtx_range("pkv_decode_attention_prefixed");
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
     if (num_groups < 0 || max_group_blocks < 0 || max_group_blocks > max_blocks_per_seq) return PKV_ERR_SHAPE;
@@ -325,7 +333,7 @@ pkv_status pkv_decode_attention_prefixed(const void* q, const void* k_cache, con
     if (flags & PKV_FLAG_CHECKED) {
         st = run_checked([&](unsigned int* verdict) {
             cudaError_t e = launch_check_decode(block_tables, max_blocks_per_seq, context_lens, batch,
-                                                desc->num_blocks, verdict, s);
+                                                desc->num_blocks, 1, verdict, s);
             if (e != cudaSuccess) return e;
             return launch_check_groups(block_tables, max_blocks_per_seq, context_lens, prefix_group, group_blocks,
                                        num_groups, max_group_blocks, batch, verdict, s);
@@ -417,6 +425,7 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
                                     int32_t num_q_heads, int32_t max_query_len, float scale, void* out,
                                     void* workspace, size_t workspace_bytes, const pkv_cache_desc* desc,
                                     uint32_t flags, const pkv_decode_opts* opts, void* stream) {
+    NvtxRange nvtx_range("pkv_multiquery_attention");
     pkv_status st = check_desc(desc);
     if (st != PKV_OK) return st;
     if (batch < 0 || !q_heads_ok(num_q_heads, desc)) return PKV_ERR_SHAPE;
@@ -446,7 +455,7 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
     if (flags & PKV_FLAG_CHECKED) {
         st = run_checked([&](unsigned int* verdict) {
             cudaError_t e = launch_check_decode(block_tables, max_blocks_per_seq, context_lens, batch,
-                                                desc->num_blocks, verdict, s);
+                                                desc->num_blocks, 0, verdict, s);
             if (e != cudaSuccess) return e;
             return launch_check_queries(context_lens, query_start, batch, max_query_len, verdict, s);
         }, s);
@@ -511,6 +520,7 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
 pkv_status pkv_append_q8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_codes,
                          void* v_codes, float* k_scales, float* v_scales, const pkv_cache_desc* desc, uint32_t flags,
                          void* stream) {
+    NvtxRange nvtx_range("pkv_append_q8");
     pkv_status st = check_desc_q8(desc, false);
     if (st != PKV_OK) return st;
     if (num_tokens < 0) return PKV_ERR_SHAPE;
@@ -537,6 +547,7 @@ pkv_status pkv_append_q8(const void* k, const void* v, const int64_t* slot_mappi
 
 pkv_status pkv_copy_blocks_q8(const int64_t* pairs, int64_t num_pairs, void* k_codes, void* v_codes, float* k_scales,
                               float* v_scales, const pkv_cache_desc* desc, uint32_t flags, void* stream) {
+    NvtxRange nvtx_range("pkv_copy_blocks_q8");
     pkv_status st = check_desc_q8(desc, false);
     if (st != PKV_OK) return st;
     if (num_pairs < 0) return PKV_ERR_SHAPE;
@@ -578,6 +589,7 @@ pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const voi
                                    int32_t num_q_heads, int32_t max_query_len, float scale, void* out,
                                    void* workspace, size_t workspace_bytes, const pkv_cache_desc* desc,
                                    uint32_t flags, const pkv_decode_opts* opts, void* stream) {
+    NvtxRange nvtx_range("pkv_decode_attention_q8");
     pkv_status st = check_desc_q8(desc, true);
     if (st != PKV_OK) return st;
     if (batch < 0 || !q_heads_ok(num_q_heads, desc)) return PKV_ERR_SHAPE;
@@ -606,7 +618,7 @@ pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const voi
     if (flags & PKV_FLAG_CHECKED) {
         st = run_checked([&](unsigned int* verdict) {
             cudaError_t e = launch_check_decode(block_tables, max_blocks_per_seq, context_lens, batch,
-                                                desc->num_blocks, verdict, s);
+                                                desc->num_blocks, query_start ? 0 : 1, verdict, s);
             if (e != cudaSuccess || query_start == nullptr) return e;
             return launch_check_queries(context_lens, query_start, batch, max_query_len, verdict, s);
         }, s);

@@ -7,9 +7,22 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "pkv.h"
 
 namespace pkv {
+
+// An NVTX range named after the API call, open for the call's host-side
+// duration (argument checks and kernel launches). Profilers (Nsight Systems,
+// Nsight Compute with --nvtx) show it; without a profiler attached a push or
+// pop costs one indirect call.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ---------------------------------------------------------------- KV moves
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int64_t num_tokens, void* k_cache,
@@ -23,8 +36,11 @@ cudaError_t launch_check_slots(const int64_t* slots, int64_t num_tokens, int64_t
                                cudaStream_t s);
 cudaError_t launch_check_pairs(const int64_t* pairs, int64_t num_pairs, int64_t num_blocks, unsigned int* verdict,
                                cudaStream_t s);
+// Context lengths must lie in [min_len, max_blocks * 16]: min_len is 1 for the
+// decode calls (a zero-length context is no decode query) and 0 where a
+// sequence may carry no queries (multi-query calls).
 cudaError_t launch_check_decode(const int32_t* tables, int32_t max_blocks, const int32_t* lens, int32_t batch,
-                                int64_t num_blocks, unsigned int* verdict, cudaStream_t s);
+                                int64_t num_blocks, int32_t min_len, unsigned int* verdict, cudaStream_t s);
 
 constexpr unsigned int kVerdictRange = 1u;
 constexpr unsigned int kVerdictOverlap = 2u;

@@ -106,10 +106,10 @@ __global__ void check_pairs_kernel(const int64_t* __restrict__ pairs, int64_t n,
 
 __global__ void check_decode_kernel(const int32_t* __restrict__ tables, int32_t max_blocks,
                                     const int32_t* __restrict__ lens, int32_t batch, int64_t num_blocks,
-                                    unsigned int* verdict) {
+                                    int32_t min_len, unsigned int* verdict) {
     for (int i = blockIdx.x; i < batch; i += gridDim.x) {
         const int32_t n = lens[i];
-        if (n < 0 || static_cast<int64_t>(n) > static_cast<int64_t>(max_blocks) * 16) {
+        if (n < min_len || static_cast<int64_t>(n) > static_cast<int64_t>(max_blocks) * 16) {
             if (threadIdx.x == 0) atomicOr(verdict, kVerdictRange);
             continue;
         }
@@ -156,9 +156,9 @@ cudaError_t launch_check_pairs(const int64_t* pairs, int64_t n, int64_t num_bloc
 }
 
 cudaError_t launch_check_decode(const int32_t* tables, int32_t max_blocks, const int32_t* lens, int32_t batch,
-                                int64_t num_blocks, unsigned int* verdict, cudaStream_t s) {
+                                int64_t num_blocks, int32_t min_len, unsigned int* verdict, cudaStream_t s) {
     const int grid = batch < 1024 ? batch : 1024;
-    check_decode_kernel<<<grid, 256, 0, s>>>(tables, max_blocks, lens, batch, num_blocks, verdict);
+    check_decode_kernel<<<grid, 256, 0, s>>>(tables, max_blocks, lens, batch, num_blocks, min_len, verdict);
     return cudaGetLastError();
 }
 
