@@ -156,6 +156,19 @@ __device__ __forceinline__ int sigma(int m) {
 // within a few fp32 steps of 1152 * sum |q|, below 2^-16 of the largest
 // score the row could reach.
 constexpr float kCodeBias = 1152.f;
+// Largest V scale for which P' = P * s_v (P <= 2^8 under the lazy rescale)
+// stays below the f16 maximum 65504 (255 * 256 = 65280).
+constexpr float kVScaleF16Safe = 255.f;
+
+// Smallest k in [0, 126] with v * 2^-k <= limit (halvings of a float are exact).
+__device__ __noinline__ int pow2_shift_to_fit(float v, float limit) {
+    int k = 0;
+    while (v > limit && k < 126) {
+        v *= 0.5f;
+        ++k;
+    }
+    return k;
+}
 __device__ __forceinline__ void codes_to_f16x2_biased(uint32_t w, uint32_t& p01, uint32_t& p23) {
     const uint32_t u = w ^ 0x80808080u;
     p01 = __byte_perm(u, 0x64646464u, 0x5140);
@@ -604,7 +617,30 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                 l0 += e0 + e2;
                 l1 += e1 + e3;
                 // P' = P times the V scale of its token (zero past the context), as f16
-                const float vA = pA < n_ctx ? vsc[tokA] : 0.f, vB = pB < n_ctx ? vsc[tokB] : 0.f;
+                float vA = pA < n_ctx ? vsc[tokA] : 0.f, vB = pB < n_ctx ? vsc[tokB] : 0.f;
+                // P <= 2^8 under the lazy rescale, so P' stays below the f16
+                // maximum while every V scale is at most kVScaleF16Safe. A block
+                // with a larger scale (rows with max |v| above ~32 000) runs its
+                // product on P' 2^-k and O 2^-k, and O is scaled back by 2^k
+                // afterwards: powers of two, exact in fp32.
+                float o_back = 1.f;
+                if (__any_sync(0xffffffffu, fmaxf(vA, vB) > kVScaleF16Safe)) {
+                    float vm = fmaxf(vA, vB);
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                    const int k2 = vm <= 3.0e38f ? pow2_shift_to_fit(vm, kVScaleF16Safe) : 0;
+                    const float down = __uint_as_float(static_cast<uint32_t>(127 - k2) << 23);
+                    o_back = __uint_as_float(static_cast<uint32_t>(127 + k2) << 23);
+                    vA *= down;
+                    vB *= down;
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        o[i][0] *= down;
+                        o[i][1] *= down;
+                        o[i][2] *= down;
+                        o[i][3] *= down;
+                    }
+                }
                 const uint32_t bh0 = movmatrix_trans(pack_f16x2(e0 * vA, e1 * vA));
                 const uint32_t bh1 = movmatrix_trans(pack_f16x2(e2 * vB, e3 * vB));
                 // ---- O^T += V^T P'^T: V coordinate rows of 16 token codes
@@ -619,6 +655,15 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                     codes_to_f16x2(w2, a0, a2);
                     codes_to_f16x2(w3, a1, a3);
                     mma_f16_16816(o[2 * ii + 1], a0, a1, a2, a3, bh0, bh1);
+                }
+                if (o_back != 1.f) {
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        o[i][0] *= o_back;
+                        o[i][1] *= o_back;
+                        o[i][2] *= o_back;
+                        o[i][3] *= o_back;
+                    }
                 }
             }
             __syncwarp();

@@ -195,6 +195,28 @@ def test_wide_scales_and_large_queries(pkv):
     assert ma <= MAX_ABS * max(1.0, float(np.abs(ref).max())) and rl <= REL_L2, (ma, rl)
 
 
+@pytest.mark.parametrize("vmax", [4.0e4, 1.0e6, 1.0e20])
+@pytest.mark.parametrize("multi", [False, True])
+def test_v_rows_beyond_the_f16_range_of_p(pkv, vmax, multi):
+    """V rows whose largest magnitude is above ~32 000 (a V scale above 255)
+    would take P' = P * s_v past the f16 maximum. The kernel runs a block
+    holding such a row on P' and O scaled down by a power of two and scales
+    O back, so the output still matches the oracle (relative bars: the
+    output is as large as V). Sequence 0 has only such rows; in the others a
+    fifth of the rows are."""
+    c = q8_case(79, [90, 200, 33, 700], 32, 8, nqs=[3, 1, 2, 4] if multi else None)
+    rng = np.random.default_rng(9)
+    big = rng.random(c["vs"].shape) < 0.2
+    big[c["tables"][0, :6]] = True
+    c["vs"] = np.where(big, np.float32(vmax / 127), c["vs"]).astype(np.float32)
+    out = run_q8(pkv, c, max_query_len=4 if multi else 1)
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert bool(torch.isfinite(out.float()).all())
+    ref = want_q8(c)
+    ma, rl = cases.attention_errors(out, ref)
+    assert ma <= MAX_ABS * max(1.0, float(np.abs(ref).max())) and rl <= REL_L2, (ma, rl)
+
+
 def test_host_rejections(pkv):
     c = q8_case(9, [30, 40], 32, 8)
     with pytest.raises(pkv.PkvError) as e:
