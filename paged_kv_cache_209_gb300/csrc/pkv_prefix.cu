@@ -60,8 +60,17 @@ __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 // [12] P store and arrival, [13] MMA wait for P, [14] MMA wait for K/V,
 // [15] TMA wait for a free stage.
 #ifdef PKV_TRACE
-#define PX_STAMP(a, i, v) \
-    (reinterpret_cast<unsigned long long*>((a).trace))[((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 16 + (i)] = (v)
+// Launches without a workspace slot for the stamps (chunked prefill) write
+// them here instead, for the first 65536 CTAs.
+__device__ unsigned long long g_px_trace[65536 * 16];
+#define PX_CTA() ((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x)
+#define PX_STAMP(a, i, v)                                                                    \
+    do {                                                                                     \
+        if ((a).trace != nullptr)                                                            \
+            (reinterpret_cast<unsigned long long*>((a).trace))[PX_CTA() * 16 + (i)] = (v);   \
+        else if (PX_CTA() < 65536)                                                           \
+            g_px_trace[PX_CTA() * 16 + (i)] = (v);                                           \
+    } while (0)
 #define PX_T(var) const unsigned long long var = global_ns()
 #define PX_ADD(acc, v) acc += (v)
 #else
@@ -616,16 +625,24 @@ struct Ux {
     static constexpr int kOffKV = kOffQ + kQBytes;
     static constexpr int kOffX = kOffKV + kStages * kStageBytes;
     static constexpr int kOffBars = kOffX + 3 * kRows * 4;
-    static constexpr int kNumBars = 2 * kStages + 7;  // kv_full, kv_empty, s_full[2], p_full[2], o_done[2], final
+    // k_full, k_empty, v_full, v_empty (per stage), s_full[2], p_full[2], o_done[2], final (PV issuer),
+    // s_free[2], final (S issuer)
+    static constexpr int kNumBars = 4 * kStages + 10;
     static constexpr int kOffInts = kOffBars + kNumBars * 8;
     static constexpr size_t kSmem =
         1024 + kOffInts + (16 + member_slots(kRows) + kMaxGroups + 2 * kMaxBatchPerLaunch + kMaxGroups) * 4;
     // warps 0-7 softmax: warp w takes rows 32 (w % 4) .. + 31 (its tensor-memory
-    // lanes) and token half w / 4 of every step; warp 8 TMA, warp 9 MMA
+    // lanes) and token half w / 4 of every step; warps 8 and 11 copy K and V
+    // (separate rings: a K stage is free once its score product is done, long
+    // before the V stage of the same step); warp 9 issues the P.V products,
+    // warp 10 the score products (two issuing threads, so that one's waits
+    // never hold back the other's stream of tensor-core work)
     static constexpr int kSoftmaxWarps = 8;
     static constexpr int kTmaWarp = 8;
     static constexpr int kMmaWarp = 9;
-    static constexpr int kThreads = 320;
+    static constexpr int kSWarp = 10;
+    static constexpr int kTmaVWarp = 11;
+    static constexpr int kThreads = 384;
     static constexpr uint32_t kColS = 0;    // S buffers: columns [0, 64) and [64, 128)
     static constexpr uint32_t kColO = 128;  // O of token half 0: [128, 128 + D); half 1: [128 + D, 128 + 2D)
     // P buffers b = 0, 1 at kColP + 64 b: bf16 pairs, hi in the first 32
@@ -644,12 +661,16 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     using C = Ux<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-    uint64_t* kv_empty = kv_full + C::kStages;
-    uint64_t* s_full = kv_empty + C::kStages;  // [2]: S buffer b holds a finished S
+    uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+    uint64_t* k_empty = k_full + C::kStages;
+    uint64_t* v_full = k_empty + C::kStages;
+    uint64_t* v_empty = v_full + C::kStages;
+    uint64_t* s_full = v_empty + C::kStages;  // [2]: S buffer b holds a finished S
     uint64_t* p_full = s_full + 2;             // [2]: P buffer b written (one arrival per softmax warp)
     uint64_t* o_done = p_full + 2;             // [2]: the PV product of step j (buffer j % 2) has completed
-    uint64_t* final_bar = o_done + 2;          // every issued MMA has completed
+    uint64_t* final_bar = o_done + 2;          // every P.V product has completed
+    uint64_t* s_free = final_bar + 1;          // [2]: S buffer b has been read (one arrival per softmax warp)
+    uint64_t* final_s = s_free + 2;            // every score product has completed
     int* info = reinterpret_cast<int*>(smem + C::kOffInts);
     int* members = info + 16;
     int* counts = members + member_slots(C::kRows);
@@ -668,8 +689,10 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         PX_STAMP(a, 6, sm_id());
         PX_STAMP(a, 7, 0);
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
@@ -677,6 +700,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             mbar_init(&o_done[b], 1);
         }
         mbar_init(final_bar, 1);
+        for (int b = 0; b < 2; ++b) mbar_init(&s_free[b], C::kSoftmaxWarps);
+        mbar_init(final_s, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -739,19 +764,24 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         fence_proxy_async_smem();
     }
     uint32_t tmem = 0;
-    if (warp != C::kTmaWarp) {
+    if (warp != C::kTmaWarp && warp != C::kTmaVWarp) {
         tc_fence_before();
-        named_barrier_sync(2, C::kThreads - 32);  // every warp but the TMA warp
+        named_barrier_sync(2, C::kThreads - 64);  // every warp but the two TMA warps
         tc_fence_after();
         tmem = *tmem_slot;
     }
     if (threadIdx.x == 0) PX_STAMP(a, 2, global_ns());
 
-    if (warp == C::kTmaWarp) {
-        // ------------------------------------------------ TMA producer
+    if (warp == C::kTmaWarp || warp == C::kTmaVWarp) {
+        // ------------------------------------------------ TMA producers (K, V)
         // Step j: blocks 4j .. 4j+3 of the chunk; lane b issues block b. A
         // block past the chunk or with an invalid id is loaded from row -16
         // (wholly out of range), which fills its box with zeros.
+        const bool is_k = warp == C::kTmaWarp;
+        uint64_t* full = is_k ? k_full : v_full;
+        uint64_t* empty = is_k ? k_empty : v_empty;
+        const CUtensorMap* map = is_k ? &tmK : &tmV;
+        const int off = is_k ? 0 : C::kKBytes;
         const uint64_t policy = l2_evict_last_policy();
         const int32_t* trow = a.tables + static_cast<long long>(info[2]) * a.max_blocks + blk0;
         bool ok = true;
@@ -766,14 +796,14 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 const int bid = __ldg(trow + C::kBlk * j + lane);
                 if (bid >= 0 && bid < a.num_blocks)
                     y = (bid * a.kv_heads + h) * 16;
-                else
+                else if (is_k)
                     atomicOr(a.status, PKV_DEVERR_RANGE);
             }
             int good = 1;
             if (lane == 0) {
                 PX_T(t0);
-                if (mbar_wait(&kv_empty[s], static_cast<uint32_t>((j / C::kStages) & 1) ^ 1u, a.status, abort_flag))
-                    mbar_arrive_expect_tx(&kv_full[s], C::kStageBytes);
+                if (mbar_wait(&empty[s], static_cast<uint32_t>((j / C::kStages) & 1) ^ 1u, a.status, abort_flag))
+                    mbar_arrive_expect_tx(&full[s], C::kKBytes);
                 else
                     good = 0;
                 PX_T(t1);
@@ -785,38 +815,36 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 break;
             }
             if (lane < C::kBlk) {
-                uint8_t* st = smem + C::kOffKV + s * C::kStageBytes + lane * 2048;
+                uint8_t* st = smem + C::kOffKV + s * C::kStageBytes + off + lane * 2048;
 #pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf) {
-                    tma_load_2d(st + hf * C::kHalfBytes, &tmK, hf * 64, y, &kv_full[s], policy);
-                    tma_load_2d(st + C::kKBytes + hf * C::kHalfBytes, &tmV, hf * 64, y, &kv_full[s], policy);
-                }
+                for (int hf = 0; hf < C::kHalves; ++hf) tma_load_2d(st + hf * C::kHalfBytes, map, hf * 64, y, &full[s], policy);
             }
             ++issued;
         }
         if (!ok && lane == 0) {  // after an abort: wait (bounded) for the copies still in flight
             const int first = issued > C::kStages ? issued - C::kStages : 0;
             for (int u = first; u < issued; ++u)
-                mbar_wait(&kv_full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
+                mbar_wait(&full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
         }
-        if (lane == 0) PX_STAMP(a, 15, tr_tma);
-    } else if (warp == C::kMmaWarp) {
-        // ------------------------------------------------ MMA issuer (one thread)
+        if (lane == 0 && is_k) PX_STAMP(a, 15, tr_tma);
+    } else if (warp == C::kSWarp) {
+        // ------------------------------------------------ score issuer (one thread)
+        // S_j = Q K_j^T into S buffer j % 2, once the softmax warps have read
+        // S_{j-2} out of it and stage j of K/V has landed. Both operands
+        // K-major; a K-step of 16 elements is 32 bytes into the swizzled row.
         if (lane == 0) {
             constexpr uint32_t idS = umma_idesc_bf16(C::kRows, C::kTok, false, false);
-            constexpr uint32_t idO = umma_idesc_bf16(C::kRows, D, false, true);
             const uint32_t q_base = smem_u32(smem + C::kOffQ);
-            bool ok = true;
 #ifdef PKV_TRACE
-            unsigned long long tr_p = 0, tr_kv = 0;
+            unsigned long long tr_kv = 0;
 #endif
-            // S_j = Q K_j^T into S buffer j % 2. Both operands K-major; a
-            // K-step of 16 elements is 32 bytes into the swizzled row.
-            auto issue_s = [&](int j) {
+            for (int j = 0; j < nsteps; ++j) {
+                if (j >= 2 &&
+                    !mbar_wait(&s_free[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), a.status, abort_flag))
+                    break;
                 const int s = j % C::kStages;
                 PX_T(t0);
-                if (!mbar_wait(&kv_full[s], static_cast<uint32_t>((j / C::kStages) & 1), a.status, abort_flag))
-                    return false;
+                if (!mbar_wait(&k_full[s], static_cast<uint32_t>((j / C::kStages) & 1), a.status, abort_flag)) break;
                 PX_T(t1);
                 PX_ADD(tr_kv, t1 - t0);
                 tc_fence_after();
@@ -827,9 +855,23 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                     const uint64_t bd = umma_desc_sw128(k_base + (kk >> 2) * C::kHalfBytes + (kk & 3) * 32, 16, 1024);
                     umma_bf16(tmem + C::kColS + (j & 1) * C::kTok, ad, bd, idS, kk > 0 ? 1u : 0u);
                 }
+                umma_commit(&k_empty[s]);  // the K stage is free once this product is done
                 umma_commit(&s_full[j & 1]);
-                return true;
-            };
+            }
+            // nothing may still run on the tensor cores when the memory is freed
+            umma_commit(final_s);
+            mbar_wait(final_s, 0, a.status, nullptr);
+            PX_STAMP(a, 14, tr_kv);
+        }
+        __syncwarp();
+    } else if (warp == C::kMmaWarp) {
+        // ------------------------------------------------ P.V issuer (one thread)
+        if (lane == 0) {
+            constexpr uint32_t idO = umma_idesc_bf16(C::kRows, D, false, true);
+            bool ok = true;
+#ifdef PKV_TRACE
+            unsigned long long tr_p = 0;
+#endif
             // prefill: the step and stage row of the first slot past the
             // sequence's end, when that slot lies in a block this CTA streams
             int tail_step = -1, tail_row = 0;
@@ -841,7 +883,6 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                     tail_row = ((bl - blk0) % C::kBlk) * 16 + (n_end & 15);
                 }
             }
-            for (int j = 0; ok && j < nsteps && j < 2; ++j) ok = issue_s(j);
             for (int j = 0; ok && j < nsteps; ++j) {
                 PX_T(t0);
                 if (!mbar_wait(&p_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.status, abort_flag)) {
@@ -857,11 +898,14 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 // per 128-byte row, the two column halves kHalfBytes apart, 8
                 // token rows per 1024-byte atom.
                 const int s = j % C::kStages;
+                if (!mbar_wait(&v_full[s], static_cast<uint32_t>((j / C::kStages) & 1), a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 if constexpr (PF) {
                     // The slots of the sequence's last block past its length may
                     // hold anything, NaN included. P is zero there, but 0 * NaN
-                    // is not, so those V rows are zeroed before the product
-                    // (their copy has landed: S_j waited for it).
+                    // is not, so those V rows are zeroed before the product.
                     if (j == tail_step) {
                         uint8_t* vt = smem + C::kOffKV + s * C::kStageBytes + C::kKBytes;
                         for (int hf = 0; hf < C::kHalves; ++hf)
@@ -887,15 +931,13 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                         }
                     }
                 }
-                umma_commit(&kv_empty[s]);
+                umma_commit(&v_empty[s]);
                 umma_commit(&o_done[j & 1]);
-                if (j + 2 < nsteps) ok = issue_s(j + 2);
             }
             // nothing may still run on the tensor cores when the memory is freed
             umma_commit(final_bar);
             mbar_wait(final_bar, 0, a.status, nullptr);
             PX_STAMP(a, 13, tr_p);
-            PX_STAMP(a, 14, tr_kv);
         }
         __syncwarp();
     }
@@ -931,6 +973,10 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             uint32_t sv[32];
             tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok + th * 32, sv);
             tmem_ld_wait();
+            // S buffer j % 2 is read: the score issuer may write S_{j+2} into it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[j & 1]);
             PX_T(t2);
             int valid = min(C::kTok, (nblk - C::kBlk * j) * 16) - th * 32;
             if constexpr (PF) valid = min(valid, lim - ((blk0 + C::kBlk * j) * 16 + th * 32) + 1);
@@ -1400,3 +1446,10 @@ cudaError_t launch_check_groups(const int32_t* tables, int32_t max_blocks, const
 }
 
 }  // namespace pkv
+
+#ifdef PKV_TRACE
+// Trace builds only: copies the prefill stamps (65536 CTAs x 16 words) to `host`.
+extern "C" __attribute__((visibility("default"))) int pkv_trace_copy_prefill(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, pkv::g_px_trace, bytes));
+}
+#endif
