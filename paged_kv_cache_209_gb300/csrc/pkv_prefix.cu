@@ -609,25 +609,32 @@ struct Ux {
     static constexpr int kTok = 64;                  // N of S = Q K^T: tokens per step
     static constexpr int kBlk = kTok / 16;           // blocks per step
     static constexpr int kHalves = D / 64;           // 64-column (128-byte) halves of a row
-    static constexpr int kStages = D == 128 ? 4 : 6;
+    // Ring depths (a K stage is released by its score product, a V stage by
+    // its P.V product). Six K stages measured slower than four on the
+    // chunked-prefill workload: the loads come mostly from L2, and more of
+    // them in flight did not arrive sooner.
+    static constexpr int kKStages = D == 128 ? 4 : 6;
+    static constexpr int kVStages = D == 128 ? 4 : 6;
     static constexpr int kQBytes = kHalves * kRows * 128;
     static constexpr int kHalfBytes = kTok * 128;    // one half of the 64 token rows of a step
-    static constexpr int kKBytes = kHalves * kHalfBytes;
-    static constexpr int kStageBytes = 2 * kKBytes;  // K then V
+    static constexpr int kKBytes = kHalves * kHalfBytes;  // one stage of K (or of V)
     // Shared memory (offsets from a 1024-byte aligned base; every operand
     // tile starts on a 1024-byte boundary, as the 128-byte swizzle wants):
-    // Q [halves][128 rows][128 B]; the K/V ring, each stage K then V as
+    // Q [halves][128 rows][128 B]; the K ring, then the V ring, each stage
     // [halves][64 token rows][128 B] (the TMA layout of four 16-row boxes);
     // the exchange of the two token halves' row states; the mbarriers; then
     // info[16], the tile's members, the per-group member counts and the
     // staged lookup inputs.
     static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kOffQ + kQBytes;
-    static constexpr int kOffX = kOffKV + kStages * kStageBytes;
+    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kOffV = kOffK + kKStages * kKBytes;
+    static constexpr int kRingBytes = (kKStages + kVStages) * kKBytes;
+    static constexpr int kOffX = kOffK + kRingBytes;
     static constexpr int kOffBars = kOffX + 3 * kRows * 4;
-    // k_full, k_empty, v_full, v_empty (per stage), s_full[2], p_full[2], o_done[2], final (PV issuer),
-    // s_free[2], final (S issuer)
-    static constexpr int kNumBars = 4 * kStages + 10;
+    // k_full, k_empty (per K stage), v_full, v_empty (per V stage), s_full, p_full, o_done (per S/P
+    // buffer), final (PV issuer), final (S issuer)
+    static constexpr int kNumBufs = 4;  // S/P buffers in tensor memory
+    static constexpr int kNumBars = 2 * (kKStages + kVStages) + 3 * kNumBufs + 2;
     static constexpr int kOffInts = kOffBars + kNumBars * 8;
     static constexpr size_t kSmem =
         1024 + kOffInts + (16 + member_slots(kRows) + kMaxGroups + 2 * kMaxBatchPerLaunch + kMaxGroups) * 4;
@@ -643,13 +650,14 @@ struct Ux {
     static constexpr int kSWarp = 10;
     static constexpr int kTmaVWarp = 11;
     static constexpr int kThreads = 384;
-    static constexpr uint32_t kColS = 0;    // S buffers: columns [0, 64) and [64, 128)
-    static constexpr uint32_t kColO = 128;  // O of token half 0: [128, 128 + D); half 1: [128 + D, 128 + 2D)
-    // P buffers b = 0, 1 at kColP + 64 b: bf16 pairs, hi in the first 32
-    // columns (token t in column t / 2), lo in the next 32
-    static constexpr uint32_t kColP = kColO + 2 * D;
+    // S/P buffers b < kNumBufs at columns 64 b: S_j (fp32, 64 tokens) in buffer
+    // j % kNumBufs, then P_j written over it (each softmax thread overwrites
+    // only the 32 columns of its own token half once it has read them: bf16
+    // pairs, hi in the first 16 columns, lo in the next 16)
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColO = kNumBufs * kTok;  // O of token half 0: [kColO, kColO + D); half 1: next D
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kColP + 128 <= kTmemCols, "tensor-memory columns");
+    static_assert(kColO + 2 * D <= kTmemCols, "tensor-memory columns");
 };
 
 // PF (chunked prefill): the queries of one sequence over its own context
@@ -662,15 +670,14 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-    uint64_t* k_empty = k_full + C::kStages;
-    uint64_t* v_full = k_empty + C::kStages;
-    uint64_t* v_empty = v_full + C::kStages;
-    uint64_t* s_full = v_empty + C::kStages;  // [2]: S buffer b holds a finished S
-    uint64_t* p_full = s_full + 2;             // [2]: P buffer b written (one arrival per softmax warp)
-    uint64_t* o_done = p_full + 2;             // [2]: the PV product of step j (buffer j % 2) has completed
-    uint64_t* final_bar = o_done + 2;          // every P.V product has completed
-    uint64_t* s_free = final_bar + 1;          // [2]: S buffer b has been read (one arrival per softmax warp)
-    uint64_t* final_s = s_free + 2;            // every score product has completed
+    uint64_t* k_empty = k_full + C::kKStages;
+    uint64_t* v_full = k_empty + C::kKStages;
+    uint64_t* v_empty = v_full + C::kVStages;
+    uint64_t* s_full = v_empty + C::kVStages;    // [buffers]: buffer b holds a finished S
+    uint64_t* p_full = s_full + C::kNumBufs;     // [buffers]: P written over it (one arrival per softmax warp)
+    uint64_t* o_done = p_full + C::kNumBufs;     // [buffers]: the P.V product reading it has completed
+    uint64_t* final_bar = o_done + C::kNumBufs;  // every P.V product has completed
+    uint64_t* final_s = final_bar + 1;           // every score product has completed
     int* info = reinterpret_cast<int*>(smem + C::kOffInts);
     int* members = info + 16;
     int* counts = members + member_slots(C::kRows);
@@ -688,19 +695,20 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         PX_STAMP(a, 0, global_ns());
         PX_STAMP(a, 6, sm_id());
         PX_STAMP(a, 7, 0);
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kNumBufs; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], C::kSoftmaxWarps);
             mbar_init(&o_done[b], 1);
         }
         mbar_init(final_bar, 1);
-        for (int b = 0; b < 2; ++b) mbar_init(&s_free[b], C::kSoftmaxWarps);
         mbar_init(final_s, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -781,7 +789,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         uint64_t* full = is_k ? k_full : v_full;
         uint64_t* empty = is_k ? k_empty : v_empty;
         const CUtensorMap* map = is_k ? &tmK : &tmV;
-        const int off = is_k ? 0 : C::kKBytes;
+        const int nst = is_k ? C::kKStages : C::kVStages;
+        uint8_t* ring = smem + (is_k ? C::kOffK : C::kOffV);
         const uint64_t policy = l2_evict_last_policy();
         const int32_t* trow = a.tables + static_cast<long long>(info[2]) * a.max_blocks + blk0;
         bool ok = true;
@@ -789,11 +798,21 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
 #ifdef PKV_TRACE
         unsigned long long tr_tma = 0;
 #endif
+        // block-table entries, 32 at a time, the next 32 already in flight:
+        // lane i holds entry b0 + i of the current batch (b0 a multiple of 32)
+        int cur = lane < nblk ? __ldg(trow + lane) : 0;
+        int nxt = 32 + lane < nblk ? __ldg(trow + 32 + lane) : 0;
         for (int j = 0; j < nsteps; ++j) {
-            const int s = j % C::kStages;
+            const int s = j % nst;
+            const int e = (C::kBlk * j) & 31;  // this step's first entry within the batch
+            if (j > 0 && e == 0) {
+                cur = nxt;
+                const int ni = C::kBlk * j + 32 + lane;
+                nxt = ni < nblk ? __ldg(trow + ni) : 0;
+            }
+            const int bid = __shfl_sync(0xffffffffu, cur, e + (lane & (C::kBlk - 1)));
             int y = -16;
             if (lane < C::kBlk && C::kBlk * j + lane < nblk) {
-                const int bid = __ldg(trow + C::kBlk * j + lane);
                 if (bid >= 0 && bid < a.num_blocks)
                     y = (bid * a.kv_heads + h) * 16;
                 else if (is_k)
@@ -802,7 +821,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             int good = 1;
             if (lane == 0) {
                 PX_T(t0);
-                if (mbar_wait(&empty[s], static_cast<uint32_t>((j / C::kStages) & 1) ^ 1u, a.status, abort_flag))
+                if (mbar_wait(&empty[s], static_cast<uint32_t>((j / nst) & 1) ^ 1u, a.status, abort_flag))
                     mbar_arrive_expect_tx(&full[s], C::kKBytes);
                 else
                     good = 0;
@@ -815,23 +834,24 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 break;
             }
             if (lane < C::kBlk) {
-                uint8_t* st = smem + C::kOffKV + s * C::kStageBytes + off + lane * 2048;
+                uint8_t* st = ring + s * C::kKBytes + lane * 2048;
 #pragma unroll
                 for (int hf = 0; hf < C::kHalves; ++hf) tma_load_2d(st + hf * C::kHalfBytes, map, hf * 64, y, &full[s], policy);
             }
             ++issued;
         }
         if (!ok && lane == 0) {  // after an abort: wait (bounded) for the copies still in flight
-            const int first = issued > C::kStages ? issued - C::kStages : 0;
+            const int first = issued > nst ? issued - nst : 0;
             for (int u = first; u < issued; ++u)
-                mbar_wait(&full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
+                mbar_wait(&full[u % nst], static_cast<uint32_t>((u / nst) & 1), a.status, nullptr);
         }
         if (lane == 0 && is_k) PX_STAMP(a, 15, tr_tma);
     } else if (warp == C::kSWarp) {
         // ------------------------------------------------ score issuer (one thread)
-        // S_j = Q K_j^T into S buffer j % 2, once the softmax warps have read
-        // S_{j-2} out of it and stage j of K/V has landed. Both operands
-        // K-major; a K-step of 16 elements is 32 bytes into the swizzled row.
+        // S_j = Q K_j^T into buffer j % kNumBufs, once the P.V product that
+        // read P_{j - kNumBufs} out of it has completed and stage j of K has
+        // landed. Both operands K-major; a K-step of 16 elements is 32 bytes
+        // into the swizzled row.
         if (lane == 0) {
             constexpr uint32_t idS = umma_idesc_bf16(C::kRows, C::kTok, false, false);
             const uint32_t q_base = smem_u32(smem + C::kOffQ);
@@ -839,24 +859,25 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             unsigned long long tr_kv = 0;
 #endif
             for (int j = 0; j < nsteps; ++j) {
-                if (j >= 2 &&
-                    !mbar_wait(&s_free[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), a.status, abort_flag))
+                const int b = j % C::kNumBufs;
+                if (j >= C::kNumBufs &&
+                    !mbar_wait(&o_done[b], static_cast<uint32_t>((j / C::kNumBufs - 1) & 1), a.status, abort_flag))
                     break;
-                const int s = j % C::kStages;
+                const int s = j % C::kKStages;
                 PX_T(t0);
-                if (!mbar_wait(&k_full[s], static_cast<uint32_t>((j / C::kStages) & 1), a.status, abort_flag)) break;
+                if (!mbar_wait(&k_full[s], static_cast<uint32_t>((j / C::kKStages) & 1), a.status, abort_flag)) break;
                 PX_T(t1);
                 PX_ADD(tr_kv, t1 - t0);
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(smem + C::kOffKV + s * C::kStageBytes);
+                const uint32_t k_base = smem_u32(smem + C::kOffK + s * C::kKBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t ad = umma_desc_sw128(q_base + (kk >> 2) * (C::kRows * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = umma_desc_sw128(k_base + (kk >> 2) * C::kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(tmem + C::kColS + (j & 1) * C::kTok, ad, bd, idS, kk > 0 ? 1u : 0u);
+                    umma_bf16(tmem + C::kColS + b * C::kTok, ad, bd, idS, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&k_empty[s]);  // the K stage is free once this product is done
-                umma_commit(&s_full[j & 1]);
+                umma_commit(&s_full[b]);
             }
             // nothing may still run on the tensor cores when the memory is freed
             umma_commit(final_s);
@@ -885,7 +906,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             }
             for (int j = 0; ok && j < nsteps; ++j) {
                 PX_T(t0);
-                if (!mbar_wait(&p_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.status, abort_flag)) {
+                const int b = j % C::kNumBufs;
+                if (!mbar_wait(&p_full[b], static_cast<uint32_t>((j / C::kNumBufs) & 1), a.status, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -897,8 +919,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 // row); V is MN-major straight from the TMA layout: 64 columns
                 // per 128-byte row, the two column halves kHalfBytes apart, 8
                 // token rows per 1024-byte atom.
-                const int s = j % C::kStages;
-                if (!mbar_wait(&v_full[s], static_cast<uint32_t>((j / C::kStages) & 1), a.status, abort_flag)) {
+                const int s = j % C::kVStages;
+                if (!mbar_wait(&v_full[s], static_cast<uint32_t>((j / C::kVStages) & 1), a.status, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -907,7 +929,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                     // hold anything, NaN included. P is zero there, but 0 * NaN
                     // is not, so those V rows are zeroed before the product.
                     if (j == tail_step) {
-                        uint8_t* vt = smem + C::kOffKV + s * C::kStageBytes + C::kKBytes;
+                        uint8_t* vt = smem + C::kOffV + s * C::kKBytes;
                         for (int hf = 0; hf < C::kHalves; ++hf)
                             for (int row = tail_row; row < (tail_row | 15) + 1; ++row)
 #pragma unroll
@@ -917,8 +939,10 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                         fence_proxy_async_smem();
                     }
                 }
-                const uint32_t v_base = smem_u32(smem + C::kOffKV + s * C::kStageBytes + C::kKBytes);
-                const uint32_t p_col = tmem + C::kColP + (j & 1) * 64;
+                const uint32_t v_base = smem_u32(smem + C::kOffV + s * C::kKBytes);
+                // token half th of P sits in columns 32 th .. 32 th + 31 of the
+                // buffer: hi of tokens 32 th + 2c, + 1 in column 32 th + c, lo 16 further
+                const uint32_t p_col = tmem + C::kColS + b * C::kTok;
 #pragma unroll
                 for (int th = 0; th < 2; ++th) {
 #pragma unroll
@@ -926,13 +950,13 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
 #pragma unroll
                         for (int kt = 2 * th; kt < 2 * th + 2; ++kt) {
                             const uint64_t bd = umma_desc_sw128(v_base + kt * 2048, C::kHalfBytes, 1024);
-                            umma_bf16_ts(tmem + C::kColO + th * D, p_col + part * 32 + kt * 8, bd, idO,
-                                         (j > 0 || part > 0 || kt > 2 * th) ? 1u : 0u);
+                            umma_bf16_ts(tmem + C::kColO + th * D, p_col + 32 * th + 16 * part + 8 * (kt & 1), bd,
+                                         idO, (j > 0 || part > 0 || kt > 2 * th) ? 1u : 0u);
                         }
                     }
                 }
                 umma_commit(&v_empty[s]);
-                umma_commit(&o_done[j & 1]);
+                umma_commit(&o_done[b]);
             }
             // nothing may still run on the tensor cores when the memory is freed
             umma_commit(final_bar);
@@ -964,19 +988,16 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
 #endif
         for (int j = 0; j < nsteps; ++j) {
             PX_T(t0);
-            if (!mbar_wait(&s_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.status, abort_flag)) {
+            const int bb = j % C::kNumBufs;
+            if (!mbar_wait(&s_full[bb], static_cast<uint32_t>((j / C::kNumBufs) & 1), a.status, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             PX_T(t1);
             uint32_t sv[32];
-            tmem_ld32(tmem + lane_base + C::kColS + (j & 1) * C::kTok + th * 32, sv);
+            tmem_ld32(tmem + lane_base + C::kColS + bb * C::kTok + th * 32, sv);
             tmem_ld_wait();
-            // S buffer j % 2 is read: the score issuer may write S_{j+2} into it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[j & 1]);
             PX_T(t2);
             int valid = min(C::kTok, (nblk - C::kBlk * j) * 16) - th * 32;
             if constexpr (PF) valid = min(valid, lim - ((blk0 + C::kBlk * j) * 16 + th * 32) + 1);
@@ -1024,15 +1045,10 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             const float psum = ps[0];
             l = l * alpha + psum;
             PX_T(t3);
-            // P buffer j % 2 was read by the PV product of step j - 2
-            if (j >= 2 && !mbar_wait(&o_done[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), a.status, abort_flag)) {
-                ok = false;
-                break;
-            }
             // rescale this half's O in tensor memory once the PV product of step j - 1 is in
             if (__any_sync(0xffffffffu, resc && j > 0)) {
-                if (!mbar_wait(&o_done[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1), a.status,
-                               abort_flag)) {
+                if (!mbar_wait(&o_done[(j - 1) % C::kNumBufs], static_cast<uint32_t>(((j - 1) / C::kNumBufs) & 1),
+                               a.status, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -1049,13 +1065,14 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 tmem_st_wait();
             }
             PX_T(t4);
-            const uint32_t p_col = tmem + lane_base + C::kColP + (j & 1) * 64 + th * 16;
+            // P over this thread's own S columns (already read)
+            const uint32_t p_col = tmem + lane_base + C::kColS + bb * C::kTok + th * 32;
             tmem_st16(p_col, hi);
-            tmem_st16(p_col + 32, lo);
+            tmem_st16(p_col + 16, lo);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[j & 1]);
+            if (lane == 0) mbar_arrive(&p_full[bb]);
             PX_T(t5);
             PX_ADD(tr_s, t1 - t0);
             PX_ADD(tr_ld, t2 - t1);
@@ -1073,7 +1090,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         }
         // the last PV product must be in before O is read or the P buffers reused
         if (ok && nsteps > 0 &&
-            !mbar_wait(&o_done[(nsteps - 1) & 1], static_cast<uint32_t>(((nsteps - 1) >> 1) & 1), a.status,
+            !mbar_wait(&o_done[(nsteps - 1) % C::kNumBufs], static_cast<uint32_t>(((nsteps - 1) / C::kNumBufs) & 1), a.status,
                        abort_flag))
             ok = false;
         tc_fence_after();
@@ -1119,12 +1136,12 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     // maxima, the sums. A CTA without the chunk, or one that gave up, leaves
     // empty rows (sum 0).
     constexpr int kPS = D + 4;
-    float* part = reinterpret_cast<float*>(smem + C::kOffKV);
+    float* part = reinterpret_cast<float*>(smem + C::kOffK);
     float* part_m = part + C::kRows * kPS;
     float* part_l = part_m + C::kRows;
     float* wts = part_l + C::kRows;  // [rows combined here][kMaxCluster + 1]
     int* rowoff = reinterpret_cast<int*>(wts + C::kRows * (kMaxCluster + 1));
-    static_assert(C::kRows * (kPS + 2 + kMaxCluster + 2) * 4 <= C::kStages * C::kStageBytes, "partial fits the ring");
+    static_assert(C::kRows * (kPS + 2 + kMaxCluster + 2) * 4 <= C::kRingBytes, "partial fits the rings");
     fence_proxy_async_smem();  // the ring was last written by TMA
     if (warp < 4) {
         const int r = threadIdx.x;
