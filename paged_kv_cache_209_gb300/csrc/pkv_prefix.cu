@@ -53,12 +53,13 @@ __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 
 // Build-time tracing (PKV_TRACE): each CTA of the tcgen05 kernel records
 // %globaltimer stamps in a row of 16 words: [0] entry, [1] tile located,
-// [2] tensor memory and Q ready, [3] softmax loop done, [4] tensor memory
-// freed, [5] exit of thread 0, [6] SM id, [7] 1 for a CTA with work; sums over
-// the steps of: [8] softmax wait for S, [9] S load from tensor memory, [10]
-// softmax arithmetic, [11] softmax waits for PV products (and O rescale),
-// [12] P store and arrival, [13] MMA wait for P, [14] MMA wait for K/V,
-// [15] TMA wait for a free stage.
+// [2] tensor memory and Q ready, [3] softmax loop done, [5] exit of thread 0,
+// [7] 1 for a CTA with work; sums over the steps of: [8] softmax wait for S,
+// [9] S load from tensor memory, [10] softmax arithmetic (with the P
+// stores), [11] softmax waits for PV products (O rescale), [12] wait for the
+// P stores and arrival, [13] P.V issuer wait for P, [4] P.V issuer wait for
+// V, [14] score issuer wait for K, [6] score issuer wait for its S/P buffer
+// (the P.V product four steps back), [15] K copy warp wait for a free stage.
 #ifdef PKV_TRACE
 // Launches without a workspace slot for the stamps (chunked prefill) write
 // them here instead, for the first 65536 CTAs.
@@ -72,10 +73,18 @@ __device__ unsigned long long g_px_trace[65536 * 16];
             g_px_trace[PX_CTA() * 16 + (i)] = (v);                                           \
     } while (0)
 #define PX_T(var) const unsigned long long var = global_ns()
+// Per-step stamps of the first CTA (steps < 256), after the per-CTA rows:
+// [0] score issue start, [1] score issue end, [2] softmax sees S, [3] softmax
+// arrives on P (warp 0, lane 0), [4] P.V issue start, [5] P.V issue end.
+#define PX_STEP(j, k)                                                                      \
+    do {                                                                                   \
+        if (PX_CTA() == 0 && (j) < 256) g_px_trace[65536 * 8 + (j) * 8 + (k)] = global_ns(); \
+    } while (0)
 #define PX_ADD(acc, v) acc += (v)
 #else
 #define PX_STAMP(a, i, v) ((void)0)
 #define PX_T(var) ((void)0)
+#define PX_STEP(j, k) ((void)0)
 #define PX_ADD(acc, v) ((void)0)
 #endif
 
@@ -615,9 +624,9 @@ struct Ux {
     // them in flight did not arrive sooner.
     static constexpr int kKStages = D == 128 ? 4 : 6;
     static constexpr int kVStages = D == 128 ? 4 : 6;
-    static constexpr int kQBytes = kHalves * kRows * 128;
     static constexpr int kHalfBytes = kTok * 128;    // one half of the 64 token rows of a step
     static constexpr int kKBytes = kHalves * kHalfBytes;  // one stage of K (or of V)
+    static constexpr int kQBytes = kHalves * kRows * 128;
     // Shared memory (offsets from a 1024-byte aligned base; every operand
     // tile starts on a 1024-byte boundary, as the 128-byte swizzle wants):
     // Q [halves][128 rows][128 B]; the K ring, then the V ring, each stage
@@ -631,29 +640,34 @@ struct Ux {
     static constexpr int kRingBytes = (kKStages + kVStages) * kKBytes;
     static constexpr int kOffX = kOffK + kRingBytes;
     static constexpr int kOffBars = kOffX + 3 * kRows * 4;
-    // k_full, k_empty (per K stage), v_full, v_empty (per V stage), s_full, p_full, o_done (per S/P
-    // buffer), final (PV issuer), final (S issuer)
+    // k_full, k_empty (per K stage), v_full, v_empty (per V stage), s_full, p_full (two token halves),
+    // o_done (per S/P buffer), final (two P.V issuers, two score issuers)
     static constexpr int kNumBufs = 4;  // S/P buffers in tensor memory
-    static constexpr int kNumBars = 2 * (kKStages + kVStages) + 3 * kNumBufs + 2;
+    static constexpr int kNumBars = 2 * (kKStages + kVStages) + 4 * kNumBufs + 4;
     static constexpr int kOffInts = kOffBars + kNumBars * 8;
     static constexpr size_t kSmem =
         1024 + kOffInts + (16 + member_slots(kRows) + kMaxGroups + 2 * kMaxBatchPerLaunch + kMaxGroups) * 4;
     // warps 0-7 softmax: warp w takes rows 32 (w % 4) .. + 31 (its tensor-memory
     // lanes) and token half w / 4 of every step; warps 8 and 11 copy K and V
     // (separate rings: a K stage is free once its score product is done, long
-    // before the V stage of the same step); warp 9 issues the P.V products,
-    // warp 10 the score products (two issuing threads, so that one's waits
-    // never hold back the other's stream of tensor-core work)
+    // before the V stage of the same step); warps 9 and 12 issue the P.V
+    // products of token halves 0 and 1, warps 10 and 13 the score products of
+    // even and odd steps. A wait that follows tensor-core issues in the same
+    // thread returns only once the tensor pipe has drained, so each issuing
+    // thread's waits leave a gap in its stream; with four issuers the others
+    // fill it.
     static constexpr int kSoftmaxWarps = 8;
     static constexpr int kTmaWarp = 8;
-    static constexpr int kMmaWarp = 9;
-    static constexpr int kSWarp = 10;
+    static constexpr int kMmaWarp = 9;     // P.V, token half 0 (and the tensor-memory allocation)
+    static constexpr int kSWarp = 10;      // scores, even steps
     static constexpr int kTmaVWarp = 11;
-    static constexpr int kThreads = 384;
+    static constexpr int kMmaWarp1 = 12;   // P.V, token half 1
+    static constexpr int kSWarp1 = 13;     // scores, odd steps
+    static constexpr int kThreads = 448;
     // S/P buffers b < kNumBufs at columns 64 b: S_j (fp32, 64 tokens) in buffer
     // j % kNumBufs, then P_j written over it (each softmax thread overwrites
     // only the 32 columns of its own token half once it has read them: bf16
-    // pairs, hi in the first 16 columns, lo in the next 16)
+    // pairs, hi in the first 16 columns, lo in the next 16). Then O.
     static constexpr uint32_t kColS = 0;
     static constexpr uint32_t kColO = kNumBufs * kTok;  // O of token half 0: [kColO, kColO + D); half 1: next D
     static constexpr uint32_t kTmemCols = 512;
@@ -673,11 +687,12 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     uint64_t* k_empty = k_full + C::kKStages;
     uint64_t* v_full = k_empty + C::kKStages;
     uint64_t* v_empty = v_full + C::kVStages;
-    uint64_t* s_full = v_empty + C::kVStages;    // [buffers]: buffer b holds a finished S
-    uint64_t* p_full = s_full + C::kNumBufs;     // [buffers]: P written over it (one arrival per softmax warp)
-    uint64_t* o_done = p_full + C::kNumBufs;     // [buffers]: the P.V product reading it has completed
-    uint64_t* final_bar = o_done + C::kNumBufs;  // every P.V product has completed
-    uint64_t* final_s = final_bar + 1;           // every score product has completed
+    uint64_t* s_full = v_empty + C::kVStages;       // [buffers]: buffer b holds a finished S
+    uint64_t* p_full = s_full + C::kNumBufs;        // [2][buffers]: token half t of P written over it
+                                                    // (one arrival per softmax warp of the half)
+    uint64_t* o_done = p_full + 2 * C::kNumBufs;    // [buffers]: both P.V products reading it have completed
+    uint64_t* final_bar = o_done + C::kNumBufs;     // [2]: every P.V product of an issuer has completed
+    uint64_t* final_s = final_bar + 2;              // [2]: every score product of an issuer has completed
     int* info = reinterpret_cast<int*>(smem + C::kOffInts);
     int* members = info + 16;
     int* counts = members + member_slots(C::kRows);
@@ -693,7 +708,6 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         PX_STAMP(a, 0, global_ns());
-        PX_STAMP(a, 6, sm_id());
         PX_STAMP(a, 7, 0);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(&k_full[s], 1);
@@ -701,15 +715,18 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         }
         for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
+            mbar_init(&v_empty[s], 2);  // released by both P.V issuers
         }
         for (int b = 0; b < C::kNumBufs; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], C::kSoftmaxWarps);
-            mbar_init(&o_done[b], 1);
+            mbar_init(&p_full[b], C::kSoftmaxWarps / 2);
+            mbar_init(&p_full[C::kNumBufs + b], C::kSoftmaxWarps / 2);
+            mbar_init(&o_done[b], 2);
         }
-        mbar_init(final_bar, 1);
-        mbar_init(final_s, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&final_bar[i], 1);
+            mbar_init(&final_s[i], 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -747,7 +764,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         tmem_relinquish();
     }
     // Q rows into shared memory (K-major, 128-byte swizzle); thread r < 128
-    // loads row r. The TMA warp does not wait for this: it starts streaming
+    // loads row r. The TMA warps do not wait for this: they start streaming
     // K and V at once.
     long long row_idx = 0;
     bool row_ok = false;
@@ -782,9 +799,16 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
 
     if (warp == C::kTmaWarp || warp == C::kTmaVWarp) {
         // ------------------------------------------------ TMA producers (K, V)
-        // Step j: blocks 4j .. 4j+3 of the chunk; lane b issues block b. A
-        // block past the chunk or with an invalid id is loaded from row -16
-        // (wholly out of range), which fills its box with zeros.
+        // Step j: blocks 4j .. 4j+3 of the chunk, each in kHalves 64-column
+        // boxes. A TMA instruction costs the issuing warp a few hundred cycles
+        // almost whatever the number of lanes issuing it, so the copies go in
+        // batches: lane group u (lanes 8u .. 8u + 7) takes step j + u, one box
+        // per lane (block lane & 3, half (lane >> 2) & 1), for the run of free
+        // stages from stage j on (at most 4, within one batch of table
+        // entries); only when stage j itself is busy does the warp wait
+        // (bounded) for it. A block past the chunk or with an invalid id is
+        // loaded from row -16 (wholly out of range), which fills its box with
+        // zeros.
         const bool is_k = warp == C::kTmaWarp;
         uint64_t* full = is_k ? k_full : v_full;
         uint64_t* empty = is_k ? k_empty : v_empty;
@@ -798,47 +822,63 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
 #ifdef PKV_TRACE
         unsigned long long tr_tma = 0;
 #endif
-        // block-table entries, 32 at a time, the next 32 already in flight:
-        // lane i holds entry b0 + i of the current batch (b0 a multiple of 32)
+        // block-table entries, 32 (8 steps) at a time, the next 32 already in
+        // flight: lane i holds entry 32 c + i of the current batch c
         int cur = lane < nblk ? __ldg(trow + lane) : 0;
         int nxt = 32 + lane < nblk ? __ldg(trow + 32 + lane) : 0;
-        for (int j = 0; j < nsteps; ++j) {
-            const int s = j % nst;
-            const int e = (C::kBlk * j) & 31;  // this step's first entry within the batch
-            if (j > 0 && e == 0) {
+        int batch = 0;
+        const int grp = lane >> 3;                      // step offset within an issue
+        const int bb = lane & (C::kBlk - 1);            // block of the step
+        const int hf = (lane >> 2) & 1;                 // 64-column half
+        const bool box_lane = hf < C::kHalves;          // head_dim 64: one half
+        while (ok && issued < nsteps) {
+            const int j = issued;
+            if ((j >> 3) != batch) {
+                batch = j >> 3;
                 cur = nxt;
-                const int ni = C::kBlk * j + 32 + lane;
+                const int ni = 32 * (batch + 1) + lane;
                 nxt = ni < nblk ? __ldg(trow + ni) : 0;
             }
-            const int bid = __shfl_sync(0xffffffffu, cur, e + (lane & (C::kBlk - 1)));
-            int y = -16;
-            if (lane < C::kBlk && C::kBlk * j + lane < nblk) {
-                if (bid >= 0 && bid < a.num_blocks)
-                    y = (bid * a.kv_heads + h) * 16;
-                else if (is_k)
-                    atomicOr(a.status, PKV_DEVERR_RANGE);
+            const int maxn = min(4, min(nsteps - j, 8 - (j & 7)));
+            bool free_stage = false;
+            if ((lane & 7) == 0 && grp < maxn)
+                free_stage = mbar_test_wait(&empty[(j + grp) % nst], static_cast<uint32_t>(((j + grp) / nst) & 1) ^ 1u);
+            const unsigned int fmask = __ballot_sync(0xffffffffu, free_stage);
+            int n = 0;
+            while (n < maxn && ((fmask >> (8 * n)) & 1u)) ++n;
+            if (n == 0) {
+                int good = 1;
+                if (lane == 0) {
+                    PX_T(t0);
+                    good = mbar_wait(&empty[j % nst], static_cast<uint32_t>((j / nst) & 1) ^ 1u, a.status, abort_flag)
+                               ? 1 : 0;
+                    PX_T(t1);
+                    PX_ADD(tr_tma, t1 - t0);
+                }
+                if (!__shfl_sync(0xffffffffu, good, 0)) {
+                    ok = false;
+                    break;
+                }
+                n = 1;
             }
-            int good = 1;
-            if (lane == 0) {
-                PX_T(t0);
-                if (mbar_wait(&empty[s], static_cast<uint32_t>((j / nst) & 1) ^ 1u, a.status, abort_flag))
-                    mbar_arrive_expect_tx(&full[s], C::kKBytes);
-                else
-                    good = 0;
-                PX_T(t1);
-                PX_ADD(tr_tma, t1 - t0);
+            const int jj = j + grp;
+            const int bid = __shfl_sync(0xffffffffu, cur, (C::kBlk * jj + bb) & 31);
+            if (grp < n) {
+                const int st = jj % nst;
+                if ((lane & 7) == 0) mbar_arrive_expect_tx(&full[st], C::kKBytes);
+                if (box_lane) {
+                    int y = -16;
+                    if (C::kBlk * jj + bb < nblk) {
+                        if (bid >= 0 && bid < a.num_blocks)
+                            y = (bid * a.kv_heads + h) * 16;
+                        else if (is_k && hf == 0)
+                            atomicOr(a.status, PKV_DEVERR_RANGE);
+                    }
+                    tma_load_2d(ring + st * C::kKBytes + hf * C::kHalfBytes + bb * 2048, map, hf * 64, y, &full[st],
+                                policy);
+                }
             }
-            good = __shfl_sync(0xffffffffu, good, 0);
-            if (!good) {
-                ok = false;
-                break;
-            }
-            if (lane < C::kBlk) {
-                uint8_t* st = ring + s * C::kKBytes + lane * 2048;
-#pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf) tma_load_2d(st + hf * C::kHalfBytes, map, hf * 64, y, &full[s], policy);
-            }
-            ++issued;
+            issued += n;
         }
         if (!ok && lane == 0) {  // after an abort: wait (bounded) for the copies still in flight
             const int first = issued > nst ? issued - nst : 0;
@@ -846,29 +886,34 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 mbar_wait(&full[u % nst], static_cast<uint32_t>((u / nst) & 1), a.status, nullptr);
         }
         if (lane == 0 && is_k) PX_STAMP(a, 15, tr_tma);
-    } else if (warp == C::kSWarp) {
-        // ------------------------------------------------ score issuer (one thread)
+    } else if (warp == C::kSWarp || warp == C::kSWarp1) {
+        // ------------------------------------------------ score issuers (one thread each)
         // S_j = Q K_j^T into buffer j % kNumBufs, once the P.V product that
         // read P_{j - kNumBufs} out of it has completed and stage j of K has
         // landed. Both operands K-major; a K-step of 16 elements is 32 bytes
         // into the swizzled row.
+        const int par = warp == C::kSWarp ? 0 : 1;  // even or odd steps
         if (lane == 0) {
             constexpr uint32_t idS = umma_idesc_bf16(C::kRows, C::kTok, false, false);
             const uint32_t q_base = smem_u32(smem + C::kOffQ);
 #ifdef PKV_TRACE
-            unsigned long long tr_kv = 0;
+            unsigned long long tr_kv = 0, tr_buf = 0;
 #endif
-            for (int j = 0; j < nsteps; ++j) {
+            for (int j = par; j < nsteps; j += 2) {
                 const int b = j % C::kNumBufs;
+                PX_T(tb0);
                 if (j >= C::kNumBufs &&
                     !mbar_wait(&o_done[b], static_cast<uint32_t>((j / C::kNumBufs - 1) & 1), a.status, abort_flag))
                     break;
+                PX_T(tb1);
+                PX_ADD(tr_buf, tb1 - tb0);
                 const int s = j % C::kKStages;
                 PX_T(t0);
                 if (!mbar_wait(&k_full[s], static_cast<uint32_t>((j / C::kKStages) & 1), a.status, abort_flag)) break;
                 PX_T(t1);
                 PX_ADD(tr_kv, t1 - t0);
                 tc_fence_after();
+                PX_STEP(j, 0);
                 const uint32_t k_base = smem_u32(smem + C::kOffK + s * C::kKBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -878,20 +923,25 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 }
                 umma_commit(&k_empty[s]);  // the K stage is free once this product is done
                 umma_commit(&s_full[b]);
+                PX_STEP(j, 1);
             }
             // nothing may still run on the tensor cores when the memory is freed
-            umma_commit(final_s);
-            mbar_wait(final_s, 0, a.status, nullptr);
-            PX_STAMP(a, 14, tr_kv);
+            umma_commit(&final_s[par]);
+            mbar_wait(&final_s[par], 0, a.status, nullptr);
+            if (par == 0) {
+                PX_STAMP(a, 14, tr_kv);
+                PX_STAMP(a, 6, tr_buf);
+            }
         }
         __syncwarp();
-    } else if (warp == C::kMmaWarp) {
-        // ------------------------------------------------ P.V issuer (one thread)
+    } else if (warp == C::kMmaWarp || warp == C::kMmaWarp1) {
+        // ------------------------------------------------ P.V issuers (one thread each, one token half each)
+        const int th = warp == C::kMmaWarp ? 0 : 1;
         if (lane == 0) {
             constexpr uint32_t idO = umma_idesc_bf16(C::kRows, D, false, true);
             bool ok = true;
 #ifdef PKV_TRACE
-            unsigned long long tr_p = 0;
+            unsigned long long tr_p = 0, tr_v = 0;
 #endif
             // prefill: the step and stage row of the first slot past the
             // sequence's end, when that slot lies in a block this CTA streams
@@ -907,13 +957,13 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             for (int j = 0; ok && j < nsteps; ++j) {
                 PX_T(t0);
                 const int b = j % C::kNumBufs;
-                if (!mbar_wait(&p_full[b], static_cast<uint32_t>((j / C::kNumBufs) & 1), a.status, abort_flag)) {
+                if (!mbar_wait(&p_full[th * C::kNumBufs + b], static_cast<uint32_t>((j / C::kNumBufs) & 1), a.status,
+                               abort_flag)) {
                     ok = false;
                     break;
                 }
                 PX_T(t1);
                 PX_ADD(tr_p, t1 - t0);
-                tc_fence_after();
                 // O_t += P_hi V + P_lo V over token half t (tokens 32t .. 32t+31)
                 // into that half's accumulator. P is K-major (tokens along the
                 // row); V is MN-major straight from the TMA layout: 64 columns
@@ -924,11 +974,14 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                     ok = false;
                     break;
                 }
+                PX_T(tv1);
+                PX_ADD(tr_v, tv1 - t1);
+                tc_fence_after();
                 if constexpr (PF) {
                     // The slots of the sequence's last block past its length may
                     // hold anything, NaN included. P is zero there, but 0 * NaN
                     // is not, so those V rows are zeroed before the product.
-                    if (j == tail_step) {
+                    if (j == tail_step && tail_row / 32 == th) {  // the tail lies in this issuer's token half
                         uint8_t* vt = smem + C::kOffV + s * C::kKBytes;
                         for (int hf = 0; hf < C::kHalves; ++hf)
                             for (int row = tail_row; row < (tail_row | 15) + 1; ++row)
@@ -939,29 +992,31 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                         fence_proxy_async_smem();
                     }
                 }
+                PX_STEP(j, 4);
                 const uint32_t v_base = smem_u32(smem + C::kOffV + s * C::kKBytes);
                 // token half th of P sits in columns 32 th .. 32 th + 31 of the
                 // buffer: hi of tokens 32 th + 2c, + 1 in column 32 th + c, lo 16 further
                 const uint32_t p_col = tmem + C::kColS + b * C::kTok;
 #pragma unroll
-                for (int th = 0; th < 2; ++th) {
+                for (int part = 0; part < 2; ++part) {
 #pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                        for (int kt = 2 * th; kt < 2 * th + 2; ++kt) {
-                            const uint64_t bd = umma_desc_sw128(v_base + kt * 2048, C::kHalfBytes, 1024);
-                            umma_bf16_ts(tmem + C::kColO + th * D, p_col + 32 * th + 16 * part + 8 * (kt & 1), bd,
-                                         idO, (j > 0 || part > 0 || kt > 2 * th) ? 1u : 0u);
-                        }
+                    for (int kt = 2 * th; kt < 2 * th + 2; ++kt) {
+                        const uint64_t bd = umma_desc_sw128(v_base + kt * 2048, C::kHalfBytes, 1024);
+                        umma_bf16_ts(tmem + C::kColO + th * D, p_col + 32 * th + 16 * part + 8 * (kt & 1), bd, idO,
+                                     (j > 0 || part > 0 || kt > 2 * th) ? 1u : 0u);
                     }
                 }
                 umma_commit(&v_empty[s]);
                 umma_commit(&o_done[b]);
+                PX_STEP(j, 5);
             }
             // nothing may still run on the tensor cores when the memory is freed
-            umma_commit(final_bar);
-            mbar_wait(final_bar, 0, a.status, nullptr);
-            PX_STAMP(a, 13, tr_p);
+            umma_commit(&final_bar[th]);
+            mbar_wait(&final_bar[th], 0, a.status, nullptr);
+            if (th == 0) {
+                PX_STAMP(a, 13, tr_p);
+                PX_STAMP(a, 4, tr_v);
+            }
         }
         __syncwarp();
     }
@@ -972,12 +1027,22 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     // accumulator; the two halves of a row are combined once, at the end.
     float m = ninf(), l = 0.f;  // running max (base 2, scaled) and sum
     bool ok = true;
-    float acc[D];               // warps 0-3: the row's output accumulator at the end
     const int q4 = warp & 3;
     const int th = (warp >> 2) & 1;  // token half of this softmax warp
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t col_o = C::kColO + th * D;
     float* xfer = reinterpret_cast<float*>(smem + C::kOffX);  // [3][128]: half 1's max, sum, status
+    // This chunk's partial of the tile's rows, in this CTA's shared memory over
+    // the K/V rings (idle once the loop is done): O unnormalised [128][D + 4],
+    // the running maxima, the sums. A CTA without the chunk, or one that gave
+    // up, leaves empty rows (sum 0).
+    constexpr int kPS = D + 4;
+    float* part = reinterpret_cast<float*>(smem + C::kOffK);
+    float* part_m = part + C::kRows * kPS;
+    float* part_l = part_m + C::kRows;
+    float* wts = part_l + C::kRows;  // [rows combined here][kMaxCluster + 1]
+    int* rowoff = reinterpret_cast<int*>(wts + C::kRows * (kMaxCluster + 1));
+    static_assert(C::kRows * (kPS + 2 + kMaxCluster + 2) * 4 <= C::kRingBytes, "partial fits the rings");
     if (warp < C::kSoftmaxWarps) {
         const int r = q4 * 32 + lane;
         const float scale_log2 = a.scale * kLog2e;
@@ -995,54 +1060,119 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             }
             tc_fence_after();
             PX_T(t1);
+            if (threadIdx.x == 0) PX_STEP(j, 2);
             uint32_t sv[32];
             tmem_ld32(tmem + lane_base + C::kColS + bb * C::kTok + th * 32, sv);
             tmem_ld_wait();
             PX_T(t2);
             int valid = min(C::kTok, (nblk - C::kBlk * j) * 16) - th * 32;
             if constexpr (PF) valid = min(valid, lim - ((blk0 + C::kBlk * j) * 16 + th * 32) + 1);
-            float x[32];
-#pragma unroll
-            for (int t = 0; t < 32; ++t) x[t] = __uint_as_float(sv[t]) * scale_log2;
-            if (valid < 32) {
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    if (t >= valid) x[t] = ninf();
-            }
-            // row maximum of the half, as a tree
-            float mt[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t) mt[t] = fmaxf(x[t], x[t + 16]);
-#pragma unroll
-            for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-                for (int t = 0; t < w; ++t) mt[t] = fmaxf(mt[t], mt[t + w]);
-            const float mx = mt[0];
-            // lazy rescale: the running max moves only when a score exceeds it by more than 8
-            const bool resc = mx > m + 8.f;
-            float alpha = 1.f;
-            if (resc) {
-                const float mn = fmaxf(m, mx);
-                alpha = m == ninf() ? 0.f : ex2(m - mn);
-                m = mn;
-            }
             // P = 2^(x - m) as bf16 hi + lo, both truncated: hi is the top half of
-            // p, lo the top half of p - hi (together ~16 significant bits)
+            // p, lo the top half of p - hi (together ~16 significant bits),
+            // written over this thread's own S columns (already read): hi of
+            // tokens 2c, 2c + 1 in column c, lo 16 columns further
+            const uint32_t p_col = tmem + lane_base + C::kColS + bb * C::kTok + th * 32;
             uint32_t hi[16], lo[16];
-            float ps[16];
-            const float base = m == ninf() ? 0.f : m;  // a half with no valid token yet
+            float psum;
+            bool resc;
+            float alpha = 1.f;
+            if (scale_log2 > 0.f) {
+                // Positive scale: the maximum of scale * s is scale times the raw
+                // maximum, and 2^(scale * s - m) takes one fused multiply-add
+                // per score (two scores per packed instruction).
+                float x[32];
 #pragma unroll
-            for (int t = 0; t < 32; t += 2) {
-                const float p0 = ex2(x[t] - base), p1 = ex2(x[t + 1] - base);
-                ps[t / 2] = p0 + p1;
-                hi[t / 2] = pack_bf16x2_trunc(p0, p1);
-                lo[t / 2] = pack_bf16x2_trunc(p0 - bf16_trunc(p0), p1 - bf16_trunc(p1));
+                for (int t = 0; t < 32; ++t) x[t] = __uint_as_float(sv[t]);
+                if (valid < 32) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (t >= valid) x[t] = ninf();
+                }
+                float m1[11];
+#pragma unroll
+                for (int k = 0; k < 10; ++k) m1[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+                m1[10] = fmaxf(x[30], x[31]);
+                const float mx = fmaxf(fmax3(fmax3(m1[0], m1[1], m1[2]), fmax3(m1[3], m1[4], m1[5]),
+                                             fmax3(m1[6], m1[7], m1[8])),
+                                       fmaxf(m1[9], m1[10])) *
+                                 scale_log2;
+                // lazy rescale: the running max moves only when a score exceeds it by more than 8
+                resc = mx > m + 8.f;
+                if (resc) {
+                    const float mn = fmaxf(m, mx);
+                    alpha = m == ninf() ? 0.f : ex2(m - mn);
+                    m = mn;
+                }
+                const float base = m == ninf() ? 0.f : m;  // a half with no valid token yet
+                const uint64_t sc2 = f32x2_pack(scale_log2, scale_log2), nb2 = f32x2_pack(-base, -base);
+                uint64_t acc0 = f32x2_pack(0.f, 0.f), acc1 = acc0;
+                // two groups of 16 tokens: the first group's stores overlap the
+                // second group's arithmetic
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+#pragma unroll
+                    for (int t = 16 * g; t < 16 * g + 16; t += 2) {
+                        float a0, a1;
+                        f32x2_unpack(f32x2_fma(f32x2_pack(x[t], x[t + 1]), sc2, nb2), a0, a1);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        hi[t / 2] = pack_bf16x2_trunc(p0, p1);
+                        const uint64_t pp = f32x2_pack(p0, p1);
+                        float r0, r1;
+                        f32x2_unpack(f32x2_sub(pp, f32x2_pack(bf16_trunc(p0), bf16_trunc(p1))), r0, r1);
+                        lo[t / 2] = pack_bf16x2_trunc(r0, r1);
+                        if ((t / 2) & 1)
+                            acc1 = f32x2_add(acc1, pp);
+                        else
+                            acc0 = f32x2_add(acc0, pp);
+                    }
+                    tmem_st8(p_col + 8 * g, hi + 8 * g);
+                    tmem_st8(p_col + 16 + 8 * g, lo + 8 * g);
+                }
+                float s0, s1, s2, s3;
+                f32x2_unpack(acc0, s0, s1);
+                f32x2_unpack(acc1, s2, s3);
+                psum = (s0 + s1) + (s2 + s3);
+            } else {
+                // zero or negative scale: scale first, then the plain maximum
+                float x[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) x[t] = __uint_as_float(sv[t]) * scale_log2;
+                if (valid < 32) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (t >= valid) x[t] = ninf();
+                }
+                float mt[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) mt[t] = fmaxf(x[t], x[t + 16]);
+#pragma unroll
+                for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                    for (int t = 0; t < w; ++t) mt[t] = fmaxf(mt[t], mt[t + w]);
+                const float mx = mt[0];
+                resc = mx > m + 8.f;
+                if (resc) {
+                    const float mn = fmaxf(m, mx);
+                    alpha = m == ninf() ? 0.f : ex2(m - mn);
+                    m = mn;
+                }
+                float ps[16];
+                const float base = m == ninf() ? 0.f : m;
+#pragma unroll
+                for (int t = 0; t < 32; t += 2) {
+                    const float p0 = ex2(x[t] - base), p1 = ex2(x[t + 1] - base);
+                    ps[t / 2] = p0 + p1;
+                    hi[t / 2] = pack_bf16x2_trunc(p0, p1);
+                    lo[t / 2] = pack_bf16x2_trunc(p0 - bf16_trunc(p0), p1 - bf16_trunc(p1));
+                }
+#pragma unroll
+                for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                    for (int t = 0; t < w; ++t) ps[t] += ps[t + w];
+                psum = ps[0];
+                tmem_st16(p_col, hi);
+                tmem_st16(p_col + 16, lo);
             }
-#pragma unroll
-            for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-                for (int t = 0; t < w; ++t) ps[t] += ps[t + w];
-            const float psum = ps[0];
             l = l * alpha + psum;
             PX_T(t3);
             // rescale this half's O in tensor memory once the PV product of step j - 1 is in
@@ -1065,14 +1195,11 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 tmem_st_wait();
             }
             PX_T(t4);
-            // P over this thread's own S columns (already read)
-            const uint32_t p_col = tmem + lane_base + C::kColS + bb * C::kTok + th * 32;
-            tmem_st16(p_col, hi);
-            tmem_st16(p_col + 16, lo);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[bb]);
+            if (lane == 0) mbar_arrive(&p_full[th * C::kNumBufs + bb]);
+            if (threadIdx.x == 0) PX_STEP(j, 3);
             PX_T(t5);
             PX_ADD(tr_s, t1 - t0);
             PX_ADD(tr_ld, t2 - t1);
@@ -1101,12 +1228,15 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         }
         named_barrier_sync(1, 32 * C::kSoftmaxWarps);
         if (th == 0) {
-            // combine the row's two halves
+            // combine the row's two halves into the partial, 32 columns at a time
             const float m1 = xfer[r], l1 = xfer[C::kRows + r];
             const bool ok1 = xfer[2 * C::kRows + r] != 0.f;
             const bool has0 = ok && l > 0.f, has1 = ok1 && l1 > 0.f;
             const float M = fmaxf(has0 ? m : ninf(), has1 ? m1 : ninf());
             const float w0 = has0 ? ex2(m - M) : 0.f, w1 = has1 ? ex2(m1 - M) : 0.f;
+            const float lc = (has0 ? w0 * l : 0.f) + (has1 ? w1 * l1 : 0.f);
+            const bool live = !*abort_flag && lc > 0.f;
+            fence_proxy_async_smem();  // the rings were last written by TMA
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
                 uint32_t o0[32], o1[32];
@@ -1114,12 +1244,18 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 tmem_ld32(tmem + lane_base + C::kColO + D + c, o1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    acc[c + e] = (has0 ? w0 * __uint_as_float(o0[e]) : 0.f) + (has1 ? w1 * __uint_as_float(o1[e]) : 0.f);
+                for (int e = 0; e < 32; e += 4) {
+                    float v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        v[u] = live ? (has0 ? w0 * __uint_as_float(o0[e + u]) : 0.f) +
+                                          (has1 ? w1 * __uint_as_float(o1[e + u]) : 0.f)
+                                    : 0.f;
+                    *reinterpret_cast<float4*>(part + r * kPS + c + e) = make_float4(v[0], v[1], v[2], v[3]);
+                }
             }
-            l = (has0 ? w0 * l : 0.f) + (has1 ? w1 * l1 : 0.f);
-            m = M;
-            ok = true;  // a half that gave up contributes nothing; the status word records it
+            part_m[r] = live ? M : ninf();
+            part_l[r] = live ? lc : 0.f;
         }
     }
     // ---- tensor memory is no longer read: free it
@@ -1129,30 +1265,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
-    if (threadIdx.x == 0) PX_STAMP(a, 4, global_ns());
 
-    // ---- this chunk's partial of the tile's rows, in this CTA's shared memory
-    // (over the now idle K/V ring): O unnormalised [128][D + 4], the running
-    // maxima, the sums. A CTA without the chunk, or one that gave up, leaves
-    // empty rows (sum 0).
-    constexpr int kPS = D + 4;
-    float* part = reinterpret_cast<float*>(smem + C::kOffK);
-    float* part_m = part + C::kRows * kPS;
-    float* part_l = part_m + C::kRows;
-    float* wts = part_l + C::kRows;  // [rows combined here][kMaxCluster + 1]
-    int* rowoff = reinterpret_cast<int*>(wts + C::kRows * (kMaxCluster + 1));
-    static_assert(C::kRows * (kPS + 2 + kMaxCluster + 2) * 4 <= C::kRingBytes, "partial fits the rings");
-    fence_proxy_async_smem();  // the ring was last written by TMA
-    if (warp < 4) {
-        const int r = threadIdx.x;
-        const bool live = ok && !*abort_flag && l > 0.f;
-#pragma unroll
-        for (int d = 0; d < D; d += 4)
-            *reinterpret_cast<float4*>(part + r * kPS + d) =
-                live ? make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-        part_m[r] = live ? m : ninf();
-        part_l[r] = live ? l : 0.f;
-    }
     cluster_sync();
     grid_dependency_wait();  // fold_o / fold_lse come from the decode kernel
 

@@ -255,3 +255,29 @@ def test_bounded_wait_runs_out_and_is_reported(pkv):
     with pytest.raises(pkv.PkvError) as e:
         run(pkv, c, d, 9, flags=pkv.PKV_FLAG_TEST_STALL)
     assert e.value.name == "PKV_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("slope", [10.0, 3.0])
+def test_prefill_running_maximum_moves_every_step(pkv, slope):
+    """Scores that climb along the context, so that the tile kernel's running
+    maximum moves past its lazy-rescale threshold in (nearly) every 64-token
+    step, at both positions of the issuer's step pairs: O and a waiting P are
+    rescaled. slope: base-2 logit increase per 32 tokens."""
+    c = cases.multiquery_case(81, [1100, 700], [40, 33], 8, 2, 128, torch.bfloat16)
+    k = c["k_pool"].float()
+    q = c["q"].float()
+    scale = c["scale"]
+    # dimension 0 of q is 20 everywhere; dimension 0 of the token at logical position t is
+    # slope / (log2(e) * scale * 20) * (t // 32), so logit_t = slope * (t // 32) / log2(e) + noise
+    q[:, :, 0] = 20.0
+    step = slope / (1.4426950408889634 * scale * 20.0)
+    for i, n in enumerate(c["lens"]):
+        for t in range(int(n)):
+            blk, off = int(c["tables"][i, t // 16]), t % 16
+            k[blk, :, off, 0] = step * (t // 32)
+    c["k_pool"] = k.to(torch.bfloat16)
+    c["q"] = q.to(torch.bfloat16)
+    d = dev(c)
+    out = run(pkv, c, d, 40)
+    assert pkv.pkv_device_status(clear=True) == 0
+    check(out, want(c))
