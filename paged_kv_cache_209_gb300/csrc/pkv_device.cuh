@@ -116,11 +116,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed. Gives up when
 // *abort becomes nonzero (another warp gave up) or after limit_ns; in the
 // second case it sets PKV_DEVERR_TIMEOUT in *status and raises *abort.
+// sleep_ns > 0: sleep that long between probes (a warp waiting well ahead of
+// need leaves the issue slots to the warps on the critical path).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
-                                          volatile int* abort, unsigned long long limit_ns = kWaitLimitNs) {
+                                          volatile int* abort, unsigned long long limit_ns = kWaitLimitNs,
+                                          unsigned int sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
+        if (sleep_ns) __nanosleep(sleep_ns);
         if (abort != nullptr && *abort) return false;
         if (global_ns() - t0 > limit_ns) {
             atomicOr(status, PKV_DEVERR_TIMEOUT);
@@ -263,10 +267,15 @@ __device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-// Maximum of three values in one instruction (sm_100 and later).
+// Maximum / minimum of three values in one instruction (sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
 

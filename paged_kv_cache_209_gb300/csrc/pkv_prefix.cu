@@ -46,10 +46,17 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxChunks = 32;
+// Sleep between probes of a wait that runs ahead of need (the score issuers
+// waiting for a free S/P buffer, the copy warps for a free stage).
+#ifndef PKV_AHEAD_SLEEP_NS
+#define PKV_AHEAD_SLEEP_NS 64
+#endif
+constexpr unsigned int kAheadSleepNs = PKV_AHEAD_SLEEP_NS;
 constexpr int kMaxCluster = 8;  // CTAs (chunks) per cluster of the tcgen05 kernel: the portable maximum
 constexpr int kMaxGroups = kMaxBatchPerLaunch;
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+
 
 // Build-time tracing (PKV_TRACE): each CTA of the tcgen05 kernel records
 // %globaltimer stamps in a row of 16 words: [0] entry, [1] tile located,
@@ -850,7 +857,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 int good = 1;
                 if (lane == 0) {
                     PX_T(t0);
-                    good = mbar_wait(&empty[j % nst], static_cast<uint32_t>((j / nst) & 1) ^ 1u, a.status, abort_flag)
+                    good = mbar_wait(&empty[j % nst], static_cast<uint32_t>((j / nst) & 1) ^ 1u, a.status, abort_flag,
+                                     kWaitLimitNs, kAheadSleepNs)
                                ? 1 : 0;
                     PX_T(t1);
                     PX_ADD(tr_tma, t1 - t0);
@@ -902,8 +910,8 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             for (int j = par; j < nsteps; j += 2) {
                 const int b = j % C::kNumBufs;
                 PX_T(tb0);
-                if (j >= C::kNumBufs &&
-                    !mbar_wait(&o_done[b], static_cast<uint32_t>((j / C::kNumBufs - 1) & 1), a.status, abort_flag))
+                if (j >= C::kNumBufs && !mbar_wait(&o_done[b], static_cast<uint32_t>((j / C::kNumBufs - 1) & 1),
+                                                   a.status, abort_flag, kWaitLimitNs, kAheadSleepNs))
                     break;
                 PX_T(tb1);
                 PX_ADD(tr_buf, tb1 - tb0);
@@ -1076,26 +1084,44 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             float psum;
             bool resc;
             float alpha = 1.f;
-            if (scale_log2 > 0.f) {
-                // Positive scale: the maximum of scale * s is scale times the raw
-                // maximum, and 2^(scale * s - m) takes one fused multiply-add
-                // per score (two scores per packed instruction).
+            {
+                // The maximum of scale * s is the scale times the raw maximum (the
+                // raw minimum for a negative scale), and 2^(scale * s - m) takes
+                // one fused multiply-add per score (two scores per packed
+                // instruction). A score past the valid range becomes an infinity
+                // that the scale turns into -inf (weight 0). A zero scale is
+                // replaced by 1e-30: every finite score then gives the same
+                // weights in float32, and an infinity stays infinite.
+                const bool pos = scale_log2 >= 0.f;
+                const float sl = scale_log2 == 0.f ? 1e-30f : scale_log2;
                 float x[32];
 #pragma unroll
                 for (int t = 0; t < 32; ++t) x[t] = __uint_as_float(sv[t]);
                 if (valid < 32) {
+                    const float kill = pos ? ninf() : -ninf();
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
-                        if (t >= valid) x[t] = ninf();
+                        if (t >= valid) x[t] = kill;
                 }
-                float m1[11];
+                float ext;
+                if (pos) {
+                    float m1[11];
 #pragma unroll
-                for (int k = 0; k < 10; ++k) m1[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
-                m1[10] = fmaxf(x[30], x[31]);
-                const float mx = fmaxf(fmax3(fmax3(m1[0], m1[1], m1[2]), fmax3(m1[3], m1[4], m1[5]),
-                                             fmax3(m1[6], m1[7], m1[8])),
-                                       fmaxf(m1[9], m1[10])) *
-                                 scale_log2;
+                    for (int k = 0; k < 10; ++k) m1[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+                    m1[10] = fmaxf(x[30], x[31]);
+                    ext = fmaxf(fmax3(fmax3(m1[0], m1[1], m1[2]), fmax3(m1[3], m1[4], m1[5]),
+                                      fmax3(m1[6], m1[7], m1[8])),
+                                fmaxf(m1[9], m1[10]));
+                } else {
+                    float m1[11];
+#pragma unroll
+                    for (int k = 0; k < 10; ++k) m1[k] = fmin3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+                    m1[10] = fminf(x[30], x[31]);
+                    ext = fminf(fmin3(fmin3(m1[0], m1[1], m1[2]), fmin3(m1[3], m1[4], m1[5]),
+                                      fmin3(m1[6], m1[7], m1[8])),
+                                fminf(m1[9], m1[10]));
+                }
+                const float mx = valid > 0 ? ext * sl : ninf();
                 // lazy rescale: the running max moves only when a score exceeds it by more than 8
                 resc = mx > m + 8.f;
                 if (resc) {
@@ -1104,7 +1130,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                     m = mn;
                 }
                 const float base = m == ninf() ? 0.f : m;  // a half with no valid token yet
-                const uint64_t sc2 = f32x2_pack(scale_log2, scale_log2), nb2 = f32x2_pack(-base, -base);
+                const uint64_t sc2 = f32x2_pack(sl, sl), nb2 = f32x2_pack(-base, -base);
                 uint64_t acc0 = f32x2_pack(0.f, 0.f), acc1 = acc0;
                 // two groups of 16 tokens: the first group's stores overlap the
                 // second group's arithmetic
@@ -1132,46 +1158,6 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
                 f32x2_unpack(acc0, s0, s1);
                 f32x2_unpack(acc1, s2, s3);
                 psum = (s0 + s1) + (s2 + s3);
-            } else {
-                // zero or negative scale: scale first, then the plain maximum
-                float x[32];
-#pragma unroll
-                for (int t = 0; t < 32; ++t) x[t] = __uint_as_float(sv[t]) * scale_log2;
-                if (valid < 32) {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        if (t >= valid) x[t] = ninf();
-                }
-                float mt[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) mt[t] = fmaxf(x[t], x[t + 16]);
-#pragma unroll
-                for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-                    for (int t = 0; t < w; ++t) mt[t] = fmaxf(mt[t], mt[t + w]);
-                const float mx = mt[0];
-                resc = mx > m + 8.f;
-                if (resc) {
-                    const float mn = fmaxf(m, mx);
-                    alpha = m == ninf() ? 0.f : ex2(m - mn);
-                    m = mn;
-                }
-                float ps[16];
-                const float base = m == ninf() ? 0.f : m;
-#pragma unroll
-                for (int t = 0; t < 32; t += 2) {
-                    const float p0 = ex2(x[t] - base), p1 = ex2(x[t + 1] - base);
-                    ps[t / 2] = p0 + p1;
-                    hi[t / 2] = pack_bf16x2_trunc(p0, p1);
-                    lo[t / 2] = pack_bf16x2_trunc(p0 - bf16_trunc(p0), p1 - bf16_trunc(p1));
-                }
-#pragma unroll
-                for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-                    for (int t = 0; t < w; ++t) ps[t] += ps[t + w];
-                psum = ps[0];
-                tmem_st16(p_col, hi);
-                tmem_st16(p_col + 16, lo);
             }
             l = l * alpha + psum;
             PX_T(t3);
