@@ -1222,6 +1222,40 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             const float w0 = has0 ? ex2(m - M) : 0.f, w1 = has1 ? ex2(m1 - M) : 0.f;
             const float lc = (has0 ? w0 * l : 0.f) + (has1 ? w1 * l1 : 0.f);
             const bool live = !*abort_flag && lc > 0.f;
+            if (PF && gridDim.y == 1) {
+                // one chunk per tile: the row is final here, so it is normalised
+                // and written at once (no partial, no cluster combine). The
+                // tensor-memory loads are warp-wide, so every lane takes part;
+                // only rows that exist are stored.
+                const int Rg = r0 + r;
+                const int t = Rg / G;
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                                      (static_cast<long long>(info[9] + t) * a.q_heads + h * G + (Rg - t * G)) * D;
+                const float inv = live ? 1.f / lc : 0.f;
+                const float v0 = w0 * inv, v1 = w1 * inv;
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o0[32], o1[32];
+                    tmem_ld32(tmem + lane_base + C::kColO + c, o0);
+                    tmem_ld32(tmem + lane_base + C::kColO + D + c, o1);
+                    tmem_ld_wait();
+                    if (r < nrows) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const float y0 = (has0 ? v0 * __uint_as_float(o0[e + 2 * u]) : 0.f) +
+                                                 (has1 ? v1 * __uint_as_float(o1[e + 2 * u]) : 0.f);
+                                const float y1 = (has0 ? v0 * __uint_as_float(o0[e + 2 * u + 1]) : 0.f) +
+                                                 (has1 ? v1 * __uint_as_float(o1[e + 2 * u + 1]) : 0.f);
+                                w[u] = pack_bf16x2(y0, y1);
+                            }
+                            *reinterpret_cast<uint4*>(orow + c + e) = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            } else {
             fence_proxy_async_smem();  // the rings were last written by TMA
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
@@ -1242,6 +1276,7 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
             }
             part_m[r] = live ? M : ninf();
             part_l[r] = live ? lc : 0.f;
+            }
         }
     }
     // ---- tensor memory is no longer read: free it
@@ -1250,6 +1285,10 @@ __global__ void __launch_bounds__(Ux<D>::kThreads, 1)
     if (warp == C::kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
+    }
+    if (PF && gridDim.y == 1) {  // the rows went out above
+        if (threadIdx.x == 0) PX_STAMP(a, 5, global_ns());
+        return;
     }
 
     cluster_sync();
