@@ -60,7 +60,9 @@ struct Mq {
     static constexpr int kIssueLanes = Q8 ? PKV_MQ8_ISSUE_LANES : PKV_MQ_ISSUE_LANES;
     static constexpr int kStages = NST;
     static constexpr int kConsumers = 4;
-    static constexpr int kThreads = (kConsumers + 1) * 32;
+    // two producer warps: one issues the K side of every block (K rows, or K
+    // codes and K scales), the other the V side, each on its own barrier
+    static constexpr int kThreads = (kConsumers + 2) * 32;
     static constexpr int kHalves = D / 64;
     static constexpr int kPoolBytes = 16 * D * 2;
     // bf16: K then V (16 rows x D each). int8: K codes [16][D] at 0, V codes
@@ -71,18 +73,19 @@ struct Mq {
     static constexpr int kStageBytes = Q8 ? 2 * 16 * D : 2 * kPoolBytes;
     static constexpr int kScaleBytes = Q8 ? 256 : 0;
     static constexpr int kVScaleOff = 128;
-    static constexpr int kTxBytes = Q8 ? 2 * 16 * D + 128 : kStageBytes;
+    static constexpr int kSideBytes = kStageBytes / 2;                     // K or V of one stage
+    static constexpr int kTxBytes = Q8 ? kSideBytes + 64 : kSideBytes;    // one side's copies
     static constexpr int kOffScales = kStages * kStageBytes;
     static_assert(kStages >= kIssueLanes && kIssueLanes < 32, "a batch of issued blocks must fit the ring");
     static_assert(kOffScales % 1024 == 0 && kScaleBytes % 128 == 0 && kVScaleOff % 128 == 0,
                   "TMA destinations must stay 128-byte aligned");
     // shared memory (offsets from a 1024-byte aligned base): the ring,
-    // full[NST], empty[NST] and the piece barrier, stage flags and the abort
+    // full[2][NST] (K side, V side), empty[NST] and the piece barrier, stage flags and the abort
     // flag, the combine scratch (two buffers of 4 warps x 8 rows x (D + 2)
     // floats, alternating between pieces), then per sequence: block prefix
     // sums and context lengths.
     static constexpr int kOffBars = kOffScales + kStages * kScaleBytes;
-    static constexpr int kOffFlags = kOffBars + (2 * kStages + 1) * 8;
+    static constexpr int kOffFlags = kOffBars + (3 * kStages + 1) * 8;
     static constexpr int kOffScratch = ((kOffFlags + kStages * 4 + 4 + 15) / 16) * 16;
     static constexpr int kScratchFloats = 2 * kConsumers * 8 * (D + 2);
     static constexpr int kOffSeq = kOffScratch + kScratchFloats * 4;
@@ -160,14 +163,14 @@ constexpr float kCodeBias = 1152.f;
 // stays below the f16 maximum 65504 (255 * 256 = 65280).
 constexpr float kVScaleF16Safe = 255.f;
 
-// Smallest k in [0, 126] with v * 2^-k <= limit (halvings of a float are exact).
-__device__ __noinline__ int pow2_shift_to_fit(float v, float limit) {
-    int k = 0;
-    while (v > limit && k < 126) {
-        v *= 0.5f;
-        ++k;
-    }
-    return k;
+// Smallest k >= 0 with v * 2^-k <= kVScaleF16Safe, for a finite v above it:
+// with v = m 2^e (m in [1, 2)), v 2^-(e-7) = 128 m lies in [128, 256), so k is
+// e - 7, or e - 6 when 128 m exceeds 255. Halvings of a float are exact.
+__device__ __forceinline__ int pow2_shift_to_fit(float v) {
+    const uint32_t b = __float_as_uint(v);
+    const int e = static_cast<int>((b >> 23) & 0xffu) - 127;
+    const float m128 = __uint_as_float((b & 0x007fffffu) | (134u << 23));
+    return e - 7 + (m128 > kVScaleF16Safe ? 1 : 0);
 }
 __device__ __forceinline__ void codes_to_f16x2_biased(uint32_t w, uint32_t& p01, uint32_t& p23) {
     const uint32_t u = w ^ 0x80808080u;
@@ -205,8 +208,8 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
     using C = Mq<D, NST, Q8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-    uint64_t* empty = full + C::kStages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);  // K side; full + kStages: V side
+    uint64_t* empty = full + 2 * C::kStages;
     uint64_t* piece_bar = empty + C::kStages;  // every consumer warp published its piece state
     int* stage_ok = reinterpret_cast<int*>(smem + C::kOffFlags);
     volatile int* abort_flag = stage_ok + C::kStages;
@@ -221,6 +224,7 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
+            mbar_init(&full[C::kStages + s], 1);
             mbar_init(&empty[s], a.wpu);  // the warps of one unit lane consume a stage
         }
         mbar_init(piece_bar, C::kConsumers);
@@ -285,9 +289,16 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
     const long long ua = range_start(cta, U, a.num_ctas);
     const long long ub = range_start(cta + 1, U, a.num_ctas);
 
-    if (warp == C::kConsumers) {
-        // ------------------------------------------------ producer warp (as in the decode kernel)
+    if (warp >= C::kConsumers) {
+        // ------------------------------------------------ producer warps (as in the decode kernel)
+        // Both walk the same blocks in the same order; warp kConsumers issues
+        // the K side and warp kConsumers + 1 the V side, each arriving on its
+        // own full barrier. One warp issuing all four copies of an int8 block
+        // (codes and scale rows) was the pace-setter: the int8 call took
+        // 107 us with one producer, 95 us without the scale copies.
         if (a.test_stall) return;  // test hook: nothing is ever issued, so every consumer wait runs out
+        const int side = warp - C::kConsumers;
+        uint64_t* fulls = full + side * C::kStages;
         const uint64_t kv_policy = l2_evict_first_policy();
         Walker wk;
         wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
@@ -329,31 +340,37 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                     const bool mine = lane < n;
                     const bool load = mine && bid >= 0 && bid < a.num_blocks;
                     if (mine) {
-                        stage_ok[s] = load ? 1 : 0;
+                        stage_ok[s] = load ? 1 : 0;  // both sides write the same flag
                         if (load) {
-                            mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+                            mbar_arrive_expect_tx(&fulls[s], C::kTxBytes);
                         } else {
-                            atomicOr(a.status, PKV_DEVERR_RANGE);
-                            mbar_arrive(&full[s]);
+                            if (side == 0) atomicOr(a.status, PKV_DEVERR_RANGE);
+                            mbar_arrive(&fulls[s]);
                         }
                     }
                     if (load) {
-                        uint8_t* st = smem + s * C::kStageBytes;
+                        uint8_t* st = smem + s * C::kStageBytes + side * C::kSideBytes;
                         const int hb = bid * a.kv_heads + pc.head;
                         if (Q8) {
-                            tma_load_2d(st, &tmK, 0, hb * 16, &full[s], kv_policy);
-                            tma_load_2d(st + 16 * D, &tmV, 0, hb * 16, &full[s], kv_policy);
-                            uint8_t* sc = smem + C::kOffScales + s * C::kScaleBytes;
-                            tma_load_2d(sc, &tmKs, 0, hb, &full[s], kv_policy);
-                            tma_load_2d(sc + C::kVScaleOff, &tmVs, 0, hb, &full[s], kv_policy);
+                            uint8_t* sc = smem + C::kOffScales + s * C::kScaleBytes + side * C::kVScaleOff;
+                            if (side == 0) {
+                                tma_load_2d(st, &tmK, 0, hb * 16, &fulls[s], kv_policy);
+                                tma_load_2d(sc, &tmKs, 0, hb, &fulls[s], kv_policy);
+                            } else {
+                                tma_load_2d(st, &tmV, 0, hb * 16, &fulls[s], kv_policy);
+                                tma_load_2d(sc, &tmVs, 0, hb, &fulls[s], kv_policy);
+                            }
                         } else {
                             const int y = hb * 16;
+                            if (side == 0) {
 #pragma unroll
-                            for (int hf = 0; hf < C::kHalves; ++hf)
-                                tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
+                                for (int hf = 0; hf < C::kHalves; ++hf)
+                                    tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &fulls[s], kv_policy);
+                            } else {
 #pragma unroll
-                            for (int hf = 0; hf < C::kHalves; ++hf)
-                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
+                                for (int hf = 0; hf < C::kHalves; ++hf)
+                                    tma_load_2d(st + hf * 2048, &tmV, hf * 64, y, &fulls[s], kv_policy);
+                            }
                         }
                     }
                     k += n;
@@ -362,10 +379,10 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                 cur = nxt;
             }
         }
-        if (!ok && lane == 0) {  // after an abort: wait (bounded) for the copies still in flight
+        if (!ok && lane == 0) {  // after an abort: wait (bounded) for this side's copies still in flight
             const long long first = k > C::kStages ? k - C::kStages : 0;
             for (long long u = first; u < k; ++u)
-                mbar_wait(&full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
+                mbar_wait(&fulls[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
         }
         return;
     }
@@ -469,11 +486,13 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
         k += skip;
         for (int blk = pc.blk_from + skip; blk < pc.blk_to; blk += UG, k += UG) {
             const int s = static_cast<int>(k % C::kStages);
-            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag,
-                           a.test_stall ? kTestWaitLimitNs : kWaitLimitNs))
-                return;
+            // K side first; the V side is waited for just before the PV product
+            const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1);
+            const unsigned long long wlim = a.test_stall ? kTestWaitLimitNs : kWaitLimitNs;
+            if (!mbar_wait(&full[s], par, a.status, abort_flag, wlim)) return;
             const int valid = min(16, n_ctx - blk * 16);
-            if (!Q8 && stage_ok[s] && active) {
+            const bool use = stage_ok[s] && active;
+            if (!Q8 && use) {
                 const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
                 const uint32_t vbase = kbase + C::kPoolBytes;
                 // four independent accumulator chains over the k-steps
@@ -532,6 +551,7 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                 const uint32_t lo23 = pack_bf16x2(e2 - bf16lo_to_f32(h23), e3 - bf16hi_to_f32(h23));
                 const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
                 const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+                if (!mbar_wait(&full[C::kStages + s], par, a.status, abort_flag, wlim)) return;
                 // rows past the context may hold anything: zero them in V
                 uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
                 if (valid < 16) {
@@ -552,7 +572,7 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                     mma_bf16_16816(o[i], a0, a1, a2, a3, bl0, bl1);
                 }
             }
-            if (Q8 && stage_ok[s] && active) {
+            if (Q8 && use) {
                 const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
                 const uint32_t vb = kb + 16 * D;
                 const float* ksc = reinterpret_cast<const float*>(smem + C::kOffScales + s * C::kScaleBytes);
@@ -587,20 +607,47 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                 const float x1 = pA <= lim1 ? (sa[1] + sb[1] - kb1) * kA * cf1 : ninf();
                 const float x2 = pB <= lim0 ? (sa[2] + sb[2] - kb0) * kB * cf0 : ninf();
                 const float x3 = pB <= lim1 ? (sa[3] + sb[3] - kb1) * kB * cf1 : ninf();
+                if (!mbar_wait(&full[C::kStages + s], par, a.status, abort_flag, wlim)) return;
+                // P' = P times the V scale of its token (zero past the context), as f16
+                float vA = pA < n_ctx ? vsc[tokA] : 0.f, vB = pB < n_ctx ? vsc[tokB] : 0.f;
+                // P <= 2^8 under the lazy rescale, so P' stays below the f16
+                // maximum while every V scale is at most kVScaleF16Safe. A block
+                // with a larger scale (rows with max |v| above ~32 000) runs its
+                // product on P' 2^-k and O 2^-k, and O is scaled back by 2^k
+                // afterwards: powers of two, exact in fp32. One vote covers both
+                // rare cases (a new running maximum, a large V scale): a second
+                // vote and branch per block cost 1.6 % of the call.
                 float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-                if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+                float o_back = 1.f;
+                if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f || fmaxf(vA, vB) > kVScaleF16Safe)) {
 #pragma unroll
                     for (int off = 4; off < 32; off <<= 1) {
                         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
                     }
+                    // a rescale to the running maximum (exact whether or not it moved)
                     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
                     const float nb0 = mn0 == ninf() ? 0.f : mn0;
                     const float nb1 = mn1 == ninf() ? 0.f : mn1;
-                    const float al0 = m0 == ninf() ? 0.f : ex2(m0 - nb0);
-                    const float al1 = m1 == ninf() ? 0.f : ex2(m1 - nb1);
+                    float al0 = m0 == ninf() ? 0.f : ex2(m0 - nb0);
+                    float al1 = m1 == ninf() ? 0.f : ex2(m1 - nb1);
                     l0 *= al0;
                     l1 *= al1;
+                    m0 = mn0;
+                    m1 = mn1;
+                    // and the block's V-scale shift, folded into the same pass over O
+                    float vm = fmaxf(vA, vB);
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                    if (vm > kVScaleF16Safe && vm <= 3.0e38f) {
+                        const int k2 = pow2_shift_to_fit(vm);
+                        const float down = __uint_as_float(static_cast<uint32_t>(127 - k2) << 23);
+                        o_back = __uint_as_float(static_cast<uint32_t>(127 + k2) << 23);
+                        vA *= down;
+                        vB *= down;
+                        al0 *= down;
+                        al1 *= down;
+                    }
 #pragma unroll
                     for (int i = 0; i < D / 16; ++i) {
                         o[i][0] *= al0;
@@ -608,39 +655,12 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                         o[i][2] *= al0;
                         o[i][3] *= al1;
                     }
-                    m0 = mn0;
-                    m1 = mn1;
                 }
                 const float b0 = m0 == ninf() ? 0.f : m0;
                 const float b1 = m1 == ninf() ? 0.f : m1;
                 const float e0 = ex2(x0 - b0), e1 = ex2(x1 - b1), e2 = ex2(x2 - b0), e3 = ex2(x3 - b1);
                 l0 += e0 + e2;
                 l1 += e1 + e3;
-                // P' = P times the V scale of its token (zero past the context), as f16
-                float vA = pA < n_ctx ? vsc[tokA] : 0.f, vB = pB < n_ctx ? vsc[tokB] : 0.f;
-                // P <= 2^8 under the lazy rescale, so P' stays below the f16
-                // maximum while every V scale is at most kVScaleF16Safe. A block
-                // with a larger scale (rows with max |v| above ~32 000) runs its
-                // product on P' 2^-k and O 2^-k, and O is scaled back by 2^k
-                // afterwards: powers of two, exact in fp32.
-                float o_back = 1.f;
-                if (__any_sync(0xffffffffu, fmaxf(vA, vB) > kVScaleF16Safe)) {
-                    float vm = fmaxf(vA, vB);
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
-                    const int k2 = vm <= 3.0e38f ? pow2_shift_to_fit(vm, kVScaleF16Safe) : 0;
-                    const float down = __uint_as_float(static_cast<uint32_t>(127 - k2) << 23);
-                    o_back = __uint_as_float(static_cast<uint32_t>(127 + k2) << 23);
-                    vA *= down;
-                    vB *= down;
-#pragma unroll
-                    for (int i = 0; i < D / 16; ++i) {
-                        o[i][0] *= down;
-                        o[i][1] *= down;
-                        o[i][2] *= down;
-                        o[i][3] *= down;
-                    }
-                }
                 const uint32_t bh0 = movmatrix_trans(pack_f16x2(e0 * vA, e1 * vA));
                 const uint32_t bh1 = movmatrix_trans(pack_f16x2(e2 * vB, e3 * vB));
                 // ---- O^T += V^T P'^T: V coordinate rows of 16 token codes
@@ -666,6 +686,8 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                     }
                 }
             }
+            // a stage is handed back only after both of its sides have landed
+            if (!use && !mbar_wait(&full[C::kStages + s], par, a.status, abort_flag, wlim)) return;
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
