@@ -449,7 +449,7 @@ def measure_workload(name, args, ws, rank, device, single_pass=False, want_host=
     qstart = w["query_start"]
     group, gblocks, mgb = w["prefix_group"], w["group_blocks"], w["max_group_blocks"]
     if q8:
-        ks_pool, vs_pool = w["k_scales"], w["v_scales"]
+        sc_pool = w["scales"]          # [blocks][heads][2][16]: K-row and V-row scales
         ws_bytes = pkv.pkv_decode_q8_workspace_size(B, HQ, MAXB, k_pool)
     elif two_phase:
         ws_bytes = pkv.pkv_decode_prefixed_workspace_size(B, HQ, MAXB, len(gblocks), mgb, k_pool)
@@ -463,7 +463,7 @@ def measure_workload(name, args, ws, rank, device, single_pass=False, want_host=
 
     def decode():
         if q8:
-            pkv.pkv_decode_attention_q8(q, k_pool, v_pool, ks_pool, vs_pool, tables, lens, scale, out=out,
+            pkv.pkv_decode_attention_q8(q, k_pool, v_pool, sc_pool, tables, lens, scale, out=out,
                                         workspace=workspace, stream=stream)
         elif nq > 1:
             pkv.pkv_multiquery_attention(q, k_pool, v_pool, tables, lens, qstart, scale, nq, out=out,
@@ -477,13 +477,13 @@ def measure_workload(name, args, ws, rank, device, single_pass=False, want_host=
 
     def copy_blocks(p):
         if q8:
-            pkv.pkv_copy_blocks_q8(p, k_pool, v_pool, ks_pool, vs_pool, stream=stream)
+            pkv.pkv_copy_blocks_q8(p, k_pool, v_pool, sc_pool, stream=stream)
         else:
             pkv.pkv_copy_blocks(p, k_pool, v_pool, stream=stream)
 
     def append():
         if q8:
-            pkv.pkv_append_q8(kn, vn, slots, k_pool, v_pool, ks_pool, vs_pool, stream=stream)
+            pkv.pkv_append_q8(kn, vn, slots, k_pool, v_pool, sc_pool, stream=stream)
         else:
             pkv.pkv_append(kn, vn, slots, k_pool, v_pool, stream=stream)
 
@@ -613,7 +613,8 @@ def measure_workload(name, args, ws, rank, device, single_pass=False, want_host=
         if q8:
             host.update(kc=k_pool.index_select(0, idx).cpu().numpy(),
                         vc=np.ascontiguousarray(v_pool.index_select(0, idx).cpu().numpy().transpose(0, 1, 3, 2)),
-                        ks=ks_pool.index_select(0, idx).cpu().numpy(), vs=vs_pool.index_select(0, idx).cpu().numpy())
+                        ks=sc_pool[:, :, 0].index_select(0, idx).cpu().numpy(),
+                        vs=sc_pool[:, :, 1].index_select(0, idx).cpu().numpy())
         else:
             host.update(kp=k_pool.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16),
                         vp=v_pool.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16))
@@ -642,13 +643,13 @@ def measure_workload(name, args, ws, rank, device, single_pass=False, want_host=
 
     def append_cur():       # on the current stream (the capture stream while capturing)
         if q8:
-            pkv.pkv_append_q8(kn, vn, slots, k_pool, v_pool, ks_pool, vs_pool)
+            pkv.pkv_append_q8(kn, vn, slots, k_pool, v_pool, sc_pool)
         else:
             pkv.pkv_append(kn, vn, slots, k_pool, v_pool)
 
     def copy_cur(p):
         if q8:
-            pkv.pkv_copy_blocks_q8(p, k_pool, v_pool, ks_pool, vs_pool)
+            pkv.pkv_copy_blocks_q8(p, k_pool, v_pool, sc_pool)
         else:
             pkv.pkv_copy_blocks(p, k_pool, v_pool)
 

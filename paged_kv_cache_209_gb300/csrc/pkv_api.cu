@@ -518,15 +518,13 @@ pkv_status pkv_multiquery_attention(const void* q, const void* k_cache, const vo
 }
 
 pkv_status pkv_append_q8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_codes,
-                         void* v_codes, float* k_scales, float* v_scales, const pkv_cache_desc* desc, uint32_t flags,
-                         void* stream) {
+                         void* v_codes, float* scales, const pkv_cache_desc* desc, uint32_t flags, void* stream) {
     NvtxRange nvtx_range("pkv_append_q8");
     pkv_status st = check_desc_q8(desc, false);
     if (st != PKV_OK) return st;
     if (num_tokens < 0) return PKV_ERR_SHAPE;
-    if (!k_codes || !v_codes || !k_scales || !v_scales) return PKV_ERR_NULL;
-    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales))
-        return PKV_ERR_ALIGN;
+    if (!k_codes || !v_codes || !scales) return PKV_ERR_NULL;
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(scales)) return PKV_ERR_ALIGN;
     if (num_tokens == 0) return PKV_OK;
     if (k == nullptr || v == nullptr || slot_mapping == nullptr) return PKV_ERR_NULL;
     if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)) return PKV_ERR_ALIGN;
@@ -539,21 +537,20 @@ pkv_status pkv_append_q8(const void* k, const void* v, const int64_t* slot_mappi
         st = run_checked([&](unsigned int* verdict) { return launch_check_slots(slot_mapping, num_tokens, num_slots, verdict, s); }, s);
         if (st != PKV_OK) return st;
     }
-    return launch_append_q8(k, v, slot_mapping, num_tokens, k_codes, v_codes, k_scales, v_scales, *desc, status, s) ==
+    return launch_append_q8(k, v, slot_mapping, num_tokens, k_codes, v_codes, scales, *desc, status, s) ==
                    cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_copy_blocks_q8(const int64_t* pairs, int64_t num_pairs, void* k_codes, void* v_codes, float* k_scales,
-                              float* v_scales, const pkv_cache_desc* desc, uint32_t flags, void* stream) {
+pkv_status pkv_copy_blocks_q8(const int64_t* pairs, int64_t num_pairs, void* k_codes, void* v_codes, float* scales,
+                              const pkv_cache_desc* desc, uint32_t flags, void* stream) {
     NvtxRange nvtx_range("pkv_copy_blocks_q8");
     pkv_status st = check_desc_q8(desc, false);
     if (st != PKV_OK) return st;
     if (num_pairs < 0) return PKV_ERR_SHAPE;
-    if (!k_codes || !v_codes || !k_scales || !v_scales) return PKV_ERR_NULL;
-    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales))
-        return PKV_ERR_ALIGN;
+    if (!k_codes || !v_codes || !scales) return PKV_ERR_NULL;
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(scales)) return PKV_ERR_ALIGN;
     if (num_pairs == 0) return PKV_OK;
     if (pairs == nullptr) return PKV_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(pairs) & 7u) return PKV_ERR_ALIGN;
@@ -567,8 +564,7 @@ pkv_status pkv_copy_blocks_q8(const int64_t* pairs, int64_t num_pairs, void* k_c
     }
     // the code pools move as whole blocks of num_kv_heads * 16 * head_dim bytes (either layout)
     if (launch_copy_blocks(pairs, num_pairs, k_codes, v_codes, *desc, status, s) != cudaSuccess) return PKV_ERR_CUDA;
-    return launch_copy_scales(pairs, num_pairs, k_scales, v_scales, *desc, status, s) == cudaSuccess ? PKV_OK
-                                                                                                    : PKV_ERR_CUDA;
+    return launch_copy_scales(pairs, num_pairs, scales, *desc, status, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 size_t pkv_decode_q8_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks_per_seq,
@@ -583,8 +579,8 @@ size_t pkv_decode_q8_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
                               mq_num_ctas(desc->head_dim, batch, opts, true), &co, &po);
 }
 
-pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
-                                   const float* v_scales, const int32_t* block_tables, int32_t max_blocks_per_seq,
+pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes, const float* scales,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
                                    const int32_t* context_lens, const int32_t* query_start, int32_t batch,
                                    int32_t num_q_heads, int32_t max_query_len, float scale, void* out,
                                    void* workspace, size_t workspace_bytes, const pkv_cache_desc* desc,
@@ -600,11 +596,9 @@ pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const voi
     if (query_start == nullptr && max_query_len != 1) return PKV_ERR_SHAPE;
     if (batch == 0) return PKV_OK;
     if (!table_width_ok(batch, max_blocks_per_seq)) return PKV_ERR_SHAPE;
-    if (!q || !k_codes || !v_codes || !k_scales || !v_scales || !block_tables || !context_lens || !out ||
-        !workspace)
+    if (!q || !k_codes || !v_codes || !scales || !block_tables || !context_lens || !out || !workspace)
         return PKV_ERR_NULL;
-    if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) ||
-        !aligned16(v_scales) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+    if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(scales) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
         (reinterpret_cast<uintptr_t>(context_lens) & 3u) || (reinterpret_cast<uintptr_t>(query_start) & 3u) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PKV_ERR_ALIGN;
@@ -635,8 +629,7 @@ pkv_status pkv_decode_attention_q8(const void* q, const void* k_codes, const voi
         a.qstart = query_start ? query_start + b0 : nullptr;
         a.k_cache = k_codes;
         a.v_cache = v_codes;
-        a.k_scales = k_scales;
-        a.v_scales = v_scales;
+        a.scales = scales;
         a.q8 = 1;
         a.tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
         a.lens = context_lens + b0;

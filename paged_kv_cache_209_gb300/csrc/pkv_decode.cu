@@ -947,7 +947,7 @@ bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_di
 }
 
 bool make_map_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
-                 uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+                 uint32_t box_inner, uint32_t box_rows, bool swizzle128, bool l2_promote) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {inner, rows};
@@ -956,7 +956,8 @@ bool make_map_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, 
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType t = dtype == PKV_INT8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     return fn(map, t, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              l2_promote ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

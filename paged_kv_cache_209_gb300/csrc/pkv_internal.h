@@ -107,9 +107,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
 // KV head), 16-row x 64-column boxes, 128-byte swizzle.
 bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim);
 // 2-D TMA view of `rows` rows of `inner` elements (PKV_INT8: uint8, else
-// float32) `row_bytes` apart; boxes of box_inner x box_rows.
+// float32) `row_bytes` apart; boxes of box_inner x box_rows; l2_promote
+// widens L2 fetches of a box to 256 bytes.
 bool make_map_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
-                 uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+                 uint32_t box_inner, uint32_t box_rows, bool swizzle128, bool l2_promote);
 
 // ---------------------------------------------------------------- shared-prefix decode
 // Chunk-first pass: for every group, the queries of all its members against
@@ -172,9 +173,9 @@ int device_sm_count();
 
 // ---------------------------------------------------------------- low-bit KV
 cudaError_t launch_append_q8(const void* k, const void* v, const int64_t* slots, int64_t num_tokens, void* k_codes,
-                             void* v_codes, float* k_scales, float* v_scales, const pkv_cache_desc& d,
+                             void* v_codes, float* scales, const pkv_cache_desc& d,
                              unsigned int* status, cudaStream_t s);
-cudaError_t launch_copy_scales(const int64_t* pairs, int64_t num_pairs, float* k_scales, float* v_scales,
+cudaError_t launch_copy_scales(const int64_t* pairs, int64_t num_pairs, float* scales,
                                const pkv_cache_desc& d, unsigned int* status, cudaStream_t s);
 
 // ---------------------------------------------------------------- multi-query decode
@@ -202,9 +203,9 @@ struct MqArgs {
     int32_t max_query_len;  // queries per sequence, at most (32 / group)
     int32_t wpu;            // warps per unit: 1, 2 or 4 row groups of 8 (from max_query_len * group)
     float scale;
-    // int8 pools (q8 != 0): k_cache / v_cache are the code pools, with these scales
-    const float* k_scales;
-    const float* v_scales;
+    // int8 pools (q8 != 0): k_cache / v_cache are the code pools, with this scale
+    // pool: [num_blocks][kv_heads][2 (K, V)][16] float
+    const float* scales;
     int32_t q8;
     int32_t test_stall;  // PKV_FLAG_TEST_STALL: the producer issues nothing
 };

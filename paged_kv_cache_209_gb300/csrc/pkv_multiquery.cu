@@ -66,19 +66,21 @@ struct Mq {
     static constexpr int kHalves = D / 64;
     static constexpr int kPoolBytes = 16 * D * 2;
     // bf16: K then V (16 rows x D each). int8: K codes [16][D] at 0, V codes
-    // [D][16] at 16 D; the 16 K scales (at 0) and the 16 V scales (at 128) of
-    // the stage sit in a ring of their own after the stages, 256 bytes per
-    // stage. Every TMA destination is 128-byte aligned (a smaller alignment
-    // faults); stages are 1024-byte aligned (the K swizzle).
+    // [D][16] at 16 D; the (block, head) scale record (16 K scales, then 16 V
+    // scales at byte 64) of the stage sits in a ring of its own after the
+    // stages, 128 bytes per stage, and comes with the K side. Every TMA
+    // destination is 128-byte aligned (a smaller alignment faults); stages
+    // are 1024-byte aligned (the K swizzle).
     static constexpr int kStageBytes = Q8 ? 2 * 16 * D : 2 * kPoolBytes;
-    static constexpr int kScaleBytes = Q8 ? 256 : 0;
-    static constexpr int kVScaleOff = 128;
-    static constexpr int kSideBytes = kStageBytes / 2;                     // K or V of one stage
-    static constexpr int kTxBytes = Q8 ? kSideBytes + 64 : kSideBytes;    // one side's copies
+    static constexpr int kScaleBytes = Q8 ? 128 : 0;
+    static constexpr int kVScaleOff = 64;
+    static constexpr int kSideBytes = kStageBytes / 2;  // K or V of one stage
+    // bytes one side's copies deliver: the K side carries the scale record
+    static constexpr int kTxK = Q8 ? kSideBytes + kScaleBytes : kSideBytes;
+    static constexpr int kTxV = kSideBytes;
     static constexpr int kOffScales = kStages * kStageBytes;
     static_assert(kStages >= kIssueLanes && kIssueLanes < 32, "a batch of issued blocks must fit the ring");
-    static_assert(kOffScales % 1024 == 0 && kScaleBytes % 128 == 0 && kVScaleOff % 128 == 0,
-                  "TMA destinations must stay 128-byte aligned");
+    static_assert(kOffScales % 1024 == 0 && kScaleBytes % 128 == 0, "TMA destinations must stay 128-byte aligned");
     // shared memory (offsets from a 1024-byte aligned base): the ring,
     // full[2][NST] (K side, V side), empty[NST] and the piece barrier, stage flags and the abort
     // flag, the combine scratch (two buffers of 4 warps x 8 rows x (D + 2)
@@ -204,7 +206,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 template <int D, int NST, bool Q8>
 __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
     mq_tc_kernel(const MqArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                 const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs) {
+                 const __grid_constant__ CUtensorMap tmS) {
     using C = Mq<D, NST, Q8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -234,10 +236,7 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
     if (threadIdx.x == 32) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        if (Q8) {
-            tma_prefetch_desc(&tmKs);
-            tma_prefetch_desc(&tmVs);
-        }
+        if (Q8) tma_prefetch_desc(&tmS);
     }
     grid_dependency_wait();
     allow_dependents();
@@ -293,7 +292,7 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
         // ------------------------------------------------ producer warps (as in the decode kernel)
         // Both walk the same blocks in the same order; warp kConsumers issues
         // the K side and warp kConsumers + 1 the V side, each arriving on its
-        // own full barrier. One warp issuing all four copies of an int8 block
+        // own full barrier. One warp issuing all the copies of an int8 block
         // (codes and scale rows) was the pace-setter: the int8 call took
         // 107 us with one producer, 95 us without the scale copies.
         if (a.test_stall) return;  // test hook: nothing is ever issued, so every consumer wait runs out
@@ -342,7 +341,7 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                     if (mine) {
                         stage_ok[s] = load ? 1 : 0;  // both sides write the same flag
                         if (load) {
-                            mbar_arrive_expect_tx(&fulls[s], C::kTxBytes);
+                            mbar_arrive_expect_tx(&fulls[s], side == 0 ? C::kTxK : C::kTxV);
                         } else {
                             if (side == 0) atomicOr(a.status, PKV_DEVERR_RANGE);
                             mbar_arrive(&fulls[s]);
@@ -352,13 +351,12 @@ __global__ void __launch_bounds__(Mq<D, NST, Q8>::kThreads, 2)
                         uint8_t* st = smem + s * C::kStageBytes + side * C::kSideBytes;
                         const int hb = bid * a.kv_heads + pc.head;
                         if (Q8) {
-                            uint8_t* sc = smem + C::kOffScales + s * C::kScaleBytes + side * C::kVScaleOff;
                             if (side == 0) {
                                 tma_load_2d(st, &tmK, 0, hb * 16, &fulls[s], kv_policy);
-                                tma_load_2d(sc, &tmKs, 0, hb, &fulls[s], kv_policy);
+                                tma_load_2d(smem + C::kOffScales + s * C::kScaleBytes, &tmS, 0, hb, &fulls[s],
+                                            kv_policy);
                             } else {
                                 tma_load_2d(st, &tmV, 0, hb * 16, &fulls[s], kv_policy);
-                                tma_load_2d(sc, &tmVs, 0, hb, &fulls[s], kv_policy);
                             }
                         } else {
                             const int y = hb * 16;
@@ -847,28 +845,28 @@ constexpr int mq_stages() { return Q8 ? kMq8Stages : kMqStages; }
 template <int D, bool Q8>
 cudaError_t run_mq(const MqArgs& a, int grid, cudaStream_t s) {
     using C = Mq<D, mq_stages<Q8>(), Q8>;
-    CUtensorMap tmK, tmV, tmKs, tmVs;
+    CUtensorMap tmK, tmV, tmS;
     if (Q8) {
         const uint64_t hb = static_cast<uint64_t>(a.num_blocks) * a.kv_heads;
-        if (!make_map_2d(&tmK, PKV_INT8, a.k_cache, D, hb * 16, D, D, 16, true) ||
+        if (!make_map_2d(&tmK, PKV_INT8, a.k_cache, D, hb * 16, D, D, 16, true, true) ||
             // the V codes of one (block, head) are D x 16 contiguous bytes: described as 16 rows of D
             // bytes, one TMA box moves them with 16 row requests instead of D requests of 16 bytes
-            !make_map_2d(&tmV, PKV_INT8, a.v_cache, D, hb * 16, D, D, 16, false) ||
-            !make_map_2d(&tmKs, PKV_F32, a.k_scales, 16, hb, 64, 16, 1, false) ||
-            !make_map_2d(&tmVs, PKV_F32, a.v_scales, 16, hb, 64, 16, 1, false))
+            !make_map_2d(&tmV, PKV_INT8, a.v_cache, D, hb * 16, D, D, 16, false, true) ||
+            // one 128-byte scale record (K row, V row) per (block, head), fetched
+            // without L2 promotion: a 256-byte fetch would bring a record of
+            // another head along, which this CTA does not read
+            !make_map_2d(&tmS, PKV_F32, a.scales, 32, hb, 128, 32, 1, false, false))
             return cudaErrorInvalidValue;
     } else {
         const int64_t rows = a.num_blocks * a.kv_heads * 16;
         if (!make_pool_map(&tmK, a.k_cache, rows, D) || !make_pool_map(&tmV, a.v_cache, rows, D))
             return cudaErrorInvalidValue;
-        tmKs = tmK;  // unused by the bf16 path
-        tmVs = tmV;
+        tmS = tmK;  // unused by the bf16 path
     }
     const size_t smem = C::smem_bytes(a.batch);
     cudaFuncSetAttribute(mq_tc_kernel<D, mq_stages<Q8>(), Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
-    return launch_pdl(mq_tc_kernel<D, mq_stages<Q8>(), Q8>, dim3(grid), dim3(C::kThreads), smem, s, a, tmK, tmV, tmKs,
-                      tmVs);
+    return launch_pdl(mq_tc_kernel<D, mq_stages<Q8>(), Q8>, dim3(grid), dim3(C::kThreads), smem, s, a, tmK, tmV, tmS);
 }
 
 }  // namespace

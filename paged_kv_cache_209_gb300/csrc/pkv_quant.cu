@@ -22,8 +22,9 @@
 //
 // Layouts: K codes [num_blocks][Hkv][16][D] (token rows), V codes
 // [num_blocks][Hkv][D][16] (the 16 token codes of one coordinate together,
-// the order the decode kernel feeds the tensor cores), K and V scales
-// [num_blocks][Hkv][16] float32.
+// the order the decode kernel feeds the tensor cores), scales
+// [num_blocks][Hkv][2][16] float32 (per block and head one 128-byte record:
+// the K-row scales, then the V-row scales).
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -50,8 +51,8 @@ __global__ void __launch_bounds__(64) append_q8_kernel(const __nv_bfloat16* __re
                                                         const __nv_bfloat16* __restrict__ v,
                                                         const int64_t* __restrict__ slots, int64_t num_tokens,
                                                         int8_t* __restrict__ kc, int8_t* __restrict__ vc,
-                                                        float* __restrict__ ks, float* __restrict__ vs,
-                                                        int64_t num_slots, int kv_heads, unsigned int* status) {
+                                                        float* __restrict__ scales, int64_t num_slots, int kv_heads,
+                                                        unsigned int* status) {
     constexpr int kPer = D / 32;
     grid_dependency_wait();  // a block copy before us may target the same block
     allow_dependents();
@@ -85,40 +86,37 @@ __global__ void __launch_bounds__(64) append_q8_kernel(const __nv_bfloat16* __re
 #pragma unroll
         for (int e = 0; e < kPer; ++e) c[e] = static_cast<int8_t>(code_of(x[e], scale));
         const int64_t blk = s >> 4, slot = s & 15;
-        const int64_t row = (blk * kv_heads + h) * 16 + slot;
+        const int64_t bh = blk * kv_heads + h;
         if (!is_v) {
-            int8_t* dst = kc + row * D + lane * kPer;
+            int8_t* dst = kc + (bh * 16 + slot) * D + lane * kPer;
 #pragma unroll
             for (int e = 0; e < kPer; ++e) dst[e] = c[e];
-            if (lane == 0) ks[row] = scale;
         } else {
 #pragma unroll
-            for (int e = 0; e < kPer; ++e) vc[((blk * kv_heads + h) * D + lane * kPer + e) * 16 + slot] = c[e];
-            if (lane == 0) vs[row] = scale;
+            for (int e = 0; e < kPer; ++e) vc[(bh * D + lane * kPer + e) * 16 + slot] = c[e];
         }
+        if (lane == 0) scales[(bh * 2 + (is_v ? 1 : 0)) * 16 + slot] = scale;  // the (block, head) record
     }
 }
 
-// Copy-on-write of the scales: 16 floats per (block, head), both pools.
+// Copy-on-write of the scales: a block's records are kv_heads * 32 contiguous
+// floats (K and V rows of every head), moved as float4.
 __global__ void __launch_bounds__(256) copy_scales_kernel(const int64_t* __restrict__ pairs, int64_t num_pairs,
-                                                          float* __restrict__ ks, float* __restrict__ vs,
-                                                          int64_t num_blocks, int per_block, unsigned int* status) {
+                                                          float4* __restrict__ scales, int64_t num_blocks,
+                                                          int per_block, unsigned int* status) {
     grid_dependency_wait();
     allow_dependents();
-    const int64_t total = num_pairs * 2 * per_block;
+    const int64_t total = num_pairs * per_block;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-        const int64_t p = idx / (2 * per_block);
-        int64_t c = idx - p * 2 * per_block;
-        const bool is_v = c >= per_block;
-        if (is_v) c -= per_block;
+        const int64_t p = idx / per_block;
+        const int64_t c = idx - p * per_block;
         const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
         if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
-            if (c == 0 && !is_v) atomicOr(status, PKV_DEVERR_RANGE);
+            if (c == 0) atomicOr(status, PKV_DEVERR_RANGE);
             continue;
         }
-        float* pool = is_v ? vs : ks;
-        pool[dst * per_block + c] = pool[src * per_block + c];
+        scales[dst * per_block + c] = scales[src * per_block + c];
     }
 }
 
@@ -131,8 +129,8 @@ int grid_of(int64_t work, int per_block) {
 }  // namespace
 
 cudaError_t launch_append_q8(const void* k, const void* v, const int64_t* slots, int64_t num_tokens, void* k_codes,
-                             void* v_codes, float* k_scales, float* v_scales, const pkv_cache_desc& d,
-                             unsigned int* status, cudaStream_t s) {
+                             void* v_codes, float* scales, const pkv_cache_desc& d, unsigned int* status,
+                             cudaStream_t s) {
     const int64_t warps = num_tokens * d.num_kv_heads * 2;
     const int grid = grid_of(warps, 2);  // 64-thread CTAs: a decode step's few hundred rows reach every SM
     const int64_t num_slots = d.num_blocks * 16;
@@ -142,17 +140,17 @@ cudaError_t launch_append_q8(const void* k, const void* v, const int64_t* slots,
     auto* vc = static_cast<int8_t*>(v_codes);
     if (d.head_dim == 128)
         return launch_pdl(append_q8_kernel<128>, dim3(grid), dim3(64), 0, s, kb, vb, slots, num_tokens, kc, vc,
-                          k_scales, v_scales, num_slots, d.num_kv_heads, status);
-    return launch_pdl(append_q8_kernel<64>, dim3(grid), dim3(64), 0, s, kb, vb, slots, num_tokens, kc, vc, k_scales,
-                      v_scales, num_slots, d.num_kv_heads, status);
+                          scales, num_slots, d.num_kv_heads, status);
+    return launch_pdl(append_q8_kernel<64>, dim3(grid), dim3(64), 0, s, kb, vb, slots, num_tokens, kc, vc, scales,
+                      num_slots, d.num_kv_heads, status);
 }
 
-cudaError_t launch_copy_scales(const int64_t* pairs, int64_t num_pairs, float* k_scales, float* v_scales,
-                               const pkv_cache_desc& d, unsigned int* status, cudaStream_t s) {
-    const int per_block = d.num_kv_heads * 16;
-    const int grid = grid_of(num_pairs * 2 * per_block, 256);
-    return launch_pdl(copy_scales_kernel, dim3(grid), dim3(256), 0, s, pairs, num_pairs, k_scales, v_scales,
-                      d.num_blocks, per_block, status);
+cudaError_t launch_copy_scales(const int64_t* pairs, int64_t num_pairs, float* scales, const pkv_cache_desc& d,
+                               unsigned int* status, cudaStream_t s) {
+    const int per_block = d.num_kv_heads * 32 / 4;  // float4 per block
+    const int grid = grid_of(num_pairs * per_block, 256);
+    return launch_pdl(copy_scales_kernel, dim3(grid), dim3(256), 0, s, pairs, num_pairs,
+                      reinterpret_cast<float4*>(scales), d.num_blocks, per_block, status);
 }
 
 }  // namespace pkv

@@ -95,13 +95,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_multiquery_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp,
                                              ctypes.c_size_t, desc_p, u32, opts_p, vp]
     lib.pkv_multiquery_attention.restype = ctypes.c_int
-    lib.pkv_append_q8.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, desc_p, u32, vp]
+    lib.pkv_append_q8.argtypes = [vp, vp, vp, i64, vp, vp, vp, desc_p, u32, vp]
     lib.pkv_append_q8.restype = ctypes.c_int
-    lib.pkv_copy_blocks_q8.argtypes = [vp, i64, vp, vp, vp, vp, desc_p, u32, vp]
+    lib.pkv_copy_blocks_q8.argtypes = [vp, i64, vp, vp, vp, desc_p, u32, vp]
     lib.pkv_copy_blocks_q8.restype = ctypes.c_int
     lib.pkv_decode_q8_workspace_size.argtypes = [i32, i32, i32, i32, desc_p, opts_p]
     lib.pkv_decode_q8_workspace_size.restype = ctypes.c_size_t
-    lib.pkv_decode_attention_q8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, ctypes.c_float, vp,
+    lib.pkv_decode_attention_q8.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, ctypes.c_float, vp,
                                             vp, ctypes.c_size_t, desc_p, u32, opts_p, vp]
     lib.pkv_decode_attention_q8.restype = ctypes.c_int
     lib.pkv_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp,
@@ -353,36 +353,35 @@ def q8_desc(k_codes: torch.Tensor) -> CacheDesc:
     return CacheDesc(nb, bs, hkv, d, PKV_INT8)
 
 
-def _check_q8_pools(k_codes, v_codes, k_scales, v_scales):
+def _check_q8_pools(k_codes, v_codes, scales):
     nb, hkv, bs, d = k_codes.shape
     if v_codes.shape != (nb, hkv, d, bs) or v_codes.dtype != torch.int8:
         raise ValueError("v_codes is int8 [num_blocks][num_kv_heads][head_dim][16]")
-    for t in (k_scales, v_scales):
-        if t.shape != (nb, hkv, bs) or t.dtype != torch.float32:
-            raise ValueError("scales are float32 [num_blocks][num_kv_heads][16]")
+    if scales.shape != (nb, hkv, 2, bs) or scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError("scales are contiguous float32 [num_blocks][num_kv_heads][2][16] (K row, V row)")
 
 
-def pkv_append_q8(k, v, slot_mapping, k_codes, v_codes, k_scales, v_scales, flags: int = 0, stream=None) -> None:
+def pkv_append_q8(k, v, slot_mapping, k_codes, v_codes, scales, flags: int = 0, stream=None) -> None:
     """Quantizing slot-mapped append of bf16 k/v [tokens][kv_heads][head_dim] into the int8 pools."""
     lib = load_library()
-    _check_q8_pools(k_codes, v_codes, k_scales, v_scales)
+    _check_q8_pools(k_codes, v_codes, scales)
     desc = q8_desc(k_codes)
     if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16 or slot_mapping.dtype != torch.int64:
         raise ValueError("k/v are bf16, slot_mapping int64")
     _check("pkv_append_q8", lib.pkv_append_q8(
         _ptr(k), _ptr(v), _ptr(slot_mapping), int(slot_mapping.numel()), _ptr(k_codes), _ptr(v_codes),
-        _ptr(k_scales), _ptr(v_scales), ctypes.byref(desc), flags, _stream(stream)))
+        _ptr(scales), ctypes.byref(desc), flags, _stream(stream)))
 
 
-def pkv_copy_blocks_q8(src_dst_pairs, k_codes, v_codes, k_scales, v_scales, flags: int = 0, stream=None) -> None:
+def pkv_copy_blocks_q8(src_dst_pairs, k_codes, v_codes, scales, flags: int = 0, stream=None) -> None:
     lib = load_library()
-    _check_q8_pools(k_codes, v_codes, k_scales, v_scales)
+    _check_q8_pools(k_codes, v_codes, scales)
     desc = q8_desc(k_codes)
     if src_dst_pairs.dtype != torch.int64:
         raise ValueError("pairs are int64 [n][2]")
     _check("pkv_copy_blocks_q8", lib.pkv_copy_blocks_q8(
         _ptr(src_dst_pairs) if src_dst_pairs.numel() else None, int(src_dst_pairs.shape[0]), _ptr(k_codes),
-        _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), ctypes.byref(desc), flags, _stream(stream)))
+        _ptr(v_codes), _ptr(scales), ctypes.byref(desc), flags, _stream(stream)))
 
 
 def pkv_decode_q8_workspace_size(batch: int, num_q_heads: int, max_blocks_per_seq: int, k_codes,
@@ -393,13 +392,13 @@ def pkv_decode_q8_workspace_size(batch: int, num_q_heads: int, max_blocks_per_se
                                                 ctypes.byref(desc), _opts(0, num_ctas)))
 
 
-def pkv_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale: float,
+def pkv_decode_attention_q8(q, k_codes, v_codes, scales, block_tables, context_lens, scale: float,
                             query_start=None, max_query_len: int = 1, out=None, workspace=None, flags: int = 0,
                             num_ctas: int = 0, stream=None):
     """Attention over the int8 pools: decode (query_start None, q [batch][q_heads][head_dim]) or
     causal multi-query (q [query_start[-1]][q_heads][head_dim]). Returns ``out`` (bf16)."""
     lib = load_library()
-    _check_q8_pools(k_codes, v_codes, k_scales, v_scales)
+    _check_q8_pools(k_codes, v_codes, scales)
     desc = q8_desc(k_codes)
     rows, q_heads, d = q.shape
     batch = int(context_lens.shape[0])
@@ -416,7 +415,7 @@ def pkv_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_table
         need = pkv_decode_q8_workspace_size(batch, q_heads, max_blocks, k_codes, max_query_len, num_ctas)
         workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
     _check("pkv_decode_attention_q8", lib.pkv_decode_attention_q8(
-        _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), max_blocks,
+        _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(scales), _ptr(block_tables), max_blocks,
         _ptr(context_lens), _ptr(query_start), batch, q_heads, max_query_len, ctypes.c_float(scale), _ptr(out),
         _ptr(workspace), workspace.numel(), ctypes.byref(desc), flags, _opts(0, num_ctas), _stream(stream)))
     return out

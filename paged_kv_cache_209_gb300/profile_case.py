@@ -47,10 +47,10 @@ def main():
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     for _ in range(args.steps):
         if q8:
-            ks, vs = w["k_scales"], w["v_scales"]
-            pkv.pkv_copy_blocks_q8(w["pairs"], w["k_pool"], w["v_pool"], ks, vs)
-            pkv.pkv_append_q8(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"], ks, vs)
-            pkv.pkv_decode_attention_q8(w["q"], w["k_pool"], w["v_pool"], ks, vs, w["tables"], w["lens"], w["scale"],
+            sc = w["scales"]
+            pkv.pkv_copy_blocks_q8(w["pairs"], w["k_pool"], w["v_pool"], sc)
+            pkv.pkv_append_q8(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"], sc)
+            pkv.pkv_decode_attention_q8(w["q"], w["k_pool"], w["v_pool"], sc, w["tables"], w["lens"], w["scale"],
                                         out=out, workspace=ws)
             continue
         pkv.pkv_copy_blocks(w["pairs"], w["k_pool"], w["v_pool"])

@@ -206,10 +206,13 @@ def device_workload(name: str, device, seed_offset: int = 0) -> dict:
     n_shared = cfg.get("prefix", 0) // BLOCK_SIZE
     group = np.zeros(B, dtype=np.int32) if n_shared else np.full(B, -1, dtype=np.int32)
     if cfg["dtype"] == "int8":
+        # scale pool [blocks][heads][2][16]: K-row and V-row scales of a block and head together;
+        # k_scales / v_scales are views of its two halves
+        scales = torch.stack([uniform((num_blocks, HKV, BLOCK_SIZE), 0.02, 0.03, seed + 5, device),
+                              uniform((num_blocks, HKV, BLOCK_SIZE), 0.02, 0.03, seed + 6, device)], dim=2)
         pools = dict(k_pool=int8_codes((num_blocks, HKV, BLOCK_SIZE, D), seed, device),
                      v_pool=int8_codes((num_blocks, HKV, D, BLOCK_SIZE), seed + 1, device),
-                     k_scales=uniform((num_blocks, HKV, BLOCK_SIZE), 0.02, 0.03, seed + 5, device),
-                     v_scales=uniform((num_blocks, HKV, BLOCK_SIZE), 0.02, 0.03, seed + 6, device))
+                     scales=scales, k_scales=scales[:, :, 0], v_scales=scales[:, :, 1])
     else:
         pools = dict(k_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed, bf, device),
                      v_pool=torch_normal((num_blocks, HKV, BLOCK_SIZE, D), seed + 1, bf, device))

@@ -212,8 +212,8 @@ def test_llama8k_q8_workload(pkv):
     vn = OA.bf16_bits_to_f64(cases.host_view(w["v_new"]))
     # the V pool is stored [block][head][d][16]; the oracle writes token rows through a transposed view
     OQ.append_tokens_q8(hkc, hvc.transpose(0, 1, 3, 2), hks, hvs, kn, vn, slots)
-    pkv.pkv_append_q8(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"], w["k_scales"], w["v_scales"])
-    out = pkv.pkv_decode_attention_q8(w["q"], w["k_pool"], w["v_pool"], w["k_scales"], w["v_scales"], w["tables"],
+    pkv.pkv_append_q8(w["k_new"], w["v_new"], w["slots"], w["k_pool"], w["v_pool"], w["scales"])
+    out = pkv.pkv_decode_attention_q8(w["q"], w["k_pool"], w["v_pool"], w["scales"], w["tables"],
                                       w["lens"], w["scale"])
     torch.cuda.synchronize()
     assert pkv.pkv_device_status(clear=True) == 0

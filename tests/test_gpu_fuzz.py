@@ -144,8 +144,8 @@ def test_int8_random(pkv, seed):
     qs = torch.from_numpy(c["query_start"]).to(dev) if multi else None
     out = pkv.pkv_decode_attention_q8(
         c["q"].to(dev), torch.from_numpy(kc).to(dev),
-        torch.from_numpy(np.ascontiguousarray(vc.transpose(0, 1, 3, 2))).to(dev), torch.from_numpy(ks).to(dev),
-        torch.from_numpy(vs).to(dev), torch.from_numpy(c["tables"]).to(dev), torch.from_numpy(c["lens"]).to(dev),
+        torch.from_numpy(np.ascontiguousarray(vc.transpose(0, 1, 3, 2))).to(dev),
+        torch.from_numpy(np.stack([ks, vs], axis=2)).to(dev), torch.from_numpy(c["tables"]).to(dev), torch.from_numpy(c["lens"]).to(dev),
         c["scale"], query_start=qs, max_query_len=mql)
     torch.cuda.synchronize()
     assert pkv.pkv_device_status(clear=True) == 0, seed

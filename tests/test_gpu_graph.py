@@ -124,7 +124,7 @@ def test_int8_step_in_a_graph(pkv):
     vc, vs = OQ.quantize_rows(OA.bf16_bits_to_f64(cases.host_view(w["host"]["v_pool"])))
     dev = torch.device("cuda", 0)
     pools0 = [torch.from_numpy(kc).to(dev), torch.from_numpy(np.ascontiguousarray(vc.transpose(0, 1, 3, 2))).to(dev),
-              torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev)]
+              torch.from_numpy(np.stack([ks, vs], axis=2)).to(dev)]
     pools = [p.clone() for p in pools0]
     out = torch.empty_like(w["q"])
     ws = torch.zeros(pkv.pkv_decode_q8_workspace_size(4, 32, w["tables"].shape[1], pools[0]), dtype=torch.uint8,

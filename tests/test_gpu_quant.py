@@ -39,7 +39,7 @@ def empty_pools(nb, hkv, d=128, seed=0):
     vc = torch.randint(-127, 128, (nb, hkv, d, 16), generator=g, dtype=torch.int8)
     ks = torch.rand((nb, hkv, 16), generator=g) * 0.05
     vs = torch.rand((nb, hkv, 16), generator=g) * 0.05
-    return kc, vc, ks, vs
+    return kc, vc, torch.stack([ks, vs], dim=2).contiguous()   # scale pool [nb][hkv][2][16]
 
 
 def host(t):
@@ -54,7 +54,7 @@ def logical_v(vc):
 @pytest.mark.parametrize("d", [128, 64])
 def test_append_and_copy_bit_exact(pkv, d):
     nb, hkv, T = 24, 4, 40
-    kc, vc, ks, vs = empty_pools(nb, hkv, d)
+    kc, vc, sc = empty_pools(nb, hkv, d)
     rng = np.random.default_rng(3)
     k = torch.from_numpy(W.numpy_normal((T, hkv, d), 31) * rng.uniform(0.01, 50, (T, hkv, 1)).astype(np.float32)).to(torch.bfloat16)
     v = torch.from_numpy(W.numpy_normal((T, hkv, d), 32)).to(torch.bfloat16)
@@ -66,24 +66,25 @@ def test_append_and_copy_bit_exact(pkv, d):
     v[9, 2] = torch.from_numpy(np.r_[254.0, tie[1, 1:]]).to(torch.bfloat16)
     slots = rng.permutation(nb * 16)[:T].astype(np.int64)
     slots[[5, 17]] = -1                                       # skipped tokens
-    hkc, hvc, hks, hvs = host(kc).copy(), logical_v(vc), host(ks).copy(), host(vs).copy()
-    OQ.append_tokens_q8(hkc, hvc, hks, hvs, OA.bf16_bits_to_f64(cases.bf16_bits(k)),
+    hkc, hvc, hsc = host(kc).copy(), logical_v(vc), host(sc).copy()
+    # the oracle keeps K and V scales apart: it writes through views of the record's two rows
+    OQ.append_tokens_q8(hkc, hvc, hsc[:, :, 0], hsc[:, :, 1], OA.bf16_bits_to_f64(cases.bf16_bits(k)),
                         OA.bf16_bits_to_f64(cases.bf16_bits(v)), slots)
-    dkc, dvc, dks, dvs = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
-    pkv.pkv_append_q8(k.cuda(), v.cuda(), torch.from_numpy(slots).cuda(), dkc, dvc, dks, dvs)
+    dkc, dvc, dsc = kc.cuda(), vc.cuda(), sc.cuda()
+    pkv.pkv_append_q8(k.cuda(), v.cuda(), torch.from_numpy(slots).cuda(), dkc, dvc, dsc)
     torch.cuda.synchronize()
     assert np.array_equal(host(dkc), hkc) and np.array_equal(logical_v(dvc), hvc)
-    assert np.array_equal(host(dks), hks) and np.array_equal(host(dvs), hvs)
+    assert np.array_equal(host(dsc), hsc)
     # two written blocks copied onto blocks 0 and 1 (no pair reads a block another one writes)
     srcs = [b for b in dict.fromkeys(int(s) // 16 for s in slots if s >= 0) if b > 1][:2]
     pairs = np.array([[srcs[0], 0], [srcs[1], 1]], dtype=np.int64)
-    for arr in (hkc, hvc, hks, hvs):
+    for arr in (hkc, hvc, hsc):
         for src, dst in pairs:
             arr[dst] = arr[src]
-    pkv.pkv_copy_blocks_q8(torch.from_numpy(pairs).cuda(), dkc, dvc, dks, dvs)
+    pkv.pkv_copy_blocks_q8(torch.from_numpy(pairs).cuda(), dkc, dvc, dsc)
     torch.cuda.synchronize()
     assert np.array_equal(host(dkc), hkc) and np.array_equal(logical_v(dvc), hvc)
-    assert np.array_equal(host(dks), hks) and np.array_equal(host(dvs), hvs)
+    assert np.array_equal(host(dsc), hsc)
     assert pkv.pkv_device_status(clear=True) == 0
 
 
@@ -106,10 +107,9 @@ def run_q8(pkv, c, **kw):
     dev = torch.device("cuda", 0)
     kc = torch.from_numpy(c["kc"]).to(dev)
     vc = torch.from_numpy(np.ascontiguousarray(c["vc"].transpose(0, 1, 3, 2))).to(dev)   # coordinate-major
-    ks = torch.from_numpy(c["ks"]).to(dev)
-    vs = torch.from_numpy(c["vs"]).to(dev)
+    sc = torch.from_numpy(np.stack([c["ks"], c["vs"]], axis=2)).to(dev)   # [blocks][heads][2][16]
     qs = torch.from_numpy(c["query_start"]).to(dev) if "query_start" in c else None
-    out = pkv.pkv_decode_attention_q8(c["q"].to(dev), kc, vc, ks, vs, torch.from_numpy(c["tables"]).to(dev),
+    out = pkv.pkv_decode_attention_q8(c["q"].to(dev), kc, vc, sc, torch.from_numpy(c["tables"]).to(dev),
                                       torch.from_numpy(c["lens"]).to(dev), c["scale"], query_start=qs, **kw)
     torch.cuda.synchronize()
     return out
