@@ -60,15 +60,43 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 #endif
 
 // ------------------------------------------------------------------ schedule
+// Cost a segment of nb blocks adds beyond its blocks in the CTA split, in
+// blocks: kSegCost when nb < kSegCostBelow, plus max(kSegMinCost - nb, 0)
+// (build knobs, passed to the kernels in DecodeArgs; all zero gives every CTA
+// the same number of blocks). Swept on the 256-sequence mixed-length layer
+// (decode call, 100 back to back): equal block counts 716 us; 4 for every
+// segment 674 us but the 8K layer (one segment start per CTA range) 2.5 %
+// slower; least cost 16 blocks 683 us; 4 below 256 blocks 674 us with the 8K
+// and 128K layers unchanged (their segments are longer).
+#ifndef PKV_SEG_COST
+#define PKV_SEG_COST 4
+#endif
+#ifndef PKV_SEG_COST_BELOW
+#define PKV_SEG_COST_BELOW 256
+#endif
+#ifndef PKV_SEG_MIN_COST
+#define PKV_SEG_MIN_COST 1
+#endif
+constexpr int kSegCost = PKV_SEG_COST;
+constexpr int kSegCostBelow = PKV_SEG_COST_BELOW;
+constexpr int kSegMinCost = PKV_SEG_MIN_COST;
+
 // s_pre[i] = sum_{i' <= i} ceil(len_i' / 16) over this launch's sequences,
-// s_len[i] = len_i clamped to [0, max_blocks * 16].
+// s_len[i] = len_i clamped to [0, max_blocks * 16], s_cost[i] = the sum over
+// sequences 0 .. i with blocks of their cost in the CTA split (blocks plus
+// seg_extra): the prefixes of the cost-weighted split.
 //
 // With shared-prefix groups (s_boff non-null) a member of a group (the rule
 // of prefix_member_blocks) attends here only its tokens past the group's
 // shared blocks: s_len[i] is that own-token count and s_boff[i] the block
 // offset at which they start, -1 for a plain sequence. A sequence that names
 // a group but fails the rule sets PKV_DEVERR_RANGE and is attended whole.
-__device__ void build_prefix(int32_t* s_pre, int32_t* s_len, int32_t* s_boff, const DecodeArgs& a) {
+__device__ __forceinline__ int seg_extra(int nb, const DecodeArgs& a) {
+    return (nb < a.seg_cost_below ? a.seg_cost : 0) + max(a.seg_min_cost - nb, 0);
+}
+__device__ __forceinline__ int seg_max_unit(const DecodeArgs& a) { return 1 + seg_extra(1, a); }
+
+__device__ void build_prefix(int32_t* s_pre, int32_t* s_len, int32_t* s_cost, int32_t* s_boff, const DecodeArgs& a) {
     const int cap = a.max_blocks * 16;
     for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
         int n = a.lens[i];
@@ -85,20 +113,31 @@ __device__ void build_prefix(int32_t* s_pre, int32_t* s_len, int32_t* s_boff, co
         }
         s_len[i] = n;
         s_pre[i] = (n + 15) >> 4;
+        s_cost[i] = n > 0 ? ((n + 15) >> 4) + seg_extra((n + 15) >> 4, a) : 0;
     }
     __syncthreads();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        int carry = 0;
+        int carry = 0, carry_c = 0;
         for (int base = 0; base < a.batch; base += 32) {
-            int x = base + lane < a.batch ? s_pre[base + lane] : 0;
+            const bool in = base + lane < a.batch;
+            int x = in ? s_pre[base + lane] : 0;
+            int xc = in ? s_cost[base + lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
+                const int yc = __shfl_up_sync(0xffffffffu, xc, o);
+                if (lane >= o) {
+                    x += y;
+                    xc += yc;
+                }
             }
-            if (base + lane < a.batch) s_pre[base + lane] = x + carry;
+            if (in) {
+                s_pre[base + lane] = x + carry;
+                s_cost[base + lane] = xc + carry_c;
+            }
             carry += __shfl_sync(0xffffffffu, x, 31);
+            carry_c += __shfl_sync(0xffffffffu, xc, 31);
         }
     }
     __syncthreads();
@@ -223,11 +262,10 @@ __device__ __forceinline__ void load_piece(PieceVals<NPER, NG>& v, const float* 
 // software-pipelined: the loads of the next two pieces are in flight while
 // the current two are combined (online log-sum-exp, per head).
 template <typename T, int D, int NPER, int NG>
-__device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long long U, int warp, int lane,
+__device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, const CostSplit& sp, int warp, int lane,
                             long long c0, int slot0, int npieces, bool fold) {
     const int S = G * D / 4;
     const int e0 = warp * S;
-    const long long C = a.num_ctas;
     const int g_first = e0 / D;
     const int ng = (e0 + S - 1) / D - g_first + 1;  // heads of the slice, <= NG
     int kj[NPER];                                   // head slot of each of the lane's elements
@@ -242,7 +280,7 @@ __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long lo
 #pragma unroll
     for (int j = 0; j < NPER; ++j) O[j] = 0.f;
     auto ptr = [&](int p) {
-        return piece_slice(a.partials, piece_cta(pc.seg_start, c0, p, U, C), p == 0 ? slot0 : 0, warp, S, G);
+        return piece_slice(a.partials, sp.piece_cta(c0, p), p == 0 ? slot0 : 0, warp, S, G);
     };
     PieceVals<NPER, NG> cur[2], nxt[2];
 #pragma unroll
@@ -309,12 +347,13 @@ __device__ void merge_slice(const Piece& pc, int G, const DecodeArgs& a, long lo
 // merges that segment's slice and puts the counter back to zero for the
 // next call.
 template <typename T, int D, int NPER, int NG>
-__device__ void signal_pending(const Piece* pending, int npending, int G, const DecodeArgs& a, long long U,
-                               int warp, int lane, const int32_t* s_boff) {
+__device__ void signal_pending(const Piece* pending, int npending, int G, const DecodeArgs& a, const int32_t* s_pre,
+                               const int32_t* s_cost, int warp, int lane, const int32_t* s_boff) {
     if (npending == 0) return;
     __threadfence();
     __syncwarp();
-    const long long C = a.num_ctas;
+    CostSplit sp;  // rebuilt from shared memory: nothing of it stays live through the stream
+    sp.init(s_pre, s_cost, a.batch, a.kv_heads, seg_max_unit(a), a.num_ctas);
     long long c0s[2];
     int nps[2];
     int* counters[2];
@@ -323,9 +362,9 @@ __device__ void signal_pending(const Piece* pending, int npending, int G, const 
     for (int i = 0; i < 2; ++i) {
         if (i >= npending) break;
         const Piece& pc = pending[i];
-        c0s[i] = cta_of(pc.seg_start, U, C);
-        const long long c1 = cta_of(pc.seg_start + pc.seg_len - 1, U, C);
-        nps[i] = pieces_of_segment(c0s[i], c1, U, C);
+        c0s[i] = sp.cta_of(pc.seg_start);
+        const long long c1 = sp.cta_of(pc.seg_start + pc.seg_len - 1);
+        nps[i] = sp.pieces(c0s[i], c1);
         counters[i] = a.counters + (static_cast<long long>(pc.seq) * a.kv_heads + pc.head) * 4 + warp;
         if (lane == 0) old[i] = atomicAdd(counters[i], 1);
     }
@@ -336,8 +375,8 @@ __device__ void signal_pending(const Piece* pending, int npending, int G, const 
         if (!last) continue;
         __threadfence();
         const Piece& pc = pending[i];
-        const int slot0 = (pc.seg_start == range_start(c0s[i], U, C)) ? 0 : 1;
-        merge_slice<T, D, NPER, NG>(pc, G, a, U, warp, lane, c0s[i], slot0, nps[i],
+        const int slot0 = (pc.seg_start == sp.start(c0s[i])) ? 0 : 1;
+        merge_slice<T, D, NPER, NG>(pc, G, a, sp, warp, lane, c0s[i], slot0, nps[i],
                                     s_boff != nullptr && s_boff[pc.seq] >= 0);
         if (lane == 0) *counters[i] = 0;
     }
@@ -398,7 +437,7 @@ struct Tc {
     static constexpr int kOffScratch = ((kOffFlags + kStages * 4 + 4 + 15) / 16) * 16;
     static constexpr size_t scratch_floats(int G) { return 2 * static_cast<size_t>(kConsumers) * G * (D + 2); }
     static size_t smem_bytes(int G, int batch) {
-        return 1024 + kOffScratch + scratch_floats(G) * 4 + 2 * static_cast<size_t>(batch) * 4;
+        return 1024 + kOffScratch + scratch_floats(G) * 4 + 3 * static_cast<size_t>(batch) * 4;
     }
 };
 
@@ -419,7 +458,8 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     const int buf_floats = C::kConsumers * G * (D + 2);
     int32_t* s_pre = reinterpret_cast<int32_t*>(scratch + 2 * buf_floats);
     int32_t* s_len = s_pre + a.batch;
-    int32_t* s_boff = a.prefix_group != nullptr ? s_len + a.batch : nullptr;  // shared-prefix mode only
+    int32_t* s_cost = s_len + a.batch;
+    int32_t* s_boff = a.prefix_group != nullptr ? s_cost + a.batch : nullptr;  // shared-prefix mode only
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -445,13 +485,17 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     // the stream (typically the append) must be complete.
     grid_dependency_wait();
     allow_dependents();
-    build_prefix(s_pre, s_len, s_boff, a);  // contains __syncthreads
+    build_prefix(s_pre, s_len, s_cost, s_boff, a);  // contains __syncthreads
     if (threadIdx.x == 0) PKV_STAMP(a, blockIdx.x, 1);
 
-    const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
     const long long cta = blockIdx.x;
-    const long long ua = range_start(cta, U, a.num_ctas);
-    const long long ub = range_start(cta + 1, U, a.num_ctas);
+    long long ua, ub;
+    {
+        CostSplit sp;
+        sp.init(s_pre, s_cost, a.batch, a.kv_heads, seg_max_unit(a), a.num_ctas);
+        ua = sp.start(cta);
+        ub = sp.start(cta + 1);
+    }
 
     if (warp == C::kConsumers) {
         // ------------------------------------------------ producer warp
@@ -716,7 +760,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     }
     // G <= 8: a warp's slice is G*D/4 <= 2*D elements, at most D/16 per lane
     // and at most three heads
-    signal_pending<__nv_bfloat16, D, D / 16, 3>(pending, npending, G, a, U, warp, lane, s_boff);
+    signal_pending<__nv_bfloat16, D, D / 16, 3>(pending, npending, G, a, s_pre, s_cost, warp, lane, s_boff);
     if (warp == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 5);
 }
 
@@ -737,17 +781,22 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
     float* sm_l = sm_m + C::kWarps * GMAX;
     int32_t* s_pre = reinterpret_cast<int32_t*>(sm_l + C::kWarps * GMAX);
     int32_t* s_len = s_pre + a.batch;
+    int32_t* s_cost = s_len + a.batch;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     grid_dependency_wait();
     allow_dependents();
-    build_prefix(s_pre, s_len, nullptr, a);
+    build_prefix(s_pre, s_len, s_cost, nullptr, a);
 
-    const long long U = static_cast<long long>(a.kv_heads) * s_pre[a.batch - 1];
     const long long cta = blockIdx.x;
-    const long long ua = range_start(cta, U, a.num_ctas);
-    const long long ub = range_start(cta + 1, U, a.num_ctas);
+    long long ua, ub;
+    {
+        CostSplit sp;
+        sp.init(s_pre, s_cost, a.batch, a.kv_heads, seg_max_unit(a), a.num_ctas);
+        ua = sp.start(cta);
+        ub = sp.start(cta + 1);
+    }
     const int G = a.group;
     const float scale_log2 = a.scale * kLog2e;
     const T* q = static_cast<const T*>(a.q);
@@ -833,7 +882,7 @@ __global__ void __launch_bounds__(128) decode_cc_kernel(const DecodeArgs a) {
         if (write_piece<T, D>(sm_o, sm_m, sm_l, GMAX, G, pc, a, cta, warp, lane, false)) pending[npending++] = pc;
         __syncthreads();
     }
-    signal_pending<T, D, GMAX * D / 128, GMAX / 4 + 1>(pending, npending, G, a, U, warp, lane, nullptr);
+    signal_pending<T, D, GMAX * D / 128, GMAX / 4 + 1>(pending, npending, G, a, s_pre, s_cost, warp, lane, nullptr);
 }
 
 // ------------------------------------------------------------------ host side
@@ -916,7 +965,7 @@ int cc_query(const void*, int threads, size_t smem) {
 
 template <typename T, int D, int GMAX>
 size_t cc_smem(int batch) {
-    return static_cast<size_t>(4) * GMAX * D * 4 + 2 * 4 * GMAX * 4 + 2 * static_cast<size_t>(batch) * 4;
+    return static_cast<size_t>(4) * GMAX * D * 4 + 2 * 4 * GMAX * 4 + 3 * static_cast<size_t>(batch) * 4;
 }
 
 int variant_of(int dtype, int D, int gmax) { return (dtype == PKV_BF16 ? 4 : 0) + (D == 128 ? 2 : 0) + (gmax == 16 ? 1 : 0); }
@@ -1045,7 +1094,11 @@ int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t
     return PKV_OK;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeArgs& args, const DecodePlan& plan, cudaStream_t s) {
+    DecodeArgs a = args;
+    a.seg_cost = kSegCost;
+    a.seg_cost_below = kSegCostBelow;
+    a.seg_min_cost = kSegMinCost;
     cudaError_t err = cudaSuccess;
     const int D = a.head_dim;
     if (plan.kernel == 2) {

@@ -67,6 +67,11 @@ struct DecodeArgs {
     int32_t dtype;
     int32_t num_ctas;
     int32_t test_stall;  // PKV_FLAG_TEST_STALL: the producer issues nothing
+    // cost model of the CTA split (set by launch_decode): a segment of nb blocks
+    // costs nb + (nb < seg_cost_below ? seg_cost : 0) + max(seg_min_cost - nb, 0)
+    int32_t seg_cost;
+    int32_t seg_cost_below;
+    int32_t seg_min_cost;
     float scale;
     // Shared-prefix groups (null for a plain call). A sequence with a group
     // attends only its own blocks past the group's shared ones here, and its

@@ -1,9 +1,12 @@
 // Stream-K schedule shared by the split decode kernels: one unit of work is
 // one (sequence i, KV head h, block b), units ordered i-major, then h, then
 // b; the units of one (i, h) form a segment. A launch of C CTAs gives CTA c
-// the contiguous units [c U / C, (c + 1) U / C), so every CTA streams the same
-// number of blocks (to within one) whatever the mix of context lengths; a
-// segment cut by a range boundary leaves one piece per CTA it touches.
+// a contiguous range of units: [c U / C, (c + 1) U / C) in the multi-query
+// kernels, so every CTA streams the same number of blocks (to within one)
+// whatever the mix of context lengths; in the decode kernels the ranges are
+// placed by cost (CostSplit below), so a CTA whose range holds many short
+// segments streams fewer blocks. A segment cut by a range boundary leaves
+// one piece per CTA it touches.
 #pragma once
 
 #include <stdint.h>
@@ -79,6 +82,87 @@ struct Walker {
 };
 
 __device__ __forceinline__ long long range_start(long long c, long long U, long long C) { return c * U / C; }
+
+// The same split weighted by cost: a segment of nb blocks costs nb + e(nb),
+// e >= 0 being the work of a segment outside its blocks (loading q,
+// combining the consumer warps' states, writing the row) that the ring of
+// staged blocks does not hide; its first unit carries e, every unit costs 1.
+// With K(u) the cost of the units before u and T = K(U), CTA c gets
+// [start(c), start(c + 1)), start(c) being the first unit with
+// K(u) >= floor(c T / C). e = 0 is the plain split. The block prefix sums
+// pre[] and the cost prefix sums cost[] (per sequence, one KV head) locate a
+// unit or a cost in O(log batch); max_unit bounds the cost of one unit.
+struct CostSplit {
+    const int32_t* pre;
+    const int32_t* cost;
+    int batch, kvh, max_unit;
+    long long U, T, C;
+
+    __device__ void init(const int32_t* pre_, const int32_t* cost_, int batch_, int kvh_, int max_unit_,
+                         long long C_) {
+        pre = pre_;
+        cost = cost_;
+        batch = batch_;
+        kvh = kvh_;
+        max_unit = max_unit_ > 1 ? max_unit_ : 1;
+        C = C_;
+        U = static_cast<long long>(kvh) * pre[batch - 1];
+        T = static_cast<long long>(kvh) * cost[batch - 1];
+    }
+    // smallest i with kvh * arr[i] > x (arr non-decreasing, x < kvh * arr[batch - 1])
+    __device__ int seq_of(const int32_t* arr, long long x) const {
+        int lo = 0, hi = batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (static_cast<long long>(kvh) * arr[mid] > x)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        return lo;
+    }
+    // K(u) for 0 <= u <= U
+    __device__ long long cost_before(long long u) const {
+        if (T == U) return u;
+        if (u >= U) return T;
+        const int i = seq_of(pre, u);
+        const int p0 = i ? pre[i - 1] : 0, q0 = i ? cost[i - 1] : 0;
+        const int nb = pre[i] - p0, e = cost[i] - q0 - nb;
+        const long long u0 = static_cast<long long>(kvh) * p0;
+        const long long h = (u - u0) / nb, b = u - u0 - h * nb;
+        return static_cast<long long>(kvh) * q0 + h * (nb + e) + (b > 0 ? e + b : 0);
+    }
+    __device__ long long start(long long c) const {
+        const long long t = c * T / C;
+        if (T == U) return t;
+        if (t >= T) return U;
+        const int i = seq_of(cost, t);
+        const int p0 = i ? pre[i - 1] : 0, q0 = i ? cost[i - 1] : 0;
+        const int nb = pre[i] - p0, e = cost[i] - q0 - nb;
+        const long long k0 = static_cast<long long>(kvh) * q0;
+        const long long h = (t - k0) / (nb + e), rr = t - k0 - h * (nb + e);
+        const long long s0 = static_cast<long long>(kvh) * p0 + h * nb;
+        return rr == 0 ? s0 : s0 + (rr - e > 1 ? rr - e : 1);
+    }
+    // the CTA whose range holds unit u: max c with start(c) <= u
+    __device__ long long cta_of(long long u) const { return ((cost_before(u) + 1) * C - 1) / T; }
+    // every range is non-empty when a range's cost share covers the dearest unit
+    __device__ bool dense() const { return T >= C * max_unit; }
+    // pieces of a segment whose units lie in CTAs c0 .. c1 (the non-empty ranges among them)
+    __device__ int pieces(long long c0, long long c1) const {
+        if (dense()) return static_cast<int>(c1 - c0 + 1);
+        int n = 0;
+        for (long long c = c0; c <= c1; ++c) n += start(c) < start(c + 1);
+        return n;
+    }
+    // CTA of piece p of a segment whose first piece is in CTA c0
+    __device__ long long piece_cta(long long c0, int p) const {
+        if (dense()) return c0 + p;
+        for (long long c = c0; c < C; ++c)
+            if (start(c) < start(c + 1) && p-- == 0) return c;
+        return C - 1;  // not reached for a valid piece index
+    }
+};
 
 // The CTA whose range holds unit u: max c with range_start(c) <= u.
 __device__ __forceinline__ long long cta_of(long long u, long long U, long long C) { return ((u + 1) * C - 1) / U; }
