@@ -274,7 +274,11 @@ def _oracle_task(task):
         from oracle import quant as OQ
         q, kc, vc, ks, vs, tables, lens = _load(paths)
         i, scale, kv_heads = args
-        OQ.decode_attention_q8(q[i:i + 1], kc, vc, ks, vs, tables[i:i + 1], lens[i:i + 1], scale, kv_heads, "bf16")
+        # the oracle dequantizes every block it is handed: hand it this sequence's blocks only
+        nblk = (int(lens[i]) + 15) // 16
+        sel = tables[i, :nblk]
+        OQ.decode_attention_q8(q[i:i + 1], kc[sel], vc[sel], ks[sel], vs[sel],
+                               np.arange(nblk, dtype=np.int32)[None, :], lens[i:i + 1], scale, kv_heads, "bf16")
         return int(lens[i]) * 2 * kv_heads * (kc.shape[-1] + 4)
     raise ValueError(kind)
 

@@ -22,15 +22,20 @@
 // a set of rows (an atomic counter per tile, head and warp) merges them.
 //
 // prefix_umma_kernel (default): 128-row tiles on the 5th-generation tensor
-// cores. A TMA warp streams 64-token steps (four blocks) of K and V through a
-// shared-memory ring; one thread issues
-//     S[128][64]  = Q[128][D] K^T      (tcgen05.mma, accumulator in tensor memory,
-//                                        two S buffers so the next S overlaps)
-//     O[128][D]  += P[128][64] V[64][D] (P as bf16 hi + lo from shared memory,
-//                                        V read MN-major straight from the TMA layout)
-// and four softmax warps, one thread per query row, read S rows from tensor
-// memory, run the online softmax (base 2, lazy rescale of O in tensor
-// memory), and write P.
+// cores, one role per warp. Two TMA warps stream 64-token steps (four
+// blocks) of K and of V through separate shared-memory rings; two warps
+// issue the score products of even and of odd steps,
+//     S[128][64]  = Q[128][D] K^T      (tcgen05.mma, fp32 accumulator in tensor
+//                                        memory, four S/P buffers)
+// and two the products of the two 32-token halves of P,
+//     O[128][D]  += P[128][32] V[32][D] (P as bf16 hi + lo written by the softmax
+//                                        over its own S columns in tensor memory,
+//                                        V read MN-major straight from the TMA
+//                                        layout, one O accumulator per half)
+// while eight softmax warps, one thread per (query row, token half), load S
+// rows from tensor memory, run the online softmax (base 2, lazy rescale of O
+// in tensor memory) and store P. The two halves of a row are combined at the
+// end.
 //
 // prefix_mma_kernel: 64-row tiles, four warps of 16 rows each on mma.sync
 // (m16n8k16) with the S accumulator fragments reused as the A operand of P;
