@@ -412,28 +412,37 @@ __device__ void zero_empty_rows(const int32_t* s_len, const int32_t* s_boff, con
 #define PKV_TC_ISSUE_LANES 4
 #endif
 constexpr int kTcIssueLanes = PKV_TC_ISSUE_LANES;
+#ifndef PKV_TC_PRODUCERS
+#define PKV_TC_PRODUCERS 2
+#endif
+constexpr int kTcProducers = PKV_TC_PRODUCERS;
 
 template <int D, int NST>
 struct Tc {
     static constexpr int kStages = NST;
     static constexpr int kConsumers = 4;
+    // Producer warps: 2 = one issues the K boxes of every block and the other
+    // the V boxes, each on its own full barrier (consumers wait for the V side
+    // just before the P.V product); 1 = one warp issues both on one barrier.
+    static constexpr int kProducers = kTcProducers;
+    static_assert(kProducers == 1 || kProducers == 2, "one or two producer warps");
     // Unit k goes to stage k % kStages and to consumer warp k % kConsumers. A
     // stage must always meet the same warp: otherwise a warp could wait on a
     // stage two phases ahead of its last use, and a parity wait cannot tell
     // those phases apart.
     static_assert(kStages % kConsumers == 0, "ring depth must be a multiple of the consumer warps");
     static_assert(kStages >= kTcIssueLanes && kTcIssueLanes < 32, "a batch of issued blocks must fit the ring");
-    static constexpr int kThreads = (kConsumers + 1) * 32;
+    static constexpr int kThreads = (kConsumers + kProducers) * 32;
     static constexpr int kHalves = D / 64;                  // 64-column TMA boxes per row
     static constexpr int kPoolBytes = 16 * D * 2;           // one block, one head, one pool
     static constexpr int kStageBytes = 2 * kPoolBytes;      // K then V
     // shared memory layout (offsets from a 1024-byte aligned base): the ring,
-    // then full[NST], empty[NST], the merge barrier, stage flags and the abort
+    // then full[producers][NST], empty[NST], the merge barrier, stage flags and the abort
     // flag, then the combine scratch (two buffers of 4 warps x G x (D + 2)
     // floats, alternating between pieces) and the per-sequence prefix sums
     // and lengths.
     static constexpr int kOffBars = kStages * kStageBytes;
-    static constexpr int kOffFlags = kOffBars + (2 * kStages + 2) * 8;
+    static constexpr int kOffFlags = kOffBars + ((1 + kProducers) * kStages + 2) * 8;
     static constexpr int kOffScratch = ((kOffFlags + kStages * 4 + 4 + 15) / 16) * 16;
     static constexpr size_t scratch_floats(int G) { return 2 * static_cast<size_t>(kConsumers) * G * (D + 2); }
     static size_t smem_bytes(int G, int batch) {
@@ -448,8 +457,8 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
     using C = Tc<D, NST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-    uint64_t* empty = full + C::kStages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);  // [producers][stages]: K side, V side
+    uint64_t* empty = full + C::kProducers * C::kStages;
     uint64_t* merge_bar = empty + C::kStages;  // all four warps published their piece state
     int* stage_ok = reinterpret_cast<int*>(smem + C::kOffFlags);
     volatile int* abort_flag = stage_ok + C::kStages;
@@ -470,7 +479,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1);
+            for (int p = 0; p < C::kProducers; ++p) mbar_init(&full[p * C::kStages + s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(merge_bar, C::kConsumers);
@@ -497,12 +506,16 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         ub = sp.start(cta + 1);
     }
 
-    if (warp == C::kConsumers) {
-        // ------------------------------------------------ producer warp
+    if (warp >= C::kConsumers) {
+        // ------------------------------------------------ producer warps
         // K/V blocks are read once per call: stream them with evict-first so
-        // the block tables, q and the merge pieces stay in L2.
+        // the block tables, q and the merge pieces stay in L2. With two
+        // producers both walk the same blocks; side 0 issues K, side 1 V.
         const uint64_t kv_policy = l2_evict_first_policy();
         if (a.test_stall) return;  // test hook: nothing is ever issued, so every consumer wait runs out
+        const int side = warp - C::kConsumers;
+        uint64_t* fulls = full + side * C::kStages;
+        constexpr int kTx = C::kProducers == 2 ? C::kPoolBytes : C::kStageBytes;
         Walker wk;
         wk.init(s_pre, a.batch, a.kv_heads, ua, ub);
         long long k = 0;
@@ -543,24 +556,28 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
                     const bool mine = lane < n;
                     const bool load = mine && bid >= 0 && bid < a.num_blocks;
                     if (mine) {
-                        stage_ok[s] = load ? 1 : 0;
+                        stage_ok[s] = load ? 1 : 0;  // both sides write the same flag
                         if (load) {
-                            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                            mbar_arrive_expect_tx(&fulls[s], kTx);
                         } else {
-                            atomicOr(a.status, PKV_DEVERR_RANGE);
-                            mbar_arrive(&full[s]);
+                            if (side == 0) atomicOr(a.status, PKV_DEVERR_RANGE);
+                            mbar_arrive(&fulls[s]);
                         }
                     }
                     if (load) {
                         uint8_t* st = smem + s * C::kStageBytes;
                         const int y = (bid * a.kv_heads + pc.head) * 16;
+                        if (C::kProducers == 1 || side == 0) {
 #pragma unroll
-                        for (int hf = 0; hf < C::kHalves; ++hf)
-                            tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &full[s], kv_policy);
+                            for (int hf = 0; hf < C::kHalves; ++hf)
+                                tma_load_2d(st + hf * 2048, &tmK, hf * 64, y, &fulls[s], kv_policy);
+                        }
+                        if (C::kProducers == 1 || side == 1) {
 #pragma unroll
-                        for (int hf = 0; hf < C::kHalves; ++hf)
-                            tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &full[s], kv_policy);
-                        if (kk == 0) PKV_STAMP(a, blockIdx.x, 2);
+                            for (int hf = 0; hf < C::kHalves; ++hf)
+                                tma_load_2d(st + C::kPoolBytes + hf * 2048, &tmV, hf * 64, y, &fulls[s], kv_policy);
+                        }
+                        if (kk == 0 && side == 0) PKV_STAMP(a, blockIdx.x, 2);
                     }
                     k += n;
                     e0 += n;
@@ -568,12 +585,12 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
                 cur = nxt;
             }
         }
-        // After an abort, wait (bounded) for the copies still in flight
-        // into the ring before the CTA may exit.
+        // After an abort, wait (bounded) for this warp's copies still in
+        // flight into the ring before the CTA may exit.
         if (!ok && lane == 0) {
             const long long first = k > C::kStages ? k - C::kStages : 0;
             for (long long u = first; u < k; ++u)
-                mbar_wait(&full[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
+                mbar_wait(&fulls[u % C::kStages], static_cast<uint32_t>((u / C::kStages) & 1), a.status, nullptr);
         }
         return;
     }
@@ -623,12 +640,13 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
         for (int blk = pc.blk_from; blk < pc.blk_to; ++blk, ++k) {
             if (static_cast<int>(k & (C::kConsumers - 1)) != warp) continue;
             const int s = static_cast<int>(k % C::kStages);
-            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / C::kStages) & 1), a.status, abort_flag,
-                           a.test_stall ? kTestWaitLimitNs : kWaitLimitNs))
-                return;
+            const uint32_t par = static_cast<uint32_t>((k / C::kStages) & 1);
+            const unsigned long long wlim = a.test_stall ? kTestWaitLimitNs : kWaitLimitNs;
+            if (!mbar_wait(&full[s], par, a.status, abort_flag, wlim)) return;
             if (k == 0 && lane == 0) PKV_STAMP(a, blockIdx.x, 3);
             const int valid = min(16, n_ctx - blk * 16);
-            if (stage_ok[s]) {
+            const bool use = stage_ok[s];
+            if (use) {
                 const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
                 const uint32_t vbase = kbase + C::kPoolBytes;
                 // ---- S^T = K Q^T, even and odd k-steps on two accumulators
@@ -691,6 +709,7 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
                 const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
                 const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
                 // ---- O^T += V^T P^T; rows past the context are zeroed (they may hold anything)
+                if (C::kProducers == 2 && !mbar_wait(&full[C::kStages + s], par, a.status, abort_flag, wlim)) return;
                 uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
                 if (valid < 16) {
                     mlo = (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
@@ -710,6 +729,9 @@ __global__ void __launch_bounds__(Tc<D, NST>::kThreads, 2)
                     mma_bf16_16816(o[i], a0, a1, a2, a3, bl0, bl1);
                 }
             }
+            // a stage is handed back only after both of its sides have landed
+            if (C::kProducers == 2 && !use && !mbar_wait(&full[C::kStages + s], par, a.status, abort_flag, wlim))
+                return;
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
@@ -1053,12 +1075,12 @@ int decode_plan(const pkv_cache_desc& d, int32_t batch, int32_t q_heads, int32_t
             int n = 0;
             if (d.head_dim == 128) {
                 sm += st == 12 ? Tc<128, 12>::smem_bytes(G, chunk) : Tc<128, 8>::smem_bytes(G, chunk);
-                n = st == 12 ? cached_occupancy(2, 128 * 100 + st, sm, 160, nullptr, tc_query<128, 12>)
-                             : cached_occupancy(2, 128 * 100 + st, sm, 160, nullptr, tc_query<128, 8>);
+                n = st == 12 ? cached_occupancy(2, 128 * 100 + st, sm, Tc<128, 12>::kThreads, nullptr, tc_query<128, 12>)
+                             : cached_occupancy(2, 128 * 100 + st, sm, Tc<128, 8>::kThreads, nullptr, tc_query<128, 8>);
             } else {
                 sm += st == 12 ? Tc<64, 12>::smem_bytes(G, chunk) : Tc<64, 8>::smem_bytes(G, chunk);
-                n = st == 12 ? cached_occupancy(2, 64 * 100 + st, sm, 160, nullptr, tc_query<64, 12>)
-                             : cached_occupancy(2, 64 * 100 + st, sm, 160, nullptr, tc_query<64, 8>);
+                n = st == 12 ? cached_occupancy(2, 64 * 100 + st, sm, Tc<64, 12>::kThreads, nullptr, tc_query<64, 12>)
+                             : cached_occupancy(2, 64 * 100 + st, sm, Tc<64, 8>::kThreads, nullptr, tc_query<64, 8>);
             }
             if (want_st == st || (want_st == 0 && st == 8)) {
                 stages = st;
