@@ -4,9 +4,10 @@
 // Work decomposition. One unit of work is one (sequence i, KV head h, block
 // b): 16 tokens of one head, 2 x 16 x head_dim elements of K and V. Units are
 // ordered i-major, then h, then b; the units of one (i, h) form a segment. A
-// launch of C CTAs gives CTA c the contiguous units [c*U/C, (c+1)*U/C), so
-// every CTA reads the same number of blocks (to within one) whatever the mix
-// of context lengths. A segment that lies wholly inside one CTA's range is
+// launch of C CTAs gives each CTA a contiguous range of units placed by cost
+// (CostSplit in pkv_schedule.cuh): a unit costs 1 and a short segment a few
+// units more, so every CTA carries about the same work whatever the mix of
+// context lengths. A segment that lies wholly inside one CTA's range is
 // finished there and its output row written directly; a segment cut by a
 // range boundary leaves one fp32 piece (unnormalised accumulator, running
 // max, running sum) per CTA it touches; the CTA that finishes the last piece
@@ -17,10 +18,10 @@
 // All query heads of a KV head (the GQA group, G <= 8) are computed from one
 // read of each K/V byte.
 //
-// Tensor-core kernel (bf16): one producer warp streams the blocks of the
-// CTA's range through an NST-stage shared-memory ring with 2-D TMA loads
-// (128-byte swizzle, so ldmatrix reads are bank-conflict free). Four consumer
-// warps take the units round robin. Per unit a warp computes
+// Tensor-core kernel (bf16): two producer warps stream the blocks of the
+// CTA's range, one the K boxes and one the V boxes, through an NST-stage
+// shared-memory ring with 2-D TMA loads (128-byte swizzle, so ldmatrix reads
+// are bank-conflict free). Four consumer warps take the units round robin. Per unit a warp computes
 //     S^T[16 tokens][8 heads] = K[16][D] * Q^T[D][8]        (mma m16n8k16)
 // runs the online softmax in fp32 on the accumulator fragments, transposes
 // P^T into the B-operand layout with movmatrix, and accumulates
