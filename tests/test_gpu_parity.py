@@ -206,6 +206,26 @@ def test_split_count_invariance_fp32(pkv, num_ctas):
     assert rel <= 1e-6 and ma <= 1e-5, (rel, ma)
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("num_ctas", [0, 5, 37, 300])
+def test_many_short_segments_with_cost_placed_ranges(pkv, kernel, num_ctas):
+    """CTA ranges are placed by cost (a segment shorter than 256 blocks costs
+    more than its blocks), so a range may hold many whole short segments and
+    few blocks, or a cut piece of a long one. 150 sequences of 1-40 tokens
+    around three long ones, at several CTA counts and on both kernels: every
+    row against the oracle, and the CTA counts agree with each other."""
+    rng = np.random.default_rng(33)
+    lens = rng.integers(1, 41, 150)
+    lens[[7, 80, 149]] = [5000, 9000, 4200]
+    c = cases.random_case(33, lens, 32, 8, 128, torch.bfloat16)
+    args = (dev(c["q"]), dev(c["k_pool"]), dev(c["v_pool"]), c["tables"], c["lens"], c["scale"])
+    got = run_attention(pkv, *args, kernel=kernel, num_ctas=num_ctas)
+    assert pkv.pkv_device_status() == 0
+    check_close(got, oracle_attention(c, c["tables"], c["lens"]))
+    ref = run_attention(pkv, *args, kernel=kernel, num_ctas=1)
+    assert (got.float() - ref.float()).abs().max().item() <= 2 ** -7
+
+
 def test_block_relabelling_gives_identical_output(pkv):
     c = cases.random_case(31, [3, 18, 35, 700], 32, 8, 128, torch.bfloat16, extra_blocks=11)
     nb = c["k_pool"].shape[0]
