@@ -52,7 +52,7 @@ __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 #define PKV_MQ_ISSUE_LANES 4
 #endif
 #ifndef PKV_MQ8_ISSUE_LANES
-#define PKV_MQ8_ISSUE_LANES 8
+#define PKV_MQ8_ISSUE_LANES 6
 #endif
 
 template <int D, int NST, bool Q8 = false>
