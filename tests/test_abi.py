@@ -140,3 +140,19 @@ def test_multiquery_workspace_routing(lib):
     assert lib.pkv_multiquery_attention(*args, 65537, *tail) == 10          # PKV_ERR_UNSUPPORTED
     tail32 = [ctypes.c_float(0.1), FAKE, FAKE, 256, ctypes.byref(_desc(dtype=0)), 0, None, None]
     assert lib.pkv_multiquery_attention(*args, 9, *tail32) == 3             # PKV_ERR_DTYPE
+
+
+def test_int8_entry_points_check_the_scale_pool(lib):
+    """The int8 calls take one scale pool ([blocks][kv_heads][2][16] float):
+    a null or misaligned pool is rejected before anything is enqueued."""
+    d = _desc(dtype=2)                            # PKV_INT8, head_dim 128
+    assert lib.pkv_append_q8(FAKE, FAKE, FAKE, 4, FAKE, FAKE, None, ctypes.byref(d), 0, None) == 1
+    assert lib.pkv_append_q8(FAKE, FAKE, FAKE, 4, FAKE, FAKE, FAKE + 4, ctypes.byref(d), 0, None) == 4
+    assert lib.pkv_copy_blocks_q8(FAKE, 1, FAKE, FAKE, None, ctypes.byref(d), 0, None) == 1
+    assert lib.pkv_copy_blocks_q8(FAKE, 1, FAKE, FAKE, FAKE + 8, ctypes.byref(d), 0, None) == 4
+    assert lib.pkv_copy_blocks_q8(None, 0, FAKE, FAKE, FAKE, ctypes.byref(d), 0, None) == 0
+    f = ctypes.c_float
+    call = lambda sc: lib.pkv_decode_attention_q8(FAKE, FAKE, FAKE, sc, FAKE, 4, FAKE, None, 2, 32, 1, f(0.1),
+                                                  FAKE, FAKE, 1 << 30, ctypes.byref(d), 0, None, None)
+    assert call(None) == 1
+    assert call(FAKE + 4) == 4
