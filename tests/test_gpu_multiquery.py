@@ -281,3 +281,25 @@ def test_prefill_running_maximum_moves_every_step(pkv, slope):
     out = run(pkv, c, d, 40)
     assert pkv.pkv_device_status(clear=True) == 0
     check(out, want(c))
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 3.0])
+@pytest.mark.parametrize("mql", [4, 40])
+def test_scale_sign_and_zero(pkv, scale, mql):
+    """A negative scale (the largest weight sits at the smallest raw score),
+    a zero scale (every visible token weighs the same: the output is the mean
+    of the visible V rows) and a large one, on the split kernel (4 queries per
+    sequence) and on the tensor-core tiles (40): every row against the
+    oracle with that scale. At scale 3 the weights are nearly one-hot, so an
+    output row is close to a single V row (entries up to ~4.5): its bf16
+    rounding alone reaches ~0.009, and the max-abs bar is taken relative to
+    the largest output, as for the int8 cache's wide scales; the relative L2
+    bar is unchanged."""
+    c = cases.multiquery_case(70 + mql, [300, 129, 1000, 64], [mql] * 4, 32, 8, 128, torch.bfloat16)
+    c["scale"] = scale
+    out = run(pkv, c, dev(c), mql)
+    assert pkv.pkv_device_status(clear=True) == 0
+    assert bool(torch.isfinite(out.float()).all())
+    ref = want(c)
+    ma, rl = cases.attention_errors(out, ref)
+    assert ma <= MAX_ABS * max(1.0, float(np.abs(ref).max())) and rl <= REL_L2, (ma, rl)
