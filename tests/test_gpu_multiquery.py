@@ -291,10 +291,10 @@ def test_scale_sign_and_zero(pkv, scale, mql):
     of the visible V rows) and a large one, on the split kernel (4 queries per
     sequence) and on the tensor-core tiles (40): every row against the
     oracle with that scale. At scale 3 the weights are nearly one-hot, so an
-    output row is close to a single V row (entries up to ~4.5): its bf16
-    rounding alone reaches ~0.009, and the max-abs bar is taken relative to
-    the largest output, as for the int8 cache's wide scales; the relative L2
-    bar is unchanged."""
+    output row is close to a single V row (entries up to ~5.5): the bf16
+    rounding of a value in [4, 8) alone is up to 0.0156, above 1e-2, so the
+    max-abs bar is taken relative to the largest output, as for the int8
+    cache's wide scales; the relative L2 bar is unchanged."""
     c = cases.multiquery_case(70 + mql, [300, 129, 1000, 64], [mql] * 4, 32, 8, 128, torch.bfloat16)
     c["scale"] = scale
     out = run(pkv, c, dev(c), mql)
