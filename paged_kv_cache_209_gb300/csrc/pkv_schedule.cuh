@@ -11,6 +11,10 @@
 
 #include <stdint.h>
 
+// The schedule is plain integer arithmetic, compiled for the host as well so
+// that tests can check it against brute force without a GPU.
+#define PKV_HD __host__ __device__
+
 namespace pkv {
 namespace {
 
@@ -31,7 +35,7 @@ struct Walker {
     int i, h, nb;
     long long seg_base;
 
-    __device__ void init(const int32_t* pre_, int batch, int kvh, long long a, long long b) {
+    PKV_HD void init(const int32_t* pre_, int batch, int kvh, long long a, long long b) {
         pre = pre_;
         kv_heads = kvh;
         start = u = a;
@@ -52,7 +56,7 @@ struct Walker {
         h = static_cast<int>((u - seg_base) / nb);
     }
 
-    __device__ bool next(Piece& p) {
+    PKV_HD bool next(Piece& p) {
         if (u >= end) return false;
         const long long s0 = seg_base + static_cast<long long>(h) * nb;
         const long long s1 = s0 + nb;
@@ -81,7 +85,7 @@ struct Walker {
     }
 };
 
-__device__ __forceinline__ long long range_start(long long c, long long U, long long C) { return c * U / C; }
+PKV_HD __forceinline__ long long range_start(long long c, long long U, long long C) { return c * U / C; }
 
 // The same split weighted by cost: a segment of nb blocks costs nb + e(nb),
 // e >= 0 being the work of a segment outside its blocks (loading q,
@@ -98,8 +102,8 @@ struct CostSplit {
     int batch, kvh, max_unit;
     long long U, T, C;
 
-    __device__ void init(const int32_t* pre_, const int32_t* cost_, int batch_, int kvh_, int max_unit_,
-                         long long C_) {
+    PKV_HD void init(const int32_t* pre_, const int32_t* cost_, int batch_, int kvh_, int max_unit_,
+                     long long C_) {
         pre = pre_;
         cost = cost_;
         batch = batch_;
@@ -110,7 +114,7 @@ struct CostSplit {
         T = static_cast<long long>(kvh) * cost[batch - 1];
     }
     // smallest i with kvh * arr[i] > x (arr non-decreasing, x < kvh * arr[batch - 1])
-    __device__ int seq_of(const int32_t* arr, long long x) const {
+    PKV_HD int seq_of(const int32_t* arr, long long x) const {
         int lo = 0, hi = batch - 1;
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
@@ -122,7 +126,7 @@ struct CostSplit {
         return lo;
     }
     // K(u) for 0 <= u <= U
-    __device__ long long cost_before(long long u) const {
+    PKV_HD long long cost_before(long long u) const {
         if (T == U) return u;
         if (u >= U) return T;
         const int i = seq_of(pre, u);
@@ -132,7 +136,7 @@ struct CostSplit {
         const long long h = (u - u0) / nb, b = u - u0 - h * nb;
         return static_cast<long long>(kvh) * q0 + h * (nb + e) + (b > 0 ? e + b : 0);
     }
-    __device__ long long start(long long c) const {
+    PKV_HD long long start(long long c) const {
         const long long t = c * T / C;
         if (T == U) return t;
         if (t >= T) return U;
@@ -145,18 +149,18 @@ struct CostSplit {
         return rr == 0 ? s0 : s0 + (rr - e > 1 ? rr - e : 1);
     }
     // the CTA whose range holds unit u: max c with start(c) <= u
-    __device__ long long cta_of(long long u) const { return ((cost_before(u) + 1) * C - 1) / T; }
+    PKV_HD long long cta_of(long long u) const { return ((cost_before(u) + 1) * C - 1) / T; }
     // every range is non-empty when a range's cost share covers the dearest unit
-    __device__ bool dense() const { return T >= C * max_unit; }
+    PKV_HD bool dense() const { return T >= C * max_unit; }
     // pieces of a segment whose units lie in CTAs c0 .. c1 (the non-empty ranges among them)
-    __device__ int pieces(long long c0, long long c1) const {
+    PKV_HD int pieces(long long c0, long long c1) const {
         if (dense()) return static_cast<int>(c1 - c0 + 1);
         int n = 0;
         for (long long c = c0; c <= c1; ++c) n += start(c) < start(c + 1);
         return n;
     }
     // CTA of piece p of a segment whose first piece is in CTA c0
-    __device__ long long piece_cta(long long c0, int p) const {
+    PKV_HD long long piece_cta(long long c0, int p) const {
         if (dense()) return c0 + p;
         for (long long c = c0; c < C; ++c)
             if (start(c) < start(c + 1) && p-- == 0) return c;
@@ -165,10 +169,10 @@ struct CostSplit {
 };
 
 // The CTA whose range holds unit u: max c with range_start(c) <= u.
-__device__ __forceinline__ long long cta_of(long long u, long long U, long long C) { return ((u + 1) * C - 1) / U; }
+PKV_HD __forceinline__ long long cta_of(long long u, long long U, long long C) { return ((u + 1) * C - 1) / U; }
 
 // Pieces of one segment: every CTA whose unit range meets [S0, S1).
-__device__ __forceinline__ int pieces_of_segment(long long c0, long long c1, long long U, long long C) {
+PKV_HD __forceinline__ int pieces_of_segment(long long c0, long long c1, long long U, long long C) {
     if (U >= C) return static_cast<int>(c1 - c0 + 1);  // no CTA range is empty
     int n = 0;
     for (long long c = c0; c <= c1; ++c) n += range_start(c, U, C) < range_start(c + 1, U, C);
@@ -179,7 +183,7 @@ __device__ __forceinline__ int pieces_of_segment(long long c0, long long c1, lon
 // whose first piece is in CTA c0. With at least one unit per CTA every range
 // is non-empty, so pieces sit in consecutive CTAs; with fewer units than CTAs
 // every non-empty range holds one unit, so piece p is unit S0 + p's CTA.
-__device__ __forceinline__ long long piece_cta(long long S0, long long c0, int p, long long U, long long C) {
+PKV_HD __forceinline__ long long piece_cta(long long S0, long long c0, int p, long long U, long long C) {
     return U >= C ? c0 + p : cta_of(S0 + p, U, C);
 }
 
